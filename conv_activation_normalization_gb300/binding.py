@@ -1,0 +1,263 @@
+"""Python binding of libgf's C ABI (``include/gf.h``).
+
+Argument marshalling only: each function checks that its tensors are CUDA,
+float32 and contiguous (the pages' host wrappers check the same), takes their
+device pointers and the current torch stream, sizes the workspace with the
+matching ``*_workspace_size`` query and calls the C entry point of the same
+name.  All arithmetic runs in the library's CUDA kernels; if ``libgf.so`` is
+missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgf.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "gf.h")
+
+GF_MODE_FP32_3XTF32 = 0
+GF_MODE_BF16 = 1
+
+_lib = None
+_lock = threading.Lock()
+
+_P, _I64, _I32, _F, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+
+_SIGS = {
+    "gf_abi_version": (_I32, []),
+    "gf_status_string": (ctypes.c_char_p, [_I32]),
+    "gf_device_status": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
+    "gf_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
+    "gf_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
+    "gf_linear_swish_bias_groupnorm_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
+    "gf_linear_swish_bias_groupnorm": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _F, _I32,
+                                              _P, _SZ, _P]),
+    "gf_linear_swish_bias_groupnorm_planes": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _F,
+                                                     _P]),
+    "gf_tf32_split": (_I32, [_P, _P, _I64, _P]),
+    "gf_linear_lse_act_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
+    "gf_linear_lse_act": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _I32, _P, _SZ, _P]),
+    "gf_ln_gelu_dconv1d_res_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
+    "gf_ln_gelu_dconv1d_res": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _F, _I32,
+                                      _P, _SZ, _P]),
+    "gf_convt3d_swish_gn_hswish_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I64, _I32, _I32, _I32,
+                                                        _I32]),
+    "gf_convt3d_swish_gn_hswish": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I32,
+                                          _I32, _I32, _I32, _F, _P, _SZ, _P]),
+}
+
+
+class GFError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgf.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libgf.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions that include/gf.h declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gf_[a-z0-9_]+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().gf_status_string(status).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def gf_device_status() -> int:
+    """Synchronise and return (and clear) the device status bits."""
+    bits = ctypes.c_int32(0)
+    st = lib().gf_device_status(ctypes.byref(bits))
+    if st not in (0, -8):
+        raise GFError(st, "gf_device_status")
+    return bits.value
+
+
+# --------------------------------------------------------------- plumbing
+_ws_cache: dict = {}
+
+
+def _workspace(device: torch.device, nbytes: int):
+    """Per-device cached scratch buffer (grown on demand)."""
+    if nbytes == 0:
+        return None
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _check(*ts):
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if t.dtype != torch.float32:
+            raise ValueError("tensors must be float32")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("tensors must be on one device")
+    return dev
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _call(name, *args):
+    st = getattr(lib(), name)(*args)
+    if st != 0:
+        raise GFError(st, name)
+
+
+def _ws_args(device, nbytes, workspace):
+    if workspace is None:
+        workspace = _workspace(device, nbytes)
+    elif workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError("workspace too small")
+    return (None if workspace is None else workspace.data_ptr()), nbytes
+
+
+# -------------------------------------------------------------- the ABI
+def gf_linear(x, W, b=None, mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None):
+    """out[M, N] = x @ W.T + b (the contraction step alone)."""
+    dev = _check(x, W, b, out)
+    M, K = x.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_linear_workspace_size(M, K, N, mode)
+        wp, nb = _ws_args(dev, nbytes, workspace)
+        _call("gf_linear", _ptr(x), _ptr(W), _ptr(b), _ptr(out), M, K, N, mode, wp, nb, _stream_ptr(stream))
+    return out
+
+
+def gf_linear_swish_bias_groupnorm(x, W, b_lin, bias, gamma, beta, groups, eps=1e-5,
+                                   mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None):
+    """out[M, N] = GroupNorm(groups)(swish(x @ W.T + b_lin) + bias) * gamma + beta."""
+    dev = _check(x, W, b_lin, bias, gamma, beta, out)
+    M, K = x.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, groups, mode)
+        wp, nb = _ws_args(dev, nbytes, workspace)
+        _call("gf_linear_swish_bias_groupnorm", _ptr(x), _ptr(W), _ptr(b_lin), _ptr(bias), _ptr(gamma),
+              _ptr(beta), _ptr(out), M, K, N, groups, eps, mode, wp, nb, _stream_ptr(stream))
+    return out
+
+
+def gf_tf32_split(src, planes=None, stream=None):
+    """planes[0] = src with the 13 low mantissa bits cleared, planes[1] = src - planes[0]."""
+    dev = _check(src, planes)
+    if planes is None:
+        planes = torch.empty((2,) + tuple(src.shape), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _call("gf_tf32_split", _ptr(src), _ptr(planes), src.numel(), _stream_ptr(stream))
+    return planes
+
+
+def gf_linear_swish_bias_groupnorm_planes(x_planes, W_planes, b_lin, bias, gamma, beta, groups, eps=1e-5, out=None,
+                                          stream=None):
+    """gf_linear_swish_bias_groupnorm on pre-split operands (x_planes [2,M,K], W_planes [2,N,K])."""
+    dev = _check(x_planes, W_planes, b_lin, bias, gamma, beta, out)
+    _, M, K = x_planes.shape
+    N = W_planes.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _call("gf_linear_swish_bias_groupnorm_planes", _ptr(x_planes), _ptr(W_planes), _ptr(b_lin), _ptr(bias),
+              _ptr(gamma), _ptr(beta), _ptr(out), M, K, N, groups, eps, _stream_ptr(stream))
+    return out
+
+
+def gf_linear_lse_act(x, W, b, negative_slope=0.01, mode=GF_MODE_FP32_3XTF32, out=None, workspace=None,
+                      stream=None):
+    """out[M, 1] = gelu(gelu(lrelu(lrelu(logsumexp(x @ W.T + b, dim=1)))))."""
+    dev = _check(x, W, b, out)
+    M, K = x.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((M, 1), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_linear_lse_act_workspace_size(M, K, N, mode)
+        wp, nb = _ws_args(dev, nbytes, workspace)
+        _call("gf_linear_lse_act", _ptr(x), _ptr(W), _ptr(b), _ptr(out), M, K, N, negative_slope, mode, wp, nb,
+              _stream_ptr(stream))
+    return out
+
+
+def gf_ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, padding, eps=1e-5,
+                           mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None):
+    """out = conv1d(gelu(layer_norm(x, [C, L])), dilation, padding) + x."""
+    dev = _check(x, ln_gamma, ln_beta, conv_w, conv_b, out)
+    B, C, L = x.shape
+    ksize = conv_w.shape[2]
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_ln_gelu_dconv1d_res_workspace_size(B, C, L, ksize, mode)
+        wp, nb = _ws_args(dev, nbytes, workspace)
+        _call("gf_ln_gelu_dconv1d_res", _ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(conv_w), _ptr(conv_b),
+              _ptr(out), B, C, L, ksize, dilation, padding, eps, mode, wp, nb, _stream_ptr(stream))
+    return out
+
+
+def convt3d_out_shape(x_shape, Cout, k, stride, pad):
+    N, _, D, H, W = x_shape
+    f = lambda i: (i - 1) * stride - 2 * pad + k  # noqa: E731
+    return (N, Cout, f(D), f(H), f(W))
+
+
+def gf_convt3d_swish_gn_hswish(x, w, b, gamma, beta, stride, pad, groups, eps=1e-5, out=None, workspace=None,
+                               stream=None):
+    """out = hardswish(GroupNorm(groups)(swish(conv_transpose3d(x, w, b, stride, pad))))."""
+    dev = _check(x, w, b, gamma, beta, out)
+    N, Cin, D, H, W = x.shape
+    Cout, k = w.shape[1], w.shape[2]
+    if out is None:
+        out = torch.empty(convt3d_out_shape(x.shape, Cout, k, stride, pad), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_convt3d_swish_gn_hswish_workspace_size(N, Cin, Cout, D, H, W, k, stride, pad, groups)
+        wp, nb = _ws_args(dev, nbytes, workspace)
+        _call("gf_convt3d_swish_gn_hswish", _ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(out),
+              N, Cin, Cout, D, H, W, k, stride, pad, groups, eps, wp, nb, _stream_ptr(stream))
+    return out

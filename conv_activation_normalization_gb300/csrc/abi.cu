@@ -1,0 +1,135 @@
+// Library-wide entry points (version, status strings, device status word) and
+// the host helpers declared in host_common.h.
+#include <cstring>
+#include <mutex>
+
+#include "host_common.h"
+
+namespace gf {
+
+// Bits recorded by kernels (see status.cuh).  One word per device.
+__device__ uint32_t g_device_status = 0;
+
+gf_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GF_OK : GF_ERR_CUDA; }
+
+gf_status check_no_alias(Span out, const Span* ins, int n) {
+  for (int i = 0; i < n; ++i)
+    if (overlaps(out, ins[i])) return GF_ERR_ALIAS;
+  return GF_OK;
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+bool g_info_ok[kMaxDevices];
+DeviceInfo g_info[kMaxDevices];
+uint32_t* g_status_ptr[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+}  // namespace
+
+gf_status current_device(DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GF_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GF_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_info_ok[dev]) {
+    DeviceInfo d{};
+    d.device = dev;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return GF_ERR_CUDA;
+    g_info[dev] = d;
+    g_info_ok[dev] = true;
+  }
+  *info = g_info[dev];
+  if (info->cc_major != 10 || info->cc_minor != 3) return GF_ERR_UNSUPPORTED_ARCH;
+  return GF_OK;
+}
+
+uint32_t* device_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                        const uint32_t* box) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return GF_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  if (rank < 1 || rank > 5 || box[0] * 4 != 128) return GF_ERR_SHAPE;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estride[5];
+  uint64_t stride = 4;
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i > 0) gstride[i - 1] = stride;
+    stride *= dims[i];
+  }
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(rank), const_cast<void*>(base),
+                              gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GF_OK : GF_ERR_CUDA;
+}
+
+}  // namespace gf
+
+extern "C" {
+
+int32_t gf_abi_version(void) { return 1; }
+
+const char* gf_status_string(gf_status s) {
+  switch (s) {
+    case GF_OK: return "ok";
+    case GF_ERR_NULL: return "a required pointer is NULL";
+    case GF_ERR_SHAPE: return "unsupported or out-of-range size";
+    case GF_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case GF_ERR_ALIAS: return "output overlaps an input or the workspace";
+    case GF_ERR_WORKSPACE: return "workspace smaller than required";
+    case GF_ERR_MODE: return "unknown or unsupported mode";
+    case GF_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case GF_ERR_DEVICE_CHECK: return "a kernel recorded a device-side error";
+    case GF_ERR_UNSUPPORTED_ARCH: return "current device is not sm_103 (GB300)";
+    default: return "unknown status";
+  }
+}
+
+gf_status gf_device_status(int32_t* device_bits) {
+  uint32_t* p = gf::device_status_word();
+  if (!p) return GF_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return GF_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return GF_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (v && cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return GF_ERR_CUDA;
+  if (device_bits) *device_bits = int32_t(v);
+  return v ? GF_ERR_DEVICE_CHECK : GF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,333 @@
+// ConvTranspose3d(k 3, stride 2, pad 1) -> Swish -> GroupNorm -> HardSwish
+//                                               (page Kimi-K2.6__l2_p60)
+//
+// Sub-pixel (phase) form of the transposed convolution.  Output index o
+// along one dimension is o = 2 i - 1 + k; splitting o into a cell q and a
+// phase p (o = 2q + p):
+//   p = 0  gets one tap:  (i = q,     k = 1)
+//   p = 1  gets two taps: (i = q + 1, k = 0) and (i = q, k = 2)
+// so the 2x2x2 outputs of cell (qd, qh, qw) read only the 2x2x2 inputs at
+// q..q+1 and every one of the 27 taps feeds exactly one phase: no zero
+// (inserted) taps are multiplied and there are no per-output branches.  The
+// last cell along a dimension (q = I - 1) has only its p = 0 output; its
+// missing input q + 1 is read as 0 and its p = 1 output is not kept.
+//
+// GroupNorm needs the statistics of the whole (sample, group) before any
+// output can be written, and the 1 GB output does not fit on chip, so:
+//   pass 1  conv + bias + Swish, per-block (sum, sum of squares) per group
+//           (fp32 within a warp, fp64 across warps) -- nothing is stored;
+//   finalize per (sample, channel): fp64 merge -> A = gamma * rstd,
+//           B = beta - mean * A;
+//   pass 2  recompute conv + bias + Swish, h = A s + B, HardSwish, store.
+// Each thread owns one cell and one group of 4 output channels at a time
+// (Cout = 16 with 4 groups, so a group is 4 channels): 32 accumulators; the
+// weights sit in shared memory as [ci][tap][co], read as float4 broadcasts.
+#include <cmath>
+
+#include "host_common.h"
+#include "kernels_common.cuh"
+
+namespace gf {
+
+constexpr int kCT_COUT = 16;
+constexpr int kCT_G = 4;
+constexpr int kCT_TX = 32, kCT_TY = 8;  // cells per block along w and h
+
+template <int CIN>
+struct CellInputs {
+  float v[CIN][2][2][2];
+};
+
+template <int CIN>
+__device__ __forceinline__ void load_cell(CellInputs<CIN>& in, const float* __restrict__ xn, int D, int H, int W,
+                                          int qd, int qh, int qw) {
+#pragma unroll
+  for (int ci = 0; ci < CIN; ++ci)
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int d = qd + a, h = qh + b, w = qw + c;
+          float v = 0.f;
+          if (d < D && h < H && w < W) v = __ldg(xn + ((size_t(ci) * D + d) * H + h) * W + w);
+          in.v[ci][a][b][c] = v;
+        }
+}
+
+// acc[co_in_group][phase], phase = pd*4 + ph*2 + pw.  ws = smem weights
+// [CIN][27][16], bias4 = conv bias of the 4 channels.
+template <int CIN>
+__device__ __forceinline__ void conv_cell(const CellInputs<CIN>& in, const float* __restrict__ ws, int cg,
+                                          float4 bias4, float (&acc)[4][8]) {
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    acc[0][p] = bias4.x;
+    acc[1][p] = bias4.y;
+    acc[2][p] = bias4.z;
+    acc[3][p] = bias4.w;
+  }
+#pragma unroll
+  for (int ci = 0; ci < CIN; ++ci)
+#pragma unroll
+    for (int kd = 0; kd < 3; ++kd)
+#pragma unroll
+      for (int kh = 0; kh < 3; ++kh)
+#pragma unroll
+        for (int kw = 0; kw < 3; ++kw) {
+          // tap k -> (phase p, input offset a): k=1 -> (0, 0); k=0 -> (1, 1); k=2 -> (1, 0)
+          const int pd = kd == 1 ? 0 : 1, ad = kd == 0 ? 1 : 0;
+          const int ph = kh == 1 ? 0 : 1, ah = kh == 0 ? 1 : 0;
+          const int pw = kw == 1 ? 0 : 1, aw = kw == 0 ? 1 : 0;
+          const int phase = pd * 4 + ph * 2 + pw;
+          const float4 w4 = *reinterpret_cast<const float4*>(ws + (ci * 27 + (kd * 3 + kh) * 3 + kw) * 16 + cg * 4);
+          const float xv = in.v[ci][ad][ah][aw];
+          acc[0][phase] = fmaf(xv, w4.x, acc[0][phase]);
+          acc[1][phase] = fmaf(xv, w4.y, acc[1][phase]);
+          acc[2][phase] = fmaf(xv, w4.z, acc[2][phase]);
+          acc[3][phase] = fmaf(xv, w4.w, acc[3][phase]);
+        }
+}
+
+// Copy w[ci][co][27] to smem as [ci][27][co].
+template <int CIN>
+__device__ __forceinline__ void stage_weights(float* ws, const float* __restrict__ w) {
+  for (int i = threadIdx.x + threadIdx.y * blockDim.x; i < CIN * 27 * kCT_COUT; i += blockDim.x * blockDim.y) {
+    const int co = i % kCT_COUT;
+    const int tap = (i / kCT_COUT) % 27;
+    const int ci = i / (kCT_COUT * 27);
+    ws[i] = __ldg(w + (size_t(ci) * kCT_COUT + co) * 27 + tap);
+  }
+}
+
+__device__ __forceinline__ uint32_t phase_mask(int qd, int qh, int qw, int D, int H, int W) {
+  // bit `phase` set when the output (2qd+pd, 2qh+ph, 2qw+pw) exists
+  uint32_t m = 0;
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    const int pd = p >> 2, ph = (p >> 1) & 1, pw = p & 1;
+    const bool ok = (pd == 0 || qd < D - 1) && (ph == 0 || qh < H - 1) && (pw == 0 || qw < W - 1);
+    m |= uint32_t(ok) << p;
+  }
+  return m;
+}
+
+// grid (ceil(W/32), ceil(H/8), D * N), block (32, 8).
+// part: [N][G][P][2] doubles, P = blocks per sample.
+template <int CIN>
+__global__ void __launch_bounds__(256) convt3d_stats_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                            const float* __restrict__ bias, double* __restrict__ part,
+                                                            int D, int H, int W) {
+  __shared__ __align__(16) float ws[CIN * 27 * kCT_COUT];
+  __shared__ double red[8][kCT_G][2];
+  stage_weights<CIN>(ws, w);
+  __syncthreads();
+  const int n = blockIdx.z / D, qd = blockIdx.z % D;
+  const int qh = blockIdx.y * kCT_TY + threadIdx.y, qw = blockIdx.x * kCT_TX + threadIdx.x;
+  const bool cell_ok = qh < H && qw < W;
+  CellInputs<CIN> in;
+  load_cell<CIN>(in, x + size_t(n) * CIN * D * H * W, D, H, W, qd, qh, qw);
+  const uint32_t pm = cell_ok ? phase_mask(qd, qh, qw, D, H, W) : 0u;
+  const int lane = threadIdx.x, wid = threadIdx.y;
+#pragma unroll 1
+  for (int cg = 0; cg < kCT_G; ++cg) {
+    const float4 b4 = bias ? __ldg(reinterpret_cast<const float4*>(bias) + cg) : make_float4(0, 0, 0, 0);
+    float acc[4][8];
+    conv_cell<CIN>(in, ws, cg, b4, acc);
+    float a = 0.f, q = 0.f;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      if ((pm >> p) & 1u) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float s = swish(acc[c][p]);
+          a += s;
+          q = fmaf(s, s, q);
+        }
+      }
+    }
+    // warp reduction in fp32; the 8 warps are summed in fp64 below
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      a += __shfl_xor_sync(0xffffffffu, a, o);
+      q += __shfl_xor_sync(0xffffffffu, q, o);
+    }
+    if (lane == 0) {
+      red[wid][cg][0] = a;
+      red[wid][cg][1] = q;
+    }
+  }
+  __syncthreads();
+  if (wid == 0 && lane < 2 * kCT_G) {
+    const int cg = lane >> 1, k = lane & 1;
+    double t = 0.0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += red[i][cg][k];
+    const int P = gridDim.x * gridDim.y * D;
+    const int blk = (qd * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    part[((size_t(n) * kCT_G + cg) * P + blk) * 2 + k] = t;
+  }
+}
+
+// grid N, block 64: merge the partials of each (n, group) -> per-channel
+// affine A = gamma * rstd, B = beta - mean * A (coef[n][co] = (A, B)).
+__global__ void convt3d_finalize_kernel(const double* __restrict__ part, const float* __restrict__ gamma,
+                                        const float* __restrict__ beta, float2* __restrict__ coef, int P,
+                                        double count, float eps) {
+  __shared__ double acc[kCT_G][2][16];
+  const int n = blockIdx.x;
+  const int t = threadIdx.x;            // 64 threads: (group, k, slice)
+  const int g = t / 16, sl = t % 16;
+  double s = 0.0, q = 0.0;
+  for (int i = sl; i < P; i += 16) {
+    const double* p = part + ((size_t(n) * kCT_G + g) * P + i) * 2;
+    s += p[0];
+    q += p[1];
+  }
+  acc[g][0][sl] = s;
+  acc[g][1][sl] = q;
+  __syncthreads();
+  if (t < kCT_COUT) {
+    const int gg = t / (kCT_COUT / kCT_G);
+    double S = 0.0, Q = 0.0;
+    for (int i = 0; i < 16; ++i) {
+      S += acc[gg][0][i];
+      Q += acc[gg][1][i];
+    }
+    const double mean = S / count;
+    const double var = fmax(Q / count - mean * mean, 0.0);
+    const double rstd = 1.0 / sqrt(var + double(eps));
+    const double A = double(gamma[t]) * rstd;
+    coef[size_t(n) * kCT_COUT + t] = make_float2(float(A), float(double(beta[t]) - mean * A));
+  }
+}
+
+__device__ __forceinline__ float hardswish(float h) { return h * fminf(fmaxf(h + 3.f, 0.f), 6.f) * (1.f / 6.f); }
+
+template <int CIN>
+__global__ void __launch_bounds__(256) convt3d_apply_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                            const float* __restrict__ bias,
+                                                            const float2* __restrict__ coef, float* __restrict__ out,
+                                                            int D, int H, int W) {
+  __shared__ __align__(16) float ws[CIN * 27 * kCT_COUT];
+  stage_weights<CIN>(ws, w);
+  __syncthreads();
+  const int n = blockIdx.z / D, qd = blockIdx.z % D;
+  const int qh = blockIdx.y * kCT_TY + threadIdx.y, qw = blockIdx.x * kCT_TX + threadIdx.x;
+  const bool cell_ok = qh < H && qw < W;
+  const int OD = 2 * D - 1, OH = 2 * H - 1, OW = 2 * W - 1;
+  CellInputs<CIN> in;
+  load_cell<CIN>(in, x + size_t(n) * CIN * D * H * W, D, H, W, qd, qh, qw);
+  const uint32_t pm = cell_ok ? phase_mask(qd, qh, qw, D, H, W) : 0u;
+#pragma unroll 1
+  for (int cg = 0; cg < kCT_G; ++cg) {
+    const float4 b4 = bias ? __ldg(reinterpret_cast<const float4*>(bias) + cg) : make_float4(0, 0, 0, 0);
+    float acc[4][8];
+    conv_cell<CIN>(in, ws, cg, b4, acc);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int co = cg * 4 + c;
+      const float2 ab = __ldg(coef + size_t(n) * kCT_COUT + co);
+      float* oc = out + (size_t(n) * kCT_COUT + co) * size_t(OD) * OH * OW;
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        if ((pm >> p) & 1u) {
+          const int od = 2 * qd + (p >> 2), oh = 2 * qh + ((p >> 1) & 1), ow = 2 * qw + (p & 1);
+          const float h = fmaf(ab.x, swish(acc[c][p]), ab.y);
+          __stcs(oc + (size_t(od) * OH + oh) * OW + ow, hardswish(h));
+        }
+      }
+    }
+  }
+}
+
+namespace {
+struct CtWs {
+  size_t part, coef, total;
+  int P;
+};
+
+CtWs ct_ws(int64_t N, int64_t D, int64_t H, int64_t W) {
+  CtWs c{};
+  c.P = int(((W + kCT_TX - 1) / kCT_TX) * ((H + kCT_TY - 1) / kCT_TY) * D);
+  c.part = 0;
+  c.coef = align_up(size_t(N) * kCT_G * c.P * 2 * sizeof(double), 256);
+  c.total = c.coef + align_up(size_t(N) * kCT_COUT * sizeof(float2), 256);
+  return c;
+}
+
+gf_status check_ct_shape(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H, int64_t W, int32_t k,
+                         int32_t stride, int32_t pad, int32_t groups) {
+  if (k != 3 || stride != 2 || pad != 1) return GF_ERR_SHAPE;
+  if (Cout != kCT_COUT || groups != kCT_G) return GF_ERR_SHAPE;
+  if (Cin < 1 || Cin > 8 || N < 1 || D < 1 || H < 1 || W < 1) return GF_ERR_SHAPE;
+  if (D * N > 65535 || (H + kCT_TY - 1) / kCT_TY > 65535 || W > (int64_t(1) << 20)) return GF_ERR_SHAPE;
+  if (D > (1 << 20) || H > (1 << 20)) return GF_ERR_SHAPE;
+  return GF_OK;
+}
+
+template <int CIN>
+void launch_ct(const float* x, const float* w, const float* b, double* part, const float* gamma, const float* beta,
+               float2* coef, float* out, int N, int D, int H, int W, int P, float eps, cudaStream_t s) {
+  const dim3 grid((W + kCT_TX - 1) / kCT_TX, (H + kCT_TY - 1) / kCT_TY, D * N), block(kCT_TX, kCT_TY);
+  convt3d_stats_kernel<CIN><<<grid, block, 0, s>>>(x, w, b, part, D, H, W);
+  const double count = double(kCT_COUT / kCT_G) * double(2 * D - 1) * double(2 * H - 1) * double(2 * W - 1);
+  convt3d_finalize_kernel<<<N, 64, 0, s>>>(part, gamma, beta, coef, P, count, eps);
+  convt3d_apply_kernel<CIN><<<grid, block, 0, s>>>(x, w, b, coef, out, D, H, W);
+}
+}  // namespace
+}  // namespace gf
+
+using namespace gf;
+
+extern "C" {
+
+size_t gf_convt3d_swish_gn_hswish_workspace_size(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H,
+                                                 int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups) {
+  if (check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) != GF_OK) return 0;
+  return ct_ws(N, D, H, W).total;
+}
+
+gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float* b, const float* gamma,
+                                     const float* beta, float* out, int64_t N, int64_t Cin, int64_t Cout, int64_t D,
+                                     int64_t H, int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups,
+                                     float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !w || !gamma || !beta || !out) return GF_ERR_NULL;
+  gf_status st = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups);
+  if (st != GF_OK) return st;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
+      (b && !aligned16(b)) || !aligned16(workspace))
+    return GF_ERR_ALIGN;
+  const CtWs wl = ct_ws(N, D, H, W);
+  if (!workspace) return GF_ERR_NULL;
+  if (workspace_bytes < wl.total) return GF_ERR_WORKSPACE;
+  const size_t outb = size_t(N) * Cout * (2 * D - 1) * (2 * H - 1) * (2 * W - 1) * 4;
+  const Span ins[] = {{x, size_t(N) * Cin * D * H * W * 4},
+                      {w, size_t(Cin) * Cout * 27 * 4},
+                      {b, size_t(Cout) * 4},
+                      {gamma, size_t(Cout) * 4},
+                      {beta, size_t(Cout) * 4},
+                      {workspace, wl.total}};
+  st = check_no_alias(Span{out, outb}, ins, 6);
+  if (st != GF_OK) return st;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != GF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  double* part = reinterpret_cast<double*>(ws + wl.part);
+  float2* coef = reinterpret_cast<float2*>(ws + wl.coef);
+  const int n = int(N), d = int(D), h = int(H), ww = int(W);
+  switch (Cin) {
+#define GF_CT_CASE(c) \
+  case c: launch_ct<c>(x, w, b, part, gamma, beta, coef, out, n, d, h, ww, wl.P, eps, s); break;
+    GF_CT_CASE(1) GF_CT_CASE(2) GF_CT_CASE(3) GF_CT_CASE(4) GF_CT_CASE(5) GF_CT_CASE(6) GF_CT_CASE(7) GF_CT_CASE(8)
+#undef GF_CT_CASE
+    default: return GF_ERR_SHAPE;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,307 @@
+// LayerNorm([C, L]) -> GELU -> dilated Conv1d -> +x   (page Kimi-K2.6__l2_p5)
+//
+//   1. ln_partial:   per (sample, chunk of 8192 elements) partial statistics
+//                    (count, mean, M2): shifted fp32 sums per thread, merged
+//                    in fp64 (Chan's pairwise formula) across the block;
+//   2. ln_finalize:  per sample, fp64 merge of the partials -> (mean, rstd);
+//   3. ln_apply:     a = GELU((x - mean) * rstd * gamma + beta), transposed to
+//                    [B][L][C] through shared memory and split into TF32 hi/lo
+//                    planes, the K-major A operand of the implicit GEMM;
+//   4. weight split: W[co][ci][t] -> planes[co][t * C + ci];
+//   5. the tcgen05 3xTF32 implicit GEMM (ConvSrc): the three dilated taps are
+//      TMA boxes of the same activation planes shifted by dilation along L,
+//      with the TMA unit's zero fill supplying the padding; its epilogue adds
+//      the conv bias and the residual x and stores out[b][co][j] (32
+//      consecutive j per warp, so every store is a full 128-byte line).
+#include <cmath>
+
+#include "gemm_tc.cuh"
+#include "host_common.h"
+#include "kernels_common.cuh"
+
+namespace gf {
+
+constexpr int kLnChunk = 8192;  // elements per ln_partial block (256 threads x 32)
+
+struct Moments {
+  double n, mean, m2;
+};
+
+__device__ __forceinline__ Moments chan_merge(Moments a, Moments b) {
+  if (a.n == 0) return b;
+  if (b.n == 0) return a;
+  const double n = a.n + b.n;
+  const double d = b.mean - a.mean;
+  return Moments{n, a.mean + d * (b.n / n), a.m2 + b.m2 + d * d * (a.n * b.n / n)};
+}
+
+// Block-wide fp64 merge of one Moments per thread (blockDim.x == 256).
+__device__ Moments block_merge(Moments m) {
+  __shared__ double sn[256], smean[256], sm2[256];
+  sn[threadIdx.x] = m.n;
+  smean[threadIdx.x] = m.mean;
+  sm2[threadIdx.x] = m.m2;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      const Moments r = chan_merge(Moments{sn[threadIdx.x], smean[threadIdx.x], sm2[threadIdx.x]},
+                                   Moments{sn[threadIdx.x + w], smean[threadIdx.x + w], sm2[threadIdx.x + w]});
+      sn[threadIdx.x] = r.n;
+      smean[threadIdx.x] = r.mean;
+      sm2[threadIdx.x] = r.m2;
+    }
+    __syncthreads();
+  }
+  return Moments{sn[0], smean[0], sm2[0]};
+}
+
+// grid (chunks, B), 256 threads.  n_per_sample = C * L (a multiple of 4).
+__global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict__ x, double* __restrict__ part,
+                                                         int64_t n_per_sample, int chunks) {
+  const int b = blockIdx.y;
+  const float* xs = x + size_t(b) * size_t(n_per_sample);
+  const int64_t begin = int64_t(blockIdx.x) * kLnChunk;
+  const int64_t end = begin + kLnChunk < n_per_sample ? begin + kLnChunk : n_per_sample;
+  const float shift = __ldg(xs);  // any value near the data keeps the shifted sums well conditioned
+  float s1 = 0.f, s2 = 0.f;
+  int cnt = 0;
+  for (int64_t i = begin + 4 * threadIdx.x; i < end; i += 4 * blockDim.x) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(xs + i));
+    const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
+    s1 += (d0 + d1) + (d2 + d3);
+    s2 += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+    cnt += 4;
+  }
+  Moments m{0.0, 0.0, 0.0};
+  if (cnt) {
+    const double n = cnt, a = s1, q = s2;
+    m = Moments{n, double(shift) + a / n, fmax(q - a * a / n, 0.0)};
+  }
+  m = block_merge(m);
+  if (threadIdx.x == 0) {
+    double* o = part + (size_t(b) * chunks + blockIdx.x) * 3;
+    o[0] = m.n;
+    o[1] = m.mean;
+    o[2] = m.m2;
+  }
+}
+
+// grid B, 256 threads: merge a sample's partials -> (mean, rstd).
+__global__ void __launch_bounds__(256) ln_finalize_kernel(const double* __restrict__ part, float2* __restrict__ stats,
+                                                          int chunks, float eps) {
+  const int b = blockIdx.x;
+  Moments m{0.0, 0.0, 0.0};
+  for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
+    const double* p = part + (size_t(b) * chunks + i) * 3;
+    m = chan_merge(m, Moments{p[0], p[1], p[2]});
+  }
+  m = block_merge(m);
+  if (threadIdx.x == 0) {
+    const double var = m.m2 / m.n;
+    stats[b] = make_float2(float(m.mean), float(1.0 / sqrt(var + double(eps))));
+  }
+}
+
+// grid (ceil(L/32), C/32, B), block (32, 8): GELU(LayerNorm(x)) for a 32x32
+// (channel, position) tile, written transposed as hi/lo planes
+// [2][B][L][C].
+__global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* __restrict__ x,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ beta,
+                                                                  const float2* __restrict__ stats,
+                                                                  float* __restrict__ planes, int C, int L, int B) {
+  __shared__ float tile[32][33];
+  const int l0 = blockIdx.x * 32, c0 = blockIdx.y * 32, b = blockIdx.z;
+  const float2 st = stats[b];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int c = c0 + ty + 8 * r, l = l0 + tx;
+    float a = 0.f;
+    if (l < L) {
+      const size_t cl = size_t(c) * L + l;
+      const float v = __ldg(x + size_t(b) * C * L + cl);
+      a = gelu_erf(fmaf((v - st.x) * st.y, __ldg(gamma + cl), __ldg(beta + cl)));
+    }
+    tile[ty + 8 * r][tx] = a;
+  }
+  __syncthreads();
+  const size_t plane = size_t(B) * L * C;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int l = l0 + ty + 8 * r, c = c0 + tx;
+    if (l < L) {
+      const float a = tile[tx][ty + 8 * r];
+      const float h = tf32_hi(a);
+      const size_t o = (size_t(b) * L + l) * C + c;
+      planes[o] = h;
+      planes[plane + o] = a - h;
+    }
+  }
+}
+
+// W[co][ci][t] -> planes[2][Cout][ksize * C] with k = t * C + ci.
+__global__ void conv_weight_split_kernel(const float* __restrict__ w, float* __restrict__ planes, int Cout, int C,
+                                         int ksize) {
+  const int64_t n = int64_t(Cout) * C * ksize;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+    const int t = int(i % ksize);
+    const int ci = int((i / ksize) % C);
+    const int64_t co = i / (int64_t(ksize) * C);
+    const float v = w[i];
+    const float h = tf32_hi(v);
+    const size_t o = size_t(co) * ksize * C + size_t(t) * C + ci;
+    planes[o] = h;
+    planes[size_t(n) + o] = v - h;
+  }
+}
+
+// Epilogue: out[b][co][j] = acc + conv_b[co] + x[b][co][j].
+struct EpiConvResidual {
+  struct Params {
+    const float* conv_b;  // may be null
+    const float* x;
+    float* out;
+    int C, L;
+  };
+  template <int BN>
+  __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
+    const int j = t.r0 + row;
+    const bool valid = j < p.L;
+#pragma unroll 1
+    for (int g = 0; g < BN / 64; ++g) {
+      const int n0 = t.n0 + g * 64;
+      if (n0 >= p.C) break;  // uniform across the warp
+      float v[64];
+      tmem_load64(taddr + uint32_t(g * 64), v);
+      const size_t base = (size_t(t.b) * p.C + n0) * size_t(p.L) + size_t(j);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        if (valid && n0 + c < p.C) {
+          const size_t idx = base + size_t(c) * p.L;
+          const float bias = p.conv_b ? __ldg(p.conv_b + n0 + c) : 0.f;
+          __stcs(p.out + idx, v[c] + bias + __ldg(p.x + idx));
+        }
+      }
+    }
+  }
+};
+
+namespace {
+constexpr int kBNConv = 256;
+
+struct ConvWs {
+  size_t part, stats, a_planes, w_planes, total;
+  int chunks;
+};
+
+ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize) {
+  ConvWs w{};
+  w.chunks = int((C * L + kLnChunk - 1) / kLnChunk);
+  size_t off = 0;
+  w.part = off;
+  off += align_up(size_t(B) * w.chunks * 3 * sizeof(double), 256);
+  w.stats = off;
+  off += align_up(size_t(B) * sizeof(float2), 256);
+  w.a_planes = off;
+  off += align_up(size_t(2) * B * L * C * 4, 256);
+  w.w_planes = off;
+  off += align_up(size_t(2) * C * ksize * C * 4, 256);
+  w.total = off;
+  return w;
+}
+
+gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize) {
+  if (B < 1 || C < 32 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
+  if (C % 32 || C > 256 || L % 4) return GF_ERR_SHAPE;
+  if (B > 65535 || L > (int64_t(1) << 30)) return GF_ERR_SHAPE;
+  return GF_OK;
+}
+}  // namespace
+}  // namespace gf
+
+using namespace gf;
+
+extern "C" {
+
+size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t mode) {
+  if (mode != GF_MODE_FP32_3XTF32 || check_conv_shape(B, C, L, ksize) != GF_OK) return 0;
+  return conv_ws(B, C, L, ksize).total;
+}
+
+gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
+                                 const float* conv_b, float* out, int64_t B, int64_t C, int64_t L, int32_t ksize,
+                                 int32_t dilation, int32_t padding, float eps, int32_t mode, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!x || !ln_gamma || !ln_beta || !conv_w || !out) return GF_ERR_NULL;
+  if (mode != GF_MODE_FP32_3XTF32) return GF_ERR_MODE;
+  gf_status st = check_conv_shape(B, C, L, ksize);
+  if (st != GF_OK) return st;
+  if (dilation < 1 || padding < 0 || int64_t(2) * padding != int64_t(dilation) * (ksize - 1)) return GF_ERR_SHAPE;
+  if (int64_t(dilation) * (ksize - 1) > (int64_t(1) << 30)) return GF_ERR_SHAPE;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(conv_w) || !aligned16(out) ||
+      (conv_b && !aligned16(conv_b)) || !aligned16(workspace))
+    return GF_ERR_ALIGN;
+  const ConvWs wl = conv_ws(B, C, L, ksize);
+  if (!workspace) return GF_ERR_NULL;
+  if (workspace_bytes < wl.total) return GF_ERR_WORKSPACE;
+  const size_t xb = size_t(B) * C * L * 4;
+  const Span ins[] = {{x, xb},
+                      {ln_gamma, size_t(C) * L * 4},
+                      {ln_beta, size_t(C) * L * 4},
+                      {conv_w, size_t(C) * C * ksize * 4},
+                      {conv_b, size_t(C) * 4},
+                      {workspace, wl.total}};
+  st = check_no_alias(Span{out, xb}, ins, 6);
+  if (st != GF_OK) return st;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != GF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  double* part = reinterpret_cast<double*>(ws + wl.part);
+  float2* stats = reinterpret_cast<float2*>(ws + wl.stats);
+  float* a_planes = reinterpret_cast<float*>(ws + wl.a_planes);
+  float* w_planes = reinterpret_cast<float*>(ws + wl.w_planes);
+
+  ln_partial_kernel<<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
+  ln_finalize_kernel<<<unsigned(B), 256, 0, s>>>(part, stats, wl.chunks, eps);
+  ln_apply_gelu_split_kernel<<<dim3(unsigned((L + 31) / 32), unsigned(C / 32), unsigned(B)), dim3(32, 8), 0, s>>>(
+      x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L), int(B));
+  {
+    const int64_t n = C * C * ksize;
+    const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
+    conv_weight_split_kernel<<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), ksize);
+  }
+  if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
+
+  using Cfg = TileCfg<kBNConv>;
+  CUtensorMap ta, tb;
+  const uint64_t da[4] = {uint64_t(C), uint64_t(L), uint64_t(B), 2};
+  const uint32_t ba[4] = {kBK, kBM, 1, 1};
+  const uint64_t db[3] = {uint64_t(ksize) * C, uint64_t(C), 2};
+  const uint32_t bb[3] = {kBK, kBNConv, 1};
+  if ((st = make_tmap_f32(&ta, a_planes, 4, da, ba)) != GF_OK) return st;
+  if ((st = make_tmap_f32(&tb, w_planes, 3, db, bb)) != GF_OK) return st;
+  ConvSrc src;
+  src.C = int(C);
+  src.pad = padding;
+  src.dil = dilation;
+  src.num_jb = int((L + kBM - 1) / kBM);
+  src.num_nb = int((C + kBNConv - 1) / kBNConv);
+  src.num_kb = int(ksize * C / kBK);
+  src.bn = kBNConv;
+  src.nsamples = int(B);
+  const int64_t tiles = int64_t(B) * src.num_jb * src.num_nb;
+  const int grid = int(tiles < dev.sm_count ? tiles : dev.sm_count);
+  EpiConvResidual::Params ep{conv_b, x, out, int(C), int(L)};
+  auto kern = gemm3xtf32_kernel<kBNConv, ConvSrc, EpiConvResidual>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+    return GF_ERR_CUDA;
+  kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, s>>>(ta, tb, src, ep, device_status_word());
+  return cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

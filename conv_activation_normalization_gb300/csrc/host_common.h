@@ -1,0 +1,57 @@
+// Host-side helpers shared by the entry points: argument checks, device
+// properties, TMA descriptor encoding and the device status word.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gf.h"
+
+namespace gf {
+
+// Pointer checks --------------------------------------------------------
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+  const void* p;
+  size_t bytes;
+};
+
+// true when [a, a+na) and [b, b+nb) share a byte.
+inline bool overlaps(Span a, Span b) {
+  if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// GF_ERR_ALIAS when `out` overlaps any of the n inputs.
+gf_status check_no_alias(Span out, const Span* ins, int n);
+
+// Device ------------------------------------------------------------------
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int cc_major, cc_minor;
+  int max_smem_optin;
+};
+// GF_OK and the current device's properties, or GF_ERR_CUDA /
+// GF_ERR_UNSUPPORTED_ARCH (anything but sm_103).
+gf_status current_device(DeviceInfo* info);
+
+// Device address of the library's status word on the current device.
+uint32_t* device_status_word();
+
+gf_status cuda_status(cudaError_t e);
+
+// TMA ---------------------------------------------------------------------
+// Tiled fp32 tensor map with 128-byte swizzle, zero fill out of bounds.
+// dims[0] is the contiguous dimension; strides are derived from a dense
+// layout.  box[0] * 4 must be 128.
+gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                        const uint32_t* box);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace gf

@@ -1,0 +1,56 @@
+// Small device functions and the hi/lo split pre-pass shared by the
+// tensor-core paths.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/gf.h"
+
+namespace gf {
+
+// Swish / SiLU: v * sigmoid(v) = v / (1 + e^-v).  For v < about -88, e^-v is
+// inf and the quotient is the correct limit -0.
+__device__ __forceinline__ float swish(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+
+// Exact GELU v * Phi(v) = 0.5 v (1 + erf(v / sqrt 2)), with CUDA's erff.
+__device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+
+// TF32 split: hi keeps the sign, exponent and top 10 mantissa bits (exactly a
+// TF32 value), lo = v - hi is exact in fp32.
+__device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
+
+static __global__ void split_tf32_kernel(const float4* __restrict__ src, float4* __restrict__ hi,
+                                         float4* __restrict__ lo, size_t n4) {
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x) {
+    const float4 v = __ldcs(src + i);
+    float4 h, l;
+    h.x = tf32_hi(v.x);
+    h.y = tf32_hi(v.y);
+    h.z = tf32_hi(v.z);
+    h.w = tf32_hi(v.w);
+    l.x = v.x - h.x;
+    l.y = v.y - h.y;
+    l.z = v.z - h.z;
+    l.w = v.w - h.w;
+    hi[i] = h;
+    lo[i] = l;
+  }
+}
+
+// n must be a multiple of 4 and all pointers 16-byte aligned.
+static inline gf_status launch_split_tf32(const float* src, float* hi, float* lo, size_t n, int sm_count,
+                                          cudaStream_t stream) {
+  const size_t n4 = n / 4;
+  if (n4 == 0) return GF_OK;
+  const int threads = 256;
+  size_t blocks = (n4 + threads - 1) / threads;
+  const size_t cap = size_t(sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  split_tf32_kernel<<<unsigned(blocks), threads, 0, stream>>>(reinterpret_cast<const float4*>(src),
+                                                             reinterpret_cast<float4*>(hi),
+                                                             reinterpret_cast<float4*>(lo), n4);
+  return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
+}
+
+}  // namespace gf

@@ -1,0 +1,196 @@
+/*
+ * gf.h -- C ABI of libgf: a dense contraction (Linear GEMM, or a convolution
+ * lowered to implicit GEMM) fused with its elementwise and normalisation
+ * epilogue, for one GB300 (sm_103a).
+ *
+ * The operator chains are the four problems of the POPCORNBENCH level-2
+ * transcripts this library follows:
+ *   gf_linear_swish_bias_groupnorm  page "Kimi-K2.6__l2_p37", turn 1
+ *   gf_linear_lse_act               page "Kimi-K2.6__l2_p64", turns 1-2
+ *   gf_ln_gelu_dconv1d_res          page "Kimi-K2.6__l2_p5",  turns 1-2
+ *   gf_convt3d_swish_gn_hswish      page "Kimi-K2.6__l2_p60", turn 1
+ *
+ * Conventions shared by every compute entry point:
+ *   - Every tensor pointer is a DEVICE pointer to fp32, contiguous and
+ *     row-major in PyTorch's layout, 16-byte aligned.  The caller owns every
+ *     buffer; the library never allocates device memory and keeps no pointer
+ *     after the call returns.
+ *   - `workspace` is caller-owned device scratch of at least the size the
+ *     matching *_workspace_size() query returns (256-byte aligned).  It may be
+ *     NULL only when that size is 0.  Its contents on entry do not matter.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued on it and the call returns without synchronising.
+ *   - Arguments are validated before anything is launched; a rejected call
+ *     launches nothing and returns a negative gf_status.  No C++ exception
+ *     crosses this boundary.
+ *   - `out` must not overlap any input or the workspace (GF_ERR_ALIAS).
+ *   - Device-side errors (a bounded wait inside a kernel that ran out) are
+ *     recorded in a device status word; gf_device_status() reads it.
+ *   - mode: GF_MODE_FP32_3XTF32 runs the contraction on the tensor cores as
+ *     three TF32 products (hi*hi + hi*lo + lo*hi of a hi/lo split of both
+ *     operands) with fp32 accumulation and an fp32 epilogue; the result
+ *     matches an fp64 evaluation within 1e-4 abs + 1e-4 rel on the pages'
+ *     workloads.  GF_MODE_BF16 (reserved) returns GF_ERR_MODE.
+ */
+#ifndef GF_H_
+#define GF_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t gf_status;
+
+#define GF_OK                    0
+#define GF_ERR_NULL             -1  /* a required pointer is NULL              */
+#define GF_ERR_SHAPE            -2  /* a size is out of range or unsupported   */
+#define GF_ERR_ALIGN            -3  /* a pointer is not 16-byte aligned        */
+#define GF_ERR_ALIAS            -4  /* out overlaps an input or the workspace  */
+#define GF_ERR_WORKSPACE        -5  /* workspace smaller than the query says   */
+#define GF_ERR_MODE             -6  /* unknown or unsupported mode             */
+#define GF_ERR_CUDA             -7  /* a CUDA runtime/driver call failed       */
+#define GF_ERR_DEVICE_CHECK     -8  /* a kernel recorded a device-side error   */
+#define GF_ERR_UNSUPPORTED_ARCH -9  /* current device is not sm_103            */
+
+#define GF_MODE_FP32_3XTF32 0
+#define GF_MODE_BF16        1
+
+/* Version of this ABI (bumped on any signature change). */
+int32_t gf_abi_version(void);
+
+/* Static, NUL-terminated description of a status code.  Never NULL. */
+const char* gf_status_string(gf_status status);
+
+/* Synchronises the current device, then writes the device status word
+ * accumulated by every kernel of this library since the last call into
+ * *device_bits (0 = no device-side error) and clears it.  Returns GF_OK, or
+ * GF_ERR_DEVICE_CHECK when the word was non-zero, or GF_ERR_CUDA.
+ * device_bits may be NULL. */
+gf_status gf_device_status(int32_t* device_bits);
+
+/* ------------------------------------------------------------------------
+ * Linear alone: out[m,n] = sum_k x[m,k] * W[n,k] + b[n]
+ *
+ * The contraction step shared by the two Linear chains (nn.Linear / addmm,
+ * page Kimi-K2.6__l2_p37 turn 1 and page Kimi-K2.6__l2_p64 turn 1), exposed
+ * so that it can be checked on its own.  x [M,K], W [N,K], b [N] (may be
+ * NULL), out [M,N].  Supported: M >= 1, K >= 4 with K % 4 == 0, N >= 1.
+ * With integer-valued x and W (|v| <= 2^11) and |out| < 2^24 the result is
+ * exact.
+ * ---------------------------------------------------------------------- */
+size_t gf_linear_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode);
+gf_status gf_linear(const float* x, const float* W, const float* b, float* out, int64_t M, int64_t K,
+                    int64_t N, int32_t mode, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Linear -> Swish -> +bias -> GroupNorm            (page Kimi-K2.6__l2_p37)
+ *
+ *   y[m,n]   = sum_k x[m,k] * W[n,k] + b_lin[n]
+ *   t[m,n]   = y * sigmoid(y) + bias[n]
+ *   out[m,n] = (t - mu[m,g]) / sqrt(var[m,g] + eps) * gamma[n] + beta[n]
+ * with g = n / (N/groups), mu and var the mean and biased variance of t over
+ * the N/groups contiguous channels of group g in row m.
+ *
+ *   x [M,K], W [N,K] (nn.Linear layout), b_lin/bias/gamma/beta [N], out [M,N].
+ *   b_lin may be NULL (no linear bias).
+ *   Supported: M >= 1, K >= 4 with K % 4 == 0, N % 64 == 0, N/groups == 64.
+ * ---------------------------------------------------------------------- */
+size_t gf_linear_swish_bias_groupnorm_workspace_size(int64_t M, int64_t K, int64_t N,
+                                                     int32_t groups, int32_t mode);
+gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const float* b_lin,
+                                         const float* bias, const float* gamma, const float* beta,
+                                         float* out, int64_t M, int64_t K, int64_t N,
+                                         int32_t groups, float eps, int32_t mode,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same operator on operands already split for the tensor cores (see
+ * gf_tf32_split): x_planes [2][M][K], W_planes [2][N][K].  It launches the
+ * fused GEMM kernel alone, so a caller can split a weight once and reuse it.
+ * Same shapes, checks and result as gf_linear_swish_bias_groupnorm. */
+gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const float* W_planes,
+                                                const float* b_lin, const float* bias,
+                                                const float* gamma, const float* beta, float* out,
+                                                int64_t M, int64_t K, int64_t N, int32_t groups,
+                                                float eps, void* stream);
+
+/* Splits n fp32 values (n % 4 == 0) into the two planes the 3xTF32
+ * contraction reads: planes[0][i] = src[i] with its 13 low mantissa bits
+ * cleared (a TF32 value) and planes[1][i] = src[i] - planes[0][i] (exact).
+ * planes holds 2*n floats and must not overlap src. */
+gf_status gf_tf32_split(const float* src, float* planes, int64_t n, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Linear -> logsumexp(dim 1) -> LeakyReLU x2 -> GELU(erf) x2
+ *                                                   (page Kimi-K2.6__l2_p64)
+ *
+ *   y[m,n]  = sum_k x[m,k] * W[n,k] + b[n]
+ *   l[m]    = max_n y + ln sum_n exp(y - max_n y)
+ *   a       = lrelu(lrelu(l)),  lrelu(v) = v > 0 ? v : negative_slope * v
+ *   out[m]  = gelu(gelu(a)),    gelu(v) = v * Phi(v)   (exact, erf form)
+ *
+ *   x [M,K], W [N,K], b [N] (may be NULL), out [M,1].
+ *   Supported: M >= 1, K >= 4 with K % 4 == 0, N >= 1.
+ * ---------------------------------------------------------------------- */
+size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode);
+gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, float* out,
+                            int64_t M, int64_t K, int64_t N, float negative_slope, int32_t mode,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * LayerNorm([C,L]) -> GELU(erf) -> dilated Conv1d -> +x
+ *                                                    (page Kimi-K2.6__l2_p5)
+ *
+ *   h[b,c,l]   = (x - mu_b) / sqrt(var_b + eps) * ln_gamma[c,l] + ln_beta[c,l]
+ *                (mu_b, var_b: mean and biased variance of x[b] over all C*L)
+ *   a          = gelu(h), and a = 0 outside 0 <= l < L (the conv's padding)
+ *   out[b,o,j] = conv_b[o] + sum_{c,t} conv_w[o,c,t] * a[b,c, j - padding + t*dilation]
+ *                + x[b,o,j]
+ *
+ *   x, out [B,C,L]; ln_gamma, ln_beta [C,L]; conv_w [C,C,ksize] (nn.Conv1d
+ *   layout, cross-correlation); conv_b [C] (may be NULL).
+ *   Supported: C % 32 == 0, C <= 256, L % 4 == 0, ksize >= 1, dilation >= 1,
+ *   2*padding == dilation*(ksize-1) (length-preserving, as the residual needs).
+ * ---------------------------------------------------------------------- */
+size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize,
+                                             int32_t mode);
+gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const float* ln_beta,
+                                 const float* conv_w, const float* conv_b, float* out,
+                                 int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t dilation,
+                                 int32_t padding, float eps, int32_t mode,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * ConvTranspose3d -> Swish -> GroupNorm -> HardSwish
+ *                                                   (page Kimi-K2.6__l2_p60)
+ *
+ *   y[n,o,od,oh,ow] = b[o] + sum x[n,c,id,ih,iw] * w[c,o,kd,kh,kw]
+ *                     over od = s*id - p + kd (and likewise for h, w)
+ *   s_ = y * sigmoid(y)
+ *   h  = GroupNorm(groups, eps, affine gamma/beta)(s_)   (per sample, per
+ *        group of Cout/groups contiguous channels x all voxels, biased var)
+ *   out = h * clamp(h + 3, 0, 6) / 6
+ *
+ *   x [N,Cin,D,H,W]; w [Cin,Cout,k,k,k] (nn.ConvTranspose3d layout);
+ *   b [Cout] (may be NULL); gamma, beta [Cout];
+ *   out [N,Cout,(D-1)s-2p+k, (H-1)s-2p+k, (W-1)s-2p+k].
+ *   Supported: k == 3, stride == 2, pad == 1, Cin <= 8, Cout == 16,
+ *   groups == 4; output_padding is 0.
+ * ---------------------------------------------------------------------- */
+size_t gf_convt3d_swish_gn_hswish_workspace_size(int64_t N, int64_t Cin, int64_t Cout,
+                                                 int64_t D, int64_t H, int64_t W, int32_t k,
+                                                 int32_t stride, int32_t pad, int32_t groups);
+gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float* b,
+                                     const float* gamma, const float* beta, float* out,
+                                     int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H,
+                                     int64_t W, int32_t k, int32_t stride, int32_t pad,
+                                     int32_t groups, float eps,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GF_H_ */

@@ -1,0 +1,144 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments with the documented status codes
+before touching the device (all pointers here are fake and never
+dereferenced)."""
+import ctypes
+
+import pytest
+
+from conv_activation_normalization_gb300 import binding
+
+
+@pytest.fixture(scope="module")
+def L():
+    from conv_activation_normalization_gb300 import build
+    build.build()
+    return binding.lib()
+
+
+GF_OK, GF_ERR_NULL, GF_ERR_SHAPE, GF_ERR_ALIGN, GF_ERR_ALIAS, GF_ERR_WORKSPACE, GF_ERR_MODE = 0, -1, -2, -3, -4, -5, -6
+
+# Fake, 256-byte aligned, far-apart "device addresses" (never dereferenced:
+# every call below fails validation first).
+BASE = 0x7f0000000000
+P = [BASE + i * (1 << 36) for i in range(16)]
+
+
+def test_exports_every_header_symbol(L):
+    names = binding.header_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in binding._SIGS, f"binding lacks a signature for {n}"
+    assert L.gf_abi_version() == 1
+
+
+def test_status_strings(L):
+    for code in range(-9, 1):
+        s = L.gf_status_string(code)
+        assert s and len(s) > 1
+    assert L.gf_status_string(12345) == b"unknown status"
+
+
+def _lgn(L, x=P[0], W=P[1], bl=P[2], bias=P[3], g=P[4], b=P[5], out=P[6], M=256, K=1024, N=4096, groups=64,
+         eps=1e-5, mode=0, ws=P[7], wsb=None):
+    if wsb is None:
+        wsb = L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, groups, mode)
+    return L.gf_linear_swish_bias_groupnorm(x, W, bl, bias, g, b, out, M, K, N, groups, eps, mode, ws, wsb, None)
+
+
+def test_linear_gn_validation(L):
+    assert _lgn(L, x=None) == GF_ERR_NULL
+    assert _lgn(L, out=None) == GF_ERR_NULL
+    assert _lgn(L, mode=1) == GF_ERR_MODE
+    assert _lgn(L, mode=7) == GF_ERR_MODE
+    assert _lgn(L, groups=32) == GF_ERR_SHAPE      # group width 128 is not supported
+    assert _lgn(L, groups=0) == GF_ERR_SHAPE
+    assert _lgn(L, K=1022) == GF_ERR_SHAPE         # K % 4
+    assert _lgn(L, M=0) == GF_ERR_SHAPE
+    assert _lgn(L, eps=float("nan")) == GF_ERR_SHAPE
+    assert _lgn(L, eps=-1.0) == GF_ERR_SHAPE
+    assert _lgn(L, x=P[0] + 4) == GF_ERR_ALIGN
+    assert _lgn(L, out=P[6] + 8) == GF_ERR_ALIGN
+    assert _lgn(L, wsb=100) == GF_ERR_WORKSPACE
+    assert _lgn(L, ws=None) == GF_ERR_NULL
+    assert _lgn(L, out=P[0]) == GF_ERR_ALIAS        # out == x
+    assert _lgn(L, out=P[7] + 1024) == GF_ERR_ALIAS  # out inside the workspace
+    assert _lgn(L, out=P[1] - 256) == GF_ERR_ALIAS  # out runs into W
+
+
+def test_workspace_sizes(L):
+    M, K, N = 32768, 1024, 4096
+    ws = L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 0)
+    assert ws == 2 * 4 * (M * K + N * K)            # hi/lo planes of x and W
+    assert L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 1) == 0
+    assert L.gf_linear_workspace_size(M, K, N, 0) == ws
+    M, K, N = 1024, 8192, 8192
+    assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 2 * 4 * (M * K + N * K) + M * (N // 256) * 8
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0) > 2 * 4 * 32 * 256 * 4096
+    assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 2, 1, 4) > 0
+    assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 1, 1, 4) == 0
+
+
+def test_lse_validation(L):
+    def call(**kw):
+        a = dict(x=P[0], W=P[1], b=P[2], out=P[3], M=1024, K=8192, N=8192, slope=0.01, mode=0, ws=P[4], wsb=None)
+        a.update(kw)
+        if a["wsb"] is None:
+            a["wsb"] = L.gf_linear_lse_act_workspace_size(a["M"], a["K"], a["N"], a["mode"])
+        return L.gf_linear_lse_act(a["x"], a["W"], a["b"], a["out"], a["M"], a["K"], a["N"], a["slope"], a["mode"],
+                                   a["ws"], a["wsb"], None)
+    assert call(W=None) == GF_ERR_NULL
+    assert call(K=6) == GF_ERR_SHAPE
+    assert call(N=0) == GF_ERR_SHAPE
+    assert call(slope=float("inf")) == GF_ERR_SHAPE
+    assert call(b=P[2] + 4) == GF_ERR_ALIGN
+    assert call(wsb=1) == GF_ERR_WORKSPACE
+    assert call(out=P[2] + 16) == GF_ERR_ALIAS
+
+
+def test_dconv1d_validation(L):
+    def call(**kw):
+        a = dict(x=P[0], g=P[1], b=P[2], w=P[3], cb=P[4], out=P[5], B=32, C=256, L=4096, k=3, d=4, p=4, eps=1e-5,
+                 mode=0, ws=P[6], wsb=None)
+        a.update(kw)
+        if a["wsb"] is None:
+            a["wsb"] = L.gf_ln_gelu_dconv1d_res_workspace_size(a["B"], a["C"], a["L"], a["k"], a["mode"])
+        return L.gf_ln_gelu_dconv1d_res(a["x"], a["g"], a["b"], a["w"], a["cb"], a["out"], a["B"], a["C"], a["L"],
+                                        a["k"], a["d"], a["p"], a["eps"], a["mode"], a["ws"], a["wsb"], None)
+    assert call(g=None) == GF_ERR_NULL
+    assert call(p=3) == GF_ERR_SHAPE               # not length-preserving
+    assert call(C=48) == GF_ERR_SHAPE              # C % 32
+    assert call(C=512) == GF_ERR_SHAPE
+    assert call(L=4094) == GF_ERR_SHAPE            # L % 4
+    assert call(mode=1) == GF_ERR_MODE
+    assert call(w=P[3] + 4) == GF_ERR_ALIGN
+    assert call(wsb=5) == GF_ERR_WORKSPACE
+    assert call(out=P[0]) == GF_ERR_ALIAS          # in-place residual is rejected
+
+
+def test_convt3d_validation(L):
+    def call(**kw):
+        a = dict(x=P[0], w=P[1], b=P[2], g=P[3], be=P[4], out=P[5], N=128, Cin=3, Cout=16, D=16, H=32, W=32, k=3, s=2,
+                 p=1, G=4, eps=1e-5, ws=P[6], wsb=None)
+        a.update(kw)
+        if a["wsb"] is None:
+            a["wsb"] = L.gf_convt3d_swish_gn_hswish_workspace_size(a["N"], a["Cin"], a["Cout"], a["D"], a["H"], a["W"],
+                                                                   a["k"], a["s"], a["p"], a["G"])
+        return L.gf_convt3d_swish_gn_hswish(a["x"], a["w"], a["b"], a["g"], a["be"], a["out"], a["N"], a["Cin"],
+                                            a["Cout"], a["D"], a["H"], a["W"], a["k"], a["s"], a["p"], a["G"], a["eps"],
+                                            a["ws"], a["wsb"], None)
+    assert call(x=None) == GF_ERR_NULL
+    assert call(G=2) == GF_ERR_SHAPE
+    assert call(Cin=9) == GF_ERR_SHAPE
+    assert call(k=5) == GF_ERR_SHAPE
+    assert call(be=None) == GF_ERR_NULL
+    assert call(g=P[3] + 4) == GF_ERR_ALIGN
+    assert call(wsb=8) == GF_ERR_WORKSPACE
+    assert call(out=P[6]) == GF_ERR_ALIAS
+
+
+def test_device_status_signature(L):
+    # the argument is optional; the call itself needs a device, so only the
+    # ctypes signature is checked here
+    assert L.gf_device_status.argtypes == [ctypes.POINTER(ctypes.c_int32)]

@@ -1,0 +1,243 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Bar: |gpu - oracle| <= 1e-4 + 1e-4 |oracle| element by element (the fp32-mode
+tolerance), on seeded synthetic inputs: small shapes that span several tiles
+and a ragged tail, degenerate cases, and the full-size workloads on samples
+the oracle can compute one by one (rows, or whole samples for the
+per-sample normalisations).  The contraction alone is checked bit for bit on
+integer-valued inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conv_activation_normalization_gb300 import binding as gf
+from conv_activation_normalization_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-4
+RTOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from conv_activation_normalization_gb300 import build
+    build.build()
+    gf.lib()
+    yield
+    assert gf.gf_device_status() == 0
+
+
+def T(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    err = np.abs(got - ref)
+    lim = ATOL + RTOL * np.abs(ref)
+    bad = ~(err <= lim)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; max err {np.nanmax(err):.3g}; "
+                             f"first {idx.tolist()}")
+
+
+# ------------------------------------------------------------ contraction
+@pytest.mark.parametrize("M,K,N", [(128, 32, 256), (300, 100, 520), (1, 4, 1), (257, 1024, 4096)])
+def test_linear_integer_exact(M, K, N):
+    r = np.random.default_rng(M * 7 + K)
+    x = r.integers(-15, 16, size=(M, K)).astype(np.float32)
+    W = r.integers(-15, 16, size=(N, K)).astype(np.float32)
+    b = r.integers(-50, 51, size=N).astype(np.float32)
+    got = gf.gf_linear(T(x), T(W), T(b)).cpu().numpy()
+    exact = x.astype(np.int64) @ W.astype(np.int64).T + b.astype(np.int64)
+    assert np.array_equal(got.astype(np.int64), exact)
+    assert np.array_equal(got, exact.astype(np.float32))
+
+
+def test_linear_3xtf32_accuracy():
+    # Values with all 24 mantissa bits in use.  Relative to the scale
+    # sqrt(sum_k (x w)^2), a single TF32 product (emulated exactly on the CPU
+    # for these inputs) is off by up to 3.5e-3 (mean 5.8e-4); the hi/lo split
+    # with exact accumulation by up to 1.6e-6.  The tensor core accumulates in
+    # fp32 with its own rounding over K/8 * 3 chained MMA steps, which adds up
+    # to ~2^-17 |y| (4.5e-5 of the scale here); the bounds sit well below
+    # what a single TF32 product gives.
+    r = np.random.default_rng(5)
+    M, K, N = 256, 1024, 512
+    x = r.standard_normal((M, K)).astype(np.float32)
+    W = r.uniform(-1, 1, (N, K)).astype(np.float32)
+    got = gf.gf_linear(T(x), T(W)).cpu().numpy().astype(np.float64)
+    ref = oracle.linear(x, W)
+    scale = np.sqrt((x.astype(np.float64) ** 2) @ (W.astype(np.float64) ** 2).T)
+    err = np.abs(got - ref)
+    assert np.max(err / scale) < 1e-4
+    assert np.mean(err / scale) < 2e-5
+
+
+# ------------------------------------------------ Linear->Swish->bias->GN
+def _lgn_case(M, K, N, groups, seed):
+    s = synth.LinearGNShape(M=M, K=K, N=N, groups=groups)
+    d = synth.linear_gn_inputs(s, seed)
+    return s, d
+
+
+def _lgn_run(s, d, rows=None):
+    out = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), T(d["b_lin"]), T(d["bias"]), T(d["gamma"]),
+                                            T(d["beta"]), s.groups, s.eps).cpu().numpy()
+    xr = d["x"] if rows is None else d["x"][rows]
+    ref = oracle.linear_swish_bias_groupnorm(xr, d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"], s.groups,
+                                             s.eps)
+    return (out if rows is None else out[rows]), ref
+
+
+def test_linear_gn_workload_m256():
+    s, seed = synth.WORKLOADS["linear_gn_m256"]
+    got, ref = _lgn_run(s, synth.linear_gn_inputs(s, seed))
+    assert_close(got, ref, "linear_gn M=256")
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4, 64), (130, 36, 320), (383, 260, 4096), (129, 1024, 192)])
+def test_linear_gn_ragged(M, K, N):
+    s, d = _lgn_case(M, K, N, N // 64, 100 + M)
+    got, ref = _lgn_run(s, d)
+    assert_close(got, ref, f"linear_gn {M}x{K}x{N}")
+
+
+def test_linear_gn_no_linear_bias_and_constant_group():
+    s, d = _lgn_case(64, 64, 256, 4, 7)
+    d["W"][:64] = 0.0      # group 0: t = swish(0) + bias = bias, varies per channel
+    d["bias"][64:128] = 0.5
+    d["W"][64:128] = 0.0   # group 1: constant t -> output beta
+    out = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), None, T(d["bias"]), T(d["gamma"]), T(d["beta"]),
+                                            s.groups, s.eps).cpu().numpy()
+    ref = oracle.linear_swish_bias_groupnorm(d["x"], d["W"], None, d["bias"], d["gamma"], d["beta"], s.groups, s.eps)
+    assert_close(out, ref, "no b_lin")
+    np.testing.assert_array_equal(out[:, 64:128], np.broadcast_to(d["beta"][64:128], (64, 64)))
+
+
+def test_linear_gn_workload_m32768_sampled():
+    s, seed = synth.WORKLOADS["linear_gn_m32768"]
+    d = synth.linear_gn_inputs(s, seed)
+    r = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(0, 130), r.integers(0, s.M, 600), np.arange(s.M - 130, s.M)]))
+    got, ref = _lgn_run(s, d, rows)
+    assert_close(got, ref, "linear_gn M=32768 (sampled rows)")
+
+
+def test_linear_gn_deterministic():
+    s, d = _lgn_case(512, 256, 1024, 16, 3)
+    a = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), T(d["b_lin"]), T(d["bias"]), T(d["gamma"]),
+                                          T(d["beta"]), s.groups).cpu().numpy()
+    b = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), T(d["b_lin"]), T(d["bias"]), T(d["gamma"]),
+                                          T(d["beta"]), s.groups).cpu().numpy()
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------- Linear->LSE->act chain
+def _lse_run(s, d, rows=None):
+    out = gf.gf_linear_lse_act(T(d["x"]), T(d["W"]), T(d["b"]), s.negative_slope).cpu().numpy()
+    xr = d["x"] if rows is None else d["x"][rows]
+    ref = oracle.linear_lse_act(xr, d["W"], d["b"], s.negative_slope)
+    return (out if rows is None else out[rows]), ref
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 4, 1), (200, 512, 1000), (129, 260, 8192), (384, 2048, 300)])
+def test_linear_lse_small(M, K, N):
+    s = synth.LinearLSEShape(M=M, K=K, N=N)
+    got, ref = _lse_run(s, synth.linear_lse_inputs(s, 200 + M))
+    assert_close(got, ref, f"lse {M}x{K}x{N}")
+
+
+def test_linear_lse_negative_branch():
+    s = synth.LinearLSEShape(M=64, K=256, N=8192)
+    d = synth.linear_lse_inputs(s, 11, bias_shift=-30.0)
+    got, ref = _lse_run(s, d)
+    assert np.all(ref < 0)
+    assert_close(got, ref, "lse negative branch")
+
+
+def test_linear_lse_workload_sampled():
+    s, seed = synth.WORKLOADS["linear_lse_m1024"]
+    d = synth.linear_lse_inputs(s, seed)
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(500, 530), np.arange(s.M - 64, s.M)]))
+    got, ref = _lse_run(s, d, rows)
+    assert_close(got, ref, "lse full workload (sampled rows)")
+
+
+# --------------------------------------------- LN->GELU->dilated conv->+x
+def _dc_run(s, d, samples=None):
+    out = gf.gf_ln_gelu_dconv1d_res(T(d["x"]), T(d["ln_gamma"]), T(d["ln_beta"]), T(d["conv_w"]), T(d["conv_b"]),
+                                    s.dilation, s.padding, s.eps).cpu().numpy()
+    xs = d["x"] if samples is None else d["x"][samples]
+    ref = oracle.ln_gelu_dconv1d_res(xs, d["ln_gamma"], d["ln_beta"], d["conv_w"], d["conv_b"], s.dilation, s.padding,
+                                     s.eps)
+    return (out if samples is None else out[samples]), ref
+
+
+@pytest.mark.parametrize("B,C,L,dil", [(2, 64, 300, 4), (1, 32, 4, 4), (3, 256, 520, 2), (2, 96, 1024, 1)])
+def test_dconv1d_small(B, C, L, dil):
+    s = synth.DConv1dShape(B=B, C=C, L=L, dilation=dil, padding=dil)
+    got, ref = _dc_run(s, synth.dconv1d_inputs(s, 300 + L, affine="perturbed"))
+    assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
+
+
+def test_dconv1d_kernel_size_5():
+    s = synth.DConv1dShape(B=2, C=64, L=256, ksize=5, dilation=3, padding=6)
+    got, ref = _dc_run(s, synth.dconv1d_inputs(s, 5, affine="perturbed"))
+    assert_close(got, ref, "dconv1d k5")
+
+
+def test_dconv1d_tap_offsets_delta_weights():
+    # one nonzero weight per output channel on one tap: shows the tap offset,
+    # the zero padding at both ends and the residual.
+    s = synth.DConv1dShape(B=1, C=32, L=256)
+    d = synth.dconv1d_inputs(s, 9, affine="perturbed")
+    w = np.zeros_like(d["conv_w"])
+    for co in range(s.C):
+        w[co, (co * 7) % s.C, co % 3] = 1.0
+    d["conv_w"] = w
+    got, ref = _dc_run(s, d)
+    assert_close(got, ref, "dconv1d delta taps")
+
+
+def test_dconv1d_workload_sampled():
+    s, seed = synth.WORKLOADS["ln_dconv1d_b32"]
+    d = synth.dconv1d_inputs(s, seed)
+    got, ref = _dc_run(s, d, samples=np.array([0, 17, 31]))
+    assert_close(got, ref, "dconv1d full workload (samples 0, 17, 31)")
+
+
+# -------------------------------------- ConvT3d->Swish->GN->HardSwish
+def _ct_run(s, d, samples=None):
+    out = gf.gf_convt3d_swish_gn_hswish(T(d["x"]), T(d["w"]), T(d["b"]), T(d["gamma"]), T(d["beta"]), s.stride,
+                                        s.pad, s.groups, s.eps)
+    out = out.cpu().numpy()
+    xs = d["x"] if samples is None else d["x"][samples]
+    ref = oracle.convt3d_swish_gn_hswish(xs, d["w"], d["b"], d["gamma"], d["beta"], s.stride, s.pad, s.groups, s.eps)
+    return (out if samples is None else out[samples]), ref
+
+
+@pytest.mark.parametrize("N,Cin,D,H,W", [(2, 3, 5, 7, 9), (1, 1, 1, 1, 1), (3, 3, 4, 33, 40), (1, 8, 3, 8, 64)])
+def test_convt3d_small(N, Cin, D, H, W):
+    s = synth.ConvT3dShape(N=N, Cin=Cin, D=D, H=H, W=W)
+    got, ref = _ct_run(s, synth.convt3d_inputs(s, 400 + W))
+    assert_close(got, ref, f"convt3d {N}x{Cin}x{D}x{H}x{W}")
+
+
+def test_convt3d_uniform_inputs():
+    s = synth.ConvT3dShape(N=2, D=6, H=12, W=12)
+    got, ref = _ct_run(s, synth.convt3d_inputs(s, 77, x_dist="uniform01"))
+    assert_close(got, ref, "convt3d U[0,1) inputs")
+
+
+def test_convt3d_workload_sampled():
+    s, seed = synth.WORKLOADS["convt3d_n128"]
+    d = synth.convt3d_inputs(s, seed)
+    got, ref = _ct_run(s, d, samples=np.array([0, 63, 127]))
+    assert got.shape == (3, 16, 31, 63, 63)
+    assert_close(got, ref, "convt3d full workload (samples 0, 63, 127)")
