@@ -1,17 +1,24 @@
-"""Benchmark of the fused Linear -> Swish -> +bias -> GroupNorm operator at
-M = 32768 (x[32768, 1024], W[4096, 1024], 64 groups of 64 channels) on GB300.
+"""Benchmark of the fused contraction + activation/normalisation operators on
+one GB300.
 
-One step = one pass of the whole operator over the batch: the TF32 hi/lo
-split of x and W and the fused tcgen05 GEMM + Swish + bias + GroupNorm
-kernel.  Inputs are seeded synthetic data resident in HBM before timing;
-x (134 MB) and out (537 MB) per step are larger than the 129 MB L2.
+Default workload (the headline): Linear -> Swish -> +bias -> GroupNorm at
+M = 32768 (x[32768, 1024], W[4096, 1024], 64 groups of 64 channels).  The
+other workloads of the same method (--workload) are measured the same way.
+
+One step = one call of the public operator over the whole batch (every
+kernel of the path: operand split, fused GEMM/epilogue, statistics passes).
+Inputs are seeded synthetic data already resident in HBM when timing starts;
+each workload's per-step traffic exceeds the 129 MB L2 or L2 is flushed (see
+the "l2" key of config).  The dominant kernel is timed by the library's own
+CUDA-event recorder (gf_profile_begin/end) on the launching stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME | --all]
 
 N > 1 runs under torch.distributed.run, one rank per GPU; every rank runs the
-full workload on its own GPU (weak scaling, no data-path collective) and rank 0
-prints one JSON line.  --impl reference times the fp64 CPU oracle on a
-bounded sample of the same workload on the host cores.
+full workload on its own GPU (replicas: weak scaling, no data-path
+collective) and rank 0 prints one JSON line.  --impl reference times the fp64
+CPU oracle on a bounded sample of the same workload on the host cores.
 """
 from __future__ import annotations
 
@@ -27,58 +34,41 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "fused Linear->Swish->bias->GroupNorm TFLOP/s at M=32768 and % of roofline, 1 GB300"
-UNIT = "TFLOP/s"
-M, K, N, GROUPS, EPS = 32768, 1024, 4096, 64, 1e-5
-FLOP = 2.0 * M * N * K  # algorithmic: the contraction (274.878 GFLOP); the epilogue is not counted
-WORKLOAD = "linear_swish_bias_groupnorm x[32768,1024] W[4096,1024] G=64"
 TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates of the part
-FALLBACK_BF16_TFLOPS = 1900.0
-
-
-def _config(extra=None):
-    c = {"workload": WORKLOAD, "M": M, "K": K, "N": N, "groups": GROUPS, "eps": EPS,
-         "mode": "fp32 (3xTF32 tensor-core contraction, fp32 epilogue)",
-         "l2": "inputs larger than L2 (x 134 MB + out 537 MB per step vs 129 MB L2); no flush",
-         "inputs": "seeded synthetic: x~N(0,1), W,b_lin~U(+-1/32), bias~N(0,1), gamma~U(0.5,1.5), beta~N(0,0.1)"}
-    if extra:
-        c.update(extra)
-    return c
+FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+SUSTAINED_AFTER_S = 2.0      # timed regions longer than this use the sustained tensor peak
 
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["bf16_tflops"]), "measured"
-    return FALLBACK_BF16_TFLOPS, "fallback"
+        return {k: float(d.get(k, FALLBACK[k])) for k in FALLBACK}, "measured"
+    return dict(FALLBACK), "fallback"
 
 
 def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
-def _kernel_traffic():
-    """DRAM traffic of the GEMM kernel from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "gemm_linear_gn_traffic.json")
-    if not os.path.exists(p):
-        return None
-    d = json.load(open(p))
-    if d.get("source_sha") != kernel_source_sha():
-        return None
-    return d.get("traffic_bytes_per_launch")
-
-
-def kernel_source_sha():
+def kernel_source_sha(files):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "conv_activation_normalization_gb300", "csrc")
-    for f in ("gemm_tc.cuh", "ptx.cuh", "linear_ops.cu", "kernels_common.cuh"):
+    for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def _kernel_traffic(wl):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was captured on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(wl.name)
+    if not d or d.get("source_sha") != kernel_source_sha(wl.sources):
+        return None
+    return d.get("traffic_bytes_per_launch")
 
 
 class ClockSampler:
@@ -88,20 +78,19 @@ class ClockSampler:
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
-        self.index = index
-        self.p = None
+        self.index, self.p, self.rows = index, None, []
 
     def __enter__(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
         except Exception:
             self.p = None
         return self
 
     def __exit__(self, *a):
-        self.rows = []
         if self.p is None:
             return
         self.p.terminate()
@@ -116,202 +105,466 @@ class ClockSampler:
                 self.rows.append(f)
 
     def summary(self):
-        if not getattr(self, "rows", None):
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
-        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        # samples taken while the GPU is busy: the upper half by power draw
+        busy = sorted(zip(pw, sm))[len(sm) // 2:] if len(pw) == len(sm) else list(zip(pw, sm))
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.rows)}
+        return {"sm_mhz": statistics.median(s for _, s in busy), "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows), "power_w_max": max(pw) if pw else None}
 
 
-# --------------------------------------------------------------- ours
-def run_ours(args):
+# ---------------------------------------------------------------- workloads
+class Workload:
+    name = ""
+    metric = ""
+    unit = "TFLOP/s"
+    bound = "tensor"
+    sources = ("gemm_tc.cuh", "ptx.cuh", "kernels_common.cuh")
+    kernel = ""
+    l2 = ""
+
+    def work_per_step(self):
+        """Algorithmic FLOP (TFLOP/s units) or bytes (GB/s units) of one step."""
+        raise NotImplementedError
+
+    def kernel_work(self):
+        """Algorithmic FLOP or bytes of one launch of the dominant kernel."""
+        return self.work_per_step()
+
+    def scale(self):
+        return 1e12 if self.unit == "TFLOP/s" else 1e9
+
+
+class LinearGN(Workload):
+    sources = Workload.sources + ("linear_ops.cu",)
+    kernel = "gemm3xtf32_kernel<LinearSrc, EpiSwishBiasGN>"
+
+    def __init__(self, M, name):
+        from conv_activation_normalization_gb300 import synth
+        self.name = name
+        self.shape = synth.LinearGNShape(M=M)
+        self.seed = synth.WORKLOADS[name][1]
+        s = self.shape
+        self.metric = ("fused Linear->Swish->bias->GroupNorm TFLOP/s at M=32768 and % of roofline, 1 GB300"
+                       if M == 32768 else f"fused Linear->Swish->bias->GroupNorm TFLOP/s at M={M}")
+        self.config = {"workload": f"linear_swish_bias_groupnorm x[{s.M},{s.K}] W[{s.N},{s.K}] groups={s.groups}",
+                       "M": s.M, "K": s.K, "N": s.N, "groups": s.groups, "eps": s.eps}
+        self.l2 = ("inputs larger than L2 (x 134 MB + out 537 MB per step vs 129 MB L2); no flush" if M >= 8192
+                   else "L2 flushed between steps (a 256 MB buffer is written)")
+
+    def work_per_step(self):
+        s = self.shape
+        return 2.0 * s.M * s.N * s.K
+
+    def inputs(self):
+        from conv_activation_normalization_gb300 import synth
+        return synth.linear_gn_inputs(self.shape, self.seed)
+
+    def setup(self, d, dev):
+        import torch
+        s = self.shape
+        t = {k: torch.from_numpy(v).to(dev) for k, v in d.items()}
+        t["out"] = torch.empty((s.M, s.N), dtype=torch.float32, device=dev)
+        return t
+
+    def step(self, gf, t, x=None):
+        s = self.shape
+        gf.gf_linear_swish_bias_groupnorm(t["x"] if x is None else x, t["W"], t["b_lin"], t["bias"], t["gamma"],
+                                          t["beta"], s.groups, s.eps, out=t["out"])
+
+    def oracle_chunk(self, d, i, chunk):
+        import oracle
+        s = self.shape
+        sl = slice(i * chunk, min(s.M, (i + 1) * chunk))
+        oracle.linear_swish_bias_groupnorm(d["x"][sl], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"],
+                                           s.groups, s.eps)
+        return (sl.stop - sl.start) / s.M
+
+    chunk = 2048
+
+
+class LinearLSE(Workload):
+    name = "linear_lse_m1024"
+    metric = "fused Linear->logsumexp->LeakyReLU x2->GELU x2 TFLOP/s at x[1024,8192], W[8192,8192]"
+    sources = Workload.sources + ("linear_ops.cu",)
+    kernel = "gemm3xtf32_kernel<LinearSrc, EpiLSEPartial>"
+    l2 = "inputs larger than L2 (W 268 MB per step vs 129 MB L2); no flush"
+    chunk = 64
+
+    def __init__(self):
+        from conv_activation_normalization_gb300 import synth
+        self.shape, self.seed = synth.WORKLOADS[self.name]
+        s = self.shape
+        self.config = {"workload": f"linear_lse_act x[{s.M},{s.K}] W[{s.N},{s.K}]", "M": s.M, "K": s.K, "N": s.N}
+
+    def work_per_step(self):
+        s = self.shape
+        return 2.0 * s.M * s.N * s.K
+
+    def inputs(self):
+        from conv_activation_normalization_gb300 import synth
+        return synth.linear_lse_inputs(self.shape, self.seed)
+
+    def setup(self, d, dev):
+        import torch
+        t = {k: torch.from_numpy(v).to(dev) for k, v in d.items()}
+        t["out"] = torch.empty((self.shape.M, 1), dtype=torch.float32, device=dev)
+        return t
+
+    def step(self, gf, t, x=None):
+        gf.gf_linear_lse_act(t["x"] if x is None else x, t["W"], t["b"], self.shape.negative_slope, out=t["out"])
+
+    def oracle_chunk(self, d, i, chunk):
+        import oracle
+        s = self.shape
+        sl = slice(i * chunk, min(s.M, (i + 1) * chunk))
+        oracle.linear_lse_act(d["x"][sl], d["W"], d["b"], s.negative_slope)
+        return (sl.stop - sl.start) / s.M
+
+
+class DConv1d(Workload):
+    name = "ln_dconv1d_b32"
+    metric = "fused LayerNorm->GELU->dilated Conv1d->residual TFLOP/s at x[32,256,4096]"
+    sources = Workload.sources + ("dconv1d.cu",)
+    kernel = "gemm3xtf32_kernel<ConvSrc, EpiConvResidual>"
+    l2 = "inputs larger than L2 (x 134 MB read twice + A planes 268 MB + out 134 MB per step); no flush"
+    chunk = 1
+
+    def __init__(self):
+        from conv_activation_normalization_gb300 import synth
+        self.shape, self.seed = synth.WORKLOADS[self.name]
+        s = self.shape
+        self.config = {"workload": f"ln_gelu_dconv1d_res x[{s.B},{s.C},{s.L}] k={s.ksize} dilation={s.dilation}",
+                       "B": s.B, "C": s.C, "L": s.L, "ksize": s.ksize, "dilation": s.dilation,
+                       "padding": s.padding, "ln_affine": "gamma=1, beta=0 (PyTorch initial values)"}
+
+    def work_per_step(self):
+        s = self.shape
+        return 2.0 * s.B * s.L * s.C * s.C * s.ksize
+
+    def inputs(self):
+        from conv_activation_normalization_gb300 import synth
+        return synth.dconv1d_inputs(self.shape, self.seed)
+
+    def setup(self, d, dev):
+        import torch
+        t = {k: torch.from_numpy(v).to(dev) for k, v in d.items()}
+        t["out"] = torch.empty_like(t["x"])
+        return t
+
+    def step(self, gf, t, x=None):
+        s = self.shape
+        gf.gf_ln_gelu_dconv1d_res(t["x"] if x is None else x, t["ln_gamma"], t["ln_beta"], t["conv_w"], t["conv_b"],
+                                  s.dilation, s.padding, s.eps, out=t["out"])
+
+    def oracle_chunk(self, d, i, chunk):
+        import oracle
+        s = self.shape
+        sl = slice(i * chunk, min(s.B, (i + 1) * chunk))
+        oracle.ln_gelu_dconv1d_res(d["x"][sl], d["ln_gamma"], d["ln_beta"], d["conv_w"], d["conv_b"], s.dilation,
+                                   s.padding, s.eps)
+        return (sl.stop - sl.start) / s.B
+
+
+class ConvT3d(Workload):
+    name = "convt3d_n128"
+    metric = "fused ConvTranspose3d->Swish->GroupNorm->HardSwish GB/s at x[128,3,16,32,32]"
+    unit = "GB/s"
+    bound = "hbm"
+    sources = ("convt3d.cu", "kernels_common.cuh")
+    kernel = "convt3d_apply_kernel<3> (pass 2: recompute, normalise, store)"
+    l2 = "inputs larger than L2 (out 1008 MB per step vs 129 MB L2); no flush"
+    chunk = 1
+
+    def __init__(self):
+        from conv_activation_normalization_gb300 import synth
+        self.shape, self.seed = synth.WORKLOADS[self.name]
+        s = self.shape
+        self.out_shape = (s.N, s.Cout, 2 * s.D - 1, 2 * s.H - 1, 2 * s.W - 1)
+        self.config = {"workload": f"convt3d_swish_gn_hswish x[{s.N},{s.Cin},{s.D},{s.H},{s.W}] -> "
+                                   f"out{list(self.out_shape)}", "k": s.k, "stride": s.stride, "pad": s.pad,
+                       "groups": s.groups,
+                       "bytes_per_step": "x read twice (2 x 25.2 MB) + out written once (1007.9 MB)"}
+
+    def _xbytes(self):
+        s = self.shape
+        return 4.0 * s.N * s.Cin * s.D * s.H * s.W
+
+    def _obytes(self):
+        n = 1
+        for v in self.out_shape:
+            n *= v
+        return 4.0 * n
+
+    def work_per_step(self):
+        return 2 * self._xbytes() + self._obytes()
+
+    def kernel_work(self):
+        return self._xbytes() + self._obytes()
+
+    def inputs(self):
+        from conv_activation_normalization_gb300 import synth
+        return synth.convt3d_inputs(self.shape, self.seed)
+
+    def setup(self, d, dev):
+        import torch
+        t = {k: torch.from_numpy(v).to(dev) for k, v in d.items()}
+        t["out"] = torch.empty(self.out_shape, dtype=torch.float32, device=dev)
+        return t
+
+    def step(self, gf, t, x=None):
+        s = self.shape
+        gf.gf_convt3d_swish_gn_hswish(t["x"] if x is None else x, t["w"], t["b"], t["gamma"], t["beta"], s.stride,
+                                      s.pad, s.groups, s.eps, out=t["out"])
+
+    def oracle_chunk(self, d, i, chunk):
+        import oracle
+        s = self.shape
+        sl = slice(i * chunk, min(s.N, (i + 1) * chunk))
+        oracle.convt3d_swish_gn_hswish(d["x"][sl], d["w"], d["b"], d["gamma"], d["beta"], s.stride, s.pad, s.groups,
+                                       s.eps)
+        return (sl.stop - sl.start) / s.N
+
+
+def make_workload(name, rows=None, samples=None):
+    """rows / samples shrink a workload for profiling captures only."""
+    import dataclasses
+    if name == "linear_gn_m32768":
+        wl = LinearGN(32768, name)
+        if rows:
+            wl.shape = dataclasses.replace(wl.shape, M=rows)
+            wl.config.update(M=rows, workload=wl.config["workload"] + f" (profiling case: M={rows})")
+        return wl
+    if name == "linear_gn_m256":
+        return LinearGN(256, name)
+    if name == "linear_lse_m1024":
+        return LinearLSE()
+    if name == "ln_dconv1d_b32":
+        wl = DConv1d()
+        if samples:
+            wl.shape = dataclasses.replace(wl.shape, B=samples)
+            wl.config.update(B=samples, workload=wl.config["workload"] + f" (profiling case: B={samples})")
+        return wl
+    if name == "convt3d_n128":
+        wl = ConvT3d()
+        if samples:
+            s = wl.shape = dataclasses.replace(wl.shape, N=samples)
+            wl.out_shape = (s.N,) + wl.out_shape[1:]
+            wl.config.update(workload=wl.config["workload"] + f" (profiling case: N={samples})")
+        return wl
+    raise SystemExit(f"unknown workload {name}")
+
+
+ALL = ["linear_gn_m32768", "linear_gn_m256", "linear_lse_m1024", "ln_dconv1d_b32", "convt3d_n128"]
+
+
+# ---------------------------------------------------------------- ours
+def run_ours(wl, args):
     import torch
     import torch.distributed as dist
 
     from conv_activation_normalization_gb300 import binding as gf
-    from conv_activation_normalization_gb300 import synth
 
     ws, rank, local = _dist()
-    if ws > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     gf.lib()
-
-    shape = synth.LinearGNShape(M=M, K=K, N=N, groups=GROUPS, eps=EPS)
-    d = synth.linear_gn_inputs(shape, synth.SEED_BASE + 2)
-    x = torch.from_numpy(d["x"]).to(dev)
-    W = torch.from_numpy(d["W"]).to(dev)
-    vec = {k: torch.from_numpy(d[k]).to(dev) for k in ("b_lin", "bias", "gamma", "beta")}
-    out = torch.empty((M, N), dtype=torch.float32, device=dev)
-    xp = torch.empty((2, M, K), dtype=torch.float32, device=dev)
-    Wp = torch.empty((2, N, K), dtype=torch.float32, device=dev)
+    d = wl.inputs()
+    t = wl.setup(d, dev)
     stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        # the public operator, split into its two stages so that the fused
-        # GEMM kernel can be timed on its own inside the step
-        gf.gf_tf32_split(x, xp)
-        gf.gf_tf32_split(W, Wp)
-        if ev is not None:
-            ev[0].record(stream)
-        gf.gf_linear_swish_bias_groupnorm_planes(xp, Wp, vec["b_lin"], vec["bias"], vec["gamma"], vec["beta"],
-                                                 GROUPS, EPS, out=out)
-        if ev is not None:
-            ev[1].record(stream)
+    flush = None
+    if "flushed" in wl.l2:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     for _ in range(args.warmup):
-        step()
+        wl.step(gf, t)
     torch.cuda.synchronize()
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.steps is None:  # aim for about half a second of timed work
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        wl.step(gf, t)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        steps = int(min(2000, max(20, 0.5e3 / max(e0.elapsed_time(e1), 1e-3))))
+    else:
+        steps = args.steps
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        t0.record(stream)
-        for i in range(args.steps):
-            step(kev[i])
-        t1.record(stream)
-        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        with gf.profile(max_calls=steps + 8) as prof:
+            for i in range(steps):
+                if flush is not None:
+                    flush.fill_(i & 0xff)
+                evs[i][0].record(stream)
+                wl.step(gf, t)
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
     if ws > 1:
         dist.barrier()
-    ms_total = t0.elapsed_time(t1)
-    gemm_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    ms_total = sum(a.elapsed_time(b) for a, b in evs)
+    kern_ms = prof.mean_ms
     if ws > 1:
-        tt = torch.tensor([ms_total, gemm_ms], device=dev)
+        tt = torch.tensor([ms_total, kern_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total, gemm_ms = tt.tolist()
-    ms_step = ms_total / args.steps
-    value = FLOP * ws / (ms_step * 1e-3) / 1e12
+        ms_total, kern_ms = tt.tolist()
+    ms_step = ms_total / steps
+    value = wl.work_per_step() * ws / (ms_step * 1e-3) / wl.scale()
 
-    # end to end through the public API: pinned host x in, host out back
     e2e = None
     if not args.no_e2e:
         xh = torch.from_numpy(d["x"]).pin_memory()
-        oh = torch.empty((M, N), dtype=torch.float32).pin_memory()
-        xd = torch.empty_like(x)
+        oh = torch.empty(tuple(t["out"].shape), dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(t["x"])
 
         def e2e_step():
             xd.copy_(xh, non_blocking=True)
-            gf.gf_linear_swish_bias_groupnorm(xd, W, vec["b_lin"], vec["bias"], vec["gamma"], vec["beta"], GROUPS,
-                                              EPS, out=out)
-            oh.copy_(out, non_blocking=True)
+            wl.step(gf, t, x=xd)
+            oh.copy_(t["out"], non_blocking=True)
 
-        for _ in range(max(1, args.warmup)):
+        for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
+        n_e2e = max(3, min(steps, 50))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2e_steps = max(3, args.steps // 2)
         e0.record(stream)
-        for _ in range(e2e_steps):
+        for _ in range(n_e2e):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
         if ws > 1:
             tt = torch.tensor([e2e_ms], device=dev)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             e2e_ms = tt.item()
-        e2e = {"value": round(FLOP * ws / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+        e2e = {"value": round(wl.work_per_step() * ws / (e2e_ms * 1e-3) / wl.scale(), 3), "unit": wl.unit,
                "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(oh.numel() * 4),
                "ms_per_step": round(e2e_ms, 4)}
 
-    bf16, src = _peaks()
-    peak = bf16 * TF32_OVER_BF16 / 3.0
-    achieved = FLOP / (gemm_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": "gemm3xtf32_kernel<EpiSwishBiasGN>", "achieved": round(achieved, 2),
-                "peak": round(peak, 2), "unit": UNIT, "frac": round(achieved / peak, 4),
-                "traffic": _kernel_traffic(),
-                "peak_note": f"3xTF32-effective: {src} bf16 dense burst {bf16} TFLOP/s x 1.1/2.25 (TF32/BF16 nominal) / 3",
-                "kernel_ms": round(gemm_ms, 4)}
+    peaks, src = _peaks()
+    achieved = wl.kernel_work() / (kern_ms * 1e-3) / wl.scale()
+    if wl.bound == "tensor":
+        sustained = t_wall > SUSTAINED_AFTER_S
+        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        peak = bf16 * TF32_OVER_BF16 / 3.0
+        note = (f"3xTF32-effective: {src} bf16 dense {'sustained' if sustained else 'burst'} {bf16} TFLOP/s "
+                f"x 1.1/2.25 (nominal TF32/BF16) / 3 (three TF32 products per fp32 product)")
+    else:
+        peak = peaks["hbm_gbs"]
+        note = f"{src} HBM copy bandwidth"
+    roofline = {"bound": wl.bound, "kernel": wl.kernel, "achieved": round(achieved, 2), "peak": round(peak, 2),
+                "unit": wl.unit, "frac": round(achieved / peak, 4), "traffic": _kernel_traffic(wl),
+                "kernel_ms": round(kern_ms, 4), "kernel_launches_timed": prof.calls, "peak_note": note}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
-        cpu = cpu_baseline(d, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(wl, d, budget_s=args.cpu_seconds)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        launches = {"linear_gn_m32768": 3, "linear_gn_m256": 3, "linear_lse_m1024": 4, "ln_dconv1d_b32": 5,
+                    "convt3d_n128": 3}[wl.name]
+        line = {"metric": wl.metric, "value": round(value, 3), "unit": wl.unit, "n_gpus": ws, "steps": steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (3xtf32)", "data": "synthetic",
-                "config": _config({"parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}),
-                "e2e": e2e, "gpu_launches": 3 * args.steps, "roofline": roofline, "cpu_baseline": cpu,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (3xtf32 contraction)" if wl.bound == "tensor"
+                else "fp32", "data": "synthetic",
+                "config": dict(wl.config, l2=wl.l2, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
+                "e2e": e2e, "gpu_launches": launches * steps, "roofline": roofline, "cpu_baseline": cpu,
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
-    if ws > 1:
-        dist.destroy_process_group()
 
 
-def cpu_baseline(d, budget_s=12.0, rows_per_chunk=2048):
-    """The fp64 oracle as it stands on a bounded sample of rows."""
-    import oracle
+def cpu_baseline(wl, d, budget_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload."""
     t0 = time.perf_counter()
-    rows = 0
-    while rows < M and time.perf_counter() - t0 < budget_s:
-        sl = slice(rows, rows + rows_per_chunk)
-        oracle.linear_swish_bias_groupnorm(d["x"][sl], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"],
-                                           GROUPS, EPS)
-        rows += rows_per_chunk
+    frac, i = 0.0, 0
+    while frac < 1.0 - 1e-9 and time.perf_counter() - t0 < budget_s:
+        frac += wl.oracle_chunk(d, i, wl.chunk)
+        i += 1
     dt = time.perf_counter() - t0
-    v = 2.0 * rows * N * K / dt / 1e12
-    return {"value": round(v, 5), "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{rows} of {M} rows of the same workload in {rows_per_chunk}-row chunks, fp64 numpy "
-                      f"(BLAS threads at their default), {dt:.1f} s"}
+    v = wl.work_per_step() * frac / dt / wl.scale()
+    return {"value": round(v, 6), "unit": wl.unit, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{frac * 100:.1f}% of one step of the same workload ({i} chunks of {wl.chunk} "
+                      f"{'rows' if 'linear' in wl.name else 'samples'}), fp64 numpy/scipy with BLAS threads at "
+                      f"their default, {dt:.1f} s"}
 
 
 # ----------------------------------------------------------- reference
-def run_reference(args):
+def run_reference(wl, args):
     ws, rank, _ = _dist()
     if rank != 0:
         return
-    from conv_activation_normalization_gb300 import synth
-    import oracle
-    shape = synth.LinearGNShape(M=M, K=K, N=N, groups=GROUPS, eps=EPS)
-    d = synth.linear_gn_inputs(shape, synth.SEED_BASE + 2)
-    rows = args.ref_rows
+    d = wl.inputs()
+    n_chunks = max(1, int(args.ref_chunks))
 
     def step():
-        oracle.linear_swish_bias_groupnorm(d["x"][:rows], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"],
-                                           GROUPS, EPS)
+        f = 0.0
+        for i in range(n_chunks):
+            f += wl.oracle_chunk(d, i, wl.chunk)
+        return f
 
-    for _ in range(args.warmup):
+    for _ in range(min(args.warmup, 1)):
         step()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = (time.perf_counter() - t0) / args.steps
-    v = 2.0 * rows * N * K / dt / 1e12
+    frac = 0.0
+    for _ in range(args.steps or 3):
+        frac = step()
+    steps = args.steps or 3
+    dt = (time.perf_counter() - t0) / steps
+    v = wl.work_per_step() * frac / dt / wl.scale()
     cores = len(os.sched_getaffinity(0))
-    line = {"metric": METRIC, "value": round(v, 5), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": _config({"parallelism": "host cores", "reference_sample_rows": rows}),
-            "cpu_baseline": {"value": round(v, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{rows} of {M} rows per step, fp64 numpy oracle"},
-            "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    sample = f"{frac * 100:.2f}% of the workload per step ({n_chunks} chunk(s) of {wl.chunk}), fp64 numpy oracle"
+    line = {"metric": wl.metric, "value": round(v, 6), "unit": wl.unit, "n_gpus": ws, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": dict(wl.config, l2=wl.l2, parallelism="host cores"),
+            "cpu_baseline": {"value": round(v, 6), "unit": wl.unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="linear_gn_m32768", choices=ALL)
+    ap.add_argument("--all", action="store_true", help="one line per workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ref-rows", type=int, default=1024)
+    ap.add_argument("--ref-chunks", type=int, default=1)
+    ap.add_argument("--rows", type=int, default=None, help="profiling only: M of the Linear->GroupNorm workload")
+    ap.add_argument("--samples", type=int, default=None, help="profiling only: batch of the conv workloads")
     args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-    if args.impl == "reference":
-        run_reference(args)
-    else:
-        run_ours(args)
+    args.warmup = max(3, args.warmup)
+    names = ALL if args.all else [args.workload]
+    for n in names:
+        wl = make_workload(n, args.rows, args.samples)
+        if args.impl == "reference":
+            run_reference(wl, args)
+        else:
+            run_ours(wl, args)
+    if args.impl == "ours" and _dist()[0] > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":

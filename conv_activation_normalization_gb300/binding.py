@@ -32,6 +32,8 @@ _SIGS = {
     "gf_abi_version": (_I32, []),
     "gf_status_string": (ctypes.c_char_p, [_I32]),
     "gf_device_status": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
+    "gf_profile_begin": (_I32, [_I32]),
+    "gf_profile_end": (_I32, [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_float)]),
     "gf_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
     "gf_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "gf_linear_swish_bias_groupnorm_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
@@ -95,6 +97,35 @@ def gf_device_status() -> int:
     if st not in (0, -8):
         raise GFError(st, "gf_device_status")
     return bits.value
+
+
+class profile:
+    """Context manager: time the dominant kernel of every library call made
+    inside it (CUDA events recorded by the library on the call's stream).
+    After exit, ``.calls`` and ``.total_ms`` hold the count and summed time."""
+
+    def __init__(self, max_calls=100000):
+        self.max_calls = max_calls
+        self.calls = 0
+        self.total_ms = 0.0
+
+    def __enter__(self):
+        st = lib().gf_profile_begin(self.max_calls)
+        if st != 0:
+            raise GFError(st, "gf_profile_begin")
+        return self
+
+    def __exit__(self, *exc):
+        c, t = ctypes.c_int32(0), ctypes.c_float(0.0)
+        st = lib().gf_profile_end(ctypes.byref(c), ctypes.byref(t))
+        self.calls, self.total_ms = c.value, t.value
+        if st != 0 and exc[0] is None:
+            raise GFError(st, "gf_profile_end")
+        return False
+
+    @property
+    def mean_ms(self):
+        return self.total_ms / self.calls if self.calls else float("nan")
 
 
 # --------------------------------------------------------------- plumbing

@@ -2,6 +2,7 @@
 // the host helpers declared in host_common.h.
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "host_common.h"
 
@@ -98,9 +99,80 @@ gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint
   return r == CUDA_SUCCESS ? GF_OK : GF_ERR_CUDA;
 }
 
+namespace {
+struct Profile {
+  bool active = false;
+  int capacity = 0, used = 0;
+  bool open = false;
+  cudaEvent_t* ev = nullptr;  // 2 * capacity
+};
+Profile g_prof;
+std::mutex g_prof_mu;
+}  // namespace
+
+void profile_mark_begin(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof.active || g_prof.used >= g_prof.capacity) return;
+  cudaEventRecord(g_prof.ev[2 * g_prof.used], s);
+  g_prof.open = true;
+}
+
+void profile_mark_end(cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof.active || !g_prof.open) return;
+  cudaEventRecord(g_prof.ev[2 * g_prof.used + 1], s);
+  g_prof.open = false;
+  ++g_prof.used;
+}
+
 }  // namespace gf
 
 extern "C" {
+
+gf_status gf_profile_begin(int32_t max_calls) {
+  using namespace gf;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof.active || max_calls < 1 || max_calls > (1 << 20)) return GF_ERR_SHAPE;
+  g_prof.ev = new (std::nothrow) cudaEvent_t[2 * size_t(max_calls)];
+  if (!g_prof.ev) return GF_ERR_CUDA;
+  for (int i = 0; i < 2 * max_calls; ++i) {
+    if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
+      delete[] g_prof.ev;
+      g_prof.ev = nullptr;
+      return GF_ERR_CUDA;
+    }
+  }
+  g_prof.capacity = max_calls;
+  g_prof.used = 0;
+  g_prof.open = false;
+  g_prof.active = true;
+  return GF_OK;
+}
+
+gf_status gf_profile_end(int32_t* calls, float* total_ms) {
+  using namespace gf;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof.active) return GF_ERR_SHAPE;
+  gf_status st = GF_OK;
+  float total = 0.f;
+  for (int i = 0; i < g_prof.used; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) {
+      st = GF_ERR_CUDA;
+      break;
+    }
+    total += ms;
+  }
+  for (int i = 0; i < 2 * g_prof.capacity; ++i) cudaEventDestroy(g_prof.ev[i]);
+  delete[] g_prof.ev;
+  if (calls) *calls = g_prof.used;
+  if (total_ms) *total_ms = total;
+  g_prof = Profile{};
+  return st;
+}
+
 
 int32_t gf_abi_version(void) { return 1; }
 

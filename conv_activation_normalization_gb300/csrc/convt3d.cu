@@ -274,7 +274,9 @@ void launch_ct(const float* x, const float* w, const float* b, double* part, con
   convt3d_stats_kernel<CIN><<<grid, block, 0, s>>>(x, w, b, part, D, H, W);
   const double count = double(kCT_COUT / kCT_G) * double(2 * D - 1) * double(2 * H - 1) * double(2 * W - 1);
   convt3d_finalize_kernel<<<N, 64, 0, s>>>(part, gamma, beta, coef, P, count, eps);
+  profile_mark_begin(s);
   convt3d_apply_kernel<CIN><<<grid, block, 0, s>>>(x, w, b, coef, out, D, H, W);
+  profile_mark_end(s);
 }
 }  // namespace
 }  // namespace gf

@@ -300,7 +300,9 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   auto kern = gemm3xtf32_kernel<kBNConv, ConvSrc, EpiConvResidual>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return GF_ERR_CUDA;
+  profile_mark_begin(s);
   kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, s>>>(ta, tb, src, ep, device_status_word());
+  profile_mark_end(s);
   return cuda_status(cudaGetLastError());
 }
 

@@ -54,4 +54,9 @@ gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Profiling: while gf_profile_begin() is active, every entry point records
+// a pair of CUDA events on its stream around its dominant kernel.
+void profile_mark_begin(cudaStream_t s);
+void profile_mark_end(cudaStream_t s);
+
 }  // namespace gf

@@ -207,7 +207,9 @@ gf_status launch_linear_gemm(const DeviceInfo& dev, const float* a_planes, const
   auto kern = gemm3xtf32_kernel<kBNLinear, LinearSrc, Epi>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return GF_ERR_CUDA;
+  profile_mark_begin(stream);
   kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, src, ep, device_status_word());
+  profile_mark_end(stream);
   return cuda_status(cudaGetLastError());
 }
 

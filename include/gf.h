@@ -71,6 +71,17 @@ const char* gf_status_string(gf_status status);
  * device_bits may be NULL. */
 gf_status gf_device_status(int32_t* device_bits);
 
+/* Profiling.  Between gf_profile_begin(max_calls) and gf_profile_end(), each
+ * compute entry point records a pair of CUDA events on its stream around its
+ * dominant kernel (the fused GEMM; for the ConvTranspose3d chain, the pass that
+ * writes the output), for up to max_calls calls.  gf_profile_end() waits for
+ * the recorded events, returns the number of calls recorded and the sum of
+ * their kernel times in milliseconds, and releases the events.  The recorder
+ * is process-wide: profile one stream at a time.  Returns GF_ERR_SHAPE when
+ * begin is called twice or end without begin. */
+gf_status gf_profile_begin(int32_t max_calls);
+gf_status gf_profile_end(int32_t* calls, float* total_ms);
+
 /* ------------------------------------------------------------------------
  * Linear alone: out[m,n] = sum_k x[m,k] * W[n,k] + b[n]
  *
