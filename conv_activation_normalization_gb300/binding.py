@@ -51,6 +51,9 @@ _SIGS = {
                                                         _I32]),
     "gf_convt3d_swish_gn_hswish": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I32,
                                           _I32, _I32, _I32, _F, _P, _SZ, _P]),
+    "gf_convt3d_noalloc_scratch_limit": (_SZ, []),
+    "gf_convt3d_swish_gn_hswish_noalloc": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                                  _I32, _I32, _I32, _I32, _F, _P]),
 }
 
 
@@ -291,4 +294,20 @@ def gf_convt3d_swish_gn_hswish(x, w, b, gamma, beta, stride, pad, groups, eps=1e
         wp, nb = _ws_args(dev, nbytes, workspace)
         _call("gf_convt3d_swish_gn_hswish", _ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(out),
               N, Cin, Cout, D, H, W, k, stride, pad, groups, eps, wp, nb, _stream_ptr(stream))
+    return out
+
+
+def gf_convt3d_swish_gn_hswish_noalloc(x, w, b, gamma, beta, stride, pad, groups, eps=1e-5, out=None, stream=None):
+    """gf_convt3d_swish_gn_hswish without a workspace: for callers that cannot
+    give the library device scratch memory; the library's own fixed scratch
+    (gf_convt3d_noalloc_scratch_limit() bytes per device) is used instead.
+    Calls that overlap on the GPU race on that scratch."""
+    dev = _check(x, w, b, gamma, beta, out)
+    N, Cin, D, H, W = x.shape
+    Cout, k = w.shape[1], w.shape[2]
+    if out is None:
+        out = torch.empty(convt3d_out_shape(x.shape, Cout, k, stride, pad), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _call("gf_convt3d_swish_gn_hswish_noalloc", _ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(out),
+              N, Cin, Cout, D, H, W, k, stride, pad, groups, eps, _stream_ptr(stream))
     return out

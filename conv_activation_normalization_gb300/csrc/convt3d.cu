@@ -23,6 +23,7 @@
 // (Cout = 16 with 4 groups, so a group is 4 channels): 32 accumulators; the
 // weights sit in shared memory as [ci][tap][co], read as float4 broadcasts.
 #include <cmath>
+#include <mutex>
 
 #include "host_common.h"
 #include "kernels_common.cuh"
@@ -279,6 +280,33 @@ void launch_ct(const float* x, const float* w, const float* b, double* part, con
   profile_mark_end(s);
 }
 }  // namespace
+
+// Fixed scratch for gf_convt3d_swish_gn_hswish_noalloc: the per-block GroupNorm
+// partial sums and the per-channel affine coefficients live here instead of in
+// a caller-provided workspace.  The array exists once per device that loads
+// this library and is shared by every call of that entry point.
+constexpr size_t kCtNoAllocScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) unsigned char g_ct_noalloc_scratch[kCtNoAllocScratchBytes];
+
+namespace {
+std::mutex g_ct_scratch_mu;
+void* g_ct_scratch_addr[64];
+
+// Device address of g_ct_noalloc_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a host-side stand-in, so
+// the kernels must be given this address instead.
+gf_status ct_scratch_address(int device, void** addr) {
+  if (device < 0 || device >= 64) return GF_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_ct_scratch_mu);
+  if (!g_ct_scratch_addr[device]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ct_noalloc_scratch) != cudaSuccess || !p) return GF_ERR_CUDA;
+    g_ct_scratch_addr[device] = p;
+  }
+  *addr = g_ct_scratch_addr[device];
+  return GF_OK;
+}
+}  // namespace
 }  // namespace gf
 
 using namespace gf;
@@ -319,6 +347,49 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
   if (st != GF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  double* part = reinterpret_cast<double*>(ws + wl.part);
+  float2* coef = reinterpret_cast<float2*>(ws + wl.coef);
+  const int n = int(N), d = int(D), h = int(H), ww = int(W);
+  switch (Cin) {
+#define GF_CT_CASE(c) \
+  case c: launch_ct<c>(x, w, b, part, gamma, beta, coef, out, n, d, h, ww, wl.P, eps, s); break;
+    GF_CT_CASE(1) GF_CT_CASE(2) GF_CT_CASE(3) GF_CT_CASE(4) GF_CT_CASE(5) GF_CT_CASE(6) GF_CT_CASE(7) GF_CT_CASE(8)
+#undef GF_CT_CASE
+    default: return GF_ERR_SHAPE;
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+size_t gf_convt3d_noalloc_scratch_limit(void) { return kCtNoAllocScratchBytes; }
+
+gf_status gf_convt3d_swish_gn_hswish_noalloc(const float* x, const float* w, const float* b, const float* gamma,
+                                             const float* beta, float* out, int64_t N, int64_t Cin, int64_t Cout,
+                                             int64_t D, int64_t H, int64_t W, int32_t k, int32_t stride, int32_t pad,
+                                             int32_t groups, float eps, void* stream) {
+  if (!x || !w || !gamma || !beta || !out) return GF_ERR_NULL;
+  gf_status st = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups);
+  if (st != GF_OK) return st;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
+      (b && !aligned16(b)))
+    return GF_ERR_ALIGN;
+  const CtWs wl = ct_ws(N, D, H, W);
+  if (wl.total > kCtNoAllocScratchBytes) return GF_ERR_WORKSPACE;  // beyond the fixed scratch
+  const size_t outb = size_t(N) * Cout * (2 * D - 1) * (2 * H - 1) * (2 * W - 1) * 4;
+  const Span ins[] = {{x, size_t(N) * Cin * D * H * W * 4},
+                      {w, size_t(Cin) * Cout * 27 * 4},
+                      {b, size_t(Cout) * 4},
+                      {gamma, size_t(Cout) * 4},
+                      {beta, size_t(Cout) * 4}};
+  st = check_no_alias(Span{out, outb}, ins, 5);
+  if (st != GF_OK) return st;
+  DeviceInfo dev;
+  st = current_device(&dev);
+  if (st != GF_OK) return st;
+  void* scratch = nullptr;
+  if ((st = ct_scratch_address(dev.device, &scratch)) != GF_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
   double* part = reinterpret_cast<double*>(ws + wl.part);
   float2* coef = reinterpret_cast<float2*>(ws + wl.coef);
   const int n = int(N), d = int(D), h = int(H), ww = int(W);

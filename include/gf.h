@@ -200,6 +200,42 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
                                      int32_t groups, float eps,
                                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * ConvTranspose3d -> Swish -> GroupNorm -> HardSwish without any workspace
+ *
+ * The source pages have no counterpart of this entry point; it exists for
+ * callers that cannot hand the library device scratch memory.  Typical ones:
+ * a host process that owns the whole device memory budget through its own
+ * pool and forbids any further cudaMalloc once it has started, or a plugin
+ * interface that passes a kernel only its input and output buffers.  Such a
+ * caller cannot call gf_convt3d_swish_gn_hswish, whose statistics need a
+ * workspace.
+ *
+ * Same operator, arguments (minus workspace), supported shapes and result as
+ * gf_convt3d_swish_gn_hswish.  The caller still owns and passes x, w, b,
+ * gamma, beta and out.  The scratch (the per-block GroupNorm sums and the
+ * per-channel affine coefficients, gf_convt3d_swish_gn_hswish_workspace_size()
+ * bytes) lives in a fixed array inside the library, 4 MiB
+ * (gf_convt3d_noalloc_scratch_limit()) on every GPU that loads the library,
+ * held until the process exits.  Shapes that need more return
+ * GF_ERR_WORKSPACE before anything is launched.  No call allocates: the
+ * entry point calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call on a device uses the same array and leaves its
+ * contents behind; the kernels overwrite all of it that they read, so nothing
+ * needs clearing between calls.  Two calls whose kernels overlap on the GPU
+ * (different streams, no ordering between them) race on the array: order
+ * them, e.g. by issuing them on one stream.
+ * ---------------------------------------------------------------------- */
+size_t gf_convt3d_noalloc_scratch_limit(void);
+gf_status gf_convt3d_swish_gn_hswish_noalloc(const float* x, const float* w, const float* b,
+                                             const float* gamma, const float* beta, float* out,
+                                             int64_t N, int64_t Cin, int64_t Cout, int64_t D,
+                                             int64_t H, int64_t W, int32_t k, int32_t stride,
+                                             int32_t pad, int32_t groups, float eps, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
