@@ -38,6 +38,15 @@ TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense TF32 / BF16 tensor rates of the par
 FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 SUSTAINED_AFTER_S = 2.0      # timed regions longer than this use the sustained tensor peak
 
+# contraction modes of the tensor-core workloads: (library mode, label,
+# peak = measured bf16 peak x this factor, in fp32-equivalent FLOP/s)
+MODES = {
+    "3xtf32": (0, "fp32 (3xTF32 tensor-core contraction, fp32 epilogue)", TF32_OVER_BF16 / 3.0),
+    "bf16": (1, "bf16 operands (one BF16 product, fp32 accumulation and epilogue)", 1.0),
+    "3xbf16": (2, "fp32-class (3xBF16 tensor-core contraction, fp32 epilogue)", 1.0 / 3.0),
+}
+MODE = "3xtf32"
+
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -147,7 +156,7 @@ class Workload:
 
 class LinearGN(Workload):
     sources = Workload.sources + ("linear_ops.cu",)
-    kernel = "gemm3xtf32_kernel<LinearSrc, EpiSwishBiasGN>"
+    kernel = "gemm_tc_kernel<256, OpTF32x3, LinearSrc, EpiSwishBiasGN>"
 
     def __init__(self, M, name):
         from conv_activation_normalization_gb300 import synth
@@ -180,7 +189,7 @@ class LinearGN(Workload):
     def step(self, gf, t, x=None):
         s = self.shape
         gf.gf_linear_swish_bias_groupnorm(t["x"] if x is None else x, t["W"], t["b_lin"], t["bias"], t["gamma"],
-                                          t["beta"], s.groups, s.eps, out=t["out"])
+                                          t["beta"], s.groups, s.eps, mode=MODES[MODE][0], out=t["out"])
 
     def oracle_chunk(self, d, i, chunk):
         import oracle
@@ -197,7 +206,7 @@ class LinearLSE(Workload):
     name = "linear_lse_m1024"
     metric = "fused Linear->logsumexp->LeakyReLU x2->GELU x2 TFLOP/s at x[1024,8192], W[8192,8192]"
     sources = Workload.sources + ("linear_ops.cu",)
-    kernel = "gemm3xtf32_kernel<LinearSrc, EpiLSEPartial>"
+    kernel = "gemm_tc_kernel<256, OpTF32x3, LinearSrc, EpiLSEPartial>"
     l2 = "inputs larger than L2 (W 268 MB per step vs 129 MB L2); no flush"
     chunk = 64
 
@@ -222,7 +231,8 @@ class LinearLSE(Workload):
         return t
 
     def step(self, gf, t, x=None):
-        gf.gf_linear_lse_act(t["x"] if x is None else x, t["W"], t["b"], self.shape.negative_slope, out=t["out"])
+        gf.gf_linear_lse_act(t["x"] if x is None else x, t["W"], t["b"], self.shape.negative_slope,
+                             mode=MODES[MODE][0], out=t["out"])
 
     def oracle_chunk(self, d, i, chunk):
         import oracle
@@ -236,7 +246,7 @@ class DConv1d(Workload):
     name = "ln_dconv1d_b32"
     metric = "fused LayerNorm->GELU->dilated Conv1d->residual TFLOP/s at x[32,256,4096]"
     sources = Workload.sources + ("dconv1d.cu",)
-    kernel = "gemm3xtf32_kernel<ConvSrc, EpiConvResidual>"
+    kernel = "gemm_tc_kernel<256, OpTF32x3, ConvSrc, EpiConvResidual>"
     l2 = "inputs larger than L2 (x 134 MB read twice + A planes 268 MB + out 134 MB per step); no flush"
     chunk = 1
 
@@ -265,7 +275,7 @@ class DConv1d(Workload):
     def step(self, gf, t, x=None):
         s = self.shape
         gf.gf_ln_gelu_dconv1d_res(t["x"] if x is None else x, t["ln_gamma"], t["ln_beta"], t["conv_w"], t["conv_b"],
-                                  s.dilation, s.padding, s.eps, out=t["out"])
+                                  s.dilation, s.padding, s.eps, mode=MODES[MODE][0], out=t["out"])
 
     def oracle_chunk(self, d, i, chunk):
         import oracle
@@ -462,9 +472,12 @@ def run_ours(wl, args):
     if wl.bound == "tensor":
         sustained = t_wall > SUSTAINED_AFTER_S
         bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-        peak = bf16 * TF32_OVER_BF16 / 3.0
-        note = (f"3xTF32-effective: {src} bf16 dense {'sustained' if sustained else 'burst'} {bf16} TFLOP/s "
-                f"x 1.1/2.25 (nominal TF32/BF16) / 3 (three TF32 products per fp32 product)")
+        peak = bf16 * MODES[MODE][2]
+        note = {"3xtf32": f"3xTF32-effective: {src} bf16 dense {'sustained' if sustained else 'burst'} {bf16} "
+                          f"TFLOP/s x 1.1/2.25 (nominal TF32/BF16) / 3 (three TF32 products per fp32 product)",
+                "bf16": f"{src} bf16 dense {'sustained' if sustained else 'burst'} {bf16} TFLOP/s",
+                "3xbf16": f"3xBF16-effective: {src} bf16 dense {'sustained' if sustained else 'burst'} {bf16} "
+                          f"TFLOP/s / 3 (three BF16 products per fp32 product)"}[MODE]
     else:
         peak = peaks["hbm_gbs"]
         note = f"{src} HBM copy bandwidth"
@@ -481,9 +494,11 @@ def run_ours(wl, args):
                     "convt3d_n128": 3}[wl.name]
         line = {"metric": wl.metric, "value": round(value, 3), "unit": wl.unit, "n_gpus": ws, "steps": steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (3xtf32 contraction)" if wl.bound == "tensor"
-                else "fp32", "data": "synthetic",
-                "config": dict(wl.config, l2=wl.l2, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": {"3xtf32": "fp32 (3xtf32 contraction)", "bf16": "bf16", "3xbf16": "fp32 (3xbf16 contraction)"}[
+                    MODE] if wl.bound == "tensor" else "fp32", "data": "synthetic",
+                "config": dict(wl.config, l2=wl.l2, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU",
+                               **({"mode": MODES[MODE][1]} if wl.bound == "tensor" else {})),
                 "e2e": e2e, "gpu_launches": launches * steps, "roofline": roofline, "cpu_baseline": cpu,
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
@@ -550,10 +565,14 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-chunks", type=int, default=1)
+    ap.add_argument("--mode", choices=list(MODES), default="3xtf32",
+                    help="contraction mode of the tensor-core workloads")
     ap.add_argument("--rows", type=int, default=None, help="profiling only: M of the Linear->GroupNorm workload")
     ap.add_argument("--samples", type=int, default=None, help="profiling only: batch of the conv workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    global MODE
+    MODE = args.mode
     names = ALL if args.all else [args.workload]
     for n in names:
         wl = make_workload(n, args.rows, args.samples)

@@ -67,8 +67,8 @@ uint32_t* device_status_word() {
   return g_status_ptr[dev];
 }
 
-gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                        const uint32_t* box) {
+gf_status make_tmap(CUtensorMap* map, const void* base, int elem_bytes, int rank, const uint64_t* dims,
+                    const uint32_t* box) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode) {
@@ -81,10 +81,11 @@ gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
   }
-  if (rank < 1 || rank > 5 || box[0] * 4 != 128) return GF_ERR_SHAPE;
+  if (rank < 1 || rank > 5 || (elem_bytes != 4 && elem_bytes != 2) || box[0] * uint32_t(elem_bytes) != 128)
+    return GF_ERR_SHAPE;
   cuuint64_t gdim[5], gstride[4];
   cuuint32_t bdim[5], estride[5];
-  uint64_t stride = 4;
+  uint64_t stride = uint64_t(elem_bytes);
   for (int i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
     bdim[i] = box[i];
@@ -92,7 +93,8 @@ gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint
     if (i > 0) gstride[i - 1] = stride;
     stride *= dims[i];
   }
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(rank), const_cast<void*>(base),
+  const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = g_encode(map, dt, cuuint32_t(rank), const_cast<void*>(base),
                               gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -34,10 +34,22 @@ constexpr int kCT_COUT = 16;
 constexpr int kCT_G = 4;
 constexpr int kCT_TX = 32, kCT_TY = 8;  // cells per block along w and h
 
+// The 2x2x2 inputs of a cell, each held twice ((v, v) pairs) so the packed
+// f32x2 FMAs below can multiply one input by the weights of two channels.
 template <int CIN>
 struct CellInputs {
-  float v[CIN][2][2][2];
+  float2 v[CIN][2][2][2];
 };
+
+// d = a * b + c on both lanes of a pair (fma.rn.f32x2).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const unsigned long long*>(&a)), "l"(*reinterpret_cast<const unsigned long long*>(&b)),
+        "l"(*reinterpret_cast<const unsigned long long*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
+}
 
 template <int CIN>
 __device__ __forceinline__ void load_cell(CellInputs<CIN>& in, const float* __restrict__ xn, int D, int H, int W,
@@ -53,21 +65,21 @@ __device__ __forceinline__ void load_cell(CellInputs<CIN>& in, const float* __re
           const int d = qd + a, h = qh + b, w = qw + c;
           float v = 0.f;
           if (d < D && h < H && w < W) v = __ldg(xn + ((size_t(ci) * D + d) * H + h) * W + w);
-          in.v[ci][a][b][c] = v;
+          in.v[ci][a][b][c] = make_float2(v, v);
         }
 }
 
-// acc[co_in_group][phase], phase = pd*4 + ph*2 + pw.  ws = smem weights
-// [CIN][27][16], bias4 = conv bias of the 4 channels.
+// Accumulators of one cell for the 4 channels of group cg, as channel pairs:
+// a01[phase] = (channel 0, channel 1), a23[phase] = (channel 2, channel 3),
+// phase = pd*4 + ph*2 + pw.  ws = smem weights [CIN][27][16], bias4 = conv
+// bias of the 4 channels.
 template <int CIN>
 __device__ __forceinline__ void conv_cell(const CellInputs<CIN>& in, const float* __restrict__ ws, int cg,
-                                          float4 bias4, float (&acc)[4][8]) {
+                                          float4 bias4, float2 (&a01)[8], float2 (&a23)[8]) {
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
-    acc[0][p] = bias4.x;
-    acc[1][p] = bias4.y;
-    acc[2][p] = bias4.z;
-    acc[3][p] = bias4.w;
+    a01[p] = make_float2(bias4.x, bias4.y);
+    a23[p] = make_float2(bias4.z, bias4.w);
   }
 #pragma unroll
   for (int ci = 0; ci < CIN; ++ci)
@@ -83,11 +95,9 @@ __device__ __forceinline__ void conv_cell(const CellInputs<CIN>& in, const float
           const int pw = kw == 1 ? 0 : 1, aw = kw == 0 ? 1 : 0;
           const int phase = pd * 4 + ph * 2 + pw;
           const float4 w4 = *reinterpret_cast<const float4*>(ws + (ci * 27 + (kd * 3 + kh) * 3 + kw) * 16 + cg * 4);
-          const float xv = in.v[ci][ad][ah][aw];
-          acc[0][phase] = fmaf(xv, w4.x, acc[0][phase]);
-          acc[1][phase] = fmaf(xv, w4.y, acc[1][phase]);
-          acc[2][phase] = fmaf(xv, w4.z, acc[2][phase]);
-          acc[3][phase] = fmaf(xv, w4.w, acc[3][phase]);
+          const float2 xv = in.v[ci][ad][ah][aw];
+          a01[phase] = fma2(xv, make_float2(w4.x, w4.y), a01[phase]);
+          a23[phase] = fma2(xv, make_float2(w4.z, w4.w), a23[phase]);
         }
 }
 
@@ -117,7 +127,7 @@ __device__ __forceinline__ uint32_t phase_mask(int qd, int qh, int qw, int D, in
 // grid (ceil(W/32), ceil(H/8), D * N), block (32, 8).
 // part: [N][G][P][2] doubles, P = blocks per sample.
 template <int CIN>
-__global__ void __launch_bounds__(256) convt3d_stats_kernel(const float* __restrict__ x, const float* __restrict__ w,
+__global__ void __launch_bounds__(256, 3) convt3d_stats_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ bias, double* __restrict__ part,
                                                             int D, int H, int W) {
   __shared__ __align__(16) float ws[CIN * 27 * kCT_COUT];
@@ -134,18 +144,15 @@ __global__ void __launch_bounds__(256) convt3d_stats_kernel(const float* __restr
 #pragma unroll 1
   for (int cg = 0; cg < kCT_G; ++cg) {
     const float4 b4 = bias ? __ldg(reinterpret_cast<const float4*>(bias) + cg) : make_float4(0, 0, 0, 0);
-    float acc[4][8];
-    conv_cell<CIN>(in, ws, cg, b4, acc);
+    float2 a01[8], a23[8];
+    conv_cell<CIN>(in, ws, cg, b4, a01, a23);
     float a = 0.f, q = 0.f;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       if ((pm >> p) & 1u) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float s = swish(acc[c][p]);
-          a += s;
-          q = fmaf(s, s, q);
-        }
+        const float s0 = swish(a01[p].x), s1 = swish(a01[p].y), s2 = swish(a23[p].x), s3 = swish(a23[p].y);
+        a += (s0 + s1) + (s2 + s3);
+        q = fmaf(s0, s0, fmaf(s1, s1, fmaf(s2, s2, fmaf(s3, s3, q))));
       }
     }
     // warp reduction in fp32; the 8 warps are summed in fp64 below
@@ -207,7 +214,7 @@ __global__ void convt3d_finalize_kernel(const double* __restrict__ part, const f
 __device__ __forceinline__ float hardswish(float h) { return h * fminf(fmaxf(h + 3.f, 0.f), 6.f) * (1.f / 6.f); }
 
 template <int CIN>
-__global__ void __launch_bounds__(256) convt3d_apply_kernel(const float* __restrict__ x, const float* __restrict__ w,
+__global__ void __launch_bounds__(256, 3) convt3d_apply_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ bias,
                                                             const float2* __restrict__ coef, float* __restrict__ out,
                                                             int D, int H, int W) {
@@ -218,26 +225,31 @@ __global__ void __launch_bounds__(256) convt3d_apply_kernel(const float* __restr
   const int qh = blockIdx.y * kCT_TY + threadIdx.y, qw = blockIdx.x * kCT_TX + threadIdx.x;
   const bool cell_ok = qh < H && qw < W;
   const int OD = 2 * D - 1, OH = 2 * H - 1, OW = 2 * W - 1;
+  const int plane = OD * OH * OW;  // < 2^31 (checked on the host)
   CellInputs<CIN> in;
   load_cell<CIN>(in, x + size_t(n) * CIN * D * H * W, D, H, W, qd, qh, qw);
   const uint32_t pm = cell_ok ? phase_mask(qd, qh, qw, D, H, W) : 0u;
+  // in-plane offsets of the cell's 8 outputs (clamped for cells outside the
+  // grid, whose outputs are masked off anyway)
+  const int cell_off = (2 * qd * OH + 2 * min(qh, H - 1)) * OW + 2 * min(qw, W - 1);
+  int poff[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) poff[p] = cell_off + ((p >> 2) * OH + ((p >> 1) & 1)) * OW + (p & 1);
 #pragma unroll 1
   for (int cg = 0; cg < kCT_G; ++cg) {
     const float4 b4 = bias ? __ldg(reinterpret_cast<const float4*>(bias) + cg) : make_float4(0, 0, 0, 0);
-    float acc[4][8];
-    conv_cell<CIN>(in, ws, cg, b4, acc);
+    float2 a01[8], a23[8];
+    conv_cell<CIN>(in, ws, cg, b4, a01, a23);
+    const float4 ab01 = __ldg(reinterpret_cast<const float4*>(coef + size_t(n) * kCT_COUT + cg * 4));
+    const float4 ab23 = __ldg(reinterpret_cast<const float4*>(coef + size_t(n) * kCT_COUT + cg * 4 + 2));
+    float* o0 = out + (size_t(n) * kCT_COUT + cg * 4) * size_t(plane);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int co = cg * 4 + c;
-      const float2 ab = __ldg(coef + size_t(n) * kCT_COUT + co);
-      float* oc = out + (size_t(n) * kCT_COUT + co) * size_t(OD) * OH * OW;
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        if ((pm >> p) & 1u) {
-          const int od = 2 * qd + (p >> 2), oh = 2 * qh + ((p >> 1) & 1), ow = 2 * qw + (p & 1);
-          const float h = fmaf(ab.x, swish(acc[c][p]), ab.y);
-          __stcs(oc + (size_t(od) * OH + oh) * OW + ow, hardswish(h));
-        }
+    for (int p = 0; p < 8; ++p) {
+      if ((pm >> p) & 1u) {
+        __stcs(o0 + poff[p], hardswish(fmaf(ab01.x, swish(a01[p].x), ab01.y)));
+        __stcs(o0 + plane + poff[p], hardswish(fmaf(ab01.z, swish(a01[p].y), ab01.w)));
+        __stcs(o0 + 2 * size_t(plane) + poff[p], hardswish(fmaf(ab23.x, swish(a23[p].x), ab23.y)));
+        __stcs(o0 + 3 * size_t(plane) + poff[p], hardswish(fmaf(ab23.z, swish(a23[p].y), ab23.w)));
       }
     }
   }
@@ -265,6 +277,7 @@ gf_status check_ct_shape(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_
   if (Cin < 1 || Cin > 8 || N < 1 || D < 1 || H < 1 || W < 1) return GF_ERR_SHAPE;
   if (D * N > 65535 || (H + kCT_TY - 1) / kCT_TY > 65535 || W > (int64_t(1) << 20)) return GF_ERR_SHAPE;
   if (D > (1 << 20) || H > (1 << 20)) return GF_ERR_SHAPE;
+  if ((2 * D - 1) * (2 * H - 1) * (2 * W - 1) >= (int64_t(1) << 31)) return GF_ERR_SHAPE;  // 32-bit in-plane offsets
   return GF_OK;
 }
 

@@ -102,14 +102,31 @@ __global__ void __launch_bounds__(256) ln_finalize_kernel(const double* __restri
   }
 }
 
+// Writes the GEMM operand planes of one activation / weight value v at
+// element offset o: 3xTF32 -> fp32 (v, v - tf32_hi(v)) (the tensor core reads
+// v itself as hi); BF16 -> bf16(v); 3xBF16 -> bf16 hi and bf16(v - hi).
+template <int MODE>
+__device__ __forceinline__ void store_planes(void* planes, size_t plane_elems, size_t o, float v) {
+  if constexpr (MODE == GF_MODE_FP32_3XTF32) {
+    float* p = static_cast<float*>(planes);
+    p[o] = v;
+    p[plane_elems + o] = v - tf32_hi(v);
+  } else {
+    __nv_bfloat16* p = static_cast<__nv_bfloat16*>(planes);
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    p[o] = h;
+    if constexpr (MODE == GF_MODE_FP32_3XBF16) p[plane_elems + o] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
 // grid (ceil(L/32), C/32, B), block (32, 8): GELU(LayerNorm(x)) for a 32x32
-// (channel, position) tile, written transposed as hi/lo planes
-// [2][B][L][C].
+// (channel, position) tile, written transposed to [B][L][C] operand planes.
+template <int MODE>
 __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta,
-                                                                  const float2* __restrict__ stats,
-                                                                  float* __restrict__ planes, int C, int L, int B) {
+                                                                  const float2* __restrict__ stats, void* planes,
+                                                                  int C, int L, int B) {
   __shared__ float tile[32][33];
   const int l0 = blockIdx.x * 32, c0 = blockIdx.y * 32, b = blockIdx.z;
   const float2 st = stats[b];
@@ -130,29 +147,19 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int l = l0 + ty + 8 * r, c = c0 + tx;
-    if (l < L) {
-      const float a = tile[tx][ty + 8 * r];
-      const float h = tf32_hi(a);
-      const size_t o = (size_t(b) * L + l) * C + c;
-      planes[o] = h;
-      planes[plane + o] = a - h;
-    }
+    if (l < L) store_planes<MODE>(planes, plane, (size_t(b) * L + l) * C + c, tile[tx][ty + 8 * r]);
   }
 }
 
-// W[co][ci][t] -> planes[2][Cout][ksize * C] with k = t * C + ci.
-__global__ void conv_weight_split_kernel(const float* __restrict__ w, float* __restrict__ planes, int Cout, int C,
-                                         int ksize) {
+// W[co][ci][t] -> planes[Cout][ksize * C] with k = t * C + ci.
+template <int MODE>
+__global__ void conv_weight_split_kernel(const float* __restrict__ w, void* planes, int Cout, int C, int ksize) {
   const int64_t n = int64_t(Cout) * C * ksize;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
     const int t = int(i % ksize);
     const int ci = int((i / ksize) % C);
     const int64_t co = i / (int64_t(ksize) * C);
-    const float v = w[i];
-    const float h = tf32_hi(v);
-    const size_t o = size_t(co) * ksize * C + size_t(t) * C + ci;
-    planes[o] = h;
-    planes[size_t(n) + o] = v - h;
+    store_planes<MODE>(planes, size_t(n), size_t(co) * ksize * C + size_t(t) * C + ci, w[i]);
   }
 }
 
@@ -175,12 +182,24 @@ struct EpiConvResidual {
       float v[64];
       tmem_load64(taddr + uint32_t(g * 64), v);
       const size_t base = (size_t(t.b) * p.C + n0) * size_t(p.L) + size_t(j);
+      if (valid) {
+        // All residual loads of a 32-column half are issued before any store:
+        // out and x may alias as far as the compiler knows, so interleaving
+        // them would serialise one DRAM latency per column.
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        if (valid && n0 + c < p.C) {
-          const size_t idx = base + size_t(c) * p.L;
-          const float bias = p.conv_b ? __ldg(p.conv_b + n0 + c) : 0.f;
-          __stcs(p.out + idx, v[c] + bias + __ldg(p.x + idx));
+        for (int h = 0; h < 2; ++h) {
+          float r[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            r[c] = (n0 + 32 * h + c < p.C) ? __ldcs(p.x + base + size_t(32 * h + c) * p.L) : 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int co = n0 + 32 * h + c;
+            if (co < p.C) {
+              const float bias = p.conv_b ? __ldg(p.conv_b + co) : 0.f;
+              __stcs(p.out + base + size_t(32 * h + c) * p.L, v[32 * h + c] + bias + r[c]);
+            }
+          }
         }
       }
     }
@@ -190,12 +209,19 @@ struct EpiConvResidual {
 namespace {
 constexpr int kBNConv = 256;
 
+bool conv_mode_ok(int32_t mode) {
+  return mode == GF_MODE_FP32_3XTF32 || mode == GF_MODE_BF16 || mode == GF_MODE_FP32_3XBF16;
+}
+
+// bytes per element of all operand planes together
+size_t plane_bytes(int32_t mode) { return mode == GF_MODE_FP32_3XTF32 ? 8 : (mode == GF_MODE_BF16 ? 2 : 4); }
+
 struct ConvWs {
   size_t part, stats, a_planes, w_planes, total;
   int chunks;
 };
 
-ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize) {
+ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   ConvWs w{};
   w.chunks = int((C * L + kLnChunk - 1) / kLnChunk);
   size_t off = 0;
@@ -204,18 +230,60 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize) {
   w.stats = off;
   off += align_up(size_t(B) * sizeof(float2), 256);
   w.a_planes = off;
-  off += align_up(size_t(2) * B * L * C * 4, 256);
+  off += align_up(size_t(B) * L * C * plane_bytes(mode), 256);
   w.w_planes = off;
-  off += align_up(size_t(2) * C * ksize * C * 4, 256);
+  off += align_up(size_t(C) * ksize * C * plane_bytes(mode), 256);
   w.total = off;
   return w;
 }
 
-gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize) {
+gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   if (B < 1 || C < 32 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
-  if (C % 32 || C > 256 || L % 4) return GF_ERR_SHAPE;
+  // a k-block (BK channels of one tap) must not straddle two taps
+  if (C % (mode == GF_MODE_FP32_3XTF32 ? 32 : 64) || C > 256 || L % 4) return GF_ERR_SHAPE;
   if (B > 65535 || L > (int64_t(1) << 30)) return GF_ERR_SHAPE;
   return GF_OK;
+}
+
+template <int MODE>
+void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
+                         const float2* stats, void* a_planes, void* w_planes, int64_t B, int64_t C, int64_t L,
+                         int32_t ksize, const DeviceInfo& dev, cudaStream_t s) {
+  ln_apply_gelu_split_kernel<MODE><<<dim3(unsigned((L + 31) / 32), unsigned(C / 32), unsigned(B)), dim3(32, 8), 0,
+                                     s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L), int(B));
+  const int64_t n = C * C * ksize;
+  const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
+  conv_weight_split_kernel<MODE><<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), ksize);
+}
+
+template <class Op>
+gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const void* w_planes, int64_t B, int64_t C,
+                           int64_t L, int32_t ksize, int32_t dilation, int32_t padding,
+                           const EpiConvResidual::Params& ep, cudaStream_t s) {
+  OperandMaps maps{};
+  const uint64_t da[3] = {uint64_t(C), uint64_t(L), uint64_t(B)};
+  const uint32_t ba[3] = {uint32_t(Op::kBK), uint32_t(kBM), 1};
+  const uint64_t db[2] = {uint64_t(ksize) * C, uint64_t(C)};
+  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(kBNConv)};
+  const size_t a_plane = size_t(B) * L * C * Op::kElem, w_plane = size_t(C) * ksize * C * Op::kElem;
+  for (int p = 0; p < Op::kPlanes; ++p) {
+    gf_status st = make_tmap(&maps.a[p], static_cast<const uint8_t*>(a_planes) + p * a_plane, Op::kElem, 3, da, ba);
+    if (st != GF_OK) return st;
+    st = make_tmap(&maps.b[p], static_cast<const uint8_t*>(w_planes) + p * w_plane, Op::kElem, 2, db, bb);
+    if (st != GF_OK) return st;
+  }
+  ConvSrc src;
+  src.C = int(C);
+  src.pad = padding;
+  src.dil = dilation;
+  src.num_jb = int((L + kBM - 1) / kBM);
+  src.num_nb = int((C + kBNConv - 1) / kBNConv);
+  src.num_kb = int(ksize * C / Op::kBK);
+  src.bn = kBNConv;
+  src.bk = Op::kBK;
+  src.nsamples = int(B);
+  const int64_t tiles = int64_t(B) * src.num_jb * src.num_nb;
+  return launch_gemm<kBNConv, Op, ConvSrc, EpiConvResidual>(dev, maps, src, tiles, ep, s);
 }
 }  // namespace
 }  // namespace gf
@@ -225,8 +293,8 @@ using namespace gf;
 extern "C" {
 
 size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t mode) {
-  if (mode != GF_MODE_FP32_3XTF32 || check_conv_shape(B, C, L, ksize) != GF_OK) return 0;
-  return conv_ws(B, C, L, ksize).total;
+  if (!conv_mode_ok(mode) || check_conv_shape(B, C, L, ksize, mode) != GF_OK) return 0;
+  return conv_ws(B, C, L, ksize, mode).total;
 }
 
 gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
@@ -234,8 +302,8 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
                                  int32_t dilation, int32_t padding, float eps, int32_t mode, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   if (!x || !ln_gamma || !ln_beta || !conv_w || !out) return GF_ERR_NULL;
-  if (mode != GF_MODE_FP32_3XTF32) return GF_ERR_MODE;
-  gf_status st = check_conv_shape(B, C, L, ksize);
+  if (!conv_mode_ok(mode)) return GF_ERR_MODE;
+  gf_status st = check_conv_shape(B, C, L, ksize, mode);
   if (st != GF_OK) return st;
   if (dilation < 1 || padding < 0 || int64_t(2) * padding != int64_t(dilation) * (ksize - 1)) return GF_ERR_SHAPE;
   if (int64_t(dilation) * (ksize - 1) > (int64_t(1) << 30)) return GF_ERR_SHAPE;
@@ -243,7 +311,7 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   if (!aligned16(x) || !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(conv_w) || !aligned16(out) ||
       (conv_b && !aligned16(conv_b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
-  const ConvWs wl = conv_ws(B, C, L, ksize);
+  const ConvWs wl = conv_ws(B, C, L, ksize, mode);
   if (!workspace) return GF_ERR_NULL;
   if (workspace_bytes < wl.total) return GF_ERR_WORKSPACE;
   const size_t xb = size_t(B) * C * L * 4;
@@ -263,47 +331,34 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   double* part = reinterpret_cast<double*>(ws + wl.part);
   float2* stats = reinterpret_cast<float2*>(ws + wl.stats);
-  float* a_planes = reinterpret_cast<float*>(ws + wl.a_planes);
-  float* w_planes = reinterpret_cast<float*>(ws + wl.w_planes);
+  void* a_planes = ws + wl.a_planes;
+  void* w_planes = ws + wl.w_planes;
 
   ln_partial_kernel<<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
   ln_finalize_kernel<<<unsigned(B), 256, 0, s>>>(part, stats, wl.chunks, eps);
-  ln_apply_gelu_split_kernel<<<dim3(unsigned((L + 31) / 32), unsigned(C / 32), unsigned(B)), dim3(32, 8), 0, s>>>(
-      x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L), int(B));
-  {
-    const int64_t n = C * C * ksize;
-    const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
-    conv_weight_split_kernel<<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), ksize);
+  switch (mode) {
+    case GF_MODE_FP32_3XTF32:
+      launch_conv_prepass<GF_MODE_FP32_3XTF32>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,
+                                               ksize, dev, s);
+      break;
+    case GF_MODE_BF16:
+      launch_conv_prepass<GF_MODE_BF16>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L, ksize, dev,
+                                        s);
+      break;
+    default:
+      launch_conv_prepass<GF_MODE_FP32_3XBF16>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,
+                                               ksize, dev, s);
   }
   if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
-
-  using Cfg = TileCfg<kBNConv>;
-  CUtensorMap ta, tb;
-  const uint64_t da[4] = {uint64_t(C), uint64_t(L), uint64_t(B), 2};
-  const uint32_t ba[4] = {kBK, kBM, 1, 1};
-  const uint64_t db[3] = {uint64_t(ksize) * C, uint64_t(C), 2};
-  const uint32_t bb[3] = {kBK, kBNConv, 1};
-  if ((st = make_tmap_f32(&ta, a_planes, 4, da, ba)) != GF_OK) return st;
-  if ((st = make_tmap_f32(&tb, w_planes, 3, db, bb)) != GF_OK) return st;
-  ConvSrc src;
-  src.C = int(C);
-  src.pad = padding;
-  src.dil = dilation;
-  src.num_jb = int((L + kBM - 1) / kBM);
-  src.num_nb = int((C + kBNConv - 1) / kBNConv);
-  src.num_kb = int(ksize * C / kBK);
-  src.bn = kBNConv;
-  src.nsamples = int(B);
-  const int64_t tiles = int64_t(B) * src.num_jb * src.num_nb;
-  const int grid = int(tiles < dev.sm_count ? tiles : dev.sm_count);
   EpiConvResidual::Params ep{conv_b, x, out, int(C), int(L)};
-  auto kern = gemm3xtf32_kernel<kBNConv, ConvSrc, EpiConvResidual>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
-    return GF_ERR_CUDA;
-  profile_mark_begin(s);
-  kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, s>>>(ta, tb, src, ep, device_status_word());
-  profile_mark_end(s);
-  return cuda_status(cudaGetLastError());
+  switch (mode) {
+    case GF_MODE_FP32_3XTF32:
+      return launch_conv_gemm<OpTF32x3>(dev, a_planes, w_planes, B, C, L, ksize, dilation, padding, ep, s);
+    case GF_MODE_BF16:
+      return launch_conv_gemm<OpBF16x1>(dev, a_planes, w_planes, B, C, L, ksize, dilation, padding, ep, s);
+    default:
+      return launch_conv_gemm<OpBF16x3>(dev, a_planes, w_planes, B, C, L, ksize, dilation, padding, ep, s);
+  }
 }
 
 }  // extern "C"

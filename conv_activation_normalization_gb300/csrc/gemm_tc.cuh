@@ -1,25 +1,34 @@
-// Persistent, warp-specialised tcgen05 GEMM with a 3xTF32 split, whose TMEM
-// accumulator drains straight into a fused epilogue (the big intermediate
-// never goes to HBM).
+// Persistent, warp-specialised tcgen05 GEMM whose TMEM accumulator drains
+// straight into a fused epilogue (the big intermediate never goes to HBM).
 //
-//   D[128 x BN] = sum_k  A_lo*B_hi + A_hi*B_lo + A_hi*B_hi     (fp32 accumulate)
-//
-// A and B arrive as hi/lo planes (hi = the fp32 value with its low 13
-// mantissa bits cleared, i.e. exactly a TF32 number; lo = value - hi, exact in
-// fp32), so each product of the split drops only the lo*lo term and the
-// rounding of lo to TF32: about 2^-21 relative per product, against 2^-11 for a
-// single TF32 product.
+// The contraction runs in one of three operand modes (MmaOp):
+//   OpTF32x3  D = sum_k A_lo*B_hi + A_hi*B_lo + A_hi*B_hi, kind::tf32.
+//             "hi" is the raw fp32 tensor itself: the tensor core reads only
+//             the top 10 mantissa bits of an fp32 operand (it truncates), so
+//             raw x acts exactly as hi = x with its 13 low mantissa bits
+//             cleared; "lo" = x - hi (exact in fp32) is a plane written by a
+//             pre-pass.  Each product drops only lo*lo and the rounding of lo
+//             to TF32: about 2^-21 relative, against 2^-11 for one TF32
+//             product.
+//   OpBF16x3  the same three products with BF16 planes hi = bf16(x),
+//             lo = bf16(x - hi), kind::f16 (twice the TF32 rate): about
+//             2^-16 relative per product.
+//   OpBF16x1  one BF16 product (the BF16 mode).
+// All modes accumulate in fp32 in TMEM.
 //
 // Roles (one CTA per SM, 192 threads):
-//   warp 0      one thread issues TMA loads of the four operand tiles of a
-//               k-block into a ring of smem stages (full/empty mbarriers);
+//   warp 0      one thread issues TMA loads of a k-block's operand tiles (one
+//               or two planes of A and of B) into a ring of smem stages
+//               (full/empty mbarriers);
 //   warp 1      owns the TMEM allocation; one thread issues tcgen05.mma into
-//               one of two TMEM accumulators (BN columns each) and commits to
-//               the stage's "empty" barrier and, per tile, to "tmem_full";
+//               one of two TMEM accumulators (BN columns each), commits to the
+//               stage's "empty" barrier and, per tile, to "tmem_full";
 //   warps 2..5  the epilogue: each thread owns one accumulator row (TMEM lane),
-//               reads it with tcgen05.ld and runs the fused epilogue, then
-//               frees the accumulator ("tmem_empty") for the tile after next.
+//               reads it with tcgen05.ld, runs the fused epilogue, then frees
+//               the accumulator ("tmem_empty") for the tile after next.
 // The two accumulators let tile i's epilogue overlap tile i+1's mainloop.
+// Every smem row is 128 bytes (32 fp32 or 64 bf16 along K) with 128-byte
+// swizzle, so one MMA K-step is always 32 bytes of the row.
 //
 // The operand source (a plain [rows, K] matrix, or the implicit-GEMM view of
 // a dilated Conv1d) and the epilogue are template policies.
@@ -27,30 +36,63 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
+#include "host_common.h"
 #include "ptx.cuh"
 
 namespace gf {
 
-constexpr int kBM = 128;        // tile rows = TMEM lanes
-constexpr int kBK = 32;         // fp32 per k-block = one 128-byte swizzle row
+constexpr int kBM = 128;  // tile rows = TMEM lanes
 constexpr int kGemmThreads = 192;
 constexpr int kEpiThreads = 128;
 
-template <int BN>
+enum class MmaKind { TF32, BF16 };
+
+template <MmaKind K, int NPROD>
+struct MmaOp {
+  static constexpr MmaKind kind = K;
+  static constexpr int kElem = K == MmaKind::TF32 ? 4 : 2;  // bytes per element
+  static constexpr int kBK = 128 / kElem;                    // K elements per k-block
+  static constexpr int kProducts = NPROD;
+  static constexpr int kPlanes = NPROD == 3 ? 2 : 1;         // hi (+ lo) per operand
+  static_assert(NPROD == 1 || NPROD == 3, "one product or the three-term split");
+  template <int BN>
+  __host__ __device__ static constexpr uint32_t idesc() {
+    return K == MmaKind::TF32 ? idesc_tf32(kBM, BN) : idesc_bf16(kBM, BN);
+  }
+  __device__ __forceinline__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (K == MmaKind::TF32)
+      mma_tf32(d, a, b, idesc, acc);
+    else
+      mma_bf16(d, a, b, idesc, acc);
+  }
+};
+using OpTF32x3 = MmaOp<MmaKind::TF32, 3>;
+using OpBF16x3 = MmaOp<MmaKind::BF16, 3>;
+using OpBF16x1 = MmaOp<MmaKind::BF16, 1>;
+
+template <int BN, class Op>
 struct TileCfg {
-  static constexpr int A_BYTES = kBM * kBK * 4;
-  static constexpr int B_BYTES = BN * kBK * 4;
-  static constexpr int STAGE_BYTES = 2 * (A_BYTES + B_BYTES);
-  static constexpr int STAGES = (208 * 1024) / STAGE_BYTES;
+  static constexpr int A_BYTES = kBM * 128;  // one plane of a 128-row tile
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = Op::kPlanes * (A_BYTES + B_BYTES);
+  static constexpr int STAGES_FIT = (208 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
   static_assert(STAGES >= 2, "need at least two smem stages");
-  static_assert(TMEM_COLS == 32 || TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 ||
-                    TMEM_COLS == 512,
+  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
                 "TMEM allocation must be a power of two >= 32 columns");
-  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128 or 256");
+};
+
+// TMA descriptors of the operand planes: a[0]/b[0] = hi (or the only
+// operand), a[1]/b[1] = lo (three-product modes).
+struct OperandMaps {
+  CUtensorMap a[2];
+  CUtensorMap b[2];
 };
 
 // One output tile: rows r0..r0+127 of sample b (b = 0 for a plain GEMM),
@@ -59,10 +101,9 @@ struct Tile {
   int b, r0, n0, nb;
 };
 
-// A = planes[2][M][K], B = planes[2][N][K]; tensor maps are 3-D
-// {K, rows, plane} with a {32, rows-per-tile, 1} box and 128-byte swizzle.
+// A = [M][K] planes (2-D maps {K, M}, box {BK, 128}), B = [N][K] planes.
 struct LinearSrc {
-  int num_mb, num_nb, num_kb, bn;
+  int num_mb, num_nb, num_kb, bn, bk;
   int m_fastest;  // tile order: consecutive tiles share an n-block (1) or an m-block (0)
   __device__ __forceinline__ int num_tiles() const { return num_mb * num_nb; }
   __device__ __forceinline__ Tile tile(int t) const {
@@ -76,27 +117,28 @@ struct LinearSrc {
     }
     return Tile{0, mb * kBM, nb * bn, nb};
   }
-  __device__ __forceinline__ void load(const CUtensorMap* ta, const CUtensorMap* tb, uint64_t* bar,
-                                       uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+  template <int PLANES>
+  __device__ __forceinline__ void load(const OperandMaps& m, uint64_t* bar, const uint32_t* sa, const uint32_t* sb,
                                        const Tile& t, int kb) const {
-    const int k0 = kb * kBK;
-    tma_load_3d(a_hi, ta, bar, k0, t.r0, 0);
-    tma_load_3d(a_lo, ta, bar, k0, t.r0, 1);
-    tma_load_3d(b_hi, tb, bar, k0, t.n0, 0);
-    tma_load_3d(b_lo, tb, bar, k0, t.n0, 1);
+    const int k0 = kb * bk;
+#pragma unroll
+    for (int p = 0; p < PLANES; ++p) {
+      tma_load_2d(sa[p], &m.a[p], bar, k0, t.r0);
+      tma_load_2d(sb[p], &m.b[p], bar, k0, t.n0);
+    }
   }
 };
 
 // Implicit GEMM of a stride-1 dilated Conv1d.  Rows are output positions j of
 // one sample, columns are output channels, and the reduction index is
-// k = tap * C + ci.  A = activation planes[2][B][L][C] (4-D map {C, L, B,
-// plane}, box {32, 128, 1, 1}); the k-block (tap, ci0..ci0+31) of tile rows
-// j0..j0+127 is the box at l = j0 - pad + tap * dil: rows outside [0, L) come
-// back as zeros from the TMA unit, which is exactly the conv's zero padding.
-// B = weight planes[2][Cout][ksize * C] (3-D map).
+// k = tap * C + ci.  A = activation planes [B][L][C] (3-D maps {C, L, B}, box
+// {BK, 128, 1}); the k-block (tap, ci0..ci0+BK-1) of tile rows j0..j0+127 is
+// the box at l = j0 - pad + tap * dil: rows outside [0, L) come back as zeros
+// from the TMA unit, which is exactly the conv's zero padding.  B = weight
+// planes [Cout][ksize * C] (2-D maps).
 struct ConvSrc {
   int C, pad, dil;
-  int num_jb, num_nb, num_kb, bn, nsamples;
+  int num_jb, num_nb, num_kb, bn, bk, nsamples;
   __device__ __forceinline__ int num_tiles() const { return nsamples * num_jb * num_nb; }
   __device__ __forceinline__ Tile tile(int t) const {
     const int nb = t % num_nb;
@@ -105,26 +147,28 @@ struct ConvSrc {
     const int b = r / num_jb;
     return Tile{b, jb * kBM, nb * bn, nb};
   }
-  __device__ __forceinline__ void load(const CUtensorMap* ta, const CUtensorMap* tb, uint64_t* bar,
-                                       uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+  template <int PLANES>
+  __device__ __forceinline__ void load(const OperandMaps& m, uint64_t* bar, const uint32_t* sa, const uint32_t* sb,
                                        const Tile& t, int kb) const {
-    const int k0 = kb * kBK;
+    const int k0 = kb * bk;
     const int tap = k0 / C;
     const int ci0 = k0 - tap * C;
     const int l = t.r0 - pad + tap * dil;
-    tma_load_4d(a_hi, ta, bar, ci0, l, t.b, 0);
-    tma_load_4d(a_lo, ta, bar, ci0, l, t.b, 1);
-    tma_load_3d(b_hi, tb, bar, k0, t.n0, 0);
-    tma_load_3d(b_lo, tb, bar, k0, t.n0, 1);
+#pragma unroll
+    for (int p = 0; p < PLANES; ++p) {
+      tma_load_3d(sa[p], &m.a[p], bar, ci0, l, t.b);
+      tma_load_2d(sb[p], &m.b[p], bar, k0, t.n0);
+    }
   }
 };
 
-template <int BN, class Src, class Epi>
+template <int BN, class Op, class Src, class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm3xtf32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const Src src, const typename Epi::Params ep, uint32_t* status) {
-  using Cfg = TileCfg<BN>;
+    gemm_tc_kernel(const __grid_constant__ OperandMaps maps, const Src src, const typename Epi::Params ep,
+                   uint32_t* status) {
+  using Cfg = TileCfg<BN, Op>;
   constexpr int S = Cfg::STAGES;
+  constexpr int P = Op::kPlanes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::STAGE_BYTES);
@@ -152,8 +196,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
+    for (int p = 0; p < P; ++p) {
+      prefetch_tmap(&maps.a[p]);
+      prefetch_tmap(&maps.b[p]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -164,6 +210,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = src.num_tiles();
+
+  // smem address of plane p of A / B in stage s
+  auto a_addr = [&](int s, int p) { return smem_u32(smem + s * Cfg::STAGE_BYTES + p * Cfg::A_BYTES); };
+  auto b_addr = [&](int s, int p) {
+    return smem_u32(smem + s * Cfg::STAGE_BYTES + P * Cfg::A_BYTES + p * Cfg::B_BYTES);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -178,10 +230,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             *abort_flag = 1;
             break;
           }
-          const uint32_t base = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+          uint32_t sa[2], sb[2];
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            sa[p] = a_addr(stage, p);
+            sb[p] = b_addr(stage, p);
+          }
           mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-          src.load(&tmA, &tmB, &full[stage], base, base + Cfg::A_BYTES, base + 2 * Cfg::A_BYTES,
-                   base + 2 * Cfg::A_BYTES + Cfg::B_BYTES, tile, kb);
+          src.template load<P>(maps, &full[stage], sa, sb, tile, kb);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -199,7 +255,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(kBM, BN);
+      constexpr uint32_t idesc = Op::template idesc<BN>();
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -216,16 +272,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t base = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-          const uint32_t a_hi = base, a_lo = base + Cfg::A_BYTES;
-          const uint32_t b_hi = base + 2 * Cfg::A_BYTES, b_lo = b_hi + Cfg::B_BYTES;
+          const uint32_t a_hi = a_addr(stage, 0), b_hi = b_addr(stage, 0);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 8; ++kk) {
-            const uint32_t off = uint32_t(kk * 32);  // 8 tf32 = 32 bytes along K
-            mma_tf32(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc,
-                     (kb | kk) != 0);
-            mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
-            mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t off = uint32_t(kk * 32);  // one MMA K-step = 32 bytes of the row
+            const uint32_t first = (kb | kk) != 0;
+            if constexpr (Op::kProducts == 3) {
+              const uint32_t a_lo = a_addr(stage, 1), b_lo = b_addr(stage, 1);
+              Op::mma(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, first);
+              Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
+              Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+            } else {
+              Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, first);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == S) {
@@ -284,6 +343,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
+}
+
+// Host: launch the persistent kernel, one CTA per SM (or per tile when there
+// are fewer tiles), on the caller's stream, with the dominant-kernel
+// profiling marks around it.
+template <int BN, class Op, class Src, class Epi>
+gf_status launch_gemm(const DeviceInfo& dev, const OperandMaps& maps, const Src& src, int64_t tiles,
+                      const typename Epi::Params& ep, cudaStream_t stream) {
+  using Cfg = TileCfg<BN, Op>;
+  const int grid = int(tiles < dev.sm_count ? tiles : dev.sm_count);
+  auto kern = gemm_tc_kernel<BN, Op, Src, Epi>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+    return GF_ERR_CUDA;
+  profile_mark_begin(stream);
+  kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, stream>>>(maps, src, ep, device_status_word());
+  profile_mark_end(stream);
+  return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
 }
 
 }  // namespace gf

@@ -46,11 +46,12 @@ uint32_t* device_status_word();
 gf_status cuda_status(cudaError_t e);
 
 // TMA ---------------------------------------------------------------------
-// Tiled fp32 tensor map with 128-byte swizzle, zero fill out of bounds.
-// dims[0] is the contiguous dimension; strides are derived from a dense
-// layout.  box[0] * 4 must be 128.
-gf_status make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                        const uint32_t* box);
+// Tiled tensor map of fp32 (elem_bytes 4) or bf16 (elem_bytes 2) data with
+// 128-byte swizzle and zero fill out of bounds.  dims[0] is the contiguous
+// dimension; strides are derived from a dense layout; box[0] * elem_bytes
+// must be 128.
+gf_status make_tmap(CUtensorMap* map, const void* base, int elem_bytes, int rank, const uint64_t* dims,
+                    const uint32_t* box);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/gf.h"
@@ -36,6 +37,63 @@ static __global__ void split_tf32_kernel(const float4* __restrict__ src, float4*
     hi[i] = h;
     lo[i] = l;
   }
+}
+
+// lo = v - tf32_hi(v) only (the tensor core reads the raw value as hi).
+static __global__ void split_lo_tf32_kernel(const float4* __restrict__ src, float4* __restrict__ lo, size_t n4) {
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x) {
+    const float4 v = __ldcs(src + i);
+    lo[i] = make_float4(v.x - tf32_hi(v.x), v.y - tf32_hi(v.y), v.z - tf32_hi(v.z), v.w - tf32_hi(v.w));
+  }
+}
+
+// BF16 split: hi = bf16(v) (round to nearest even), lo = bf16(v - hi); with
+// lo == nullptr only hi is written.
+struct Bf16x4 {
+  __nv_bfloat162 a, b;
+};
+__device__ __forceinline__ void bf16_split4(float4 v, Bf16x4& h, Bf16x4& l) {
+  h.a = __floats2bfloat162_rn(v.x, v.y);
+  h.b = __floats2bfloat162_rn(v.z, v.w);
+  const float2 ha = __bfloat1622float2(h.a), hb = __bfloat1622float2(h.b);
+  l.a = __floats2bfloat162_rn(v.x - ha.x, v.y - ha.y);
+  l.b = __floats2bfloat162_rn(v.z - hb.x, v.w - hb.y);
+}
+
+static __global__ void split_bf16_kernel(const float4* __restrict__ src, Bf16x4* __restrict__ hi,
+                                         Bf16x4* __restrict__ lo, size_t n4) {
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += size_t(gridDim.x) * blockDim.x) {
+    Bf16x4 h, l;
+    bf16_split4(__ldcs(src + i), h, l);
+    hi[i] = h;
+    if (lo) lo[i] = l;
+  }
+}
+
+static inline int split_blocks(size_t n4, int sm_count) {
+  const size_t blocks = (n4 + 255) / 256;
+  const size_t cap = size_t(sm_count) * 8;
+  return int(blocks > cap ? cap : blocks);
+}
+
+// n must be a multiple of 4; src and the fp32 planes 16-byte aligned, the
+// bf16 planes 8-byte aligned.
+static inline gf_status launch_split_lo_tf32(const float* src, float* lo, size_t n, int sm_count,
+                                             cudaStream_t stream) {
+  const size_t n4 = n / 4;
+  if (n4 == 0) return GF_OK;
+  split_lo_tf32_kernel<<<split_blocks(n4, sm_count), 256, 0, stream>>>(reinterpret_cast<const float4*>(src),
+                                                                       reinterpret_cast<float4*>(lo), n4);
+  return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
+}
+
+static inline gf_status launch_split_bf16(const float* src, void* hi, void* lo, size_t n, int sm_count,
+                                          cudaStream_t stream) {
+  const size_t n4 = n / 4;
+  if (n4 == 0) return GF_OK;
+  split_bf16_kernel<<<split_blocks(n4, sm_count), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(src), static_cast<Bf16x4*>(hi), static_cast<Bf16x4*>(lo), n4);
+  return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
 }
 
 // n must be a multiple of 4 and all pointers 16-byte aligned.

@@ -172,51 +172,106 @@ namespace {
 
 constexpr int kBNLinear = 256;
 
-size_t planes_bytes(int64_t rows, int64_t K) { return align_up(size_t(2) * size_t(rows) * size_t(K) * 4, 256); }
+bool mode_ok(int32_t mode) {
+  return mode == GF_MODE_FP32_3XTF32 || mode == GF_MODE_BF16 || mode == GF_MODE_FP32_3XBF16;
+}
 
-gf_status check_linear_shape(int64_t M, int64_t K, int64_t N) {
+// Bytes of one operand's pre-pass planes in the workspace: the lo plane
+// (3xTF32: hi is the raw tensor), bf16 hi (BF16) or bf16 hi + lo (3xBF16).
+size_t operand_ws_bytes(int64_t rows, int64_t K, int32_t mode) {
+  const size_t n = size_t(rows) * size_t(K);
+  switch (mode) {
+    case GF_MODE_FP32_3XTF32: return align_up(n * 4, 256);
+    case GF_MODE_BF16: return align_up(n * 2, 256);
+    default: return align_up(n * 4, 256);  // two bf16 planes
+  }
+}
+
+gf_status check_linear_shape(int64_t M, int64_t K, int64_t N, int32_t mode) {
   if (M < 1 || K < 4 || N < 1) return GF_ERR_SHAPE;
-  if (K % 4) return GF_ERR_SHAPE;                        // TMA row stride must be 16-byte aligned
+  // TMA row strides must be multiples of 16 bytes: K % 4 for fp32 rows,
+  // K % 8 for the bf16 planes.
+  if (K % (mode == GF_MODE_FP32_3XTF32 ? 4 : 8)) return GF_ERR_SHAPE;
   if (M > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 64)
-    return GF_ERR_SHAPE;                                 // TMA coordinates are int32
+    return GF_ERR_SHAPE;  // TMA coordinates are int32
   return GF_OK;
 }
 
-template <class Epi>
-gf_status launch_linear_gemm(const DeviceInfo& dev, const float* a_planes, const float* b_planes, int64_t M,
-                             int64_t K, int64_t N, int m_fastest, const typename Epi::Params& ep,
-                             cudaStream_t stream) {
-  using Cfg = TileCfg<kBNLinear>;
-  CUtensorMap ta, tb;
-  const uint64_t da[3] = {uint64_t(K), uint64_t(M), 2};
-  const uint32_t ba[3] = {kBK, kBM, 1};
-  const uint64_t db[3] = {uint64_t(K), uint64_t(N), 2};
-  const uint32_t bb[3] = {kBK, kBNLinear, 1};
-  gf_status st = make_tmap_f32(&ta, a_planes, 3, da, ba);
-  if (st != GF_OK) return st;
-  st = make_tmap_f32(&tb, b_planes, 3, db, bb);
-  if (st != GF_OK) return st;
+// Planes the GEMM reads for one operand: p[0] = hi (or the only operand),
+// p[1] = lo.
+struct Planes {
+  const void* p[2];
+};
+
+// Run the split pre-pass of one operand into `ws` and return its planes.
+gf_status prepare_operand(const float* src, int64_t rows, int64_t K, int32_t mode, void* ws, const DeviceInfo& dev,
+                          cudaStream_t s, Planes* out) {
+  const size_t n = size_t(rows) * size_t(K);
+  switch (mode) {
+    case GF_MODE_FP32_3XTF32:
+      out->p[0] = src;
+      out->p[1] = ws;
+      return launch_split_lo_tf32(src, static_cast<float*>(ws), n, dev.sm_count, s);
+    case GF_MODE_BF16:
+      out->p[0] = ws;
+      out->p[1] = nullptr;
+      return launch_split_bf16(src, ws, nullptr, n, dev.sm_count, s);
+    default: {
+      void* lo = static_cast<uint8_t*>(ws) + n * 2;
+      out->p[0] = ws;
+      out->p[1] = lo;
+      return launch_split_bf16(src, ws, lo, n, dev.sm_count, s);
+    }
+  }
+}
+
+template <class Op, class Epi>
+gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K, int64_t N,
+                          int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
+  OperandMaps maps{};
+  const uint64_t da[2] = {uint64_t(K), uint64_t(M)};
+  const uint32_t ba[2] = {uint32_t(Op::kBK), uint32_t(kBM)};
+  const uint64_t db[2] = {uint64_t(K), uint64_t(N)};
+  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(kBNLinear)};
+  for (int p = 0; p < Op::kPlanes; ++p) {
+    gf_status st = make_tmap(&maps.a[p], a.p[p], Op::kElem, 2, da, ba);
+    if (st != GF_OK) return st;
+    st = make_tmap(&maps.b[p], b.p[p], Op::kElem, 2, db, bb);
+    if (st != GF_OK) return st;
+  }
   LinearSrc src;
   src.num_mb = int((M + kBM - 1) / kBM);
   src.num_nb = int((N + kBNLinear - 1) / kBNLinear);
-  src.num_kb = int((K + kBK - 1) / kBK);
+  src.num_kb = int((K + Op::kBK - 1) / Op::kBK);
   src.bn = kBNLinear;
+  src.bk = Op::kBK;
   src.m_fastest = m_fastest;
   const int64_t tiles = int64_t(src.num_mb) * src.num_nb;
-  const int grid = int(tiles < dev.sm_count ? tiles : dev.sm_count);
-  auto kern = gemm3xtf32_kernel<kBNLinear, LinearSrc, Epi>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
-    return GF_ERR_CUDA;
-  profile_mark_begin(stream);
-  kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, stream>>>(ta, tb, src, ep, device_status_word());
-  profile_mark_end(stream);
-  return cuda_status(cudaGetLastError());
+  return launch_gemm<kBNLinear, Op, LinearSrc, Epi>(dev, maps, src, tiles, ep, stream);
 }
 
-gf_status split_planes(const float* src, float* planes, int64_t rows, int64_t K, const DeviceInfo& dev,
-                       cudaStream_t stream) {
-  const size_t n = size_t(rows) * size_t(K);
-  return launch_split_tf32(src, planes, planes + n, n, dev.sm_count, stream);
+template <class Epi>
+gf_status run_linear(int32_t mode, const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
+                     int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
+  switch (mode) {
+    case GF_MODE_FP32_3XTF32: return run_linear_gemm<OpTF32x3, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    case GF_MODE_BF16: return run_linear_gemm<OpBF16x1, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    default: return run_linear_gemm<OpBF16x3, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+  }
+}
+
+// Split both operands into the workspace, then run the fused GEMM.
+template <class Epi>
+gf_status split_and_run(int32_t mode, const float* x, const float* W, int64_t M, int64_t K, int64_t N, void* ws,
+                        int m_fastest, const typename Epi::Params& ep, cudaStream_t s) {
+  DeviceInfo dev;
+  gf_status st = current_device(&dev);
+  if (st != GF_OK) return st;
+  Planes a, b;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  if ((st = prepare_operand(x, M, K, mode, w8, dev, s, &a)) != GF_OK) return st;
+  if ((st = prepare_operand(W, N, K, mode, w8 + operand_ws_bytes(M, K, mode), dev, s, &b)) != GF_OK) return st;
+  return run_linear<Epi>(mode, dev, a, b, M, K, N, m_fastest, ep, s);
 }
 
 }  // namespace
@@ -229,8 +284,8 @@ extern "C" {
 size_t gf_linear_swish_bias_groupnorm_workspace_size(int64_t M, int64_t K, int64_t N, int32_t groups,
                                                      int32_t mode) {
   (void)groups;
-  if (mode != GF_MODE_FP32_3XTF32 || check_linear_shape(M, K, N) != GF_OK) return 0;
-  return planes_bytes(M, K) + planes_bytes(N, K);
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
+  return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode);
 }
 
 gf_status gf_tf32_split(const float* src, float* planes, int64_t n, void* stream) {
@@ -250,7 +305,7 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
                                                 int64_t M, int64_t K, int64_t N, int32_t groups, float eps,
                                                 void* stream) {
   if (!x_planes || !W_planes || !bias || !gamma || !beta || !out) return GF_ERR_NULL;
-  gf_status st = check_linear_shape(M, K, N);
+  gf_status st = check_linear_shape(M, K, N, GF_MODE_FP32_3XTF32);
   if (st != GF_OK) return st;
   if (groups < 1 || N % groups != 0 || N / groups != 64) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
@@ -263,11 +318,10 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
   if (st != GF_OK) return st;
   DeviceInfo dev;
   if ((st = current_device(&dev)) != GF_OK) return st;
+  const Planes a{{x_planes, x_planes + size_t(M) * K}}, b{{W_planes, W_planes + size_t(N) * K}};
   EpiSwishBiasGN::Params ep{b_lin, bias, gamma, beta, out, int(M), int(N), eps};
-  // n-blocks fastest: the CTAs in flight share a few m-blocks of x, while all
-  // of W (N x K planes) stays resident in L2.
-  return launch_linear_gemm<EpiSwishBiasGN>(dev, x_planes, W_planes, M, K, N, /*m_fastest=*/0, ep,
-                                            static_cast<cudaStream_t>(stream));
+  return run_linear<EpiSwishBiasGN>(GF_MODE_FP32_3XTF32, dev, a, b, M, K, N, /*m_fastest=*/0, ep,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const float* b_lin, const float* bias,
@@ -275,8 +329,8 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
                                          int64_t K, int64_t N, int32_t groups, float eps, int32_t mode,
                                          void* workspace, size_t workspace_bytes, void* stream) {
   if (!x || !W || !bias || !gamma || !beta || !out) return GF_ERR_NULL;
-  if (mode != GF_MODE_FP32_3XTF32) return GF_ERR_MODE;
-  gf_status st = check_linear_shape(M, K, N);
+  if (!mode_ok(mode)) return GF_ERR_MODE;
+  gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
   if (groups < 1 || N % groups != 0 || N / groups != 64) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
@@ -291,29 +345,23 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
                       {workspace, need}};
   st = check_no_alias(Span{out, size_t(M) * N * 4}, ins, 7);
   if (st != GF_OK) return st;
-  DeviceInfo dev;
-  st = current_device(&dev);
-  if (st != GF_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  float* a_planes = static_cast<float*>(workspace);
-  float* b_planes = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + planes_bytes(M, K));
-  if ((st = split_planes(x, a_planes, M, K, dev, s)) != GF_OK) return st;
-  if ((st = split_planes(W, b_planes, N, K, dev, s)) != GF_OK) return st;
-  return gf_linear_swish_bias_groupnorm_planes(a_planes, b_planes, b_lin, bias, gamma, beta, out, M, K, N, groups,
-                                               eps, stream);
+  EpiSwishBiasGN::Params ep{b_lin, bias, gamma, beta, out, int(M), int(N), eps};
+  // n-blocks fastest: the CTAs in flight share a few m-blocks of x, while all
+  // of W stays resident in L2.
+  return split_and_run<EpiSwishBiasGN>(mode, x, W, M, K, N, workspace, /*m_fastest=*/0, ep,
+                                       static_cast<cudaStream_t>(stream));
 }
 
 size_t gf_linear_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {
-  if (mode != GF_MODE_FP32_3XTF32 || check_linear_shape(M, K, N) != GF_OK) return 0;
-  return planes_bytes(M, K) + planes_bytes(N, K);
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
+  return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode);
 }
 
 gf_status gf_linear(const float* x, const float* W, const float* b, float* out, int64_t M, int64_t K, int64_t N,
                     int32_t mode, void* workspace, size_t workspace_bytes, void* stream) {
   if (!x || !W || !out) return GF_ERR_NULL;
-  if (mode != GF_MODE_FP32_3XTF32) return GF_ERR_MODE;
-  gf_status st = check_linear_shape(M, K, N);
+  if (!mode_ok(mode)) return GF_ERR_MODE;
+  gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
   if (!aligned16(x) || !aligned16(W) || !aligned16(out) || (b && !aligned16(b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
@@ -323,30 +371,24 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
   const Span ins[] = {{x, size_t(M) * K * 4}, {W, size_t(N) * K * 4}, {b, size_t(N) * 4}, {workspace, need}};
   st = check_no_alias(Span{out, size_t(M) * N * 4}, ins, 4);
   if (st != GF_OK) return st;
-  DeviceInfo dev;
-  st = current_device(&dev);
-  if (st != GF_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* a_planes = static_cast<float*>(workspace);
-  float* b_planes = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + planes_bytes(M, K));
-  if ((st = split_planes(x, a_planes, M, K, dev, s)) != GF_OK) return st;
-  if ((st = split_planes(W, b_planes, N, K, dev, s)) != GF_OK) return st;
   EpiStore::Params ep{b, out, int(M), int(N)};
-  return launch_linear_gemm<EpiStore>(dev, a_planes, b_planes, M, K, N, /*m_fastest=*/0, ep, s);
+  return split_and_run<EpiStore>(mode, x, W, M, K, N, workspace, /*m_fastest=*/0, ep,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {
-  if (mode != GF_MODE_FP32_3XTF32 || check_linear_shape(M, K, N) != GF_OK) return 0;
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
   const int64_t nb = (N + kBNLinear - 1) / kBNLinear;
-  return planes_bytes(M, K) + planes_bytes(N, K) + align_up(size_t(M) * nb * sizeof(float2), 256);
+  return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode) +
+         align_up(size_t(M) * nb * sizeof(float2), 256);
 }
 
 gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, float* out, int64_t M, int64_t K,
-                            int64_t N, float negative_slope, int32_t mode, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+                            int64_t N, float negative_slope, int32_t mode, void* workspace, size_t workspace_bytes,
+                            void* stream) {
   if (!x || !W || !out) return GF_ERR_NULL;
-  if (mode != GF_MODE_FP32_3XTF32) return GF_ERR_MODE;
-  gf_status st = check_linear_shape(M, K, N);
+  if (!mode_ok(mode)) return GF_ERR_MODE;
+  gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
   if (!std::isfinite(negative_slope)) return GF_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(W) || !aligned16(out) || (b && !aligned16(b)) || !aligned16(workspace))
@@ -357,22 +399,14 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
   const Span ins[] = {{x, size_t(M) * K * 4}, {W, size_t(N) * K * 4}, {b, size_t(N) * 4}, {workspace, need}};
   st = check_no_alias(Span{out, size_t(M) * 4}, ins, 4);
   if (st != GF_OK) return st;
-  DeviceInfo dev;
-  st = current_device(&dev);
-  if (st != GF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* a_planes = reinterpret_cast<float*>(ws);
-  float* b_planes = reinterpret_cast<float*>(ws + planes_bytes(M, K));
-  float2* part = reinterpret_cast<float2*>(ws + planes_bytes(M, K) + planes_bytes(N, K));
+  float2* part = reinterpret_cast<float2*>(ws + operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode));
   const int nb = int((N + kBNLinear - 1) / kBNLinear);
-  if ((st = split_planes(x, a_planes, M, K, dev, s)) != GF_OK) return st;
-  if ((st = split_planes(W, b_planes, N, K, dev, s)) != GF_OK) return st;
   EpiLSEPartial::Params ep{b, part, int(M), int(N), nb};
   // m-blocks fastest: the CTAs in flight share n-blocks, so each W tile is
   // fetched from HBM once and reused by every m-block from L2.
-  if ((st = launch_linear_gemm<EpiLSEPartial>(dev, a_planes, b_planes, M, K, N, /*m_fastest=*/1, ep, s)) != GF_OK)
+  if ((st = split_and_run<EpiLSEPartial>(mode, x, W, M, K, N, workspace, /*m_fastest=*/1, ep, s)) != GF_OK)
     return st;
   const int threads = 256;
   const int blocks = int((M * 32 + threads - 1) / threads);

@@ -26,11 +26,18 @@
  *   - `out` must not overlap any input or the workspace (GF_ERR_ALIAS).
  *   - Device-side errors (a bounded wait inside a kernel that ran out) are
  *     recorded in a device status word; gf_device_status() reads it.
- *   - mode: GF_MODE_FP32_3XTF32 runs the contraction on the tensor cores as
- *     three TF32 products (hi*hi + hi*lo + lo*hi of a hi/lo split of both
- *     operands) with fp32 accumulation and an fp32 epilogue; the result
- *     matches an fp64 evaluation within 1e-4 abs + 1e-4 rel on the pages'
- *     workloads.  GF_MODE_BF16 (reserved) returns GF_ERR_MODE.
+ *   - mode selects how the contraction runs on the tensor cores; every mode
+ *     accumulates in fp32 and runs the epilogue in fp32:
+ *       GF_MODE_FP32_3XTF32  three TF32 products (hi*hi + hi*lo + lo*hi of a
+ *                            hi/lo split of both operands); matches an fp64
+ *                            evaluation within 1e-4 abs + 1e-4 rel on the
+ *                            pages' workloads.  The default.
+ *       GF_MODE_BF16         one BF16 product (operands rounded to bf16);
+ *                            within 3e-2 abs + 3e-2 rel.
+ *       GF_MODE_FP32_3XBF16  three BF16 products of a bf16 hi/lo split, at
+ *                            twice the TF32 tensor rate; within 1e-4 abs +
+ *                            1e-4 rel on the pages' workloads.
+ *     K must be a multiple of 8 (C a multiple of 64) in the BF16 modes.
  */
 #ifndef GF_H_
 #define GF_H_
@@ -57,6 +64,7 @@ typedef int32_t gf_status;
 
 #define GF_MODE_FP32_3XTF32 0
 #define GF_MODE_BF16        1
+#define GF_MODE_FP32_3XBF16 2
 
 /* Version of this ABI (bumped on any signature change). */
 int32_t gf_abi_version(void);
@@ -107,7 +115,8 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
  *
  *   x [M,K], W [N,K] (nn.Linear layout), b_lin/bias/gamma/beta [N], out [M,N].
  *   b_lin may be NULL (no linear bias).
- *   Supported: M >= 1, K >= 4 with K % 4 == 0, N % 64 == 0, N/groups == 64.
+ *   Supported: M >= 1, K >= 4 with K % 4 == 0 (K % 8 == 0 in the BF16 modes),
+ *   N % 64 == 0, N/groups == 64.
  * ---------------------------------------------------------------------- */
 size_t gf_linear_swish_bias_groupnorm_workspace_size(int64_t M, int64_t K, int64_t N,
                                                      int32_t groups, int32_t mode);
@@ -162,7 +171,8 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
  *
  *   x, out [B,C,L]; ln_gamma, ln_beta [C,L]; conv_w [C,C,ksize] (nn.Conv1d
  *   layout, cross-correlation); conv_b [C] (may be NULL).
- *   Supported: C % 32 == 0, C <= 256, L % 4 == 0, ksize >= 1, dilation >= 1,
+ *   Supported: C % 32 == 0 (C % 64 == 0 in the BF16 modes), C <= 256,
+ *   L % 4 == 0, 1 <= ksize <= 16, dilation >= 1,
  *   2*padding == dilation*(ksize-1) (length-preserving, as the residual needs).
  * ---------------------------------------------------------------------- */
 size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize,

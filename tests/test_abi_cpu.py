@@ -50,8 +50,10 @@ def _lgn(L, x=P[0], W=P[1], bl=P[2], bias=P[3], g=P[4], b=P[5], out=P[6], M=256,
 def test_linear_gn_validation(L):
     assert _lgn(L, x=None) == GF_ERR_NULL
     assert _lgn(L, out=None) == GF_ERR_NULL
-    assert _lgn(L, mode=1) == GF_ERR_MODE
-    assert _lgn(L, mode=7) == GF_ERR_MODE
+    assert _lgn(L, mode=3) == GF_ERR_MODE
+    assert _lgn(L, mode=-1) == GF_ERR_MODE
+    assert _lgn(L, K=1020, mode=1) == GF_ERR_SHAPE  # bf16 planes need K % 8
+    assert _lgn(L, K=1020, mode=2) == GF_ERR_SHAPE
     assert _lgn(L, groups=32) == GF_ERR_SHAPE      # group width 128 is not supported
     assert _lgn(L, groups=0) == GF_ERR_SHAPE
     assert _lgn(L, K=1022) == GF_ERR_SHAPE         # K % 4
@@ -70,11 +72,13 @@ def test_linear_gn_validation(L):
 def test_workspace_sizes(L):
     M, K, N = 32768, 1024, 4096
     ws = L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 0)
-    assert ws == 2 * 4 * (M * K + N * K)            # hi/lo planes of x and W
-    assert L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 1) == 0
+    assert ws == 4 * (M * K + N * K)                # fp32 lo planes (the raw operands serve as hi)
+    assert L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 1) == 2 * (M * K + N * K)  # bf16 hi
+    assert L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 2) == 4 * (M * K + N * K)  # bf16 hi+lo
+    assert L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 3) == 0
     assert L.gf_linear_workspace_size(M, K, N, 0) == ws
     M, K, N = 1024, 8192, 8192
-    assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 2 * 4 * (M * K + N * K) + M * (N // 256) * 8
+    assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (N // 256) * 8
     assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0) > 2 * 4 * 32 * 256 * 4096
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 2, 1, 4) > 0
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 1, 1, 4) == 0
@@ -111,7 +115,8 @@ def test_dconv1d_validation(L):
     assert call(C=48) == GF_ERR_SHAPE              # C % 32
     assert call(C=512) == GF_ERR_SHAPE
     assert call(L=4094) == GF_ERR_SHAPE            # L % 4
-    assert call(mode=1) == GF_ERR_MODE
+    assert call(mode=5) == GF_ERR_MODE
+    assert call(C=96, mode=1) == GF_ERR_SHAPE      # bf16 k-blocks are 64 channels
     assert call(w=P[3] + 4) == GF_ERR_ALIGN
     assert call(wsb=5) == GF_ERR_WORKSPACE
     assert call(out=P[0]) == GF_ERR_ALIAS          # in-place residual is rejected
