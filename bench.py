@@ -191,6 +191,13 @@ class LinearGN(Workload):
         gf.gf_linear_swish_bias_groupnorm(t["x"] if x is None else x, t["W"], t["b_lin"], t["bias"], t["gamma"],
                                           t["beta"], s.groups, s.eps, mode=MODES[MODE][0], out=t["out"])
 
+    def host_step(self, gf, t, xh, oh):
+        """The public host-buffer call: chunks copied in, computed and copied
+        out in an overlapped pipeline."""
+        s = self.shape
+        gf.gf_linear_swish_bias_groupnorm_host(xh, t["W"], t["b_lin"], t["bias"], t["gamma"], t["beta"], s.groups,
+                                               s.eps, mode=MODES[MODE][0], out_host=oh)
+
     def oracle_chunk(self, d, i, chunk):
         import oracle
         s = self.shape
@@ -444,9 +451,12 @@ def run_ours(wl, args):
         xd = torch.empty_like(t["x"])
 
         def e2e_step():
-            xd.copy_(xh, non_blocking=True)
-            wl.step(gf, t, x=xd)
-            oh.copy_(t["out"], non_blocking=True)
+            if hasattr(wl, "host_step"):
+                wl.host_step(gf, t, xh, oh)
+            else:
+                xd.copy_(xh, non_blocking=True)
+                wl.step(gf, t, x=xd)
+                oh.copy_(t["out"], non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -465,7 +475,9 @@ def run_ours(wl, args):
             e2e_ms = tt.item()
         e2e = {"value": round(wl.work_per_step() * ws / (e2e_ms * 1e-3) / wl.scale(), 3), "unit": wl.unit,
                "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(oh.numel() * 4),
-               "ms_per_step": round(e2e_ms, 4)}
+               "ms_per_step": round(e2e_ms, 4),
+               "path": ("gf_linear_swish_bias_groupnorm_host (pipelined chunks, pinned host buffers)"
+                        if hasattr(wl, "host_step") else "pinned H2D copy, device call, D2H copy")}
 
     peaks, src = _peaks()
     achieved = wl.kernel_work() / (kern_ms * 1e-3) / wl.scale()

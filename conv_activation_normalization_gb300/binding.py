@@ -42,6 +42,9 @@ _SIGS = {
     "gf_linear_swish_bias_groupnorm_planes": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _F,
                                                      _P]),
     "gf_tf32_split": (_I32, [_P, _P, _I64, _P]),
+    "gf_linear_swish_bias_groupnorm_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32, _I64]),
+    "gf_linear_swish_bias_groupnorm_host": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _F, _I32,
+                                                   _I64, _P, _SZ, _P]),
     "gf_linear_lse_act_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
     "gf_linear_lse_act": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _I32, _P, _SZ, _P]),
     "gf_ln_gelu_dconv1d_res_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
@@ -241,6 +244,31 @@ def gf_linear_swish_bias_groupnorm_planes(x_planes, W_planes, b_lin, bias, gamma
         _call("gf_linear_swish_bias_groupnorm_planes", _ptr(x_planes), _ptr(W_planes), _ptr(b_lin), _ptr(bias),
               _ptr(gamma), _ptr(beta), _ptr(out), M, K, N, groups, eps, _stream_ptr(stream))
     return out
+
+
+def gf_linear_swish_bias_groupnorm_host(x_host, W, b_lin, bias, gamma, beta, groups, eps=1e-5,
+                                        mode=GF_MODE_FP32_3XTF32, out_host=None, chunk_rows=0, workspace=None,
+                                        stream=None):
+    """gf_linear_swish_bias_groupnorm on host tensors: x_host (CPU, float32,
+    ideally pinned) in, out_host (CPU) out; the weights are CUDA tensors.
+    Chunks of rows are copied in, computed and copied out in an overlapped
+    pipeline.  Enqueues and returns; synchronise the stream before reading
+    out_host."""
+    dev = _check(W, b_lin, bias, gamma, beta)
+    for t in (x_host, out_host):
+        if t is not None and (t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError("host tensors must be contiguous float32 CPU tensors")
+    M, K = x_host.shape
+    N = W.shape[0]
+    if out_host is None:
+        out_host = torch.empty((M, N), dtype=torch.float32, pin_memory=x_host.is_pinned())
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_linear_swish_bias_groupnorm_host_workspace_size(M, K, N, groups, mode, chunk_rows)
+        wp, nb = _ws_args(dev, nbytes, workspace)
+        _call("gf_linear_swish_bias_groupnorm_host", x_host.data_ptr(), _ptr(W), _ptr(b_lin), _ptr(bias),
+              _ptr(gamma), _ptr(beta), out_host.data_ptr(), M, K, N, groups, eps, mode, chunk_rows, wp, nb,
+              _stream_ptr(stream))
+    return out_host
 
 
 def gf_linear_lse_act(x, W, b, negative_slope=0.01, mode=GF_MODE_FP32_3XTF32, out=None, workspace=None,

@@ -127,7 +127,7 @@ __device__ __forceinline__ uint32_t phase_mask(int qd, int qh, int qw, int D, in
 // grid (ceil(W/32), ceil(H/8), D * N), block (32, 8).
 // part: [N][G][P][2] doubles, P = blocks per sample.
 template <int CIN>
-__global__ void __launch_bounds__(256, 3) convt3d_stats_kernel(const float* __restrict__ x, const float* __restrict__ w,
+__global__ void __launch_bounds__(256, CIN <= 4 ? 3 : 2) convt3d_stats_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ bias, double* __restrict__ part,
                                                             int D, int H, int W) {
   __shared__ __align__(16) float ws[CIN * 27 * kCT_COUT];
@@ -211,10 +211,15 @@ __global__ void convt3d_finalize_kernel(const double* __restrict__ part, const f
   }
 }
 
-__device__ __forceinline__ float hardswish(float h) { return h * fminf(fmaxf(h + 3.f, 0.f), 6.f) * (1.f / 6.f); }
+// HardSwish h * clamp(h + 3, 0, 6) / 6 written as h * sat(h / 6 + 1/2): one
+// saturating FMA and one multiply.
+__device__ __forceinline__ float hardswish(float h) { return h * __saturatef(fmaf(h, 1.f / 6.f, 0.5f)); }
+
+// GroupNorm affine of Swish: A * swish(y) + B.
+__device__ __forceinline__ float gn_swish(float y, float A, float B) { return fmaf(A, swish(y), B); }
 
 template <int CIN>
-__global__ void __launch_bounds__(256, 3) convt3d_apply_kernel(const float* __restrict__ x, const float* __restrict__ w,
+__global__ void __launch_bounds__(256, CIN <= 4 ? 3 : 2) convt3d_apply_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                             const float* __restrict__ bias,
                                                             const float2* __restrict__ coef, float* __restrict__ out,
                                                             int D, int H, int W) {
@@ -229,12 +234,10 @@ __global__ void __launch_bounds__(256, 3) convt3d_apply_kernel(const float* __re
   CellInputs<CIN> in;
   load_cell<CIN>(in, x + size_t(n) * CIN * D * H * W, D, H, W, qd, qh, qw);
   const uint32_t pm = cell_ok ? phase_mask(qd, qh, qw, D, H, W) : 0u;
-  // in-plane offsets of the cell's 8 outputs (clamped for cells outside the
+  // in-plane offset of the cell's first output (clamped for cells outside the
   // grid, whose outputs are masked off anyway)
   const int cell_off = (2 * qd * OH + 2 * min(qh, H - 1)) * OW + 2 * min(qw, W - 1);
-  int poff[8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p) poff[p] = cell_off + ((p >> 2) * OH + ((p >> 1) & 1)) * OW + (p & 1);
+  const int OHW = OH * OW;
 #pragma unroll 1
   for (int cg = 0; cg < kCT_G; ++cg) {
     const float4 b4 = bias ? __ldg(reinterpret_cast<const float4*>(bias) + cg) : make_float4(0, 0, 0, 0);
@@ -246,10 +249,11 @@ __global__ void __launch_bounds__(256, 3) convt3d_apply_kernel(const float* __re
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       if ((pm >> p) & 1u) {
-        __stcs(o0 + poff[p], hardswish(fmaf(ab01.x, swish(a01[p].x), ab01.y)));
-        __stcs(o0 + plane + poff[p], hardswish(fmaf(ab01.z, swish(a01[p].y), ab01.w)));
-        __stcs(o0 + 2 * size_t(plane) + poff[p], hardswish(fmaf(ab23.x, swish(a23[p].x), ab23.y)));
-        __stcs(o0 + 3 * size_t(plane) + poff[p], hardswish(fmaf(ab23.z, swish(a23[p].y), ab23.w)));
+        const int po = cell_off + (p >> 2) * OHW + ((p >> 1) & 1) * OW + (p & 1);
+        __stcs(o0 + po, hardswish(gn_swish(a01[p].x, ab01.x, ab01.y)));
+        __stcs(o0 + plane + po, hardswish(gn_swish(a01[p].y, ab01.z, ab01.w)));
+        __stcs(o0 + 2 * size_t(plane) + po, hardswish(gn_swish(a23[p].x, ab23.x, ab23.y)));
+        __stcs(o0 + 3 * size_t(plane) + po, hardswish(gn_swish(a23[p].y, ab23.z, ab23.w)));
       }
     }
   }

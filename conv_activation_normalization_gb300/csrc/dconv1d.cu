@@ -1,9 +1,9 @@
 // LayerNorm([C, L]) -> GELU -> dilated Conv1d -> +x   (page Kimi-K2.6__l2_p5)
 //
-//   1. ln_partial:   per (sample, chunk of 8192 elements) partial statistics
-//                    (count, mean, M2): shifted fp32 sums per thread, merged
-//                    in fp64 (Chan's pairwise formula) across the block;
-//   2. ln_finalize:  per sample, fp64 merge of the partials -> (mean, rstd);
+//   1. ln_partial:   per (sample, chunk of 8192 elements) the shifted sums
+//                    S1, S2 about one shift per sample: fp32 per thread and
+//                    warp, fp64 across warps;
+//   2. ln_finalize:  per sample, fp64 sum of the partials -> (mean, rstd);
 //   3. ln_apply:     a = GELU((x - mean) * rstd * gamma + beta), transposed to
 //                    [B][L][C] through shared memory and split into TF32 hi/lo
 //                    planes, the K-major A operand of the implicit GEMM;
@@ -23,82 +23,86 @@ namespace gf {
 
 constexpr int kLnChunk = 8192;  // elements per ln_partial block (256 threads x 32)
 
-struct Moments {
-  double n, mean, m2;
-};
-
-__device__ __forceinline__ Moments chan_merge(Moments a, Moments b) {
-  if (a.n == 0) return b;
-  if (b.n == 0) return a;
-  const double n = a.n + b.n;
-  const double d = b.mean - a.mean;
-  return Moments{n, a.mean + d * (b.n / n), a.m2 + b.m2 + d * d * (a.n * b.n / n)};
-}
-
-// Block-wide fp64 merge of one Moments per thread (blockDim.x == 256).
-__device__ Moments block_merge(Moments m) {
-  __shared__ double sn[256], smean[256], sm2[256];
-  sn[threadIdx.x] = m.n;
-  smean[threadIdx.x] = m.mean;
-  sm2[threadIdx.x] = m.m2;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
-      const Moments r = chan_merge(Moments{sn[threadIdx.x], smean[threadIdx.x], sm2[threadIdx.x]},
-                                   Moments{sn[threadIdx.x + w], smean[threadIdx.x + w], sm2[threadIdx.x + w]});
-      sn[threadIdx.x] = r.n;
-      smean[threadIdx.x] = r.mean;
-      sm2[threadIdx.x] = r.m2;
-    }
-    __syncthreads();
-  }
-  return Moments{sn[0], smean[0], sm2[0]};
+// The statistics of a sample are taken as shifted sums S1 = sum (x - c) and
+// S2 = sum (x - c)^2 about one shift c per sample (the mean of the sample's
+// first 32 values, which every block computes identically).  With a common
+// shift the sums are additive, so they are reduced in fp32 within a thread
+// and a warp and in fp64 across warps and blocks; c near the data keeps
+// var = S2/n - (S1/n)^2 well conditioned.
+__device__ __forceinline__ float sample_shift(const float* __restrict__ xs, int64_t n_per_sample) {
+  const int lane = threadIdx.x & 31;
+  float v = lane < n_per_sample ? __ldg(xs + lane) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v / float(n_per_sample < 32 ? n_per_sample : 32);
 }
 
 // grid (chunks, B), 256 threads.  n_per_sample = C * L (a multiple of 4).
-__global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict__ x, double* __restrict__ part,
+// part[b][chunk] = (S1, S2) of the chunk's elements, in fp64.
+__global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict__ x, double2* __restrict__ part,
                                                          int64_t n_per_sample, int chunks) {
+  __shared__ double2 red[8];
   const int b = blockIdx.y;
   const float* xs = x + size_t(b) * size_t(n_per_sample);
   const int64_t begin = int64_t(blockIdx.x) * kLnChunk;
   const int64_t end = begin + kLnChunk < n_per_sample ? begin + kLnChunk : n_per_sample;
-  const float shift = __ldg(xs);  // any value near the data keeps the shifted sums well conditioned
+  const float shift = sample_shift(xs, n_per_sample);
   float s1 = 0.f, s2 = 0.f;
-  int cnt = 0;
+#pragma unroll 4
   for (int64_t i = begin + 4 * threadIdx.x; i < end; i += 4 * blockDim.x) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(xs + i));
+    const float4 v = __ldcs(reinterpret_cast<const float4*>(xs + i));
     const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
     s1 += (d0 + d1) + (d2 + d3);
-    s2 += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
-    cnt += 4;
+    s2 += fmaf(d0, d0, d1 * d1) + fmaf(d2, d2, d3 * d3);
   }
-  Moments m{0.0, 0.0, 0.0};
-  if (cnt) {
-    const double n = cnt, a = s1, q = s2;
-    m = Moments{n, double(shift) + a / n, fmax(q - a * a / n, 0.0)};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, o);
   }
-  m = block_merge(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_double2(s1, s2);
+  __syncthreads();
   if (threadIdx.x == 0) {
-    double* o = part + (size_t(b) * chunks + blockIdx.x) * 3;
-    o[0] = m.n;
-    o[1] = m.mean;
-    o[2] = m.m2;
+    double a = 0.0, q = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      a += red[w].x;
+      q += red[w].y;
+    }
+    part[size_t(b) * chunks + blockIdx.x] = make_double2(a, q);
   }
 }
 
-// grid B, 256 threads: merge a sample's partials -> (mean, rstd).
-__global__ void __launch_bounds__(256) ln_finalize_kernel(const double* __restrict__ part, float2* __restrict__ stats,
-                                                          int chunks, float eps) {
+// grid B, 256 threads: sum a sample's partials -> (mean, rstd).
+__global__ void __launch_bounds__(256) ln_finalize_kernel(const float* __restrict__ x, const double2* __restrict__ part,
+                                                          float2* __restrict__ stats, int64_t n_per_sample, int chunks,
+                                                          float eps) {
+  __shared__ double2 red[8];
   const int b = blockIdx.x;
-  Moments m{0.0, 0.0, 0.0};
+  double a = 0.0, q = 0.0;
   for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
-    const double* p = part + (size_t(b) * chunks + i) * 3;
-    m = chan_merge(m, Moments{p[0], p[1], p[2]});
+    const double2 p = part[size_t(b) * chunks + i];
+    a += p.x;
+    q += p.y;
   }
-  m = block_merge(m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    q += __shfl_xor_sync(0xffffffffu, q, o);
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_double2(a, q);
+  const float shift = sample_shift(x + size_t(b) * size_t(n_per_sample), n_per_sample);
+  __syncthreads();
   if (threadIdx.x == 0) {
-    const double var = m.m2 / m.n;
-    stats[b] = make_float2(float(m.mean), float(1.0 / sqrt(var + double(eps))));
+    double A = 0.0, Q = 0.0;
+    for (int w = 0; w < 8; ++w) {
+      A += red[w].x;
+      Q += red[w].y;
+    }
+    const double n = double(n_per_sample);
+    const double m = A / n;
+    const double var = fmax(Q / n - m * m, 0.0);
+    stats[b] = make_float2(float(double(shift) + m), float(1.0 / sqrt(var + double(eps))));
   }
 }
 
@@ -165,6 +169,7 @@ __global__ void conv_weight_split_kernel(const float* __restrict__ w, void* plan
 
 // Epilogue: out[b][co][j] = acc + conv_b[co] + x[b][co][j].
 struct EpiConvResidual {
+  static constexpr bool kFixedBN = true;
   struct Params {
     const float* conv_b;  // may be null
     const float* x;
@@ -226,7 +231,7 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   w.chunks = int((C * L + kLnChunk - 1) / kLnChunk);
   size_t off = 0;
   w.part = off;
-  off += align_up(size_t(B) * w.chunks * 3 * sizeof(double), 256);
+  off += align_up(size_t(B) * w.chunks * sizeof(double2), 256);
   w.stats = off;
   off += align_up(size_t(B) * sizeof(float2), 256);
   w.a_planes = off;
@@ -329,13 +334,13 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  double* part = reinterpret_cast<double*>(ws + wl.part);
+  double2* part = reinterpret_cast<double2*>(ws + wl.part);
   float2* stats = reinterpret_cast<float2*>(ws + wl.stats);
   void* a_planes = ws + wl.a_planes;
   void* w_planes = ws + wl.w_planes;
 
   ln_partial_kernel<<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
-  ln_finalize_kernel<<<unsigned(B), 256, 0, s>>>(part, stats, wl.chunks, eps);
+  ln_finalize_kernel<<<unsigned(B), 256, 0, s>>>(x, part, stats, C * L, wl.chunks, eps);
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
       launch_conv_prepass<GF_MODE_FP32_3XTF32>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,

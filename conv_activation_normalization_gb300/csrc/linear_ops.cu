@@ -17,6 +17,7 @@ namespace gf {
 // thread owns one row, a group is 64 consecutive columns, so the group's mean
 // and (two-pass, biased) variance are computed in the thread's registers.
 struct EpiSwishBiasGN {
+  static constexpr bool kFixedBN = false;
   struct Params {
     const float* b_lin;  // may be null
     const float* bias;
@@ -74,6 +75,7 @@ struct EpiSwishBiasGN {
 // Linear -> per-row (max, sum exp(y - max)) over the tile's BN columns,
 // written as one float2 partial per (row, n-block).
 struct EpiLSEPartial {
+  static constexpr bool kFixedBN = true;  // one partial per 256-column block
   struct Params {
     const float* b;  // may be null
     float2* part;    // [M][n_blocks]
@@ -109,6 +111,7 @@ struct EpiLSEPartial {
 
 // Plain Linear: out[m, n] = acc + b[n] (the contraction step alone).
 struct EpiStore {
+  static constexpr bool kFixedBN = false;
   struct Params {
     const float* b;  // may be null
     float* out;
@@ -225,14 +228,14 @@ gf_status prepare_operand(const float* src, int64_t rows, int64_t K, int32_t mod
   }
 }
 
-template <class Op, class Epi>
+template <int BN, class Op, class Epi>
 gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K, int64_t N,
                           int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
   OperandMaps maps{};
   const uint64_t da[2] = {uint64_t(K), uint64_t(M)};
   const uint32_t ba[2] = {uint32_t(Op::kBK), uint32_t(kBM)};
   const uint64_t db[2] = {uint64_t(K), uint64_t(N)};
-  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(kBNLinear)};
+  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(BN)};
   for (int p = 0; p < Op::kPlanes; ++p) {
     gf_status st = make_tmap(&maps.a[p], a.p[p], Op::kElem, 2, da, ba);
     if (st != GF_OK) return st;
@@ -241,22 +244,41 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
   }
   LinearSrc src;
   src.num_mb = int((M + kBM - 1) / kBM);
-  src.num_nb = int((N + kBNLinear - 1) / kBNLinear);
+  src.num_nb = int((N + BN - 1) / BN);
   src.num_kb = int((K + Op::kBK - 1) / Op::kBK);
-  src.bn = kBNLinear;
+  src.bn = BN;
   src.bk = Op::kBK;
   src.m_fastest = m_fastest;
   const int64_t tiles = int64_t(src.num_mb) * src.num_nb;
-  return launch_gemm<kBNLinear, Op, LinearSrc, Epi>(dev, maps, src, tiles, ep, stream);
+  return launch_gemm<BN, Op, LinearSrc, Epi>(dev, maps, src, tiles, ep, stream);
+}
+
+// Tile width: 256 columns when that gives every SM at least one tile;
+// otherwise (small M) 128 or 64, trading per-tile efficiency for parallelism.
+// Epilogues whose output layout depends on the tile width (the LSE partials)
+// always use 256.
+template <class Op, class Epi>
+gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
+                             int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
+  if constexpr (Epi::kFixedBN) {
+    return run_linear_gemm<kBNLinear, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+  } else {
+    const int64_t mb = (M + kBM - 1) / kBM;
+    if (mb * ((N + 255) / 256) >= dev.sm_count)
+      return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    if (mb * ((N + 127) / 128) >= dev.sm_count)
+      return run_linear_gemm<128, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    return run_linear_gemm<64, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+  }
 }
 
 template <class Epi>
 gf_status run_linear(int32_t mode, const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
                      int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
   switch (mode) {
-    case GF_MODE_FP32_3XTF32: return run_linear_gemm<OpTF32x3, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-    case GF_MODE_BF16: return run_linear_gemm<OpBF16x1, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-    default: return run_linear_gemm<OpBF16x3, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    case GF_MODE_FP32_3XTF32: return run_linear_gemm_bn<OpTF32x3, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    case GF_MODE_BF16: return run_linear_gemm_bn<OpBF16x1, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    default: return run_linear_gemm_bn<OpBF16x3, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
   }
 }
 
@@ -350,6 +372,155 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
   // of W stays resident in L2.
   return split_and_run<EpiSwishBiasGN>(mode, x, W, M, K, N, workspace, /*m_fastest=*/0, ep,
                                        static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- host path
+namespace {
+
+// Default rows per chunk: a whole number of waves of 128 x 256 tiles (the
+// m-blocks per chunk times the n-blocks is a multiple of the SM count), at
+// least 4096 rows.
+int64_t host_chunk_rows(int64_t M, int64_t N, int sm_count) {
+  const int64_t nb = (N + kBNLinear - 1) / kBNLinear;
+  int64_t a = sm_count, b = nb;
+  while (b) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  const int64_t wave_mb = sm_count / a;  // m-blocks that fill whole waves
+  int64_t mb = wave_mb;
+  while (mb * kBM < 4096) mb += wave_mb;
+  const int64_t rows = mb * kBM;
+  return rows < M ? rows : M;
+}
+
+struct HostWs {
+  size_t w_planes, x[2], xp[2], out[2], total;
+};
+
+HostWs host_ws(int64_t chunk, int64_t K, int64_t N, int32_t mode) {
+  HostWs w{};
+  size_t off = 0;
+  w.w_planes = off;
+  off += operand_ws_bytes(N, K, mode);
+  for (int i = 0; i < 2; ++i) {
+    w.x[i] = off;
+    off += align_up(size_t(chunk) * K * 4, 256);
+    w.xp[i] = off;
+    off += operand_ws_bytes(chunk, K, mode);
+    w.out[i] = off;
+    off += align_up(size_t(chunk) * N * 4, 256);
+  }
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+size_t gf_linear_swish_bias_groupnorm_host_workspace_size(int64_t M, int64_t K, int64_t N, int32_t groups,
+                                                          int32_t mode, int64_t chunk_rows) {
+  (void)groups;
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || chunk_rows < 0) return 0;
+  if (chunk_rows == 0) {
+    DeviceInfo dev;
+    if (current_device(&dev) != GF_OK) return 0;
+    chunk_rows = host_chunk_rows(M, N, dev.sm_count);
+  }
+  return host_ws(chunk_rows < M ? chunk_rows : M, K, N, mode).total;
+}
+
+gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* W, const float* b_lin,
+                                              const float* bias, const float* gamma, const float* beta,
+                                              float* out_host, int64_t M, int64_t K, int64_t N, int32_t groups,
+                                              float eps, int32_t mode, int64_t chunk_rows, void* workspace,
+                                              size_t workspace_bytes, void* stream) {
+  if (!x_host || !W || !bias || !gamma || !beta || !out_host) return GF_ERR_NULL;
+  if (!mode_ok(mode)) return GF_ERR_MODE;
+  gf_status st = check_linear_shape(M, K, N, mode);
+  if (st != GF_OK) return st;
+  if (groups < 1 || N % groups != 0 || N / groups != 64 || chunk_rows < 0) return GF_ERR_SHAPE;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
+      (b_lin && !aligned16(b_lin)) || !aligned16(workspace))
+    return GF_ERR_ALIGN;
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != GF_OK) return st;
+  const int64_t chunk = chunk_rows == 0 ? host_chunk_rows(M, N, dev.sm_count) : (chunk_rows < M ? chunk_rows : M);
+  const HostWs wl = host_ws(chunk, K, N, mode);
+  if (!workspace) return GF_ERR_NULL;
+  if (workspace_bytes < wl.total) return GF_ERR_WORKSPACE;
+  const Span ins[] = {{W, size_t(N) * K * 4}, {b_lin, size_t(N) * 4}, {bias, size_t(N) * 4},
+                      {gamma, size_t(N) * 4}, {beta, size_t(N) * 4}};
+  if ((st = check_no_alias(Span{workspace, wl.total}, ins, 5)) != GF_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // Copy streams and the events that order the three stages; destroyed at
+  // the end of the call (their resources are released once the enqueued work
+  // completes).
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+  auto cleanup = [&]() {
+    for (int i = 0; i < 2; ++i) {
+      if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+      if (ev_comp[i]) cudaEventDestroy(ev_comp[i]);
+      if (ev_out[i]) cudaEventDestroy(ev_out[i]);
+    }
+    if (ev_start) cudaEventDestroy(ev_start);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+  };
+  bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < 2; ++i)
+    ok = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    cleanup();
+    return GF_ERR_CUDA;
+  }
+
+  // The copy streams start after everything already queued on `stream`.
+  ok = cudaEventRecord(ev_start, s) == cudaSuccess && cudaStreamWaitEvent(s_in, ev_start, 0) == cudaSuccess &&
+       cudaStreamWaitEvent(s_out, ev_start, 0) == cudaSuccess;
+  Planes wp{};
+  if (ok) ok = prepare_operand(W, N, K, mode, ws + wl.w_planes, dev, s, &wp) == GF_OK;
+  const int64_t nchunks = (M + chunk - 1) / chunk;
+  for (int64_t i = 0; ok && i < nchunks; ++i) {
+    const int bi = int(i & 1);
+    const int64_t r0 = i * chunk, rows = (M - r0) < chunk ? (M - r0) : chunk;
+    float* xd = reinterpret_cast<float*>(ws + wl.x[bi]);
+    float* od = reinterpret_cast<float*>(ws + wl.out[bi]);
+    // stage 1: x rows in (after the compute that last read this buffer)
+    ok = cudaStreamWaitEvent(s_in, ev_comp[bi], 0) == cudaSuccess &&
+         cudaMemcpyAsync(xd, x_host + size_t(r0) * K, size_t(rows) * K * 4, cudaMemcpyHostToDevice, s_in) ==
+             cudaSuccess &&
+         cudaEventRecord(ev_in[bi], s_in) == cudaSuccess;
+    // stage 2: split + fused GEMM on the caller's stream (after the copy-out
+    // that last read this output buffer)
+    if (ok)
+      ok = cudaStreamWaitEvent(s, ev_in[bi], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev_out[bi], 0) == cudaSuccess;
+    if (ok) {
+      Planes xp{};
+      EpiSwishBiasGN::Params ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps};
+      ok = prepare_operand(xd, rows, K, mode, ws + wl.xp[bi], dev, s, &xp) == GF_OK &&
+           run_linear<EpiSwishBiasGN>(mode, dev, xp, wp, rows, K, N, /*m_fastest=*/0, ep, s) == GF_OK &&
+           cudaEventRecord(ev_comp[bi], s) == cudaSuccess;
+    }
+    // stage 3: out rows back
+    if (ok)
+      ok = cudaStreamWaitEvent(s_out, ev_comp[bi], 0) == cudaSuccess &&
+           cudaMemcpyAsync(out_host + size_t(r0) * N, od, size_t(rows) * N * 4, cudaMemcpyDeviceToHost, s_out) ==
+               cudaSuccess &&
+           cudaEventRecord(ev_out[bi], s_out) == cudaSuccess;
+  }
+  // The caller's stream completes only after the last copy-out.
+  if (ok) ok = cudaStreamWaitEvent(s, ev_out[0], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev_out[1], 0) == cudaSuccess;
+  cleanup();
+  return ok ? GF_OK : GF_ERR_CUDA;
 }
 
 size_t gf_linear_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {

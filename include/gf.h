@@ -136,6 +136,27 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
                                                 int64_t M, int64_t K, int64_t N, int32_t groups,
                                                 float eps, void* stream);
 
+/* The same operator on HOST buffers: x_host [M,K] in, out_host [M,N] out
+ * (page-locked host memory lets the copies overlap the compute; pageable
+ * memory works but serialises them).  W, b_lin, bias, gamma and beta are
+ * device pointers as above.  Rows are processed in chunks of chunk_rows
+ * (0 = a size that fills whole waves of tiles, at least 4096 rows): chunk i
+ * is copied in on an internal stream while chunk i-1 is computed on `stream`
+ * and chunk i-2 is copied out on a second internal stream, through two device
+ * staging buffers in the workspace.  Returns once everything is enqueued;
+ * out_host is complete when `stream` reaches that point (synchronise it
+ * before reading).  Workspace: the matching *_host_workspace_size() query.
+ * The internal streams and events are created and released by each call. */
+size_t gf_linear_swish_bias_groupnorm_host_workspace_size(int64_t M, int64_t K, int64_t N,
+                                                          int32_t groups, int32_t mode,
+                                                          int64_t chunk_rows);
+gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* W, const float* b_lin,
+                                              const float* bias, const float* gamma, const float* beta,
+                                              float* out_host, int64_t M, int64_t K, int64_t N,
+                                              int32_t groups, float eps, int32_t mode,
+                                              int64_t chunk_rows, void* workspace,
+                                              size_t workspace_bytes, void* stream);
+
 /* Splits n fp32 values (n % 4 == 0) into the two planes the 3xTF32
  * contraction reads: planes[0][i] = src[i] with its 13 low mantissa bits
  * cleared (a TF32 value) and planes[1][i] = src[i] - planes[0][i] (exact).

@@ -241,3 +241,36 @@ def test_convt3d_workload_sampled():
     got, ref = _ct_run(s, d, samples=np.array([0, 63, 127]))
     assert got.shape == (3, 16, 31, 63, 63)
     assert_close(got, ref, "convt3d full workload (samples 0, 63, 127)")
+
+
+# ------------------------------------------------- host-buffer pipeline
+@pytest.mark.parametrize("pinned,chunk", [(True, 0), (True, 200), (False, 384)])
+def test_linear_gn_host_pipeline_matches_device_call(pinned, chunk):
+    # Rows are independent and each chunk runs the same kernels, so the
+    # pipelined host-buffer call must reproduce the device call bit for bit.
+    s, d = _lgn_case(1000, 256, 512, 8, 4242)
+    dev = {k: T(d[k]) for k in ("W", "b_lin", "bias", "gamma", "beta")}
+    ref = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), dev["W"], dev["b_lin"], dev["bias"], dev["gamma"],
+                                            dev["beta"], s.groups, s.eps).cpu()
+    xh = torch.from_numpy(d["x"])
+    if pinned:
+        xh = xh.pin_memory()
+    oh = torch.full((s.M, s.N), float("nan"), dtype=torch.float32, pin_memory=pinned)
+    gf.gf_linear_swish_bias_groupnorm_host(xh, dev["W"], dev["b_lin"], dev["bias"], dev["gamma"], dev["beta"],
+                                           s.groups, s.eps, out_host=oh, chunk_rows=chunk)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(oh, ref)
+    ref64 = oracle.linear_swish_bias_groupnorm(d["x"], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"],
+                                               s.groups, s.eps)
+    assert_close(oh.numpy(), ref64, "host pipeline")
+
+
+@pytest.mark.gpu
+def test_dconv1d_offset_input_statistics():
+    # mean 100, std 0.01: the LayerNorm statistics must not lose the variance
+    # to cancellation.
+    s = synth.DConv1dShape(B=2, C=64, L=512)
+    d = synth.dconv1d_inputs(s, 31, affine="perturbed")
+    d["x"] = (d["x"] * np.float32(0.01) + np.float32(100.0)).astype(np.float32)
+    got, ref = _dc_run(s, d)
+    assert_close(got, ref, "dconv1d offset input")
