@@ -387,6 +387,7 @@ ALL = ["linear_gn_m32768", "linear_gn_m256", "linear_lse_m1024", "ln_dconv1d_b32
 
 # ---------------------------------------------------------------- ours
 def run_ours(wl, args):
+    global MODE
     import torch
     import torch.distributed as dist
 
@@ -497,6 +498,34 @@ def run_ours(wl, args):
                 "unit": wl.unit, "frac": round(achieved / peak, 4), "traffic": _kernel_traffic(wl),
                 "kernel_ms": round(kern_ms, 4), "kernel_launches_timed": prof.calls, "peak_note": note}
 
+    # the same workload in the other contraction modes, reported separately
+    other = None
+    if wl.bound == "tensor" and not args.no_other_modes:
+        base_mode, other = MODE, {}
+        for m in MODES:
+            if m == base_mode:
+                continue
+            MODE = m
+            for _ in range(3):
+                wl.step(gf, t)
+            torch.cuda.synchronize()
+            n = max(20, steps // 4)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with gf.profile(max_calls=n + 8) as pm:
+                e0.record(stream)
+                for _ in range(n):
+                    wl.step(gf, t)
+                e1.record(stream)
+                torch.cuda.synchronize()
+            ms_m = e0.elapsed_time(e1) / n
+            pk = peaks["bf16_tflops"] * MODES[m][2]
+            ach = wl.kernel_work() / (pm.mean_ms * 1e-3) / wl.scale()
+            other[m] = {"value": round(wl.work_per_step() / (ms_m * 1e-3) / wl.scale(), 3), "unit": wl.unit,
+                        "ms_per_step": round(ms_m, 4), "steps": n, "mode": MODES[m][1],
+                        "roofline": {"achieved": round(ach, 2), "peak": round(pk, 2), "frac": round(ach / pk, 4),
+                                     "kernel_ms": round(pm.mean_ms, 4)}}
+        MODE = base_mode
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = cpu_baseline(wl, d, budget_s=args.cpu_seconds)
@@ -512,6 +541,7 @@ def run_ours(wl, args):
                 "config": dict(wl.config, l2=wl.l2, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU",
                                **({"mode": MODES[MODE][1]} if wl.bound == "tensor" else {})),
                 "e2e": e2e, "gpu_launches": launches * steps, "roofline": roofline, "cpu_baseline": cpu,
+                "other_modes": other,
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
 
@@ -575,6 +605,7 @@ def main():
     ap.add_argument("--all", action="store_true", help="one line per workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-other-modes", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-chunks", type=int, default=1)
     ap.add_argument("--mode", choices=list(MODES), default="3xtf32",
