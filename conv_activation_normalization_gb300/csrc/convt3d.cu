@@ -25,6 +25,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "convt3d_tc.cuh"
 #include "host_common.h"
 #include "kernels_common.cuh"
 
@@ -211,6 +212,47 @@ __global__ void convt3d_finalize_kernel(const double* __restrict__ part, const f
   }
 }
 
+// Same merge for float2 partials (the tensor-core path writes one per tile and
+// epilogue warp): grid (N, groups), block 256; fp64 sums.
+__global__ void __launch_bounds__(256) convt3d_finalize_f2_kernel(const float2* __restrict__ part,
+                                                                  const float* __restrict__ gamma,
+                                                                  const float* __restrict__ beta,
+                                                                  float2* __restrict__ coef, int P, double count,
+                                                                  float eps) {
+  __shared__ double red[8][2];
+  const int n = blockIdx.x, g = blockIdx.y;
+  const float2* pg = part + (size_t(n) * kCT_G + g) * P;
+  double s = 0.0, q = 0.0;
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    const float2 v = __ldg(pg + i);
+    s += v.x;
+    q += v.y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    q += __shfl_xor_sync(0xffffffffu, q, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5][0] = s;
+    red[threadIdx.x >> 5][1] = q;
+  }
+  __syncthreads();
+  if (threadIdx.x < kCT_COUT / kCT_G) {
+    double S = 0.0, Q = 0.0;
+    for (int w = 0; w < 8; ++w) {
+      S += red[w][0];
+      Q += red[w][1];
+    }
+    const double mean = S / count;
+    const double var = fmax(Q / count - mean * mean, 0.0);
+    const double rstd = 1.0 / sqrt(var + double(eps));
+    const int c = g * (kCT_COUT / kCT_G) + threadIdx.x;
+    const double A = double(gamma[c]) * rstd;
+    coef[size_t(n) * kCT_COUT + c] = make_float2(float(A), float(double(beta[c]) - mean * A));
+  }
+}
+
 // HardSwish h * clamp(h + 3, 0, 6) / 6 written as h * sat(h / 6 + 1/2): one
 // saturating FMA and one multiply.
 __device__ __forceinline__ float hardswish(float h) { return h * __saturatef(fmaf(h, 1.f / 6.f, 0.5f)); }
@@ -296,6 +338,69 @@ void launch_ct(const float* x, const float* w, const float* b, double* part, con
   convt3d_apply_kernel<CIN><<<grid, block, 0, s>>>(x, w, b, coef, out, D, H, W);
   profile_mark_end(s);
 }
+// Tensor-core path (Cin <= 4): partials [N][4][P][kCtTcEpiWarps] float2 +
+// coefficients.
+struct CtTcWs {
+  size_t part, coef, total;
+  int P;  // tiles per sample
+};
+
+CtTcWs ct_tc_ws(int64_t N, int64_t D, int64_t H, int64_t W) {
+  CtTcWs c{};
+  c.P = int(D * ((H * W + 127) / 128));
+  c.part = 0;
+  c.coef = align_up(size_t(N) * kCT_G * c.P * kCtTcEpiWarps * sizeof(float2), 256);
+  c.total = c.coef + align_up(size_t(N) * kCT_COUT * sizeof(float2), 256);
+  return c;
+}
+
+template <int CIN>
+gf_status launch_ct_tc_passes(const CtTcParams& prm, const float* gamma, const float* beta, float2* coef, int P,
+                              int grid, float eps, cudaStream_t s) {
+  if (cudaFuncSetAttribute(convt3d_tc_kernel<1, CIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCtTcSmem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(convt3d_tc_kernel<2, CIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCtTcSmem) !=
+          cudaSuccess)
+    return GF_ERR_CUDA;
+  uint32_t* status = device_status_word();
+  convt3d_tc_kernel<1, CIN><<<grid, kCtTcThreads, kCtTcSmem, s>>>(prm, status);
+  const double count =
+      double(kCT_COUT / kCT_G) * double(2 * prm.D - 1) * double(2 * prm.H - 1) * double(2 * prm.W - 1);
+  convt3d_finalize_f2_kernel<<<dim3(unsigned(prm.N), kCT_G), 256, 0, s>>>(prm.part, gamma, beta, coef,
+                                                                           P * kCtTcEpiWarps, count, eps);
+  profile_mark_begin(s);
+  convt3d_tc_kernel<2, CIN><<<grid, kCtTcThreads, kCtTcSmem, s>>>(prm, status);
+  profile_mark_end(s);
+  return cuda_status(cudaGetLastError());
+}
+
+gf_status launch_ct_tc(const float* x, const float* w, const float* b, const float* gamma, const float* beta,
+                       float* out, int64_t N, int64_t Cin, int64_t D, int64_t H, int64_t W, float eps, void* ws,
+                       const DeviceInfo& dev, cudaStream_t s) {
+  const CtTcWs wl = ct_tc_ws(N, D, H, W);
+  CtTcParams prm{};
+  prm.x = x;
+  prm.w = w;
+  prm.bias = b;
+  prm.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + wl.part);
+  float2* coef = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + wl.coef);
+  prm.coef = coef;
+  prm.out = out;
+  prm.N = int(N);
+  prm.Cin = int(Cin);
+  prm.D = int(D);
+  prm.H = int(H);
+  prm.W = int(W);
+  prm.bpp = int((H * W + 127) / 128);
+  prm.num_tiles = int(N * D * prm.bpp);
+  const int grid = prm.num_tiles < dev.sm_count ? prm.num_tiles : dev.sm_count;
+  switch (Cin) {
+    case 1: return launch_ct_tc_passes<1>(prm, gamma, beta, coef, wl.P, grid, eps, s);
+    case 2: return launch_ct_tc_passes<2>(prm, gamma, beta, coef, wl.P, grid, eps, s);
+    case 3: return launch_ct_tc_passes<3>(prm, gamma, beta, coef, wl.P, grid, eps, s);
+    default: return launch_ct_tc_passes<4>(prm, gamma, beta, coef, wl.P, grid, eps, s);
+  }
+}
 }  // namespace
 
 // Fixed scratch for gf_convt3d_swish_gn_hswish_noalloc: the per-block GroupNorm
@@ -333,7 +438,7 @@ extern "C" {
 size_t gf_convt3d_swish_gn_hswish_workspace_size(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H,
                                                  int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups) {
   if (check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) != GF_OK) return 0;
-  return ct_ws(N, D, H, W).total;
+  return Cin <= 4 ? ct_tc_ws(N, D, H, W).total : ct_ws(N, D, H, W).total;
 }
 
 gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float* b, const float* gamma,
@@ -347,22 +452,25 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
   if (!aligned16(x) || !aligned16(w) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
       (b && !aligned16(b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
-  const CtWs wl = ct_ws(N, D, H, W);
+  const size_t need = gf_convt3d_swish_gn_hswish_workspace_size(N, Cin, Cout, D, H, W, k, stride, pad, groups);
   if (!workspace) return GF_ERR_NULL;
-  if (workspace_bytes < wl.total) return GF_ERR_WORKSPACE;
+  if (workspace_bytes < need) return GF_ERR_WORKSPACE;
   const size_t outb = size_t(N) * Cout * (2 * D - 1) * (2 * H - 1) * (2 * W - 1) * 4;
   const Span ins[] = {{x, size_t(N) * Cin * D * H * W * 4},
                       {w, size_t(Cin) * Cout * 27 * 4},
                       {b, size_t(Cout) * 4},
                       {gamma, size_t(Cout) * 4},
                       {beta, size_t(Cout) * 4},
-                      {workspace, wl.total}};
+                      {workspace, need}};
   st = check_no_alias(Span{out, outb}, ins, 6);
   if (st != GF_OK) return st;
   DeviceInfo dev;
   st = current_device(&dev);
   if (st != GF_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Cin <= 4: the contraction runs on the tensor cores (K = 8 Cin <= 32)
+  if (Cin <= 4) return launch_ct_tc(x, w, b, gamma, beta, out, N, Cin, D, H, W, eps, workspace, dev, s);
+  const CtWs wl = ct_ws(N, D, H, W);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   double* part = reinterpret_cast<double*>(ws + wl.part);
   float2* coef = reinterpret_cast<float2*>(ws + wl.coef);

@@ -52,6 +52,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `ns` nanoseconds pass, instead of spinning and taking
+// issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // A wait that gives up.  Every legitimate wait in these kernels ends within
 // milliseconds; after kWaitLimitNs the caller records GF_DEV_WAIT_TIMEOUT and
 // unwinds instead of spinning forever.
@@ -66,9 +81,22 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   }
 }
 
+static __device__ __noinline__ bool mbar_wait_slow_sleep(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 2000)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// kSleep: waiting threads sleep between polls (for kernels with many waiting
+// warps that share the SM with the warps doing the arithmetic); otherwise they
+// poll (lowest wake-up latency, for the single-thread producer/MMA loops).
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity);
+  return kSleep ? mbar_wait_slow_sleep(bar, parity) : mbar_wait_slow(bar, parity);
 }
 
 // ----------------------------------------------------------------------- TMA

@@ -222,7 +222,8 @@ def _ct_run(s, d, samples=None):
     return (out if samples is None else out[samples]), ref
 
 
-@pytest.mark.parametrize("N,Cin,D,H,W", [(2, 3, 5, 7, 9), (1, 1, 1, 1, 1), (3, 3, 4, 33, 40), (1, 8, 3, 8, 64)])
+@pytest.mark.parametrize("N,Cin,D,H,W", [(2, 3, 5, 7, 9), (1, 1, 1, 1, 1), (3, 3, 4, 33, 40), (1, 8, 3, 8, 64),
+                                         (2, 4, 3, 6, 10), (1, 2, 2, 5, 130), (2, 5, 3, 4, 9)])
 def test_convt3d_small(N, Cin, D, H, W):
     s = synth.ConvT3dShape(N=N, Cin=Cin, D=D, H=H, W=W)
     got, ref = _ct_run(s, synth.convt3d_inputs(s, 400 + W))
