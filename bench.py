@@ -298,8 +298,8 @@ class ConvT3d(Workload):
     metric = "fused ConvTranspose3d->Swish->GroupNorm->HardSwish GB/s at x[128,3,16,32,32]"
     unit = "GB/s"
     bound = "hbm"
-    sources = ("convt3d.cu", "kernels_common.cuh")
-    kernel = "convt3d_apply_kernel<3> (pass 2: recompute, normalise, store)"
+    sources = ("convt3d.cu", "convt3d_tc.cuh", "ptx.cuh", "kernels_common.cuh")
+    kernel = "convt3d_tc_kernel<2, 3> (pass 2: tcgen05 contraction, GroupNorm, HardSwish, store)"
     l2 = "inputs larger than L2 (out 1008 MB per step vs 129 MB L2); no flush"
     chunk = 1
 

@@ -393,6 +393,9 @@ gf_status launch_ct_tc(const float* x, const float* w, const float* b, const flo
   prm.W = int(W);
   prm.bpp = int((H * W + 127) / 128);
   prm.num_tiles = int(N * D * prm.bpp);
+  prm.div_dp = make_fastdiv(uint32_t(D * prm.bpp));
+  prm.div_bpp = make_fastdiv(uint32_t(prm.bpp));
+  prm.div_w = make_fastdiv(uint32_t(W));
   const int grid = prm.num_tiles < dev.sm_count ? prm.num_tiles : dev.sm_count;
   switch (Cin) {
     case 1: return launch_ct_tc_passes<1>(prm, gamma, beta, coef, wl.P, grid, eps, s);

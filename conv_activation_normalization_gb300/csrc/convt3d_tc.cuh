@@ -21,7 +21,7 @@
 //               the hi/lo rows of the A tile into an smem ring (128-byte
 //               swizzle written by hand), fence.proxy.async, arrive;
 //   warp 4      TMEM owner; one thread issues the 12 MMAs of a tile into one
-//               of two 128-column accumulators and commits;
+//               of kCtTcAccBufs 128-column accumulators and commits;
 //   warps 5-20  epilogue: warp (5 + e) reads TMEM lane quadrant (warp % 4)
 //               and columns 32*(e / 4) .. +31 (output phases pd = e / 8,
 //               ph = (e / 4) % 2, both pw), releases the accumulator, then
@@ -47,10 +47,30 @@ constexpr int kCtTcMmaWarp = 4;
 constexpr int kCtTcEpiWarp0 = 5;
 constexpr int kCtTcEpiThreads = kCtTcEpiWarps * 32;
 constexpr int kCtTcStages = 4;
+constexpr int kCtTcAccBufs = 2;  // TMEM accumulators of 128 columns
+constexpr int kCtTcTmemCols = kCtTcAccBufs * 128 <= 256 ? 256 : 512;
 constexpr int kCtTcPlane = 128 * 128;              // one 128-row x 128-byte tile
 constexpr int kCtTcStageBytes = 2 * kCtTcPlane;    // A hi + lo
 constexpr int kCtTcBBytes = 2 * kCtTcPlane;        // B hi + lo
 constexpr int kCtTcSmem = kCtTcStages * kCtTcStageBytes + kCtTcBBytes + 1024 /*bars, scratch*/ + 1024 /*align*/;
+
+// Division by a runtime constant as a multiply-shift (Granlund and
+// Montgomery's round-up method): q = (umulhi(n, m) + n) >> l with
+// l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1; exact for n < 2^31.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+  return FastDiv{d, uint32_t(m), l};
+}
+
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  return int((__umulhi(uint32_t(n), f.m) + uint32_t(n)) >> f.l);
+}
 
 struct CtTcParams {
   const float* x;
@@ -62,7 +82,22 @@ struct CtTcParams {
   int N, Cin, D, H, W;
   int bpp;               // tiles per (n, qd) plane: ceil(H*W / 128)
   int num_tiles;         // N * D * bpp
+  FastDiv div_dp, div_bpp, div_w;  // by D * bpp, bpp and W
 };
+
+// tile t -> sample n, tile index within the sample rem, depth cell qd and the
+// first flattened (qh, qw) cell index of the tile
+struct CtTile {
+  int n, rem, qd, c0;
+};
+__device__ __forceinline__ CtTile ct_tile(const CtTcParams& p, int t) {
+  CtTile r;
+  r.n = fdiv(t, p.div_dp);
+  r.rem = t - r.n * int(p.div_dp.d);
+  r.qd = fdiv(r.rem, p.div_bpp);
+  r.c0 = (r.rem - r.qd * p.bpp) * 128;
+  return r;
+}
 
 // byte offset of fp32 element k of row r in a K-major 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
@@ -87,8 +122,8 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
   uint64_t* full = reinterpret_cast<uint64_t*>(b_tile + kCtTcBBytes);
   uint64_t* empty = full + kCtTcStages;
   uint64_t* tfull = empty + kCtTcStages;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + kCtTcAccBufs;
+  uint64_t* drain = tempty + kCtTcAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -102,7 +137,7 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
       mbar_init(&full[s], kCtTcProducerThreads);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kCtTcAccBufs; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], kCtTcEpiThreads);
     }
@@ -141,7 +176,7 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
   }
   fence_proxy_async_smem();
   if (warp == kCtTcMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_alloc(smem_u32(tmem_slot), kCtTcTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -155,10 +190,10 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
     int stage = 0;
     uint32_t phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-      const int n = t / (p.D * p.bpp), rem = t % (p.D * p.bpp);
-      const int qd = rem / p.bpp, c = (rem % p.bpp) * 128 + r;
+      const CtTile tl = ct_tile(p, t);
+      const int n = tl.n, qd = tl.qd, c = tl.c0 + r;
       const bool cv = c < HW;
-      const int qh = cv ? c / p.W : 0, qw = cv ? c % p.W : 0;
+      const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
       bool ok = mbar_wait<true>(&empty[stage], phase ^ 1);
       if (!ok) {
         record_error(status, GF_DEV_WAIT_TIMEOUT);
@@ -224,7 +259,7 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
           stage = 0;
           phase ^= 1;
         }
-        if (++acc == 2) {
+        if (++acc == kCtTcAccBufs) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -250,10 +285,10 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      const int n = t / (p.D * p.bpp), rem = t % (p.D * p.bpp);
-      const int qd = rem / p.bpp, c = (rem % p.bpp) * 128 + row;
+      const CtTile tl = ct_tile(p, t);
+      const int n = tl.n, rem = tl.rem, qd = tl.qd, c = tl.c0 + row;
       const bool cv = c < HW;
-      const int qh = cv ? c / p.W : 0, qw = cv ? c % p.W : 0;
+      const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
       // GroupNorm coefficients of this sample, fetched before the wait: lane
       // co < 16 holds channel co's (A, B), read back with shuffles
       float2 abl = make_float2(0.f, 0.f);
@@ -272,7 +307,7 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
       GF_TMEM_WAIT32(r32);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
+      if (++acc == kCtTcAccBufs) {
         acc = 0;
         acc_phase ^= 1;
       }
@@ -343,7 +378,7 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
   __syncthreads();
   if (warp == kCtTcMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 256);
+    tmem_dealloc(tmem_base, kCtTcTmemCols);
   }
 }
 
