@@ -25,6 +25,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "convt3d_fused.cuh"
 #include "convt3d_tc.cuh"
 #include "host_common.h"
 #include "kernels_common.cuh"
@@ -41,16 +42,6 @@ template <int CIN>
 struct CellInputs {
   float2 v[CIN][2][2][2];
 };
-
-// d = a * b + c on both lanes of a pair (fma.rn.f32x2).
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<const unsigned long long*>(&a)), "l"(*reinterpret_cast<const unsigned long long*>(&b)),
-        "l"(*reinterpret_cast<const unsigned long long*>(&c)));
-  return *reinterpret_cast<float2*>(&d);
-}
 
 template <int CIN>
 __device__ __forceinline__ void load_cell(CellInputs<CIN>& in, const float* __restrict__ xn, int D, int H, int W,
@@ -217,7 +208,7 @@ __global__ void convt3d_finalize_kernel(const double* __restrict__ part, const f
 __global__ void __launch_bounds__(256) convt3d_finalize_f2_kernel(const float2* __restrict__ part,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta,
-                                                                  float2* __restrict__ coef, int P, double count,
+                                                                  float4* __restrict__ coef, int P, double count,
                                                                   float eps) {
   __shared__ double red[8][2];
   const int n = blockIdx.x, g = blockIdx.y;
@@ -249,7 +240,8 @@ __global__ void __launch_bounds__(256) convt3d_finalize_f2_kernel(const float2* 
     const double rstd = 1.0 / sqrt(var + double(eps));
     const int c = g * (kCT_COUT / kCT_G) + threadIdx.x;
     const double A = double(gamma[c]) * rstd;
-    coef[size_t(n) * kCT_COUT + c] = make_float2(float(A), float(double(beta[c]) - mean * A));
+    const float Af = float(A), Bf = float(double(beta[c]) - mean * A);
+    coef[size_t(n) * kCT_COUT + c] = make_float4(Af, Af, Bf, Bf);
   }
 }
 
@@ -312,7 +304,7 @@ CtWs ct_ws(int64_t N, int64_t D, int64_t H, int64_t W) {
   c.P = int(((W + kCT_TX - 1) / kCT_TX) * ((H + kCT_TY - 1) / kCT_TY) * D);
   c.part = 0;
   c.coef = align_up(size_t(N) * kCT_G * c.P * 2 * sizeof(double), 256);
-  c.total = c.coef + align_up(size_t(N) * kCT_COUT * sizeof(float2), 256);
+  c.total = c.coef + align_up(size_t(N) * kCT_COUT * sizeof(float4), 256);
   return c;
 }
 
@@ -350,12 +342,12 @@ CtTcWs ct_tc_ws(int64_t N, int64_t D, int64_t H, int64_t W) {
   c.P = int(D * ((H * W + 127) / 128));
   c.part = 0;
   c.coef = align_up(size_t(N) * kCT_G * c.P * kCtTcEpiWarps * sizeof(float2), 256);
-  c.total = c.coef + align_up(size_t(N) * kCT_COUT * sizeof(float2), 256);
+  c.total = c.coef + align_up(size_t(N) * kCT_COUT * sizeof(float4), 256);
   return c;
 }
 
 template <int CIN>
-gf_status launch_ct_tc_passes(const CtTcParams& prm, const float* gamma, const float* beta, float2* coef, int P,
+gf_status launch_ct_tc_passes(const CtTcParams& prm, const float* gamma, const float* beta, float4* coef, int P,
                               int grid, float eps, cudaStream_t s) {
   if (cudaFuncSetAttribute(convt3d_tc_kernel<1, CIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCtTcSmem) !=
           cudaSuccess ||
@@ -374,20 +366,94 @@ gf_status launch_ct_tc_passes(const CtTcParams& prm, const float* gamma, const f
   return cuda_status(cudaGetLastError());
 }
 
-gf_status launch_ct_tc(const float* x, const float* w, const float* b, const float* gamma, const float* beta,
-                       float* out, int64_t N, int64_t Cin, int64_t D, int64_t H, int64_t W, float eps, void* ws,
-                       const DeviceInfo& dev, cudaStream_t s) {
+// Single-kernel path: per-sample counters of finished tiles (zeroed by a
+// memset before each launch) and per-tile slots of 8 partial sums.
+struct CfWs {
+  size_t done, part, total;
+};
+
+CfWs cf_ws(int64_t N, int64_t D, int64_t H, int64_t W) {
+  const int64_t tiles = N * D * ((H * W + 127) / 128);
+  CfWs c{};
+  c.done = 0;
+  c.part = align_up(size_t(N) * sizeof(uint32_t), 256);
+  c.total = c.part + align_up(size_t(tiles) * 8 * sizeof(float), 256);
+  return c;
+}
+
+template <int CIN>
+gf_status launch_ct_fused(const CfParams& prm, int grid, cudaStream_t s) {
+  if (cudaFuncSetAttribute(convt3d_fused_kernel<CIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCfSmem) !=
+      cudaSuccess)
+    return GF_ERR_CUDA;
+  uint32_t* status = device_status_word();
+  CfParams p = prm;
+  void* args[] = {&p, &status};
+  profile_mark_begin(s);
+  const cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&convt3d_fused_kernel<CIN>),
+                                                    dim3(unsigned(grid)), dim3(kCfThreads), args, kCfSmem, s);
+  profile_mark_end(s);
+  return cuda_status(e);
+}
+
+// The single-kernel path needs every CTA resident (one per SM) and a sample
+// of at most grid + 1 tiles (see convt3d_fused.cuh).
+template <int CIN>
+bool ct_fused_fits(int P, int grid, int device) {
+  int coop = 0, blocks = 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device) != cudaSuccess || !coop) return false;
+  if (cudaFuncSetAttribute(convt3d_fused_kernel<CIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCfSmem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, convt3d_fused_kernel<CIN>, kCfThreads, kCfSmem) !=
+          cudaSuccess)
+    return false;
+  return blocks >= 1 && P <= grid + 1;
+}
+
+template <int CIN>
+gf_status launch_ct_tensor_core(const float* x, const float* w, const float* b, const float* gamma,
+                                const float* beta, float* out, int64_t N, int64_t D, int64_t H, int64_t W, float eps,
+                                void* ws, const DeviceInfo& dev, cudaStream_t s) {
+  const int bpp = int((H * W + 127) / 128), P = int(D) * bpp, num_tiles = int(N) * P;
+  const int grid = num_tiles < dev.sm_count ? num_tiles : dev.sm_count;
+  if (ct_fused_fits<CIN>(P, grid, dev.device)) {
+    const CfWs cw = cf_ws(N, D, H, W);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    if (cudaMemsetAsync(base + cw.done, 0, cw.part - cw.done, s) != cudaSuccess) return GF_ERR_CUDA;
+    CfParams p{};
+    p.x = x;
+    p.w = w;
+    p.bias = b;
+    p.gamma = gamma;
+    p.beta = beta;
+    p.out = out;
+    p.part = reinterpret_cast<float*>(base + cw.part);
+    p.done = reinterpret_cast<uint32_t*>(base + cw.done);
+    p.N = int(N);
+    p.D = int(D);
+    p.H = int(H);
+    p.W = int(W);
+    p.bpp = bpp;
+    p.num_tiles = num_tiles;
+    p.rounds = (num_tiles + grid - 1) / grid;
+    p.div_dp = make_fastdiv(uint32_t(P));
+    p.div_bpp = make_fastdiv(uint32_t(bpp));
+    p.div_w = make_fastdiv(uint32_t(W));
+    p.inv_count = 1.0 / (double(kCT_COUT / kCT_G) * double(2 * D - 1) * double(2 * H - 1) * double(2 * W - 1));
+    p.eps = eps;
+    return launch_ct_fused<CIN>(p, grid, s);
+  }
   const CtTcWs wl = ct_tc_ws(N, D, H, W);
   CtTcParams prm{};
   prm.x = x;
   prm.w = w;
   prm.bias = b;
   prm.part = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + wl.part);
-  float2* coef = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + wl.coef);
+  float4* coef = reinterpret_cast<float4*>(static_cast<uint8_t*>(ws) + wl.coef);
   prm.coef = coef;
   prm.out = out;
   prm.N = int(N);
-  prm.Cin = int(Cin);
+  prm.Cin = CIN;
   prm.D = int(D);
   prm.H = int(H);
   prm.W = int(W);
@@ -396,12 +462,17 @@ gf_status launch_ct_tc(const float* x, const float* w, const float* b, const flo
   prm.div_dp = make_fastdiv(uint32_t(D * prm.bpp));
   prm.div_bpp = make_fastdiv(uint32_t(prm.bpp));
   prm.div_w = make_fastdiv(uint32_t(W));
-  const int grid = prm.num_tiles < dev.sm_count ? prm.num_tiles : dev.sm_count;
+  return launch_ct_tc_passes<CIN>(prm, gamma, beta, coef, wl.P, grid, eps, s);
+}
+
+gf_status launch_ct_tc(const float* x, const float* w, const float* b, const float* gamma, const float* beta,
+                       float* out, int64_t N, int64_t Cin, int64_t D, int64_t H, int64_t W, float eps, void* ws,
+                       const DeviceInfo& dev, cudaStream_t s) {
   switch (Cin) {
-    case 1: return launch_ct_tc_passes<1>(prm, gamma, beta, coef, wl.P, grid, eps, s);
-    case 2: return launch_ct_tc_passes<2>(prm, gamma, beta, coef, wl.P, grid, eps, s);
-    case 3: return launch_ct_tc_passes<3>(prm, gamma, beta, coef, wl.P, grid, eps, s);
-    default: return launch_ct_tc_passes<4>(prm, gamma, beta, coef, wl.P, grid, eps, s);
+    case 1: return launch_ct_tensor_core<1>(x, w, b, gamma, beta, out, N, D, H, W, eps, ws, dev, s);
+    case 2: return launch_ct_tensor_core<2>(x, w, b, gamma, beta, out, N, D, H, W, eps, ws, dev, s);
+    case 3: return launch_ct_tensor_core<3>(x, w, b, gamma, beta, out, N, D, H, W, eps, ws, dev, s);
+    default: return launch_ct_tensor_core<4>(x, w, b, gamma, beta, out, N, D, H, W, eps, ws, dev, s);
   }
 }
 }  // namespace
@@ -441,7 +512,10 @@ extern "C" {
 size_t gf_convt3d_swish_gn_hswish_workspace_size(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H,
                                                  int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups) {
   if (check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) != GF_OK) return 0;
-  return Cin <= 4 ? ct_tc_ws(N, D, H, W).total : ct_ws(N, D, H, W).total;
+  if (Cin > 4) return ct_ws(N, D, H, W).total;
+  // the single-kernel or the two-pass tensor-core path, chosen per device
+  const size_t a = ct_tc_ws(N, D, H, W).total, c = cf_ws(N, D, H, W).total;
+  return a > c ? a : c;
 }
 
 gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float* b, const float* gamma,

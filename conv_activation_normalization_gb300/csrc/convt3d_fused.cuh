@@ -1,0 +1,404 @@
+// ConvTranspose3d(k 3, stride 2, pad 1) -> Swish -> GroupNorm -> HardSwish in
+// one persistent kernel, the contraction on tcgen05 with the tiles, producer
+// warps and MMA issuer of convt3d_tc.cuh.
+//
+// GroupNorm needs the statistics of a whole sample before any of its outputs
+// can be written.  The two-pass kernels therefore run the contraction twice.
+// Here every CTA keeps the Swish values of its last tiles in tensor memory
+// instead, and the CTAs (all resident: cooperative launch, one per SM)
+// exchange the statistics through global memory:
+//
+//   round r      CTA b of G computes tile t = r*G + b: MMA into TMEM buffer
+//                r % 4, Swish, s written back over the accumulator
+//                (tcgen05.st); the tile's per-group (sum s, sum s^2) go to
+//                the tile's own slot in global memory and the sample's
+//                counter of finished tiles is incremented;
+//   round r + 3  (first thing in the round) once all tiles of t's sample
+//                are counted, the CTA sums their slots in fp64, turns the
+//                totals into the per-channel affine (A, B) and writes tile t,
+//                HardSwish(A s + B), straight from TMEM; that frees buffer
+//                r % 4 for the MMAs of tile r + 4.
+//
+// A sample's tiles are consecutive, so with at most G + 1 tiles per sample it
+// is complete at most one round after any of its tiles.  Between a CTA's own
+// statistics of round r + 1 and its output of tile r lie the output of tile
+// r - 1 and the statistics work of round r + 2, which hide the wait for the
+// other CTAs; four 128-column TMEM buffers (all 512 columns) hold tiles
+// r + 1 .. r + 3 and the MMA's target r + 4.  The host uses the two-pass
+// kernels when a sample has more tiles than that.
+//
+// Roles (736 threads):
+//   warps 0-3    producers, warp 4 TMEM owner and MMA issuer (as in the
+//                two-pass kernel, with 4 accumulator buffers);
+//   warp 5       publisher: per round, sums the epilogue warps' partial sums
+//                into the tile's slot and counts the tile for its sample;
+//   warp 6       coefficients: per tile, waits (bounded) until every tile of
+//                the tile's sample is counted, reduces the sample's slots and
+//                writes the tile's 16 (A, A, B, B) into a shared slot;
+//   warps 7-22   epilogue: warp (7 + e) owns TMEM lane quadrant (warp % 4)
+//                and the 32 columns of chunk e / 4 (output phases
+//                pd = chunk / 2, ph = chunk % 2, 16 channels x both pw); per
+//                round it writes the tile from three rounds earlier, then
+//                does the statistics work of the new tile.
+#pragma once
+
+#include "convt3d_tc.cuh"
+
+namespace gf {
+
+constexpr int kCfEpiWarps = 16;
+constexpr int kCfPubWarp = 5;
+constexpr int kCfCoefWarp = 6;
+constexpr int kCfEpiWarp0 = 7;
+constexpr int kCfThreads = (kCfEpiWarp0 + kCfEpiWarps) * 32;
+constexpr int kCfBufs = 4;                          // TMEM tile buffers of 128 columns
+constexpr int kCfLag = 3;                           // rounds between a tile's statistics and its output
+constexpr int kCfCoefFloats = 16 * 4;               // per buffer: 16 channels x (A, A, B, B)
+constexpr int kCfPartFloats = kCfEpiWarps * 8;      // per round: 8 sums per epilogue warp
+constexpr int kCfSmem = kCtTcStages * kCtTcStageBytes + kCtTcBBytes + kCfBufs * kCfCoefFloats * 4 +
+                        2 * kCfPartFloats * 4 + 1024 /*barriers*/ + 1024 /*alignment*/;
+
+struct CfParams {
+  const float* x;
+  const float* w;
+  const float* bias;  // may be null
+  const float* gamma;
+  const float* beta;
+  float* out;
+  float* part;        // [num_tiles][8]: per tile and group g, (sum s, sum s^2) at 2g, 2g + 1
+  uint32_t* done;     // [N]: tiles of the sample whose slot is written; zero at launch
+  int N, D, H, W;
+  int bpp;            // tiles per (n, qd) plane: ceil(H*W / 128)
+  int num_tiles;      // N * D * bpp
+  int rounds;         // ceil(num_tiles / gridDim.x)
+  FastDiv div_dp, div_bpp, div_w;  // by D * bpp (tiles per sample), bpp and W
+  double inv_count;   // 1 / elements per (sample, group)
+  float eps;
+};
+
+// Wait until `need` tiles of a sample are counted; false after the time
+// limit.  Every lane polls with acquire loads, so each lane's later reads see
+// the slots written before the increments.
+__device__ __forceinline__ bool cf_wait_count(const uint32_t* cnt, uint32_t need) {
+  if (ld_acquire_gpu(cnt) >= need) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(cnt) >= need) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+template <int CIN>
+__global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfParams p, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* a_ring = smem;                                          // [S][hi, lo]
+  uint8_t* b_tile = smem + kCtTcStages * kCtTcStageBytes;          // [hi, lo]
+  float* coef_s = reinterpret_cast<float*>(b_tile + kCtTcBBytes);  // [kCfBufs][16][4]
+  float* part_s = coef_s + kCfBufs * kCfCoefFloats;                // [2][kCfEpiWarps][8]
+  uint64_t* full = reinterpret_cast<uint64_t*>(part_s + 2 * kCfPartFloats);
+  uint64_t* empty = full + kCtTcStages;
+  uint64_t* tfull = empty + kCtTcStages;  // accumulator of buffer b written by the MMAs
+  uint64_t* tempty = tfull + kCfBufs;     // buffer b written out, free for the MMAs
+  uint64_t* cfull = tempty + kCfBufs;     // coefficients of buffer b's tile ready
+  uint64_t* cempty = cfull + kCfBufs;     // coefficient slot b read
+  uint64_t* pfull = cempty + kCfBufs;     // [2] partial sums of the round written
+  uint64_t* pempty = pfull + 2;           // [2] partial sums consumed
+  uint64_t* drain = pempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  constexpr int K = 8 * CIN;
+  constexpr uint32_t kFull = 0xffffffffu;
+  const int HW = p.H * p.W;
+  const int G = int(gridDim.x);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kCtTcStages; ++s) {
+      mbar_init(&full[s], kCtTcProducerThreads / 32);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kCfBufs; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kCfEpiWarps);
+      mbar_init(&cfull[b], 1);
+      mbar_init(&cempty[b], kCfEpiWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&pfull[i], kCfEpiWarps);
+      mbar_init(&pempty[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  ct_fill_tiles<CIN>(p.w, p.bias, a_ring, b_tile);
+  fence_proxy_async_smem();
+  if (warp == kCtTcMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kCfBufs * 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&]() {
+    record_error(status, GF_DEV_WAIT_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ producers
+    ct_produce<CIN>(p, a_ring, full, empty, abort_flag, status);
+  } else if (warp == kCtTcMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0)
+      ct_mma<kCfBufs>(p, tmem_base, a_ring, b_tile, full, empty, tfull, tempty, drain, abort_flag, status);
+    __syncwarp();
+  } else if (warp == kCfPubWarp) {
+    // ----------------------------------------------------------- publisher
+    bool ok = true;
+    for (int r = 0; r < p.rounds; ++r) {
+      const int t = blockIdx.x + r * G;
+      if (!(ok = __all_sync(kFull, mbar_wait<true>(&pfull[r & 1], (r >> 1) & 1)) &&
+                 !__any_sync(kFull, *abort_flag)))
+        break;
+      float v = 0.f;
+      if (t < p.num_tiles && lane < 8) {
+        // value v = lane: sum s (even) or sum s^2 (odd) of group lane / 2
+        const float* ps = part_s + (r & 1) * kCfPartFloats + lane;
+#pragma unroll
+        for (int e = 0; e < kCfEpiWarps; ++e) v += ps[e * 8];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pempty[r & 1]);
+      if (t < p.num_tiles) {
+        if (lane < 8) p.part[size_t(t) * 8 + lane] = v;
+        // release: the slot reaches L2 before the count says so
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.done + fdiv(t, p.div_dp), 1u);
+      }
+    }
+    if (!ok) {
+      fail();
+      // the other CTAs must not wait for this one's tiles
+      if (lane == 0)
+        for (int n = 0; n < p.N; ++n) atomicAdd(p.done + n, 1u << 20);
+    }
+  } else if (warp == kCfCoefWarp) {
+    // -------------------------------------------------------- coefficients
+    // lane c < 16: channel c's GroupNorm affine
+    const float gam = lane < 16 ? __ldg(p.gamma + lane) : 0.f, bet = lane < 16 ? __ldg(p.beta + lane) : 0.f;
+    const int P = int(p.div_dp.d);
+    for (int rt = 0; rt < p.rounds; ++rt) {
+      const int t = blockIdx.x + rt * G;
+      if (t >= p.num_tiles) break;
+      const int slot = rt % kCfBufs, n = fdiv(t, p.div_dp);
+      if (!__all_sync(kFull, mbar_wait<true>(&cempty[slot], ((rt / kCfBufs) & 1) ^ 1)) ||
+          __any_sync(kFull, *abort_flag) || !__all_sync(kFull, cf_wait_count(p.done + n, uint32_t(P)))) {
+        fail();
+        break;
+      }
+      // the sample's P slots of 8 floats: lane l sums the float4 halves
+      // (l & 1) of tiles l / 2, l / 2 + 16, ... (loads of a batch in flight
+      // together, fp32 within the lane), then lanes of equal parity combine
+      // in fp64
+      const float4* sp = reinterpret_cast<const float4*>(p.part + size_t(n) * P * 8);
+      double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+      for (int i0 = 0; i0 < 2 * P; i0 += 8 * 32) {
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = i0 + lane + 32 * j;
+          v[j] = i < 2 * P ? __ldcg(sp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4 f = v[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) {
+          f.x += v[j].x;
+          f.y += v[j].y;
+          f.z += v[j].z;
+          f.w += v[j].w;
+        }
+        a0 += f.x;
+        a1 += f.y;
+        a2 += f.z;
+        a3 += f.w;
+      }
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) {
+        a0 += __shfl_xor_sync(kFull, a0, o);
+        a1 += __shfl_xor_sync(kFull, a1, o);
+        a2 += __shfl_xor_sync(kFull, a2, o);
+        a3 += __shfl_xor_sync(kFull, a3, o);
+      }
+      // lane 0 holds groups 0-1 (s, s^2, s, s^2), lane 1 groups 2-3; channel
+      // lane c < 16 takes group c / 4 from lane (c / 8)
+      const int src = (lane >> 3) & 1;
+      const double gs0 = __shfl_sync(kFull, a0, src), gq0 = __shfl_sync(kFull, a1, src);
+      const double gs1 = __shfl_sync(kFull, a2, src), gq1 = __shfl_sync(kFull, a3, src);
+      if (lane < 16) {
+        const bool hi = (lane >> 2) & 1;
+        const double mean = (hi ? gs1 : gs0) * p.inv_count;
+        const double var = fmax((hi ? gq1 : gq0) * p.inv_count - mean * mean, 0.0);
+        const float A = gam * rsqrtf(float(var) + p.eps);
+        const float B = bet - float(mean) * A;
+        reinterpret_cast<float4*>(coef_s + slot * kCfCoefFloats)[lane] = make_float4(A, A, B, B);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cfull[slot]);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - kCfEpiWarp0;
+    const int quad = warp & 3, chunk = e >> 2;
+    const int pd = chunk >> 1, hh = chunk & 1;  // depth and height phase of the warp's columns
+    const int row = quad * 32 + lane;
+    const int OD = 2 * p.D - 1, OH = 2 * p.H - 1, OW = 2 * p.W - 1;
+    const int OHW = OH * OW;
+    const size_t plane = size_t(OD) * OHW;
+    const uint32_t lane_base = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(chunk * 32);
+    for (int r = 0; r < p.rounds + kCfLag; ++r) {
+      if (__any_sync(kFull, *abort_flag)) break;
+      if (r >= kCfLag) {
+        // -------- output of the tile of round r - kCfLag
+        const int ro = r - kCfLag, t = blockIdx.x + ro * G;
+        if (t < p.num_tiles) {
+          const int buf = ro % kCfBufs;
+          if (!__all_sync(kFull, mbar_wait<true>(&cfull[buf], (ro / kCfBufs) & 1))) {
+            fail();
+            break;
+          }
+          const CtTile tl = ct_tile(p, t);
+          const int n = tl.n, qd = tl.qd, c = tl.c0 + row;
+          const bool cv = c < HW;
+          const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
+          const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
+          const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
+          uint32_t r32[32];
+          GF_TMEM_LD32(lane_base + uint32_t(buf * 128), r32);
+          GF_TMEM_WAIT32(r32);
+          // the buffer is read: the MMAs of tile ro + kCfBufs may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[buf]);
+          const float* cf = coef_s + buf * kCfCoefFloats;
+          // GroupNorm affine A s + B, then HardSwish h sat(h / 6 + 1/2), on
+          // (pw 0, pw 1) pairs; the pair's two outputs are adjacent in memory
+          float* oc = p.out + size_t(n) * 16 * plane + size_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
+#pragma unroll
+          for (int co = 0; co < 16; ++co) {
+            const float2 sv = make_float2(__uint_as_float(r32[2 * co]), __uint_as_float(r32[2 * co + 1]));
+            const float4 ab = reinterpret_cast<const float4*>(cf)[co];  // (A, A, B, B), a broadcast read
+            const float2 h = fma2(make_float2(ab.x, ab.y), sv, make_float2(ab.z, ab.w));
+            // (f32x2 FMAs have no saturating form)
+            const float2 o = mul2(h, make_float2(__saturatef(fmaf(h.x, 1.f / 6.f, 0.5f)),
+                                                 __saturatef(fmaf(h.y, 1.f / 6.f, 0.5f))));
+            if (pv0) __stcs(oc, o.x);
+            if (pv1) __stcs(oc + 1, o.y);
+            oc += plane;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cempty[buf]);
+        }
+      }
+      if (r < p.rounds) {
+        // -------- statistics of the tile of round r
+        const int t = blockIdx.x + r * G;
+        if (!__all_sync(kFull, mbar_wait<true>(&pempty[r & 1], ((r >> 1) & 1) ^ 1))) {
+          fail();
+          break;
+        }
+        if (t < p.num_tiles) {
+          const int buf = r % kCfBufs;
+          if (!__all_sync(kFull, mbar_wait<true>(&tfull[buf], (r / kCfBufs) & 1))) {
+            fail();
+            break;
+          }
+          tc_fence_after();
+          const CtTile tl = ct_tile(p, t);
+          const int qd = tl.qd, c = tl.c0 + row;
+          const bool cv = c < HW;
+          const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
+          const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
+          const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
+          const uint32_t taddr = lane_base + uint32_t(buf * 128);
+          uint32_t r32[32];
+          GF_TMEM_LD32(taddr, r32);
+          GF_TMEM_WAIT32(r32);
+          // r32[2 co + pw] is channel co at phase (pd, hh, pw); outputs
+          // outside the volume are zeroed before Swish (Swish(0) = 0)
+          const float2 m = make_float2(pv0 ? 1.f : 0.f, pv1 ? 1.f : 0.f);
+          float2 gs[4], gq[4];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) gs[g] = gq[g] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int co = 0; co < 16; ++co) {
+            float2 y = make_float2(__uint_as_float(r32[2 * co]), __uint_as_float(r32[2 * co + 1]));
+            if constexpr (K == 32) {  // no padding column: the bias is added here
+              if (p.bias) {
+                const float b = __ldg(p.bias + co);
+                y = add2(y, make_float2(b, b));
+              }
+            }
+            const float2 sv = swish2(mul2(y, m));
+            gs[co >> 2] = add2(gs[co >> 2], sv);
+            gq[co >> 2] = fma2(sv, sv, gq[co >> 2]);
+            r32[2 * co] = __float_as_uint(sv.x);
+            r32[2 * co + 1] = __float_as_uint(sv.y);
+          }
+          GF_TMEM_ST32(taddr, r32);
+          // reduce-scatter of the 8 sums over the warp's 32 lanes (9
+          // shuffles): afterwards lane l holds the full sum of value
+          // v = 4*b4 + 2*b3 + b2 (b_i = bit i of l), value v being gs[v/2]
+          // (even v) or gq[v/2] (odd v)
+          float rs[8];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            rs[2 * g] = gs[g].x + gs[g].y;
+            rs[2 * g + 1] = gq[g].x + gq[g].y;
+          }
+          {
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float send = b4 ? rs[i] : rs[4 + i];
+              const float keep = b4 ? rs[4 + i] : rs[i];
+              rs[i] = keep + __shfl_xor_sync(kFull, send, 16);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const float send = b3 ? rs[i] : rs[2 + i];
+              const float keep = b3 ? rs[2 + i] : rs[i];
+              rs[i] = keep + __shfl_xor_sync(kFull, send, 8);
+            }
+            {
+              const float send = b2 ? rs[0] : rs[1];
+              const float keep = b2 ? rs[1] : rs[0];
+              rs[0] = keep + __shfl_xor_sync(kFull, send, 4);
+            }
+            rs[0] += __shfl_xor_sync(kFull, rs[0], 2);
+            rs[0] += __shfl_xor_sync(kFull, rs[0], 1);
+          }
+          if ((lane & 3) == 0) part_s[(r & 1) * kCfPartFloats + e * 8 + (lane >> 2)] = rs[0];
+          tmem_wait_st();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pfull[r & 1]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kCtTcMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kCfBufs * 128);
+  }
+}
+
+}  // namespace gf

@@ -4,31 +4,39 @@
 // from the 2x2x2 inputs at q..q+1, and every tap feeds exactly one output
 // phase.  So per cell the transposed conv is a tiny dense product
 //
-//   Y[cell][phase*16 + co] = sum_k  A[cell][k] * B[phase*16 + co][k]
-//   A[cell][pos*Cin + ci]   = x[n, ci, qd+a, qh+b, qw+c]   (pos = 4a + 2b + c)
-//   B[(p)*16 + co][pos*Cin + ci] = w[ci, co, kd, kh, kw] when input offset a
-//        feeds phase p in every dimension (a=0 -> k=1 for p=0, k=2 for p=1;
+//   Y[cell][col] = sum_k  A[cell][k] * B[col][k],  col = (pd*2 + ph)*32 + co*2 + pw
+//   A[cell][pos*Cin + ci] = x[n, ci, qd+a, qh+b, qw+c]   (pos = 4a + 2b + c)
+//   B[col][pos*Cin + ci]  = w[ci, co, kd, kh, kw] when input offset a feeds
+//        phase p in every dimension (a=0 -> k=1 for p=0, k=2 for p=1;
 //        a=1 -> k=0 for p=1), else 0
+//
+// The column order puts the two width phases of a channel side by side, so a
+// 32-column slice of the accumulator is 16 (pw 0, pw 1) pairs that the
+// epilogue processes with packed f32x2 arithmetic.
 //
 // with K = 8 * Cin <= 32 (one 128-byte k-block), M = 128 cells per tile and
 // N = 128 = 8 phases x 16 channels: a 128x128x32 3xTF32 MMA per tile (raw
 // fp32 as hi, the tensor core truncates; lo = x - trunc(x)).  When K < 32 the
 // conv bias rides in the padding: A[cell][K] = 1 and B[row][K] = bias[co].
 //
-// Roles (672 threads, one CTA per SM, persistent over tiles of 128 cells
-// that run along the flattened (qh, qw) plane of one (n, qd)):
-//   warps 0-3   producers: thread r gathers cell r's 8*Cin inputs and writes
-//               the hi/lo rows of the A tile into an smem ring (128-byte
-//               swizzle written by hand), fence.proxy.async, arrive;
+// Roles (5 + kCtTcEpiWarps warps, one CTA per SM, persistent over tiles of
+// 128 cells that run along the flattened (qh, qw) plane of one (n, qd)):
+//   warps 0-3   producers: thread r gathers cell r's 8*Cin inputs with
+//               cp.async straight into the A hi row of a ring stage (128-byte
+//               swizzle computed by hand), several tiles in flight; once a
+//               tile has landed it writes the lo row, fence.proxy.async, and
+//               each warp arrives once;
 //   warp 4      TMEM owner; one thread issues the 12 MMAs of a tile into one
 //               of kCtTcAccBufs 128-column accumulators and commits;
-//   warps 5-20  epilogue: warp (5 + e) reads TMEM lane quadrant (warp % 4)
-//               and columns 32*(e / 4) .. +31 (output phases pd = e / 8,
-//               ph = (e / 4) % 2, both pw), releases the accumulator, then
+//   warps 5-    epilogue: warp (5 + e) reads TMEM lane quadrant (warp % 4)
+//               and kCtTcEpiChunks chunks of 32 columns (chunk j = output
+//               phases pd = j / 2, ph = j % 2, 16 channels x both pw), one
+//               chunk at a time, releases the accumulator after the last
+//               load, then
 //                 PASS 1: Swish and per-group sums of s and s^2, reduced
-//                         over the warp's 32 cells x 32 columns in fp32, one
-//                         float2 per (sample, group, tile, warp), merged in
-//                         fp64 by the finalize kernel;
+//                         over the warp's 32 cells in fp32, one float2 per
+//                         (sample, group, tile, warp), merged in fp64 by the
+//                         finalize kernel;
 //                 PASS 2: Swish, GroupNorm affine, HardSwish, stores.
 // The weights tile B (hi/lo) is built once per CTA.
 #pragma once
@@ -40,19 +48,23 @@
 
 namespace gf {
 
-constexpr int kCtTcEpiWarps = 16;  // 4 per TMEM lane quadrant, 32 columns each
+constexpr int kCtTcEpiWarps = 16;  // a multiple of 4 (one per TMEM lane quadrant)
+constexpr int kCtTcEpiChunks = 16 / kCtTcEpiWarps;  // 32-column accumulator chunks per epilogue warp
 constexpr int kCtTcThreads = (5 + kCtTcEpiWarps) * 32;
 constexpr int kCtTcProducerThreads = 128;
 constexpr int kCtTcMmaWarp = 4;
 constexpr int kCtTcEpiWarp0 = 5;
 constexpr int kCtTcEpiThreads = kCtTcEpiWarps * 32;
 constexpr int kCtTcStages = 4;
+constexpr int kCtTcGatherDepth = kCtTcStages - 1;  // tiles whose input gathers are in flight
 constexpr int kCtTcAccBufs = 2;  // TMEM accumulators of 128 columns
 constexpr int kCtTcTmemCols = kCtTcAccBufs * 128 <= 256 ? 256 : 512;
 constexpr int kCtTcPlane = 128 * 128;              // one 128-row x 128-byte tile
 constexpr int kCtTcStageBytes = 2 * kCtTcPlane;    // A hi + lo
 constexpr int kCtTcBBytes = 2 * kCtTcPlane;        // B hi + lo
-constexpr int kCtTcSmem = kCtTcStages * kCtTcStageBytes + kCtTcBBytes + 1024 /*bars, scratch*/ + 1024 /*align*/;
+constexpr int kCtTcCoefBytes = kCtTcEpiWarps * 16 * 16;  // per epilogue warp: 16 channels x (A, A, B, B)
+constexpr int kCtTcSmem =
+    kCtTcStages * kCtTcStageBytes + kCtTcBBytes + kCtTcCoefBytes + 1024 /*bars, scratch*/ + 1024 /*align*/;
 
 // Division by a runtime constant as a multiply-shift (Granlund and
 // Montgomery's round-up method): q = (umulhi(n, m) + n) >> l with
@@ -77,7 +89,7 @@ struct CtTcParams {
   const float* w;
   const float* bias;     // may be null
   float2* part;          // PASS 1: [N][4][P][16] (sum s, sum s^2) per tile and epilogue warp
-  const float2* coef;    // PASS 2: [N][16] (A, B)
+  const float4* coef;    // PASS 2: [N][16] (A, A, B, B)
   float* out;            // PASS 2
   int N, Cin, D, H, W;
   int bpp;               // tiles per (n, qd) plane: ceil(H*W / 128)
@@ -90,7 +102,8 @@ struct CtTcParams {
 struct CtTile {
   int n, rem, qd, c0;
 };
-__device__ __forceinline__ CtTile ct_tile(const CtTcParams& p, int t) {
+template <class Prm>
+__device__ __forceinline__ CtTile ct_tile(const Prm& p, int t) {
   CtTile r;
   r.n = fdiv(t, p.div_dp);
   r.rem = t - r.n * int(p.div_dp.d);
@@ -113,13 +126,171 @@ __device__ __forceinline__ bool ct_phase_ok(int p, int qd, int qh, int qw, int D
   return ((p >> 2) == 0 || qd < D - 1) && (((p >> 1) & 1) == 0 || qh < H - 1) && ((p & 1) == 0 || qw < W - 1);
 }
 
+// The weights tile B (hi/lo, rows in accumulator-column order) and the K
+// padding of every A ring row: 1 in column K of the hi plane (so the GEMM
+// adds the bias column of B) and zeros elsewhere.  All threads of the CTA
+// take part; the caller fences and synchronises.
+template <int CIN>
+__device__ __forceinline__ void ct_fill_tiles(const float* w, const float* bias, uint8_t* a_ring, uint8_t* b_tile) {
+  constexpr int K = 8 * CIN;
+  for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
+    const int row = i / 32, k = i % 32;  // row = (pd*2 + ph)*32 + co*2 + pw
+    const int co = (row >> 1) & 15, ph3 = ((row >> 5) << 1) | (row & 1);
+    float v = 0.f;
+    if (k == K && K < 32) {
+      v = bias ? __ldg(bias + co) : 0.f;  // the bias column (A holds 1 there)
+    } else if (k < K) {
+      const int pos = k / CIN, ci = k % CIN;
+      // per dimension d (depth, height, width = bit 2, 1, 0 of pos and ph3):
+      // input offset a feeds phase: a=0 -> (p=0, k=1) or (p=1, k=2);
+      // a=1 -> (p=1, k=0); (a=1, p=0) is no tap
+      const int ad = (pos >> 2) & 1, ah = (pos >> 1) & 1, aw = pos & 1;
+      const int pd_ = (ph3 >> 2) & 1, ph_ = (ph3 >> 1) & 1, pw_ = ph3 & 1;
+      const bool used = (ad <= pd_) && (ah <= ph_) && (aw <= pw_);
+      const int kd = ad ? 0 : (pd_ ? 2 : 1), kh = ah ? 0 : (ph_ ? 2 : 1), kw = aw ? 0 : (pw_ ? 2 : 1);
+      const int tap = (kd * 3 + kh) * 3 + kw;
+      if (used) v = __ldg(w + (size_t(ci) * 16 + co) * 27 + tap);
+    }
+    *reinterpret_cast<float*>(b_tile + sw128_offset(row, k)) = v;
+    *reinterpret_cast<float*>(b_tile + kCtTcPlane + sw128_offset(row, k)) = v - tf32_hi(v);
+  }
+  for (int i = threadIdx.x; i < kCtTcStages * 2 * 128 * 32; i += blockDim.x) {
+    const int k = i % 32, row = (i / 32) % 128, plane = (i / (32 * 128)) & 1;
+    if (k >= K)
+      *reinterpret_cast<float*>(a_ring + (i / (32 * 128)) * kCtTcPlane + sw128_offset(row, k)) =
+          (k == K && plane == 0) ? 1.f : 0.f;
+  }
+}
+
+// Producer warps 0-3 (thread r = cell row r of the tile).
+template <int CIN, class Prm>
+__device__ __forceinline__ void ct_produce(const Prm& p, uint8_t* a_ring, uint64_t* full, uint64_t* empty,
+                                           volatile uint32_t* abort_flag, uint32_t* status) {
+  constexpr int K = 8 * CIN;
+  const int lane = threadIdx.x % 32;
+  const int HW = p.H * p.W;
+  // The gathers of up to kCtTcGatherDepth tiles are in flight at once:
+  // thread r copies cell r's inputs straight into the A hi plane of a ring
+  // stage with 4-byte cp.async (zero-filled outside the input), and once a
+  // tile's copies have landed it writes the lo plane from them and marks
+  // the stage full.
+  const int r = threadIdx.x;  // cell row of the tile
+  int istage = 0, fstage = 0, pending = 0;
+  uint32_t iphase = 0;
+  auto finish_oldest = [&]() {
+    uint8_t* a_hi = a_ring + fstage * kCtTcStageBytes;
+    uint8_t* a_lo = a_hi + kCtTcPlane;
+#pragma unroll
+    for (int ch = 0; ch < K / 4; ++ch) {
+      const uint32_t off = sw128_offset(r, ch * 4);
+      const float4 v = *reinterpret_cast<const float4*>(a_hi + off);
+      *reinterpret_cast<float4*>(a_lo + off) =
+          make_float4(v.x - tf32_hi(v.x), v.y - tf32_hi(v.y), v.z - tf32_hi(v.z), v.w - tf32_hi(v.w));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&full[fstage]);
+    if (++fstage == kCtTcStages) fstage = 0;
+    --pending;
+  };
+  for (int t = blockIdx.x;; t += gridDim.x) {
+    // decisions are warp-uniform: the warp arrives once for all its lanes
+    bool more = t < p.num_tiles && !__any_sync(0xffffffffu, *abort_flag);
+    if (more && !__all_sync(0xffffffffu, mbar_wait<true>(&empty[istage], iphase ^ 1))) {
+      record_error(status, GF_DEV_WAIT_TIMEOUT);
+      *abort_flag = 1;
+      more = false;
+    }
+    if (!more) {
+      // drain: every issued tile is completed and marked full, so the MMA
+      // issuer never waits on a stage that will not fill
+      cp_async_wait<0>();
+      while (pending > 0) finish_oldest();
+      break;
+    }
+    const CtTile tl = ct_tile(p, t);
+    const int n = tl.n, qd = tl.qd, c = tl.c0 + r;
+    const bool cv = c < HW;
+    const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
+    const bool vd = qd + 1 < p.D, vh = qh + 1 < p.H, vw = qw + 1 < p.W;
+    const float* xc = p.x + (size_t(n) * CIN * p.D + qd) * HW + size_t(qh) * p.W + qw;
+    const uint32_t a_hi = smem_u32(a_ring + istage * kCtTcStageBytes);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int pos = k / CIN, ci = k % CIN;
+      const int a = pos >> 2, b = (pos >> 1) & 1, cc = pos & 1;
+      const bool ok = cv && (a == 0 || vd) && (b == 0 || vh) && (cc == 0 || vw);
+      const float* src = ok ? xc + size_t(ci) * p.D * HW + a * HW + b * p.W + cc : p.x;
+      cp_async4(a_hi + sw128_offset(r, k), src, ok ? 4u : 0u);
+    }
+    cp_async_commit();
+    ++pending;
+    if (++istage == kCtTcStages) {
+      istage = 0;
+      iphase ^= 1;
+    }
+    if (pending == kCtTcGatherDepth) {
+      cp_async_wait<kCtTcGatherDepth - 1>();
+      finish_oldest();
+    }
+  }
+}
+
+// The MMA issuer (one thread): per tile 12 MMAs (3xTF32 over 4 k-steps of 8)
+// into TMEM accumulator (tile count % NBUF), then commits to the ring stage's
+// empty barrier and the accumulator's full barrier.
+template <int NBUF, class Prm>
+__device__ __forceinline__ void ct_mma(const Prm& p, uint32_t tmem_base, uint8_t* a_ring, uint8_t* b_tile,
+                                       uint64_t* full, uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
+                                       uint64_t* drain, volatile uint32_t* abort_flag, uint32_t* status) {
+  constexpr uint32_t idesc = idesc_tf32(128, 128);
+  const uint32_t b_hi = smem_u32(b_tile), b_lo = b_hi + kCtTcPlane;
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < p.num_tiles && ok && !*abort_flag; t += gridDim.x) {
+    // the MMA thread polls: one thread costs few issue slots, and its
+    // wake-up latency is on the critical path
+    if (!(ok = mbar_wait(&tempty[acc], acc_phase ^ 1))) break;
+    tc_fence_after();
+    if (!(ok = mbar_wait(&full[stage], phase))) break;
+    tc_fence_after();
+    const uint32_t d = tmem_base + uint32_t(acc * 128);
+    const uint32_t a_hi = smem_u32(a_ring + stage * kCtTcStageBytes), a_lo = a_hi + kCtTcPlane;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint32_t off = uint32_t(kk * 32);
+      mma_tf32(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, kk != 0);
+      mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
+      mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+    }
+    mma_commit(&empty[stage]);
+    mma_commit(&tfull[acc]);
+    if (++stage == kCtTcStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+    if (++acc == NBUF) {
+      acc = 0;
+      acc_phase ^= 1;
+    }
+  }
+  if (!ok) {
+    record_error(status, GF_DEV_WAIT_TIMEOUT);
+    *abort_flag = 1;
+  }
+  mma_commit(drain);
+  if (!mbar_wait<true>(drain, 0)) record_error(status, GF_DEV_WAIT_TIMEOUT);
+}
+
 template <int PASS, int CIN>
 __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcParams p, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_ring = smem;                                    // [S][hi, lo]
   uint8_t* b_tile = smem + kCtTcStages * kCtTcStageBytes;    // [hi, lo]
-  uint64_t* full = reinterpret_cast<uint64_t*>(b_tile + kCtTcBBytes);
+  float* coef_s = reinterpret_cast<float*>(b_tile + kCtTcBBytes);  // [epilogue warp][16][4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(b_tile + kCtTcBBytes + kCtTcCoefBytes);
   uint64_t* empty = full + kCtTcStages;
   uint64_t* tfull = empty + kCtTcStages;
   uint64_t* tempty = tfull + kCtTcAccBufs;
@@ -134,46 +305,18 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
   // ---- setup: barriers, B tile, zero padding of the A ring, TMEM
   if (threadIdx.x == 0) {
     for (int s = 0; s < kCtTcStages; ++s) {
-      mbar_init(&full[s], kCtTcProducerThreads);
+      mbar_init(&full[s], kCtTcProducerThreads / 32);  // one arrival per producer warp
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < kCtTcAccBufs; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kCtTcEpiThreads);
+      mbar_init(&tempty[a], kCtTcEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
-    const int row = i / 32, k = i % 32;  // row = phase*16 + co
-    float v = 0.f;
-    if (k == K && K < 32) {
-      v = p.bias ? __ldg(p.bias + row % 16) : 0.f;  // the bias column (A holds 1 there)
-    } else if (k < K) {
-      const int pos = k / CIN, ci = k % CIN;
-      const int ph3 = row / 16, co = row % 16;
-      // per dimension d (depth, height, width = bit 2, 1, 0 of pos and ph3):
-      // input offset a feeds phase: a=0 -> (p=0, k=1) or (p=1, k=2);
-      // a=1 -> (p=1, k=0); (a=1, p=0) is no tap
-      const int ad = (pos >> 2) & 1, ah = (pos >> 1) & 1, aw = pos & 1;
-      const int pd_ = (ph3 >> 2) & 1, ph_ = (ph3 >> 1) & 1, pw_ = ph3 & 1;
-      const bool used = (ad <= pd_) && (ah <= ph_) && (aw <= pw_);
-      const int kd = ad ? 0 : (pd_ ? 2 : 1), kh = ah ? 0 : (ph_ ? 2 : 1), kw = aw ? 0 : (pw_ ? 2 : 1);
-      const int tap = (kd * 3 + kh) * 3 + kw;
-      if (used) v = __ldg(p.w + (size_t(ci) * 16 + co) * 27 + tap);
-    }
-    *reinterpret_cast<float*>(b_tile + sw128_offset(row, k)) = v;
-    *reinterpret_cast<float*>(b_tile + kCtTcPlane + sw128_offset(row, k)) = v - tf32_hi(v);
-  }
-  // the K padding of every A row is written once: 1 in column K of the hi
-  // plane (so the GEMM adds the bias column of B) and zeros elsewhere
-  for (int i = threadIdx.x; i < kCtTcStages * 2 * 128 * 32; i += blockDim.x) {
-    const int k = i % 32, row = (i / 32) % 128, plane = (i / (32 * 128)) & 1;
-    if (k >= K)
-      *reinterpret_cast<float*>(a_ring + (i / (32 * 128)) * kCtTcPlane + sw128_offset(row, k)) =
-          (k == K && plane == 0) ? 1.f : 0.f;
-  }
+  ct_fill_tiles<CIN>(p.w, p.bias, a_ring, b_tile);
   fence_proxy_async_smem();
   if (warp == kCtTcMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kCtTcTmemCols);
@@ -186,102 +329,21 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
 
   if (warp < 4) {
     // ------------------------------------------------------------ producers
-    const int r = threadIdx.x;  // cell row of the tile
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles && !*abort_flag; t += gridDim.x) {
-      const CtTile tl = ct_tile(p, t);
-      const int n = tl.n, qd = tl.qd, c = tl.c0 + r;
-      const bool cv = c < HW;
-      const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
-      bool ok = mbar_wait<true>(&empty[stage], phase ^ 1);
-      if (!ok) {
-        record_error(status, GF_DEV_WAIT_TIMEOUT);
-        *abort_flag = 1;
-        break;
-      }
-      // all gathers first (independent loads in flight together), then the
-      // swizzled hi/lo rows of the A tile
-      const bool vd = qd + 1 < p.D, vh = qh + 1 < p.H, vw = qw + 1 < p.W;
-      const float* xc = p.x + (size_t(n) * CIN * p.D + qd) * HW + size_t(qh) * p.W + qw;
-      float v[K];
-#pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const int pos = k / CIN, ci = k % CIN;
-        const int a = pos >> 2, b = (pos >> 1) & 1, c = pos & 1;
-        const bool ok = cv && (a == 0 || vd) && (b == 0 || vh) && (c == 0 || vw);
-        v[k] = ok ? __ldg(xc + size_t(ci) * p.D * HW + a * HW + b * p.W + c) : 0.f;
-      }
-      uint8_t* a_hi = a_ring + stage * kCtTcStageBytes;
-      uint8_t* a_lo = a_hi + kCtTcPlane;
-#pragma unroll
-      for (int ch = 0; ch < K / 4; ++ch) {
-        const float v0 = v[4 * ch], v1 = v[4 * ch + 1], v2 = v[4 * ch + 2], v3 = v[4 * ch + 3];
-        const uint32_t off = sw128_offset(r, ch * 4);
-        *reinterpret_cast<float4*>(a_hi + off) = make_float4(v0, v1, v2, v3);
-        *reinterpret_cast<float4*>(a_lo + off) =
-            make_float4(v0 - tf32_hi(v0), v1 - tf32_hi(v1), v2 - tf32_hi(v2), v3 - tf32_hi(v3));
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&full[stage]);
-      if (++stage == kCtTcStages) {
-        stage = 0;
-        phase ^= 1;
-      }
-    }
+    ct_produce<CIN>(p, a_ring, full, empty, abort_flag, status);
   } else if (warp == kCtTcMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(128, 128);
-      const uint32_t b_hi = smem_u32(b_tile), b_lo = b_hi + kCtTcPlane;
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok && !*abort_flag; t += gridDim.x) {
-        // the MMA thread polls: one thread costs few issue slots, and its
-        // wake-up latency is on the critical path
-        if (!(ok = mbar_wait(&tempty[acc], acc_phase ^ 1))) break;
-        tc_fence_after();
-        if (!(ok = mbar_wait(&full[stage], phase))) break;
-        tc_fence_after();
-        const uint32_t d = tmem_base + uint32_t(acc * 128);
-        const uint32_t a_hi = smem_u32(a_ring + stage * kCtTcStageBytes), a_lo = a_hi + kCtTcPlane;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t off = uint32_t(kk * 32);
-          mma_tf32(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, kk != 0);
-          mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
-          mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
-        }
-        mma_commit(&empty[stage]);
-        mma_commit(&tfull[acc]);
-        if (++stage == kCtTcStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (++acc == kCtTcAccBufs) {
-          acc = 0;
-          acc_phase ^= 1;
-        }
-      }
-      if (!ok) {
-        record_error(status, GF_DEV_WAIT_TIMEOUT);
-        *abort_flag = 1;
-      }
-      mma_commit(drain);
-      if (!mbar_wait<true>(drain, 0)) record_error(status, GF_DEV_WAIT_TIMEOUT);
-    }
+    if (lane == 0)
+      ct_mma<kCtTcAccBufs>(p, tmem_base, a_ring, b_tile, full, empty, tfull, tempty, drain, abort_flag, status);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - kCtTcEpiWarp0;  // 0..15
-    const int quad = warp & 3, chunk = e >> 2;
-    const int pd = chunk >> 1, hh = chunk & 1;  // depth and height phase of the chunk
+    const int e = warp - kCtTcEpiWarp0;
+    const int quad = warp & 3;                       // TMEM lane quadrant of the warp
+    const int chunk0 = (e >> 2) * kCtTcEpiChunks;    // first 32-column chunk of the warp
     const int row = quad * 32 + lane;
     const int OD = 2 * p.D - 1, OH = 2 * p.H - 1, OW = 2 * p.W - 1;
     const int OHW = OH * OW;
     const size_t plane = size_t(OD) * OHW;
-    const bool bias_in_epi = K == 32 && p.bias != nullptr;  // otherwise the GEMM added it
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
@@ -289,12 +351,12 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
       const int n = tl.n, rem = tl.rem, qd = tl.qd, c = tl.c0 + row;
       const bool cv = c < HW;
       const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
-      // GroupNorm coefficients of this sample, fetched before the wait: lane
-      // co < 16 holds channel co's (A, B), read back with shuffles
-      float2 abl = make_float2(0.f, 0.f);
-      if constexpr (PASS == 2) abl = __ldg(p.coef + size_t(n) * 16 + (lane & 15));
+      // GroupNorm coefficients of the tile's sample, fetched before the wait
+      // (lane co < 16 holds channel co's (A, A, B, B))
+      float4 cpre = make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (PASS == 2) cpre = __ldg(p.coef + size_t(n) * 16 + (lane & 15));
       bool ok = __all_sync(0xffffffffu, mbar_wait<true>(&tfull[acc], acc_phase));
-      if (!ok || *abort_flag) {
+      if (!ok || __any_sync(0xffffffffu, *abort_flag)) {
         if (!ok) {
           record_error(status, GF_DEV_WAIT_TIMEOUT);
           *abort_flag = 1;
@@ -302,34 +364,87 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
         break;
       }
       tc_fence_after();
-      uint32_t r32[32];
-      GF_TMEM_LD32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * 128 + chunk * 32), r32);
-      GF_TMEM_WAIT32(r32);
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      float* cf = coef_s + e * 64;  // the warp's coefficient slot: 16 x (A, A, B, B) (pass 2)
+      if constexpr (PASS == 2) {
+        // the sync before the write keeps lanes still reading the previous
+        // tile's values safe
+        __syncwarp();
+        if (lane < 16) reinterpret_cast<float4*>(cf)[lane] = cpre;
+        __syncwarp();
+      }
+      float2 gs[4], gq[4];  // pass 1: per-group (sum s, sum s^2) of the thread, as pairs
+#pragma unroll
+      for (int g = 0; g < 4; ++g) gs[g] = gq[g] = make_float2(0.f, 0.f);
+#pragma unroll 1
+      for (int cc = 0; cc < kCtTcEpiChunks; ++cc) {
+        const int chunk = chunk0 + cc, pd = chunk >> 1, hh = chunk & 1;  // depth and height phase
+        uint32_t r32[32];
+        GF_TMEM_LD32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * 128 + chunk * 32), r32);
+        GF_TMEM_WAIT32(r32);
+        if (cc == kCtTcEpiChunks - 1) {  // the accumulator is fully read: release it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+        // r32[2 co + pw] is channel co at phase (pd, hh, pw); pv0 / pv1 say
+        // whether the pw = 0 / 1 output lies inside the output volume
+        const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
+        const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
+        if constexpr (PASS == 1) {
+          // outputs outside the volume are zeroed before Swish (Swish(0) = 0),
+          // so no branch separates the 16 pair chains
+          const float2 m = make_float2(pv0 ? 1.f : 0.f, pv1 ? 1.f : 0.f);
+#pragma unroll
+          for (int co = 0; co < 16; ++co) {
+            float2 y = make_float2(__uint_as_float(r32[2 * co]), __uint_as_float(r32[2 * co + 1]));
+            if constexpr (K == 32) {  // no padding column: the bias is added here
+              if (p.bias) {
+                const float b = __ldg(p.bias + co);
+                y = add2(y, make_float2(b, b));
+              }
+            }
+            const float2 sv = swish2(mul2(y, m));
+            gs[co >> 2] = add2(gs[co >> 2], sv);
+            gq[co >> 2] = fma2(sv, sv, gq[co >> 2]);
+          }
+        } else {
+          // GroupNorm affine A s + B, then HardSwish h sat(h / 6 + 1/2), on
+          // (pw 0, pw 1) pairs; the pair's two outputs are adjacent in memory
+          float* oc = p.out + size_t(n) * 16 * plane + size_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
+#pragma unroll
+          for (int co = 0; co < 16; ++co) {
+            float2 y = make_float2(__uint_as_float(r32[2 * co]), __uint_as_float(r32[2 * co + 1]));
+            if constexpr (K == 32) {
+              if (p.bias) {
+                const float b = __ldg(p.bias + co);
+                y = add2(y, make_float2(b, b));
+              }
+            }
+            const float4 ab = reinterpret_cast<const float4*>(cf)[co];  // (A, A, B, B), a broadcast read
+            const float2 h = fma2(make_float2(ab.x, ab.y), swish2(y), make_float2(ab.z, ab.w));
+            // (f32x2 FMAs have no saturating form)
+            const float2 o = mul2(h, make_float2(__saturatef(fmaf(h.x, 1.f / 6.f, 0.5f)),
+                                                 __saturatef(fmaf(h.y, 1.f / 6.f, 0.5f))));
+            if (pv0) __stcs(oc, o.x);
+            if (pv1) __stcs(oc + 1, o.y);
+            oc += plane;
+          }
+        }
+      }
       if (++acc == kCtTcAccBufs) {
         acc = 0;
         acc_phase ^= 1;
       }
-      // columns (pw, co) of phase (pd, hh, pw); masks as 0/1 factors so no
-      // branch separates the 32 Swish chains
-      const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
-      const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
       if constexpr (PASS == 1) {
-        const float m0 = pv0 ? 1.f : 0.f, m1 = pv1 ? 1.f : 0.f;
-        float gs[4] = {0.f, 0.f, 0.f, 0.f}, gq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int co = 0; co < 16; ++co) {
-          const float b = bias_in_epi ? __ldg(p.bias + co) : 0.f;
-          const float s0 = swish(__uint_as_float(r32[co]) + b) * m0;
-          const float s1 = swish(__uint_as_float(r32[16 + co]) + b) * m1;
-          gs[co >> 2] += s0 + s1;
-          gq[co >> 2] = fmaf(s0, s0, fmaf(s1, s1, gq[co >> 2]));
-        }
         // reduce-scatter of the 8 sums over the warp's 32 lanes (9 shuffles):
         // afterwards lane l holds the full sum of value v = 4*b4 + 2*b3 + b2
         // (b_i = bit i of l), value v being gs[v/2] (even v) or gq[v/2] (odd)
-        float r[8] = {gs[0], gq[0], gs[1], gq[1], gs[2], gq[2], gs[3], gq[3]};
+        float r[8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          r[2 * g] = gs[g].x + gs[g].y;
+          r[2 * g + 1] = gq[g].x + gq[g].y;
+        }
         {
           const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
 #pragma unroll
@@ -357,18 +472,6 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
           float* dst = reinterpret_cast<float*>(p.part) +
                        (((size_t(n) * 4 + (v >> 1)) * size_t(p.D * p.bpp) + rem) * kCtTcEpiWarps + e) * 2 + (v & 1);
           *dst = r[0];
-        }
-      } else {
-        float* ob = p.out + size_t(n) * 16 * plane + size_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
-#pragma unroll
-        for (int co = 0; co < 16; ++co) {
-          const float b = bias_in_epi ? __ldg(p.bias + co) : 0.f;
-          const float2 ab = make_float2(__shfl_sync(0xffffffffu, abl.x, co), __shfl_sync(0xffffffffu, abl.y, co));
-          const float h0 = fmaf(ab.x, swish(__uint_as_float(r32[co]) + b), ab.y);
-          const float h1 = fmaf(ab.x, swish(__uint_as_float(r32[16 + co]) + b), ab.y);
-          float* oc = ob + size_t(co) * plane;
-          if (pv0) __stcs(oc, h0 * __saturatef(fmaf(h0, 1.f / 6.f, 0.5f)));
-          if (pv1) __stcs(oc + 1, h1 * __saturatef(fmaf(h1, 1.f / 6.f, 0.5f)));
         }
       }
     }

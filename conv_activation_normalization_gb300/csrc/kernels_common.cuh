@@ -14,6 +14,50 @@ namespace gf {
 // inf and the quotient is the correct limit -0.
 __device__ __forceinline__ float swish(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
+// Packed pair arithmetic: one f32x2 instruction (round to nearest) works on
+// both lanes of a float2.
+__device__ __forceinline__ unsigned long long f2_as_u64(float2 a) { return *reinterpret_cast<unsigned long long*>(&a); }
+__device__ __forceinline__ float2 u64_as_f2(unsigned long long a) { return *reinterpret_cast<float2*>(&a); }
+
+// d = a * b + c on both lanes of a pair (fma.rn.f32x2).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_as_u64(a)), "l"(f2_as_u64(b)), "l"(f2_as_u64(c)));
+  return u64_as_f2(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_as_u64(a)), "l"(f2_as_u64(b)));
+  return u64_as_f2(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_as_u64(a)), "l"(f2_as_u64(b)));
+  return u64_as_f2(d);
+}
+
+// The special-function unit's 2^t and 1/d (ex2.approx / rcp.approx, denormal
+// results flushed to zero).
+__device__ __forceinline__ float ex2_approx(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+  return r;
+}
+
+// Swish of a pair, v * 1 / (1 + 2^(-v log2 e)), with the multiplies and the
+// add packed.  Same limits as swish(): e^-v = inf gives 1/inf = 0 and -0.
+__device__ __forceinline__ float2 swish2(float2 v) {
+  constexpr float kNegLog2e = -1.4426950408889634f;
+  const float2 t = mul2(v, make_float2(kNegLog2e, kNegLog2e));
+  const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.f, 1.f));
+  return mul2(v, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
 // Exact GELU v * Phi(v) = 0.5 v (1 + erf(v / sqrt 2)), with CUDA's erff.
 __device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
 
