@@ -38,8 +38,8 @@
 //   warps 7-22   epilogue: warp (7 + e) owns TMEM lane quadrant (warp % 4)
 //                and the 32 columns of chunk e / 4 (output phases
 //                pd = chunk / 2, ph = chunk % 2, 16 channels x both pw); per
-//                round it writes the tile from three rounds earlier, then
-//                does the statistics work of the new tile.
+//                round it writes the tile from three rounds earlier and does
+//                the statistics work of the new tile, the two interleaved.
 #pragma once
 
 #include "convt3d_tc.cuh"
@@ -86,6 +86,79 @@ __device__ __forceinline__ bool cf_wait_count(const uint32_t* cnt, uint32_t need
     __nanosleep(64);
     if (ld_acquire_gpu(cnt) >= need) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// One round of an epilogue warp: the output of an earlier tile (OUT) and the
+// statistics work of the new tile (P1), interleaved channel by channel, a few
+// columns at a time, so that the Swish of one and the stores of the other
+// overlap.  Columns 2 co + pw of the warp's chunk are channel co at width
+// phase pw.
+struct CfOutSide {
+  uint32_t taddr;     // TMEM address of the warp's 32 columns (Swish values)
+  float* oc;          // output of channel 0, width phase 0
+  const float* cf;    // (A, A, B, B) per channel
+  bool pv0, pv1;      // the width-phase-0 / 1 outputs lie inside the volume
+  uint64_t* tempty;   // released once the columns are read
+};
+struct CfStatSide {
+  uint32_t taddr;     // TMEM address of the warp's 32 columns (accumulator)
+  float2 m;           // 1 / 0 per width phase: inside the volume or not
+};
+
+template <bool OUT, bool P1, int K>
+__device__ __forceinline__ void cf_round(const CfOutSide& o, const CfStatSide& q, const float* bias, size_t plane,
+                                         int lane, float2 (&gs)[4], float2 (&gq)[4]) {
+  float* oc = o.oc;
+  // columns in pieces of kPiece (TMEM loads of 8 keep the registers down)
+  constexpr int kPiece = 8;
+#pragma unroll
+  for (int part = 0; part < 32 / kPiece; ++part) {
+    uint32_t ry[kPiece], rz[kPiece];
+    if constexpr (P1) GF_TMEM_LD8(q.taddr + uint32_t(part * kPiece), ry);
+    if constexpr (OUT) GF_TMEM_LD8(o.taddr + uint32_t(part * kPiece), rz);
+    if constexpr (P1) GF_TMEM_WAIT8(ry);
+    if constexpr (OUT) {
+      GF_TMEM_WAIT8(rz);
+      if (part == 32 / kPiece - 1) {  // all columns read: the MMAs may overwrite the buffer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o.tempty);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPiece / 2; ++j) {
+      const int co = part * (kPiece / 2) + j;
+      if constexpr (P1) {
+        float2 y = make_float2(__uint_as_float(ry[2 * j]), __uint_as_float(ry[2 * j + 1]));
+        if constexpr (K == 32) {  // no padding column: the bias is added here
+          if (bias) {
+            const float b = __ldg(bias + co);
+            y = add2(y, make_float2(b, b));
+          }
+        }
+        // outputs outside the volume are zeroed before Swish (Swish(0) = 0)
+        const float2 sv = swish2(mul2(y, q.m));
+        gs[co >> 2] = add2(gs[co >> 2], sv);
+        gq[co >> 2] = fma2(sv, sv, gq[co >> 2]);
+        ry[2 * j] = __float_as_uint(sv.x);
+        ry[2 * j + 1] = __float_as_uint(sv.y);
+      }
+      if constexpr (OUT) {
+        // GroupNorm affine A s + B, then HardSwish h sat(h / 6 + 1/2); the
+        // pair's two outputs are adjacent in memory
+        const float2 sv = make_float2(__uint_as_float(rz[2 * j]), __uint_as_float(rz[2 * j + 1]));
+        const float4 ab = reinterpret_cast<const float4*>(o.cf)[co];  // a broadcast read
+        const float2 h = fma2(make_float2(ab.x, ab.y), sv, make_float2(ab.z, ab.w));
+        // (f32x2 FMAs have no saturating form)
+        const float2 v = mul2(h, make_float2(__saturatef(fmaf(h.x, 1.f / 6.f, 0.5f)),
+                                             __saturatef(fmaf(h.y, 1.f / 6.f, 0.5f))));
+        if (o.pv0) __stcs(oc, v.x);
+        if (o.pv1) __stcs(oc + 1, v.y);
+        oc += plane;
+      }
+    }
+    if constexpr (P1) GF_TMEM_ST8(q.taddr + uint32_t(part * kPiece), ry);
   }
 }
 
@@ -264,129 +337,99 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
     const uint32_t lane_base = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(chunk * 32);
     for (int r = 0; r < p.rounds + kCfLag; ++r) {
       if (__any_sync(kFull, *abort_flag)) break;
-      if (r >= kCfLag) {
-        // -------- output of the tile of round r - kCfLag
-        const int ro = r - kCfLag, t = blockIdx.x + ro * G;
-        if (t < p.num_tiles) {
-          const int buf = ro % kCfBufs;
-          if (!__all_sync(kFull, mbar_wait<true>(&cfull[buf], (ro / kCfBufs) & 1))) {
-            fail();
-            break;
-          }
-          const CtTile tl = ct_tile(p, t);
-          const int n = tl.n, qd = tl.qd, c = tl.c0 + row;
-          const bool cv = c < HW;
-          const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
-          const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
-          const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
-          uint32_t r32[32];
-          GF_TMEM_LD32(lane_base + uint32_t(buf * 128), r32);
-          GF_TMEM_WAIT32(r32);
-          // the buffer is read: the MMAs of tile ro + kCfBufs may overwrite it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
-          const float* cf = coef_s + buf * kCfCoefFloats;
-          // GroupNorm affine A s + B, then HardSwish h sat(h / 6 + 1/2), on
-          // (pw 0, pw 1) pairs; the pair's two outputs are adjacent in memory
-          float* oc = p.out + size_t(n) * 16 * plane + size_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
-#pragma unroll
-          for (int co = 0; co < 16; ++co) {
-            const float2 sv = make_float2(__uint_as_float(r32[2 * co]), __uint_as_float(r32[2 * co + 1]));
-            const float4 ab = reinterpret_cast<const float4*>(cf)[co];  // (A, A, B, B), a broadcast read
-            const float2 h = fma2(make_float2(ab.x, ab.y), sv, make_float2(ab.z, ab.w));
-            // (f32x2 FMAs have no saturating form)
-            const float2 o = mul2(h, make_float2(__saturatef(fmaf(h.x, 1.f / 6.f, 0.5f)),
-                                                 __saturatef(fmaf(h.y, 1.f / 6.f, 0.5f))));
-            if (pv0) __stcs(oc, o.x);
-            if (pv1) __stcs(oc + 1, o.y);
-            oc += plane;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&cempty[buf]);
-        }
-      }
-      if (r < p.rounds) {
-        // -------- statistics of the tile of round r
-        const int t = blockIdx.x + r * G;
-        if (!__all_sync(kFull, mbar_wait<true>(&pempty[r & 1], ((r >> 1) & 1) ^ 1))) {
+      // output of the tile of round r - kCfLag, statistics of the tile of round r
+      const int ro = r - kCfLag, to = blockIdx.x + ro * G, tp = blockIdx.x + r * G;
+      const bool has_out = r >= kCfLag && to < p.num_tiles, has_p1 = r < p.rounds && tp < p.num_tiles;
+      CfOutSide o{};
+      CfStatSide q{};
+      int ob = 0;
+      if (has_out) {
+        ob = ro % kCfBufs;
+        if (!__all_sync(kFull, mbar_wait<true>(&cfull[ob], (ro / kCfBufs) & 1))) {
           fail();
           break;
         }
-        if (t < p.num_tiles) {
-          const int buf = r % kCfBufs;
-          if (!__all_sync(kFull, mbar_wait<true>(&tfull[buf], (r / kCfBufs) & 1))) {
-            fail();
-            break;
+        const CtTile tl = ct_tile(p, to);
+        const int qd = tl.qd, c = tl.c0 + row;
+        const bool cv = c < HW;
+        const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
+        o.pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
+        o.pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
+        o.taddr = lane_base + uint32_t(ob * 128);
+        o.oc = p.out + size_t(tl.n) * 16 * plane + size_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
+        o.cf = coef_s + ob * kCfCoefFloats;
+        o.tempty = &tempty[ob];
+      }
+      if (r < p.rounds && !__all_sync(kFull, mbar_wait<true>(&pempty[r & 1], ((r >> 1) & 1) ^ 1))) {
+        fail();
+        break;
+      }
+      if (has_p1) {
+        const int buf = r % kCfBufs;
+        if (!__all_sync(kFull, mbar_wait<true>(&tfull[buf], (r / kCfBufs) & 1))) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const CtTile tl = ct_tile(p, tp);
+        const int qd = tl.qd, c = tl.c0 + row;
+        const bool cv = c < HW;
+        const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
+        const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
+        const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
+        q.taddr = lane_base + uint32_t(buf * 128);
+        q.m = make_float2(pv0 ? 1.f : 0.f, pv1 ? 1.f : 0.f);
+      }
+      float2 gs[4], gq[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) gs[g] = gq[g] = make_float2(0.f, 0.f);
+      if (has_out && has_p1)
+        cf_round<true, true, K>(o, q, p.bias, plane, lane, gs, gq);
+      else if (has_out)
+        cf_round<true, false, K>(o, q, p.bias, plane, lane, gs, gq);
+      else if (has_p1)
+        cf_round<false, true, K>(o, q, p.bias, plane, lane, gs, gq);
+      if (has_out) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cempty[ob]);
+      }
+      if (has_p1) {
+        // reduce-scatter of the 8 sums over the warp's 32 lanes (9
+        // shuffles): afterwards lane l holds the full sum of value
+        // v = 4*b4 + 2*b3 + b2 (b_i = bit i of l), value v being gs[v/2]
+        // (even v) or gq[v/2] (odd v)
+        float rs[8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          rs[2 * g] = gs[g].x + gs[g].y;
+          rs[2 * g + 1] = gq[g].x + gq[g].y;
+        }
+        {
+          const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float send = b4 ? rs[i] : rs[4 + i];
+            const float keep = b4 ? rs[4 + i] : rs[i];
+            rs[i] = keep + __shfl_xor_sync(kFull, send, 16);
           }
-          tc_fence_after();
-          const CtTile tl = ct_tile(p, t);
-          const int qd = tl.qd, c = tl.c0 + row;
-          const bool cv = c < HW;
-          const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
-          const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
-          const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
-          const uint32_t taddr = lane_base + uint32_t(buf * 128);
-          uint32_t r32[32];
-          GF_TMEM_LD32(taddr, r32);
-          GF_TMEM_WAIT32(r32);
-          // r32[2 co + pw] is channel co at phase (pd, hh, pw); outputs
-          // outside the volume are zeroed before Swish (Swish(0) = 0)
-          const float2 m = make_float2(pv0 ? 1.f : 0.f, pv1 ? 1.f : 0.f);
-          float2 gs[4], gq[4];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) gs[g] = gq[g] = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int co = 0; co < 16; ++co) {
-            float2 y = make_float2(__uint_as_float(r32[2 * co]), __uint_as_float(r32[2 * co + 1]));
-            if constexpr (K == 32) {  // no padding column: the bias is added here
-              if (p.bias) {
-                const float b = __ldg(p.bias + co);
-                y = add2(y, make_float2(b, b));
-              }
-            }
-            const float2 sv = swish2(mul2(y, m));
-            gs[co >> 2] = add2(gs[co >> 2], sv);
-            gq[co >> 2] = fma2(sv, sv, gq[co >> 2]);
-            r32[2 * co] = __float_as_uint(sv.x);
-            r32[2 * co + 1] = __float_as_uint(sv.y);
-          }
-          GF_TMEM_ST32(taddr, r32);
-          // reduce-scatter of the 8 sums over the warp's 32 lanes (9
-          // shuffles): afterwards lane l holds the full sum of value
-          // v = 4*b4 + 2*b3 + b2 (b_i = bit i of l), value v being gs[v/2]
-          // (even v) or gq[v/2] (odd v)
-          float rs[8];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            rs[2 * g] = gs[g].x + gs[g].y;
-            rs[2 * g + 1] = gq[g].x + gq[g].y;
+          for (int i = 0; i < 2; ++i) {
+            const float send = b3 ? rs[i] : rs[2 + i];
+            const float keep = b3 ? rs[2 + i] : rs[i];
+            rs[i] = keep + __shfl_xor_sync(kFull, send, 8);
           }
           {
-            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float send = b4 ? rs[i] : rs[4 + i];
-              const float keep = b4 ? rs[4 + i] : rs[i];
-              rs[i] = keep + __shfl_xor_sync(kFull, send, 16);
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const float send = b3 ? rs[i] : rs[2 + i];
-              const float keep = b3 ? rs[2 + i] : rs[i];
-              rs[i] = keep + __shfl_xor_sync(kFull, send, 8);
-            }
-            {
-              const float send = b2 ? rs[0] : rs[1];
-              const float keep = b2 ? rs[1] : rs[0];
-              rs[0] = keep + __shfl_xor_sync(kFull, send, 4);
-            }
-            rs[0] += __shfl_xor_sync(kFull, rs[0], 2);
-            rs[0] += __shfl_xor_sync(kFull, rs[0], 1);
+            const float send = b2 ? rs[0] : rs[1];
+            const float keep = b2 ? rs[1] : rs[0];
+            rs[0] = keep + __shfl_xor_sync(kFull, send, 4);
           }
-          if ((lane & 3) == 0) part_s[(r & 1) * kCfPartFloats + e * 8 + (lane >> 2)] = rs[0];
-          tmem_wait_st();
+          rs[0] += __shfl_xor_sync(kFull, rs[0], 2);
+          rs[0] += __shfl_xor_sync(kFull, rs[0], 1);
         }
+        if ((lane & 3) == 0) part_s[(r & 1) * kCfPartFloats + e * 8 + (lane >> 2)] = rs[0];
+        tmem_wait_st();
+      }
+      if (r < p.rounds) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[r & 1]);
       }

@@ -244,6 +244,55 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
                :                                                                                           \
                : "memory")
 
+// 32 lanes x 8 consecutive 32-bit TMEM columns -> 8 registers per thread.
+#define GF_TMEM_LD8(taddr, r)                                                                               \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"                     \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),        \
+                 "=r"(r[7])                                                                                \
+               : "r"(taddr))
+
+#define GF_TMEM_WAIT8(r)                                                                                    \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                                            \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),        \
+                 "+r"(r[7])                                                                                \
+               :                                                                                           \
+               : "memory")
+
+#define GF_TMEM_ST8(taddr, r)                                                                               \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"                     \
+               :                                                                                           \
+               : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),    \
+                 "r"(r[7])                                                                                 \
+               : "memory")
+
+// 32 lanes x 16 consecutive 32-bit TMEM columns -> 16 registers per thread.
+#define GF_TMEM_LD16(taddr, r)                                                                              \
+  asm volatile(                                                                                            \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "                                                            \
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"                                    \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),     \
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),             \
+        "=r"(r[15])                                                                                        \
+      : "r"(taddr))
+
+#define GF_TMEM_WAIT16(r)                                                                                   \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                                            \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),        \
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),    \
+                 "+r"(r[14]), "+r"(r[15])                                                                  \
+               :                                                                                           \
+               : "memory")
+
+// 16 registers per thread -> 32 lanes x 16 consecutive 32-bit TMEM columns.
+#define GF_TMEM_ST16(taddr, r)                                                                              \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "                                              \
+               "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"                                  \
+               :                                                                                           \
+               : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),    \
+                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),           \
+                 "r"(r[14]), "r"(r[15])                                                                    \
+               : "memory")
+
 // 32 registers per thread -> 32 lanes x 32 consecutive 32-bit TMEM columns.
 #define GF_TMEM_ST32(taddr, r)                                                                              \
   asm volatile(                                                                                            \
