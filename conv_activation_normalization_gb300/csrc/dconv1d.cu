@@ -123,35 +123,66 @@ __device__ __forceinline__ void store_planes(void* planes, size_t plane_elems, s
   }
 }
 
-// grid (ceil(L/32), C/32, B), block (32, 8): GELU(LayerNorm(x)) for a 32x32
-// (channel, position) tile, written transposed to [B][L][C] operand planes.
+// The operand planes of 4 consecutive channels (element offset o, a
+// multiple of 4): one 16-byte store per fp32 plane, 8 bytes per bf16 plane.
+template <int MODE>
+__device__ __forceinline__ void store_planes4(void* planes, size_t plane_elems, size_t o, float4 v) {
+  if constexpr (MODE == GF_MODE_FP32_3XTF32) {
+    float* p = static_cast<float*>(planes);
+    __stcs(reinterpret_cast<float4*>(p + o), v);
+    __stcs(reinterpret_cast<float4*>(p + plane_elems + o),
+           make_float4(v.x - tf32_hi(v.x), v.y - tf32_hi(v.y), v.z - tf32_hi(v.z), v.w - tf32_hi(v.w)));
+  } else {
+    __nv_bfloat16* p = static_cast<__nv_bfloat16*>(planes);
+    Bf16x4 h, l;
+    bf16_split4(v, h, l);
+    *reinterpret_cast<Bf16x4*>(p + o) = h;
+    if constexpr (MODE == GF_MODE_FP32_3XBF16) *reinterpret_cast<Bf16x4*>(p + plane_elems + o) = l;
+  }
+}
+
+// grid (ceil(L/128), C/32, B), 256 threads: GELU(LayerNorm(x)) for a tile of
+// 32 channels x 128 positions, read as float4 along L (x, gamma, beta),
+// transposed through shared memory and written 4 channels at a time to the
+// [B][L][C] operand planes.  L is a multiple of 4.
 template <int MODE>
 __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta,
                                                                   const float2* __restrict__ stats, void* planes,
                                                                   int C, int L, int B) {
-  __shared__ float tile[32][33];
-  const int l0 = blockIdx.x * 32, c0 = blockIdx.y * 32, b = blockIdx.z;
+  __shared__ __align__(16) float tile[32][132];  // [channel][position]; 16-byte rows, 4-way reads
+  const int l0 = blockIdx.x * 128, c0 = blockIdx.y * 32, b = blockIdx.z;
   const float2 st = stats[b];
-  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int t = threadIdx.x;
+  const float* xb = x + size_t(b) * C * L;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int c = c0 + ty + 8 * r, l = l0 + tx;
-    float a = 0.f;
+  for (int i = 0; i < 4; ++i) {
+    const int item = t + 256 * i, cc = item >> 5, q = item & 31;  // a warp: one channel, 128 positions
+    const int l = l0 + 4 * q;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (l < L) {
-      const size_t cl = size_t(c) * L + l;
-      const float v = __ldg(x + size_t(b) * C * L + cl);
-      a = gelu_erf(fmaf((v - st.x) * st.y, __ldg(gamma + cl), __ldg(beta + cl)));
+      const size_t cl = size_t(c0 + cc) * L + l;
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(xb + cl));
+      const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + cl));
+      const float4 be = __ldg(reinterpret_cast<const float4*>(beta + cl));
+      a.x = gelu_erf(fmaf((v.x - st.x) * st.y, g.x, be.x));
+      a.y = gelu_erf(fmaf((v.y - st.x) * st.y, g.y, be.y));
+      a.z = gelu_erf(fmaf((v.z - st.x) * st.y, g.z, be.z));
+      a.w = gelu_erf(fmaf((v.w - st.x) * st.y, g.w, be.w));
     }
-    tile[ty + 8 * r][tx] = a;
+    *reinterpret_cast<float4*>(&tile[cc][4 * q]) = a;
   }
   __syncthreads();
   const size_t plane = size_t(B) * L * C;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int l = l0 + ty + 8 * r, c = c0 + tx;
-    if (l < L) store_planes<MODE>(planes, plane, (size_t(b) * L + l) * C + c, tile[tx][ty + 8 * r]);
+  for (int i = 0; i < 4; ++i) {
+    const int item = t + 256 * i, pl = item >> 3, cq = item & 7;  // a warp: 4 positions x 32 channels
+    const int l = l0 + pl;
+    if (l < L)
+      store_planes4<MODE>(planes, plane, (size_t(b) * L + l) * C + c0 + 4 * cq,
+                          make_float4(tile[4 * cq][pl], tile[4 * cq + 1][pl], tile[4 * cq + 2][pl],
+                                      tile[4 * cq + 3][pl]));
   }
 }
 
@@ -254,8 +285,8 @@ template <int MODE>
 void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
                          const float2* stats, void* a_planes, void* w_planes, int64_t B, int64_t C, int64_t L,
                          int32_t ksize, const DeviceInfo& dev, cudaStream_t s) {
-  ln_apply_gelu_split_kernel<MODE><<<dim3(unsigned((L + 31) / 32), unsigned(C / 32), unsigned(B)), dim3(32, 8), 0,
-                                     s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L), int(B));
+  ln_apply_gelu_split_kernel<MODE><<<dim3(unsigned((L + 127) / 128), unsigned(C / 32), unsigned(B)), 256, 0, s>>>(
+      x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L), int(B));
   const int64_t n = C * C * ksize;
   const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
   conv_weight_split_kernel<MODE><<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), ksize);
