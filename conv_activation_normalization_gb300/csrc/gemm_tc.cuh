@@ -16,16 +16,20 @@
 //   OpBF16x1  one BF16 product (the BF16 mode).
 // All modes accumulate in fp32 in TMEM.
 //
-// Roles (one CTA per SM, 192 threads):
+// Roles (one CTA per SM, 320 threads):
 //   warp 0      one thread issues TMA loads of a k-block's operand tiles (one
 //               or two planes of A and of B) into a ring of smem stages
 //               (full/empty mbarriers);
 //   warp 1      owns the TMEM allocation; one thread issues tcgen05.mma into
 //               one of two TMEM accumulators (BN columns each), commits to the
 //               stage's "empty" barrier and, per tile, to "tmem_full";
-//   warps 2..5  the epilogue: each thread owns one accumulator row (TMEM lane),
-//               reads it with tcgen05.ld, runs the fused epilogue, then frees
-//               the accumulator ("tmem_empty") for the tile after next.
+//   warps 2..9  the epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (one
+//               accumulator row per thread) and, for tiles of 128 or more
+//               columns, half of the columns (warps 2..5 the first half,
+//               6..9 the second), runs the fused epilogue on them, then frees
+//               the accumulator ("tmem_empty") for the tile after next.  The
+//               epilogue sees its half as a tile of BN / 2 columns starting at
+//               n0 + half * BN / 2 with n-block index 2 nb + half.
 // The two accumulators let tile i's epilogue overlap tile i+1's mainloop.
 // Every smem row is 128 bytes (32 fp32 or 64 bf16 along K) with 128-byte
 // swizzle, so one MMA K-step is always 32 bytes of the row.
@@ -44,8 +48,10 @@
 namespace gf {
 
 constexpr int kBM = 128;  // tile rows = TMEM lanes
-constexpr int kGemmThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
+// column halves of a BN-wide tile served by separate epilogue warps
+__host__ __device__ constexpr int epi_halves(int bn) { return bn >= 128 ? 2 : 1; }
 
 enum class MmaKind { TF32, BF16 };
 
@@ -189,7 +195,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiThreads);
+      mbar_init(&tempty[a], 128 * epi_halves(BN));  // every thread of the active epilogue warps
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -310,15 +316,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    constexpr int H = epi_halves(BN), BNW = BN / H;
     const int quad = warp & 3;  // TMEM lanes this warp may read: 32*quad ..
     const int row = quad * 32 + lane;
+    const int half = (warp - 2) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    // narrow tiles (H == 1): the second set of epilogue warps idles
+    for (int t = blockIdx.x; half < H && t < num_tiles; t += gridDim.x) {
       const Tile tile = src.tile(t);
       bool ok = mbar_wait(&tfull[acc], acc_phase);
       ok = __all_sync(0xffffffffu, ok);
-      if (!ok || *abort_flag) {
+      if (!ok || __any_sync(0xffffffffu, *abort_flag)) {
         if (!ok) {
           record_error(status, GF_DEV_WAIT_TIMEOUT);
           *abort_flag = 1;
@@ -326,8 +335,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
-      Epi::template apply<BN>(ep, taddr, tile, row);
+      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN + half * BNW);
+      const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
+      Epi::template apply<BNW>(ep, taddr, part, row);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       if (++acc == 2) {

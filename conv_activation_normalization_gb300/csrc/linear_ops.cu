@@ -27,6 +27,9 @@ struct EpiSwishBiasGN {
     int M, N;
     float eps;
   };
+  // Per 64-column group (one GroupNorm group of the row): t = Swish(y + b_lin)
+  // + bias, mean and centred second moment of t in registers, then
+  // (t - mean) rstd gamma + beta; pairs of columns share packed f32x2 ops.
   template <int BN>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
     const int m = t.r0 + row;
@@ -37,36 +40,41 @@ struct EpiSwishBiasGN {
       if (n0 >= p.N) break;  // uniform across the warp
       float v[64];
       tmem_load64(taddr + uint32_t(g * 64), v);
-      float sum = 0.f;
+      float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < 64; j += 4) {
         const float4 bl = p.b_lin ? __ldg(reinterpret_cast<const float4*>(p.b_lin + n0 + j)) : make_float4(0, 0, 0, 0);
         const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + j));
-        v[j + 0] = swish(v[j + 0] + bl.x) + bb.x;
-        v[j + 1] = swish(v[j + 1] + bl.y) + bb.y;
-        v[j + 2] = swish(v[j + 2] + bl.z) + bb.z;
-        v[j + 3] = swish(v[j + 3] + bl.w) + bb.w;
-        sum += (v[j] + v[j + 1]) + (v[j + 2] + v[j + 3]);
+        const float2 a = add2(swish2(add2(make_float2(v[j], v[j + 1]), make_float2(bl.x, bl.y))),
+                              make_float2(bb.x, bb.y));
+        const float2 c = add2(swish2(add2(make_float2(v[j + 2], v[j + 3]), make_float2(bl.z, bl.w))),
+                              make_float2(bb.z, bb.w));
+        v[j] = a.x;
+        v[j + 1] = a.y;
+        v[j + 2] = c.x;
+        v[j + 3] = c.y;
+        sum = add2(sum, add2(a, c));
       }
-      const float mean = sum * (1.f / 64.f);
-      float m2 = 0.f;
+      const float mean = (sum.x + sum.y) * (1.f / 64.f);
+      const float2 nmean = make_float2(-mean, -mean);
+      float2 m2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float d = v[j] - mean;
-        m2 = fmaf(d, d, m2);
+      for (int j = 0; j < 64; j += 2) {
+        const float2 d = add2(make_float2(v[j], v[j + 1]), nmean);
+        m2 = fma2(d, d, m2);
       }
-      const float rstd = rsqrtf(m2 * (1.f / 64.f) + p.eps);
+      const float rstd = rsqrtf((m2.x + m2.y) * (1.f / 64.f) + p.eps);
+      const float2 r2 = make_float2(rstd, rstd);
       float* orow = p.out + size_t(m) * size_t(p.N) + n0;
 #pragma unroll
       for (int j = 0; j < 64; j += 4) {
         const float4 ga = __ldg(reinterpret_cast<const float4*>(p.gamma + n0 + j));
         const float4 be = __ldg(reinterpret_cast<const float4*>(p.beta + n0 + j));
-        float4 o;
-        o.x = fmaf((v[j + 0] - mean) * rstd, ga.x, be.x);
-        o.y = fmaf((v[j + 1] - mean) * rstd, ga.y, be.y);
-        o.z = fmaf((v[j + 2] - mean) * rstd, ga.z, be.z);
-        o.w = fmaf((v[j + 3] - mean) * rstd, ga.w, be.w);
-        if (valid) __stcs(reinterpret_cast<float4*>(orow + j), o);
+        const float2 a = fma2(mul2(add2(make_float2(v[j], v[j + 1]), nmean), r2), make_float2(ga.x, ga.y),
+                              make_float2(be.x, be.y));
+        const float2 c = fma2(mul2(add2(make_float2(v[j + 2], v[j + 3]), nmean), r2), make_float2(ga.z, ga.w),
+                              make_float2(be.z, be.w));
+        if (valid) __stcs(reinterpret_cast<float4*>(orow + j), make_float4(a.x, a.y, c.x, c.y));
       }
     }
   }
@@ -78,7 +86,7 @@ struct EpiLSEPartial {
   static constexpr bool kFixedBN = true;  // one partial per 256-column block
   struct Params {
     const float* b;  // may be null
-    float2* part;    // [M][n_blocks]
+    float2* part;    // [M][n_blocks]: one per row and epilogue column range
     int M, N, n_blocks;
   };
   template <int BN>
@@ -148,6 +156,7 @@ __global__ void lse_merge_act_kernel(const float2* __restrict__ part, float* __r
   float mx = -INFINITY, s = 0.f;
   for (int i = lane; i < n_blocks; i += 32) {
     const float2 q = part[size_t(warp) * n_blocks + i];
+    if (q.x == -INFINITY) continue;  // a column range with no valid column
     const float nm = fmaxf(mx, q.x);
     s = s * __expf(mx - nm) + q.y * __expf(q.x - nm);
     mx = nm;
@@ -549,7 +558,8 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
 
 size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {
   if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
-  const int64_t nb = (N + kBNLinear - 1) / kBNLinear;
+  // one (max, sum) partial per row and epilogue column half of each n-block
+  const int64_t nb = (N + kBNLinear - 1) / kBNLinear * epi_halves(kBNLinear);
   return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode) +
          align_up(size_t(M) * nb * sizeof(float2), 256);
 }
@@ -573,7 +583,7 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float2* part = reinterpret_cast<float2*>(ws + operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode));
-  const int nb = int((N + kBNLinear - 1) / kBNLinear);
+  const int nb = int((N + kBNLinear - 1) / kBNLinear) * epi_halves(kBNLinear);
   EpiLSEPartial::Params ep{b, part, int(M), int(N), nb};
   // m-blocks fastest: the CTAs in flight share n-blocks, so each W tile is
   // fetched from HBM once and reused by every m-block from L2.
