@@ -55,8 +55,12 @@ constexpr int kCfBufs = 4;                          // TMEM tile buffers of 128 
 constexpr int kCfLag = 3;                           // rounds between a tile's statistics and its output
 constexpr int kCfCoefFloats = 16 * 4;               // per buffer: 16 channels x (A, A, B, B)
 constexpr int kCfPartFloats = kCfEpiWarps * 8;      // per round: 8 sums per epilogue warp
+// per buffer and epilogue thread: the tile's output offset with the two
+// in-volume flags in bits 62 and 63, written with the statistics work and
+// read back three rounds later for the output
+constexpr int kCfDecBytes = kCfBufs * kCfEpiWarps * 32 * 8;
 constexpr int kCfSmem = kCtTcStages * kCtTcStageBytes + kCtTcBBytes + kCfBufs * kCfCoefFloats * 4 +
-                        2 * kCfPartFloats * 4 + 1024 /*barriers*/ + 1024 /*alignment*/;
+                        2 * kCfPartFloats * 4 + kCfDecBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 
 struct CfParams {
   const float* x;
@@ -87,6 +91,32 @@ __device__ __forceinline__ bool cf_wait_count(const uint32_t* cnt, uint32_t need
     if (ld_acquire_gpu(cnt) >= need) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// Double-float arithmetic for the GroupNorm totals (fp64 is slow on this
+// part): a value is an unevaluated sum hi + lo of two floats.
+// Knuth's TwoSum: a + b = s + e exactly (round to nearest, no reassociation).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// (hi, lo) += v
+__device__ __forceinline__ void df_add(float& hi, float& lo, float v) {
+  float e;
+  two_sum(hi, v, hi, e);
+  lo = __fadd_rn(lo, e);
+}
+// (hi, lo) += (h2, l2)
+__device__ __forceinline__ void df_add2(float& hi, float& lo, float h2, float l2) {
+  float e;
+  two_sum(hi, h2, hi, e);
+  lo = __fadd_rn(lo, __fadd_rn(e, l2));
+}
+// (hi, lo) * f with the product's rounding error kept (an FMA gives it exactly)
+__device__ __forceinline__ void df_mul(float hi, float lo, float f, float& ph, float& pl) {
+  ph = __fmul_rn(hi, f);
+  pl = __fadd_rn(__fmaf_rn(hi, f, -ph), __fmul_rn(lo, f));
 }
 
 // One round of an epilogue warp: the output of an earlier tile (OUT) and the
@@ -170,7 +200,8 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
   uint8_t* b_tile = smem + kCtTcStages * kCtTcStageBytes;          // [hi, lo]
   float* coef_s = reinterpret_cast<float*>(b_tile + kCtTcBBytes);  // [kCfBufs][16][4]
   float* part_s = coef_s + kCfBufs * kCfCoefFloats;                // [2][kCfEpiWarps][8]
-  uint64_t* full = reinterpret_cast<uint64_t*>(part_s + 2 * kCfPartFloats);
+  uint64_t* dec_s = reinterpret_cast<uint64_t*>(part_s + 2 * kCfPartFloats);  // [kCfBufs][warps][32]
+  uint64_t* full = dec_s + kCfBufs * kCfEpiWarps * 32;
   uint64_t* empty = full + kCtTcStages;
   uint64_t* tfull = empty + kCtTcStages;  // accumulator of buffer b written by the MMAs
   uint64_t* tempty = tfull + kCfBufs;     // buffer b written out, free for the MMAs
@@ -278,10 +309,9 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
       }
       // the sample's P slots of 8 floats: lane l sums the float4 halves
       // (l & 1) of tiles l / 2, l / 2 + 16, ... (loads of a batch in flight
-      // together, fp32 within the lane), then lanes of equal parity combine
-      // in fp64
+      // together), then lanes of equal parity combine; all sums double-float
       const float4* sp = reinterpret_cast<const float4*>(p.part + size_t(n) * P * 8);
-      double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+      float h[4] = {0.f, 0.f, 0.f, 0.f}, l[4] = {0.f, 0.f, 0.f, 0.f};
       for (int i0 = 0; i0 < 2 * P; i0 += 8 * 32) {
         float4 v[8];
 #pragma unroll
@@ -289,37 +319,42 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
           const int i = i0 + lane + 32 * j;
           v[j] = i < 2 * P ? __ldcg(sp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float4 f = v[0];
 #pragma unroll
-        for (int j = 1; j < 8; ++j) {
-          f.x += v[j].x;
-          f.y += v[j].y;
-          f.z += v[j].z;
-          f.w += v[j].w;
+        for (int j = 0; j < 8; ++j) {
+          df_add(h[0], l[0], v[j].x);
+          df_add(h[1], l[1], v[j].y);
+          df_add(h[2], l[2], v[j].z);
+          df_add(h[3], l[3], v[j].w);
         }
-        a0 += f.x;
-        a1 += f.y;
-        a2 += f.z;
-        a3 += f.w;
       }
 #pragma unroll
-      for (int o = 2; o < 32; o <<= 1) {
-        a0 += __shfl_xor_sync(kFull, a0, o);
-        a1 += __shfl_xor_sync(kFull, a1, o);
-        a2 += __shfl_xor_sync(kFull, a2, o);
-        a3 += __shfl_xor_sync(kFull, a3, o);
+      for (int o = 2; o < 32; o <<= 1)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float h2 = __shfl_xor_sync(kFull, h[c], o), l2 = __shfl_xor_sync(kFull, l[c], o);
+          df_add2(h[c], l[c], h2, l2);
+        }
+      // lane 0 holds groups 0-1 as (s, s^2, s, s^2), lane 1 groups 2-3;
+      // channel lane c < 16 takes group c / 4 from lane c / 8
+      const int src = (lane >> 3) & 1, k = ((lane >> 2) & 1) * 2;
+      float sh[4], sl[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        sh[c] = __shfl_sync(kFull, h[c], src);
+        sl[c] = __shfl_sync(kFull, l[c], src);
       }
-      // lane 0 holds groups 0-1 (s, s^2, s, s^2), lane 1 groups 2-3; channel
-      // lane c < 16 takes group c / 4 from lane (c / 8)
-      const int src = (lane >> 3) & 1;
-      const double gs0 = __shfl_sync(kFull, a0, src), gq0 = __shfl_sync(kFull, a1, src);
-      const double gs1 = __shfl_sync(kFull, a2, src), gq1 = __shfl_sync(kFull, a3, src);
       if (lane < 16) {
-        const bool hi = (lane >> 2) & 1;
-        const double mean = (hi ? gs1 : gs0) * p.inv_count;
-        const double var = fmax((hi ? gq1 : gq0) * p.inv_count - mean * mean, 0.0);
-        const float A = gam * rsqrtf(float(var) + p.eps);
-        const float B = bet - float(mean) * A;
+        const float inv = float(p.inv_count);
+        float mh, ml, qh, ql, ph, pl, vh, ve;
+        df_mul(k ? sh[2] : sh[0], k ? sl[2] : sl[0], inv, mh, ml);  // mean
+        df_mul(k ? sh[3] : sh[1], k ? sl[3] : sl[1], inv, qh, ql);  // E[s^2]
+        // mean^2 = mh^2 + 2 mh ml (+ ml^2, below the precision kept)
+        ph = __fmul_rn(mh, mh);
+        pl = __fadd_rn(__fmaf_rn(mh, mh, -ph), __fmul_rn(2.f * mh, ml));
+        two_sum(qh, -ph, vh, ve);
+        const float var = fmaxf(__fadd_rn(vh, __fadd_rn(ve, __fsub_rn(ql, pl))), 0.f);
+        const float A = gam * rsqrtf(var + p.eps);
+        const float B = bet - __fadd_rn(mh, ml) * A;
         reinterpret_cast<float4*>(coef_s + slot * kCfCoefFloats)[lane] = make_float4(A, A, B, B);
       }
       __syncwarp();
@@ -349,14 +384,11 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
           fail();
           break;
         }
-        const CtTile tl = ct_tile(p, to);
-        const int qd = tl.qd, c = tl.c0 + row;
-        const bool cv = c < HW;
-        const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
-        o.pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
-        o.pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
+        const uint64_t dv = dec_s[(ob * kCfEpiWarps + e) * 32 + lane];
+        o.pv0 = (dv >> 62) & 1;
+        o.pv1 = dv >> 63;
         o.taddr = lane_base + uint32_t(ob * 128);
-        o.oc = p.out + size_t(tl.n) * 16 * plane + size_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
+        o.oc = p.out + (dv & ((uint64_t(1) << 62) - 1));
         o.cf = coef_s + ob * kCfCoefFloats;
         o.tempty = &tempty[ob];
       }
@@ -379,6 +411,10 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
         const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
         q.taddr = lane_base + uint32_t(buf * 128);
         q.m = make_float2(pv0 ? 1.f : 0.f, pv1 ? 1.f : 0.f);
+        // for the output of this tile three rounds later
+        const uint64_t off =
+            uint64_t(tl.n) * 16 * plane + uint64_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
+        dec_s[(buf * kCfEpiWarps + e) * 32 + lane] = off | (uint64_t(pv0) << 62) | (uint64_t(pv1) << 63);
       }
       float2 gs[4], gq[4];
 #pragma unroll
