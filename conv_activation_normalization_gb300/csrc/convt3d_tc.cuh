@@ -117,10 +117,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
   return uint32_t(r) * 128u + ((uint32_t(k >> 2) ^ uint32_t(r & 7)) << 4) + uint32_t(k & 3) * 4u;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // phase p = pd*4 + ph*2 + pw exists for the cell
 __device__ __forceinline__ bool ct_phase_ok(int p, int qd, int qh, int qw, int D, int H, int W) {
   return ((p >> 2) == 0 || qd < D - 1) && (((p >> 1) & 1) == 0 || qh < H - 1) && ((p & 1) == 0 || qw < W - 1);
