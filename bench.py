@@ -388,6 +388,26 @@ def make_workload(name, rows=None, samples=None):
 ALL = ["linear_gn_m32768", "linear_gn_m256", "linear_lse_m1024", "ln_dconv1d_b32", "convt3d_n128"]
 
 
+# ------------------------------------------------------- multi-rank logic
+def reduce_over_ranks(values, device=None):
+    """Each timing's maximum over the ranks of the job (unchanged at world
+    size 1): the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_value(work_per_step, world_size, ms_step, scale):
+    """Whole-job throughput: every rank runs the full workload on its own GPU
+    (weak scaling, no data exchange), so the job does world_size times the
+    work of one rank in the slowest rank's time."""
+    return work_per_step * world_size / (ms_step * 1e-3) / scale
+
+
 # ---------------------------------------------------------------- ours
 def run_ours(wl, args):
     global MODE
@@ -440,13 +460,9 @@ def run_ours(wl, args):
     if ws > 1:
         dist.barrier()
     ms_total = sum(a.elapsed_time(b) for a, b in evs)
-    kern_ms = prof.mean_ms
-    if ws > 1:
-        tt = torch.tensor([ms_total, kern_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total, kern_ms = tt.tolist()
+    ms_total, kern_ms = reduce_over_ranks([ms_total, prof.mean_ms], device=dev)
     ms_step = ms_total / steps
-    value = wl.work_per_step() * ws / (ms_step * 1e-3) / wl.scale()
+    value = job_value(wl.work_per_step(), ws, ms_step, wl.scale())
 
     e2e = None
     if not args.no_e2e:
