@@ -85,13 +85,16 @@ struct TileCfg {
   static constexpr int STAGE_BYTES = Op::kPlanes * (A_BYTES + B_BYTES);
   static constexpr int STAGES_FIT = (208 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int TMEM_COLS = 2 * BN;
+  // two accumulators, each starting on a multiple of TMEM_COLS / 2
+  static constexpr int TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
+  static constexpr int ACC_STRIDE = TMEM_COLS / 2;
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
   static_assert(STAGES >= 2, "need at least two smem stages");
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
                 "TMEM allocation must be a power of two >= 32 columns");
-  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128 or 256");
+  // epilogue halves of BN / 2 columns are read in pieces of 16
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN must be a multiple of 32 in [64, 256]");
 };
 
 // TMA descriptors of the operand planes: a[0]/b[0] = hi (or the only
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + uint32_t(acc * BN);
+        const uint32_t d = tmem_base + uint32_t(acc * Cfg::ACC_STRIDE);
         for (int kb = 0; kb < src.num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase)) {
             ok = false;
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN + half * BNW);
+      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * Cfg::ACC_STRIDE + half * BNW);
       const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
       Epi::template apply<BNW>(ep, taddr, part, row);
       tc_fence_before();

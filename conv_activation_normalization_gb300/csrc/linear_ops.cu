@@ -81,9 +81,10 @@ struct EpiSwishBiasGN {
 };
 
 // Linear -> per-row (max, sum exp(y - max)) over the tile's BN columns,
-// written as one float2 partial per (row, n-block).
+// written as one float2 partial per (row, n-block); columns are read 16 at a
+// time, so BN may be any multiple of 16 (the tile widths are 256 and 224).
 struct EpiLSEPartial {
-  static constexpr bool kFixedBN = true;  // one partial per 256-column block
+  static constexpr bool kFixedBN = true;  // the partials' layout follows the tile width
   struct Params {
     const float* b;  // may be null
     float2* part;    // [M][n_blocks]: one per row and epilogue column range
@@ -91,26 +92,29 @@ struct EpiLSEPartial {
   };
   template <int BN>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
+    static_assert(BN % 16 == 0, "16-column pieces");
     const int m = t.r0 + row;
     float mx = -INFINITY, s = 0.f;
 #pragma unroll 1
-    for (int g = 0; g < BN / 64; ++g) {
-      const int n0 = t.n0 + g * 64;
+    for (int g = 0; g < BN / 16; ++g) {
+      const int n0 = t.n0 + g * 16;
       if (n0 >= p.N) break;  // uniform across the warp
-      float v[64];
-      tmem_load64(taddr + uint32_t(g * 64), v);
+      uint32_t r[16];
+      GF_TMEM_LD16(taddr + uint32_t(g * 16), r);
+      GF_TMEM_WAIT16(r);
+      float v[16];
       float cm = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
+      for (int j = 0; j < 16; ++j) {
         const int n = n0 + j;
         const float bj = (p.b && n < p.N) ? __ldg(p.b + n) : 0.f;
-        v[j] = n < p.N ? v[j] + bj : -INFINITY;
+        v[j] = n < p.N ? __uint_as_float(r[j]) + bj : -INFINITY;
         cm = fmaxf(cm, v[j]);
       }
       const float nm = fmaxf(mx, cm);
       s *= __expf(mx - nm);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) s += __expf(v[j] - nm);
+      for (int j = 0; j < 16; ++j) s += __expf(v[j] - nm);
       mx = nm;
     }
     if (m < p.M) p.part[size_t(m) * p.n_blocks + t.nb] = make_float2(mx, s);
@@ -183,6 +187,21 @@ __global__ void lse_merge_act_kernel(const float2* __restrict__ part, float* __r
 namespace {
 
 constexpr int kBNLinear = 256;
+
+// Tile width of the LSE chain: 256 columns unless 224-column tiles fill the
+// SMs' waves noticeably better (e.g. 1024 x 8192: 256 tiles = 1.68 waves of
+// 152 SMs against 296 tiles = 1.95 waves).
+int lse_tile_width(int64_t M, int64_t N, int sm_count) {
+  const int64_t mb = (M + 127) / 128;
+  auto eff = [&](int bn) {
+    const int64_t tiles = mb * ((N + bn - 1) / bn);
+    const int64_t waves = (tiles + sm_count - 1) / sm_count;
+    return double(tiles) / double(waves * sm_count) * (double(N) / double(((N + bn - 1) / bn) * bn));
+  };
+  return eff(224) > 1.05 * eff(256) ? 224 : 256;
+}
+// Partials per row for a tile width: one per epilogue column half.
+int64_t lse_parts(int64_t N, int bn) { return (N + bn - 1) / bn * epi_halves(bn); }
 
 bool mode_ok(int32_t mode) {
   return mode == GF_MODE_FP32_3XTF32 || mode == GF_MODE_BF16 || mode == GF_MODE_FP32_3XBF16;
@@ -270,6 +289,10 @@ template <class Op, class Epi>
 gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
                              int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
   if constexpr (Epi::kFixedBN) {
+    // the LSE partials: 256- or 224-column tiles, whichever fills the waves
+    // of SMs better (the caller sized the partials with lse_tile_width)
+    if (lse_tile_width(M, N, dev.sm_count) == 224)
+      return run_linear_gemm<224, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
     return run_linear_gemm<kBNLinear, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
   } else {
     const int64_t mb = (M + kBM - 1) / kBM;
@@ -558,8 +581,9 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
 
 size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {
   if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
-  // one (max, sum) partial per row and epilogue column half of each n-block
-  const int64_t nb = (N + kBNLinear - 1) / kBNLinear * epi_halves(kBNLinear);
+  // one (max, sum) partial per row and epilogue column half of each n-block,
+  // sized for the narrower of the two tile widths
+  const int64_t nb = lse_parts(N, 224);
   return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode) +
          align_up(size_t(M) * nb * sizeof(float2), 256);
 }
@@ -583,7 +607,9 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float2* part = reinterpret_cast<float2*>(ws + operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode));
-  const int nb = int((N + kBNLinear - 1) / kBNLinear) * epi_halves(kBNLinear);
+  DeviceInfo dev;
+  if ((st = current_device(&dev)) != GF_OK) return st;
+  const int nb = int(lse_parts(N, lse_tile_width(M, N, dev.sm_count)));
   EpiLSEPartial::Params ep{b, part, int(M), int(N), nb};
   // m-blocks fastest: the CTAs in flight share n-blocks, so each W tile is
   // fetched from HBM once and reused by every m-block from L2.

@@ -78,8 +78,9 @@ def test_workspace_sizes(L):
     assert L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 3) == 0
     assert L.gf_linear_workspace_size(M, K, N, 0) == ws
     M, K, N = 1024, 8192, 8192
-    # one (max, sum) float2 per row and 128-column half of each 256-column block
-    assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (N // 128) * 8
+    # one (max, sum) float2 per row and column half of each n-block, sized for
+    # the narrower (224-column) of the two tile widths
+    assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (-(-N // 224) * 2) * 8
     assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0) > 2 * 4 * 32 * 256 * 4096
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 2, 1, 4) > 0
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 1, 1, 4) == 0
