@@ -283,8 +283,8 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
 
 // Tile width: 256 columns when that gives every SM at least one tile;
 // otherwise (small M) 128 or 64, trading per-tile efficiency for parallelism.
-// Epilogues whose output layout depends on the tile width (the LSE partials)
-// always use 256.
+// The LSE partials' layout follows the tile width, which lse_tile_width picks
+// (256 or 224 columns).
 template <class Op, class Epi>
 gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
                              int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
