@@ -224,11 +224,13 @@ def _ct_run(s, d, samples=None):
 
 # Cin <= 4 runs the single-kernel tensor-core path while a sample has at most
 # (CTAs + 1) tiles of 128 cells: (9, 3, 8, 24, 24) spans three rounds of tiles
-# with samples straddling rounds; (1, 3, 40, 40, 40) has 520 tiles in its one
-# sample and takes the two-pass tensor-core kernels; Cin > 4 the SIMT kernels.
+# with samples straddling rounds; (1, 3, 40, 40, 40) and (1, 4, 40, 40, 40)
+# have 520 tiles in their one sample and take the two-pass tensor-core kernels
+# (Cin = 4 fills K = 32, so the conv bias is added in the epilogue instead of
+# riding in the K padding); Cin > 4 the SIMT kernels.
 @pytest.mark.parametrize("N,Cin,D,H,W", [(2, 3, 5, 7, 9), (1, 1, 1, 1, 1), (3, 3, 4, 33, 40), (1, 8, 3, 8, 64),
                                          (2, 4, 3, 6, 10), (1, 2, 2, 5, 130), (2, 5, 3, 4, 9), (9, 3, 8, 24, 24),
-                                         (1, 3, 40, 40, 40)])
+                                         (1, 3, 40, 40, 40), (1, 4, 40, 40, 40)])
 def test_convt3d_small(N, Cin, D, H, W):
     s = synth.ConvT3dShape(N=N, Cin=Cin, D=D, H=H, W=W)
     got, ref = _ct_run(s, synth.convt3d_inputs(s, 400 + W))
