@@ -220,6 +220,14 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
  *   out [N,Cout,(D-1)s-2p+k, (H-1)s-2p+k, (W-1)s-2p+k].
  *   Supported: k == 3, stride == 2, pad == 1, Cin <= 8, Cout == 16,
  *   groups == 4; output_padding is 0.
+ *
+ *   With Cin <= 4 and at most (number of SMs + 1) tiles of 128 (h, w) cells
+ *   per sample the call is one cooperative kernel (one CTA per SM, every CTA
+ *   resident) that exchanges the GroupNorm statistics through the workspace;
+ *   the workspace's counters are zeroed by a memset on `stream` first, so two
+ *   calls that run at the same time must not share a workspace.  Otherwise
+ *   the call runs two passes (statistics, then output).  Results are the same
+ *   either way up to rounding.
  * ---------------------------------------------------------------------- */
 size_t gf_convt3d_swish_gn_hswish_workspace_size(int64_t N, int64_t Cin, int64_t Cout,
                                                  int64_t D, int64_t H, int64_t W, int32_t k,
