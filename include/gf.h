@@ -140,7 +140,7 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
  * (page-locked host memory lets the copies overlap the compute; pageable
  * memory works but serialises them).  W, b_lin, bias, gamma and beta are
  * device pointers as above.  Rows are processed in chunks of chunk_rows
- * (0 = a size that fills whole waves of tiles, at least 4096 rows): chunk i
+ * (0 = a size that fills whole waves of tiles, at least 2048 rows): chunk i
  * is copied in on an internal stream while chunk i-1 is computed on `stream`
  * and chunk i-2 is copied out on a second internal stream, through two device
  * staging buffers in the workspace.  Returns once everything is enqueued;
