@@ -14,35 +14,44 @@ namespace gf {
 
 // ------------------------------------------------------------- epilogues
 // Linear -> Swish -> +bias -> GroupNorm on a 128 x BN accumulator tile; one
-// thread owns one row, a group is 64 consecutive columns, so the group's mean
-// and (two-pass, biased) variance are computed in the thread's registers.
-struct EpiSwishBiasGN {
+// thread owns one row.  A group is gw consecutive columns (gw = 16, 32, 64 or
+// 128).  Columns are handled 64 at a time: the mean and the (two-pass,
+// biased) variance of each 16-column quarter's group are formed in the
+// thread's registers.  A 128-column group spans two such halves: the first
+// half's t is parked in TMEM (over its accumulator), the halves' (mean, M2)
+// are merged with the pairwise update of Chan, Golub and LeVeque, and the
+// first half is read back for its output.
+struct GNParams {
+  const float* b_lin;  // may be null
+  const float* bias;
+  const float* gamma;
+  const float* beta;
+  float* out;
+  int M, N;
+  float eps;
+  int gw;              // group width (the epilogue's GW)
+};
+template <int GW>
+struct EpiSwishBiasGNT {
+  static_assert(GW == 16 || GW == 32 || GW == 64 || GW == 128, "group width");
   static constexpr bool kFixedBN = false;
-  struct Params {
-    const float* b_lin;  // may be null
-    const float* bias;
-    const float* gamma;
-    const float* beta;
-    float* out;
-    int M, N;
-    float eps;
-  };
-  // Per 64-column group (one GroupNorm group of the row): t = Swish(y + b_lin)
-  // + bias, mean and centred second moment of t in registers, then
-  // (t - mean) rstd gamma + beta; pairs of columns share packed f32x2 ops.
-  template <int BN>
-  __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
-    const int m = t.r0 + row;
-    const bool valid = m < p.M;
-#pragma unroll 1
-    for (int g = 0; g < BN / 64; ++g) {
-      const int n0 = t.n0 + g * 64;
-      if (n0 >= p.N) break;  // uniform across the warp
-      float v[64];
-      tmem_load64(taddr + uint32_t(g * 64), v);
+  // narrowest tile whose epilogue warps own whole groups: a 128-column group
+  // takes a warp's whole half of a 256-column tile
+  static constexpr int kMinBN = GW == 128 ? 256 : 64;
+  using Params = GNParams;
+
+  // t = Swish(y + b_lin) + bias over the 64 columns n0.., in place; q[i] =
+  // sum of quarter i's t.  Quarters from nq on lie past the last column
+  // (N is a multiple of the group width, so only when GW < 64) and are left
+  // alone.
+  __device__ __forceinline__ static void swish_bias(const Params& p, int n0, int nq, float (&v)[64], float (&q)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q[i] = 0.f;
+      if (i >= nq) continue;  // uniform across the warp
       float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
+      for (int j = 16 * i; j < 16 * i + 16; j += 4) {
         const float4 bl = p.b_lin ? __ldg(reinterpret_cast<const float4*>(p.b_lin + n0 + j)) : make_float4(0, 0, 0, 0);
         const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + j));
         const float2 a = add2(swish2(add2(make_float2(v[j], v[j + 1]), make_float2(bl.x, bl.y))),
@@ -55,30 +64,160 @@ struct EpiSwishBiasGN {
         v[j + 3] = c.y;
         sum = add2(sum, add2(a, c));
       }
-      const float mean = (sum.x + sum.y) * (1.f / 64.f);
-      const float2 nmean = make_float2(-mean, -mean);
-      float2 m2 = make_float2(0.f, 0.f);
+      q[i] = sum.x + sum.y;
+    }
+  }
+  // per quarter: the sum of its group's quarters (GW <= 64)
+  __device__ __forceinline__ static void group_sums(const float (&q)[4], float (&g)[4]) {
+    const float s01 = q[0] + q[1], s23 = q[2] + q[3], s = s01 + s23;
+    g[0] = GW == 16 ? q[0] : GW == 32 ? s01 : s;
+    g[1] = GW == 16 ? q[1] : GW == 32 ? s01 : s;
+    g[2] = GW == 16 ? q[2] : GW == 32 ? s23 : s;
+    g[3] = GW == 16 ? q[3] : GW == 32 ? s23 : s;
+  }
+  // sum of squared deviations of quarter i's t from mu[i]
+  __device__ __forceinline__ static void quarter_m2(const float (&v)[64], const float (&mu)[4], float (&m2)[4]) {
 #pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float2 d = add2(make_float2(v[j], v[j + 1]), nmean);
-        m2 = fma2(d, d, m2);
+    for (int i = 0; i < 4; ++i) {
+      const float2 nm = make_float2(-mu[i], -mu[i]);
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 16 * i; j < 16 * i + 16; j += 2) {
+        const float2 d = add2(make_float2(v[j], v[j + 1]), nm);
+        acc = fma2(d, d, acc);
       }
-      const float rstd = rsqrtf((m2.x + m2.y) * (1.f / 64.f) + p.eps);
-      const float2 r2 = make_float2(rstd, rstd);
-      float* orow = p.out + size_t(m) * size_t(p.N) + n0;
+      m2[i] = acc.x + acc.y;
+    }
+  }
+  // (t - mu) rstd gamma + beta over the 64 columns n0.. of the row (the
+  // first nq quarters)
+  __device__ __forceinline__ static void normalize_store(const Params& p, int n0, int nq, const float (&v)[64],
+                                                         const float (&mu)[4], const float (&rstd)[4], float* orow,
+                                                         bool valid) {
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        const float4 ga = __ldg(reinterpret_cast<const float4*>(p.gamma + n0 + j));
-        const float4 be = __ldg(reinterpret_cast<const float4*>(p.beta + n0 + j));
-        const float2 a = fma2(mul2(add2(make_float2(v[j], v[j + 1]), nmean), r2), make_float2(ga.x, ga.y),
-                              make_float2(be.x, be.y));
-        const float2 c = fma2(mul2(add2(make_float2(v[j + 2], v[j + 3]), nmean), r2), make_float2(ga.z, ga.w),
-                              make_float2(be.z, be.w));
-        if (valid) __stcs(reinterpret_cast<float4*>(orow + j), make_float4(a.x, a.y, c.x, c.y));
+    for (int j = 0; j < 64; j += 4) {
+      if (j / 16 >= nq) break;  // uniform across the warp
+      const float2 nm = make_float2(-mu[j / 16], -mu[j / 16]), r2 = make_float2(rstd[j / 16], rstd[j / 16]);
+      const float4 ga = __ldg(reinterpret_cast<const float4*>(p.gamma + n0 + j));
+      const float4 be = __ldg(reinterpret_cast<const float4*>(p.beta + n0 + j));
+      const float2 a = fma2(mul2(add2(make_float2(v[j], v[j + 1]), nm), r2), make_float2(ga.x, ga.y),
+                            make_float2(be.x, be.y));
+      const float2 c = fma2(mul2(add2(make_float2(v[j + 2], v[j + 3]), nm), r2), make_float2(ga.z, ga.w),
+                            make_float2(be.z, be.w));
+      if (valid) __stcs(reinterpret_cast<float4*>(orow + j), make_float4(a.x, a.y, c.x, c.y));
+    }
+  }
+
+  template <int BN>
+  __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
+    const int m = t.r0 + row;
+    const bool valid = m < p.M;
+    float* orow = p.out + size_t(m) * size_t(p.N);
+    if constexpr (GW == 128) {  // the warp's 128 columns are one group
+      static_assert(GW != 128 || BN == 128, "128-column groups need 256-column tiles");
+      const int n0 = t.n0;
+      if (n0 >= p.N) return;  // uniform across the warp
+      float v[64], q[4], mu[4], m2[4], rs[4];
+      // first half: t and its (mean, M2); t parked over the accumulator
+      tmem_load64(taddr, v);
+      swish_bias(p, n0, 4, v, q);
+      const float mean0 = (q[0] + q[1] + q[2] + q[3]) * (1.f / 64.f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mu[i] = mean0;
+      quarter_m2(v, mu, m2);
+      const float m2a = m2[0] + m2[1] + m2[2] + m2[3];
+      {
+        uint32_t lo[32], hi[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          lo[i] = __float_as_uint(v[i]);
+          hi[i] = __float_as_uint(v[32 + i]);
+        }
+        GF_TMEM_ST32(taddr, lo);
+        GF_TMEM_ST32(taddr + 32, hi);
+      }
+      // second half
+      tmem_load64(taddr + 64, v);
+      swish_bias(p, n0 + 64, 4, v, q);
+      const float mean1 = (q[0] + q[1] + q[2] + q[3]) * (1.f / 64.f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mu[i] = mean1;
+      quarter_m2(v, mu, m2);
+      const float m2b = m2[0] + m2[1] + m2[2] + m2[3];
+      // merge the halves: M2 = M2a + M2b + delta^2 * 64 * 64 / 128
+      const float delta = mean1 - mean0;
+      const float mean = 0.5f * (mean0 + mean1);
+      const float rstd = rsqrtf((m2a + m2b + delta * delta * 32.f) * (1.f / 128.f) + p.eps);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mu[i] = mean;
+        rs[i] = rstd;
+      }
+      normalize_store(p, n0 + 64, 4, v, mu, rs, orow + n0 + 64, valid);
+      tmem_wait_st();
+      tmem_load64(taddr, v);
+      normalize_store(p, n0, 4, v, mu, rs, orow + n0, valid);
+      return;
+    }
+#pragma unroll 1
+    for (int g = 0; g < BN / 64; ++g) {
+      const int n0 = t.n0 + g * 64;
+      if (n0 >= p.N) break;  // uniform across the warp
+      // quarters inside the row (all four unless GW < 64 and N % 64 != 0)
+      const int nq = GW >= 64 ? 4 : min(4, (p.N - n0) / 16);
+      float v[64], q[4], mu[4], m2[4], rs[4];
+      tmem_load64(taddr + uint32_t(g * 64), v);
+      swish_bias(p, n0, nq, v, q);
+      if constexpr (GW == 64) {  // one group: one mean, one M2
+        float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sum.x += q[i];
+        const float mean = sum.x * (1.f / 64.f);
+        const float2 nmean = make_float2(-mean, -mean);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+          const float2 d = add2(make_float2(v[j], v[j + 1]), nmean);
+          acc = fma2(d, d, acc);
+        }
+        const float rstd = rsqrtf((acc.x + acc.y) * (1.f / 64.f) + p.eps);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          mu[i] = mean;
+          rs[i] = rstd;
+        }
+        normalize_store(p, n0, nq, v, mu, rs, orow + n0, valid);
+      } else {
+        constexpr float inv = 1.f / float(GW);  // a power of two: exact
+        float gs[4], gm2[4];
+        group_sums(q, gs);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mu[i] = gs[i] * inv;
+        quarter_m2(v, mu, m2);
+        group_sums(m2, gm2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rs[i] = rsqrtf(gm2[i] * inv + p.eps);
+        normalize_store(p, n0, nq, v, mu, rs, orow + n0, valid);
       }
     }
   }
 };
+
+// Runs f(TypeTag<epilogue>) with the epilogue of group width gw.
+template <class T>
+struct TypeTag {
+  using type = T;
+};
+template <class F>
+gf_status with_gn_epilogue(int gw, F&& f) {
+  switch (gw) {
+    case 16: return f(TypeTag<EpiSwishBiasGNT<16>>{});
+    case 32: return f(TypeTag<EpiSwishBiasGNT<32>>{});
+    case 64: return f(TypeTag<EpiSwishBiasGNT<64>>{});
+    case 128: return f(TypeTag<EpiSwishBiasGNT<128>>{});
+    default: return GF_ERR_SHAPE;
+  }
+}
 
 // Linear -> per-row (max, sum exp(y - max)) over the tile's BN columns,
 // written as one float2 partial per (row, n-block); columns are read 16 at a
@@ -129,6 +268,7 @@ struct EpiStore {
     float* out;
     int M, N;
   };
+  static constexpr int kMinBN = 64;
   template <int BN>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
     const int m = t.r0 + row;
@@ -228,6 +368,13 @@ gf_status check_linear_shape(int64_t M, int64_t K, int64_t N, int32_t mode) {
   return GF_OK;
 }
 
+// GroupNorm group widths the epilogue handles: 16, 32, 64 or 128 columns.
+bool gn_width_ok(int64_t N, int32_t groups) {
+  if (groups < 1 || N % groups != 0) return false;
+  const int64_t w = N / groups;
+  return w == 16 || w == 32 || w == 64 || w == 128;
+}
+
 // Planes the GEMM reads for one operand: p[0] = hi (or the only operand),
 // p[1] = lo.
 struct Planes {
@@ -296,11 +443,16 @@ gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Plane
     return run_linear_gemm<kBNLinear, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
   } else {
     const int64_t mb = (M + kBM - 1) / kBM;
-    if (mb * ((N + 255) / 256) >= dev.sm_count)
+    // (the epilogue's groups must not straddle warps: Epi::kMinBN)
+    if constexpr (Epi::kMinBN > 128) {
       return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-    if (mb * ((N + 127) / 128) >= dev.sm_count)
-      return run_linear_gemm<128, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-    return run_linear_gemm<64, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    } else {
+      if (mb * ((N + 255) / 256) >= dev.sm_count)
+        return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+      if (mb * ((N + 127) / 128) >= dev.sm_count)
+        return run_linear_gemm<128, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+      return run_linear_gemm<64, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    }
   }
 }
 
@@ -361,7 +513,7 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
   if (!x_planes || !W_planes || !bias || !gamma || !beta || !out) return GF_ERR_NULL;
   gf_status st = check_linear_shape(M, K, N, GF_MODE_FP32_3XTF32);
   if (st != GF_OK) return st;
-  if (groups < 1 || N % groups != 0 || N / groups != 64) return GF_ERR_SHAPE;
+  if (!gn_width_ok(N, groups)) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(x_planes) || !aligned16(W_planes) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       !aligned16(out) || (b_lin && !aligned16(b_lin)))
@@ -373,9 +525,11 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
   DeviceInfo dev;
   if ((st = current_device(&dev)) != GF_OK) return st;
   const Planes a{{x_planes, x_planes + size_t(M) * K}}, b{{W_planes, W_planes + size_t(N) * K}};
-  EpiSwishBiasGN::Params ep{b_lin, bias, gamma, beta, out, int(M), int(N), eps};
-  return run_linear<EpiSwishBiasGN>(GF_MODE_FP32_3XTF32, dev, a, b, M, K, N, /*m_fastest=*/0, ep,
-                                    static_cast<cudaStream_t>(stream));
+  const GNParams ep{b_lin, bias, gamma, beta, out, int(M), int(N), eps, int(N / groups)};
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return with_gn_epilogue(ep.gw, [&](auto tag) {
+    return run_linear<typename decltype(tag)::type>(GF_MODE_FP32_3XTF32, dev, a, b, M, K, N, 0, ep, s);
+  });
 }
 
 gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const float* b_lin, const float* bias,
@@ -386,7 +540,7 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
-  if (groups < 1 || N % groups != 0 || N / groups != 64) return GF_ERR_SHAPE;
+  if (!gn_width_ok(N, groups)) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(W) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       !aligned16(out) || (b_lin && !aligned16(b_lin)) || !aligned16(workspace))
@@ -399,11 +553,13 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
                       {workspace, need}};
   st = check_no_alias(Span{out, size_t(M) * N * 4}, ins, 7);
   if (st != GF_OK) return st;
-  EpiSwishBiasGN::Params ep{b_lin, bias, gamma, beta, out, int(M), int(N), eps};
-  // n-blocks fastest: the CTAs in flight share a few m-blocks of x, while all
-  // of W stays resident in L2.
-  return split_and_run<EpiSwishBiasGN>(mode, x, W, M, K, N, workspace, /*m_fastest=*/0, ep,
-                                       static_cast<cudaStream_t>(stream));
+  const GNParams ep{b_lin, bias, gamma, beta, out, int(M), int(N), eps, int(N / groups)};
+  // n-blocks fastest (m_fastest 0): the CTAs in flight share a few m-blocks
+  // of x, while all of W stays resident in L2.
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return with_gn_epilogue(ep.gw, [&](auto tag) {
+    return split_and_run<typename decltype(tag)::type>(mode, x, W, M, K, N, workspace, 0, ep, s);
+  });
 }
 
 // ---------------------------------------------------------------- host path
@@ -474,7 +630,7 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
-  if (groups < 1 || N % groups != 0 || N / groups != 64 || chunk_rows < 0) return GF_ERR_SHAPE;
+  if (!gn_width_ok(N, groups) || chunk_rows < 0) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(W) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       (b_lin && !aligned16(b_lin)) || !aligned16(workspace))
@@ -540,9 +696,11 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
       ok = cudaStreamWaitEvent(s, ev_in[bi], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev_out[bi], 0) == cudaSuccess;
     if (ok) {
       Planes xp{};
-      EpiSwishBiasGN::Params ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps};
+      const GNParams ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps, int(N / groups)};
       ok = prepare_operand(xd, rows, K, mode, ws + wl.xp[bi], dev, s, &xp) == GF_OK &&
-           run_linear<EpiSwishBiasGN>(mode, dev, xp, wp, rows, K, N, /*m_fastest=*/0, ep, s) == GF_OK &&
+           with_gn_epilogue(ep.gw, [&](auto tag) {
+             return run_linear<typename decltype(tag)::type>(mode, dev, xp, wp, rows, K, N, 0, ep, s);
+           }) == GF_OK &&
            cudaEventRecord(ev_comp[bi], s) == cudaSuccess;
     }
     // stage 3: out rows back

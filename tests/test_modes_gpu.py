@@ -77,6 +77,18 @@ def test_linear_gn_modes(mode, M, K, N):
     assert_close(out, ref, TOL[mode], f"linear_gn mode {mode}")
 
 
+@pytest.mark.parametrize("mode", [BF16, X3BF16])
+@pytest.mark.parametrize("M,K,N,gw", [(130, 40, 320, 16), (200, 64, 512, 128)])
+def test_linear_gn_modes_group_widths(mode, M, K, N, gw):
+    s = synth.LinearGNShape(M=M, K=K, N=N, groups=N // gw)
+    d = synth.linear_gn_inputs(s, 600 + gw)
+    out = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), T(d["b_lin"]), T(d["bias"]), T(d["gamma"]),
+                                            T(d["beta"]), s.groups, s.eps, mode=mode).cpu().numpy()
+    ref = oracle.linear_swish_bias_groupnorm(d["x"], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"], s.groups,
+                                             s.eps)
+    assert_close(out, ref, TOL[mode], f"linear_gn mode {mode} groups of {gw}")
+
+
 def test_linear_gn_3xbf16_workload_m32768_sampled():
     s, seed = synth.WORKLOADS["linear_gn_m32768"]
     d = synth.linear_gn_inputs(s, seed)

@@ -108,6 +108,28 @@ def test_linear_gn_ragged(M, K, N):
     assert_close(got, ref, f"linear_gn {M}x{K}x{N}")
 
 
+# GroupNorm groups of 16, 32 and 128 columns (64 is the workloads' width):
+# ragged rows and columns, a 128-column group in the partial last tile, and a
+# single row
+@pytest.mark.parametrize("M,K,N,gw", [(130, 36, 320, 16), (383, 260, 4096, 32), (1, 4, 48, 16), (257, 64, 96, 32),
+                                      (300, 64, 384, 128), (129, 100, 512, 128), (1, 4, 128, 128),
+                                      (200, 1024, 4096, 128)])
+def test_linear_gn_group_widths(M, K, N, gw):
+    s, d = _lgn_case(M, K, N, N // gw, 300 + gw + M)
+    got, ref = _lgn_run(s, d)
+    assert_close(got, ref, f"linear_gn {M}x{K}x{N} groups of {gw}")
+
+
+def test_linear_gn_group_width_128_halves_differ():
+    # a 128-column group whose halves have very different means: the merge of
+    # the halves' (mean, M2) must carry the between-halves term
+    s, d = _lgn_case(96, 32, 256, 2, 11)
+    d["bias"][:64] += 3.0
+    d["bias"][128:192] -= 2.0
+    got, ref = _lgn_run(s, d)
+    assert_close(got, ref, "linear_gn groups of 128, shifted halves")
+
+
 def test_linear_gn_no_linear_bias_and_constant_group():
     s, d = _lgn_case(64, 64, 256, 4, 7)
     d["W"][:64] = 0.0      # group 0: t = swish(0) + bias = bias, varies per channel
@@ -252,11 +274,12 @@ def test_convt3d_workload_sampled():
 
 
 # ------------------------------------------------- host-buffer pipeline
-@pytest.mark.parametrize("pinned,chunk", [(True, 0), (True, 200), (False, 384)])
-def test_linear_gn_host_pipeline_matches_device_call(pinned, chunk):
+@pytest.mark.parametrize("pinned,chunk,groups", [(True, 0, 8), (True, 200, 8), (False, 384, 8), (True, 200, 4),
+                                                 (True, 0, 16)])
+def test_linear_gn_host_pipeline_matches_device_call(pinned, chunk, groups):
     # Rows are independent and each chunk runs the same kernels, so the
     # pipelined host-buffer call must reproduce the device call bit for bit.
-    s, d = _lgn_case(1000, 256, 512, 8, 4242)
+    s, d = _lgn_case(1000, 256, 512, groups, 4242)
     dev = {k: T(d[k]) for k in ("W", "b_lin", "bias", "gamma", "beta")}
     ref = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), dev["W"], dev["b_lin"], dev["bias"], dev["gamma"],
                                             dev["beta"], s.groups, s.eps).cpu()
