@@ -19,6 +19,7 @@ equivalence and float64 torch library cross-checks).  No function is
 from .ops import (  # noqa: F401
     silu,
     gelu_erf,
+    gelu_tanh,
     hardswish,
     leaky_relu,
     group_norm_rows,

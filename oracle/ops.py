@@ -46,6 +46,15 @@ def gelu_erf(v):
     return 0.5 * v * (1.0 + _erf(v / np.sqrt(2.0)))
 
 
+def gelu_tanh(v):
+    """The tanh approximation of GELU,
+    ``0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))``: the form page
+    Kimi-K2.6__l2_p5 turn 2 takes for the module's GELU (an opt-in variant
+    here; the erf form stays the default)."""
+    v = _f64(v)
+    return 0.5 * v * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (v + 0.044715 * v ** 3)))
+
+
 def hardswish(v):
     """HardSwish ``v * clamp(v + 3, 0, 6) / 6`` (page Kimi-K2.6__l2_p60, turn 1)."""
     v = _f64(v)
@@ -172,10 +181,14 @@ def dilated_conv1d(a, w, b, dilation, padding):
     return out
 
 
-def ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, padding, eps=1e-5):
+def ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, padding, eps=1e-5, gelu="erf"):
     """O3.  ``out = Conv1d(GELU(LayerNorm(x))) + x`` (page Kimi-K2.6__l2_p5,
-    turns 1-2).  The residual requires the length-preserving padding."""
-    a = gelu_erf(layer_norm_sample(x, ln_gamma, ln_beta, eps))
+    turns 1-2).  The residual requires the length-preserving padding.
+    ``gelu="tanh"`` takes the tanh approximation (the page's turn-2 reading)."""
+    if gelu not in ("erf", "tanh"):
+        raise ValueError("gelu must be 'erf' or 'tanh'")
+    act = gelu_erf if gelu == "erf" else gelu_tanh
+    a = act(layer_norm_sample(x, ln_gamma, ln_beta, eps))
     y = dilated_conv1d(a, conv_w, conv_b, dilation, padding)
     if y.shape != np.shape(x):
         raise ValueError("residual needs L_out == L")

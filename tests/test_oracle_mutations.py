@@ -59,6 +59,15 @@ def _gelu_tanh(v):
     return 0.5 * v * (1 + np.tanh(np.sqrt(2 / np.pi) * (v + 0.044715 * v ** 3)))
 
 
+def _gelu_tanh_wrong_cubic(v):
+    v = np.asarray(v, np.float64)
+    return 0.5 * v * (1 + np.tanh(np.sqrt(2 / np.pi) * (v + 0.0447 * v ** 2)))
+
+
+def _gelu_tanh_is_erf(v):
+    return oracle.gelu_erf(v)
+
+
 def _silu_is_sigmoid(v):
     v = np.asarray(v, np.float64)
     return 1.0 / (1.0 + np.exp(-v))
@@ -88,6 +97,8 @@ MUTATIONS = [
     ("logsumexp_rows", _lse_no_max_log, [P.test_o2_constant_row_closed_form]),
     ("layer_norm_sample", _ln_no_eps, [P.test_o3_ln_invariant]),
     ("gelu_erf", _gelu_tanh, [P.test_gelu_is_erf_not_tanh]),
+    ("gelu_tanh", _gelu_tanh_wrong_cubic, [P.test_gelu_tanh_form, P.test_o3_tanh_gelu_variant]),
+    ("gelu_tanh", _gelu_tanh_is_erf, [P.test_gelu_tanh_form, P.test_o3_tanh_gelu_variant]),
     ("leaky_relu", _lrelu_wrong_slope, [P.test_o2_negative_branch]),
     ("linear", _linear_transposed_w, [P.test_o2_brute_force_tiny]),
 ]

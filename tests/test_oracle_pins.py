@@ -206,6 +206,36 @@ def test_gelu_is_erf_not_tanh():
     assert np.abs(oracle.gelu_erf(v) - F.gelu(_t(v), approximate="tanh").numpy()).max() > 1e-5
 
 
+def test_gelu_tanh_form():
+    # against torch's independent tanh-approximate GELU, the odd-part identity
+    # g(v) - g(-v) = v shared by both forms (0.5 (1 + h) with h odd), the
+    # limits, and the known gap to the erf form (largest near |v| = 2, a few
+    # 1e-4, never above 1e-3)
+    v = np.linspace(-6, 6, 97)
+    np.testing.assert_allclose(oracle.gelu_tanh(v), F.gelu(_t(v), approximate="tanh").numpy(), rtol=1e-14,
+                               atol=1e-15)
+    np.testing.assert_allclose(oracle.gelu_tanh(v) - oracle.gelu_tanh(-v), v, rtol=0, atol=1e-14)
+    assert oracle.gelu_tanh(0.0) == 0.0
+    assert abs(oracle.gelu_tanh(30.0) - 30.0) < 1e-12 and abs(oracle.gelu_tanh(-30.0)) < 1e-12
+    gap = np.abs(oracle.gelu_tanh(v) - oracle.gelu_erf(v))
+    assert 1e-4 < gap.max() < 1e-3
+
+
+def test_o3_tanh_gelu_variant():
+    r = rng(17)
+    B, C, L = 2, 8, 40
+    x = r.normal(size=(B, C, L))
+    g, be = r.uniform(0.5, 1.5, (C, L)), r.normal(size=(C, L)) * 0.1
+    w, cb = r.uniform(-0.2, 0.2, (C, C, 3)), r.uniform(-0.2, 0.2, C)
+    a = F.gelu(F.layer_norm(_t(x), (C, L), _t(g), _t(be), 1e-5), approximate="tanh")
+    ref = F.conv1d(a, _t(w), _t(cb), padding=2, dilation=2) + _t(x)
+    got = oracle.ln_gelu_dconv1d_res(x, g, be, w, cb, 2, 2, gelu="tanh")
+    np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.abs(got - oracle.ln_gelu_dconv1d_res(x, g, be, w, cb, 2, 2)).max() > 1e-6
+    with pytest.raises(ValueError):
+        oracle.ln_gelu_dconv1d_res(x, g, be, w, cb, 2, 2, gelu="sigmoid")
+
+
 def test_o2_page_flop_counts():
     for key in ("linear_gn_gflop", "linear_lse_gflop"):
         f = GOLDEN[key]
