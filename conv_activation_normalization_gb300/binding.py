@@ -22,6 +22,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "gf.h")
 
 GF_MODE_FP32_3XTF32 = 0
 GF_MODE_BF16 = 1
+GF_MODE_FP32_3XBF16 = 2
+GF_FLAG_GELU_TANH = 0x100  # OR'd into the Conv1d chain's mode: tanh-approximate GELU
 
 _lib = None
 _lock = threading.Lock()
@@ -288,8 +290,13 @@ def gf_linear_lse_act(x, W, b, negative_slope=0.01, mode=GF_MODE_FP32_3XTF32, ou
 
 
 def gf_ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, padding, eps=1e-5,
-                           mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None):
-    """out = conv1d(gelu(layer_norm(x, [C, L])), dilation, padding) + x."""
+                           mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None, gelu="erf"):
+    """out = conv1d(gelu(layer_norm(x, [C, L])), dilation, padding) + x.
+    gelu: "erf" (exact) or "tanh" (the tanh approximation)."""
+    if gelu not in ("erf", "tanh"):
+        raise ValueError("gelu must be 'erf' or 'tanh'")
+    if gelu == "tanh":
+        mode |= GF_FLAG_GELU_TANH
     dev = _check(x, ln_gamma, ln_beta, conv_w, conv_b, out)
     B, C, L = x.shape
     ksize = conv_w.shape[2]

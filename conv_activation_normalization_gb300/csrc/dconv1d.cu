@@ -144,8 +144,9 @@ __device__ __forceinline__ void store_planes4(void* planes, size_t plane_elems, 
 // grid (ceil(L/128), C/32, B), 256 threads: GELU(LayerNorm(x)) for a tile of
 // 32 channels x 128 positions, read as float4 along L (x, gamma, beta),
 // transposed through shared memory and written 4 channels at a time to the
-// [B][L][C] operand planes.  L is a multiple of 4.
-template <int MODE>
+// [B][L][C] operand planes.  L is a multiple of 4.  TANH: GELU's tanh
+// approximation instead of the erf form.
+template <int MODE, bool TANH>
 __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta,
@@ -166,10 +167,12 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
       const float4 v = __ldcs(reinterpret_cast<const float4*>(xb + cl));
       const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + cl));
       const float4 be = __ldg(reinterpret_cast<const float4*>(beta + cl));
-      a.x = gelu_erf(fmaf((v.x - st.x) * st.y, g.x, be.x));
-      a.y = gelu_erf(fmaf((v.y - st.x) * st.y, g.y, be.y));
-      a.z = gelu_erf(fmaf((v.z - st.x) * st.y, g.z, be.z));
-      a.w = gelu_erf(fmaf((v.w - st.x) * st.y, g.w, be.w));
+      const float4 h = make_float4(fmaf((v.x - st.x) * st.y, g.x, be.x), fmaf((v.y - st.x) * st.y, g.y, be.y),
+                                   fmaf((v.z - st.x) * st.y, g.z, be.z), fmaf((v.w - st.x) * st.y, g.w, be.w));
+      if constexpr (TANH)
+        a = make_float4(gelu_tanh(h.x), gelu_tanh(h.y), gelu_tanh(h.z), gelu_tanh(h.w));
+      else
+        a = make_float4(gelu_erf(h.x), gelu_erf(h.y), gelu_erf(h.z), gelu_erf(h.w));
     }
     *reinterpret_cast<float4*>(&tile[cc][4 * q]) = a;
   }
@@ -284,9 +287,14 @@ gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize, int32
 template <int MODE>
 void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
                          const float2* stats, void* a_planes, void* w_planes, int64_t B, int64_t C, int64_t L,
-                         int32_t ksize, const DeviceInfo& dev, cudaStream_t s) {
-  ln_apply_gelu_split_kernel<MODE><<<dim3(unsigned((L + 127) / 128), unsigned(C / 32), unsigned(B)), 256, 0, s>>>(
-      x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L), int(B));
+                         int32_t ksize, bool tanh_gelu, const DeviceInfo& dev, cudaStream_t s) {
+  const dim3 grid(unsigned((L + 127) / 128), unsigned(C / 32), unsigned(B));
+  if (tanh_gelu)
+    ln_apply_gelu_split_kernel<MODE, true><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L),
+                                                                int(B));
+  else
+    ln_apply_gelu_split_kernel<MODE, false><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C),
+                                                                 int(L), int(B));
   const int64_t n = C * C * ksize;
   const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
   conv_weight_split_kernel<MODE><<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), ksize);
@@ -329,6 +337,8 @@ using namespace gf;
 extern "C" {
 
 size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t mode) {
+  if (mode & ~(GF_FLAG_GELU_TANH | 0xff)) return 0;
+  mode &= 0xff;
   if (!conv_mode_ok(mode) || check_conv_shape(B, C, L, ksize, mode) != GF_OK) return 0;
   return conv_ws(B, C, L, ksize, mode).total;
 }
@@ -338,6 +348,9 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
                                  int32_t dilation, int32_t padding, float eps, int32_t mode, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   if (!x || !ln_gamma || !ln_beta || !conv_w || !out) return GF_ERR_NULL;
+  if (mode & ~(GF_FLAG_GELU_TANH | 0xff)) return GF_ERR_MODE;
+  const bool tanh_gelu = (mode & GF_FLAG_GELU_TANH) != 0;
+  mode &= 0xff;
   if (!conv_mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_conv_shape(B, C, L, ksize, mode);
   if (st != GF_OK) return st;
@@ -375,15 +388,15 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
       launch_conv_prepass<GF_MODE_FP32_3XTF32>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,
-                                               ksize, dev, s);
+                                               ksize, tanh_gelu, dev, s);
       break;
     case GF_MODE_BF16:
-      launch_conv_prepass<GF_MODE_BF16>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L, ksize, dev,
-                                        s);
+      launch_conv_prepass<GF_MODE_BF16>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L, ksize,
+                                        tanh_gelu, dev, s);
       break;
     default:
       launch_conv_prepass<GF_MODE_FP32_3XBF16>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,
-                                               ksize, dev, s);
+                                               ksize, tanh_gelu, dev, s);
   }
   if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
   EpiConvResidual::Params ep{conv_b, x, out, int(C), int(L)};

@@ -60,6 +60,11 @@ __device__ __forceinline__ float2 swish2(float2 v) {
 
 // Exact GELU v * Phi(v) = 0.5 v (1 + erf(v / sqrt 2)), with CUDA's erff.
 __device__ __forceinline__ float gelu_erf(float v) { return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f)); }
+// GELU's tanh approximation 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))),
+// with CUDA's tanhf.
+__device__ __forceinline__ float gelu_tanh(float v) {
+  return 0.5f * v * (1.0f + tanhf(0.79788456080286536f * fmaf(0.044715f * v, v * v, v)));
+}
 
 // TF32 split: hi keeps the sign, exponent and top 10 mantissa bits (exactly a
 // TF32 value), lo = v - hi is exact in fp32.

@@ -66,6 +66,13 @@ typedef int32_t gf_status;
 #define GF_MODE_BF16        1
 #define GF_MODE_FP32_3XBF16 2
 
+/* Flag OR'd into the mode of gf_ln_gelu_dconv1d_res (and its workspace
+ * query): GELU in its tanh approximation,
+ * 0.5 h (1 + tanh(sqrt(2/pi) (h + 0.044715 h^3))), the form page
+ * Kimi-K2.6__l2_p5 turn 2 reads the module's GELU as, instead of the exact
+ * erf form.  Other calls reject it (GF_ERR_MODE). */
+#define GF_FLAG_GELU_TANH 0x100
+
 /* Version of this ABI (bumped on any signature change). */
 int32_t gf_abi_version(void);
 
@@ -187,7 +194,9 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
  *
  *   h[b,c,l]   = (x - mu_b) / sqrt(var_b + eps) * ln_gamma[c,l] + ln_beta[c,l]
  *                (mu_b, var_b: mean and biased variance of x[b] over all C*L)
- *   a          = gelu(h), and a = 0 outside 0 <= l < L (the conv's padding)
+ *   a          = gelu(h), and a = 0 outside 0 <= l < L (the conv's padding);
+ *                gelu is 0.5 h (1 + erf(h / sqrt 2)), or its tanh
+ *                approximation when mode carries GF_FLAG_GELU_TANH
  *   out[b,o,j] = conv_b[o] + sum_{c,t} conv_w[o,c,t] * a[b,c, j - padding + t*dilation]
  *                + x[b,o,j]
  *

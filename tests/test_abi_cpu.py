@@ -52,6 +52,7 @@ def test_linear_gn_validation(L):
     assert _lgn(L, out=None) == GF_ERR_NULL
     assert _lgn(L, mode=3) == GF_ERR_MODE
     assert _lgn(L, mode=-1) == GF_ERR_MODE
+    assert _lgn(L, mode=0x100) == GF_ERR_MODE     # the GELU flag belongs to the Conv1d chain
     assert _lgn(L, K=1020, mode=1) == GF_ERR_SHAPE  # bf16 planes need K % 8
     assert _lgn(L, K=1020, mode=2) == GF_ERR_SHAPE
     assert _lgn(L, groups=16) == GF_ERR_SHAPE      # group width 256 is not supported
@@ -84,6 +85,12 @@ def test_workspace_sizes(L):
     # the narrower (224-column) of the two tile widths
     assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (-(-N // 224) * 2) * 8
     assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0) > 2 * 4 * 32 * 256 * 4096
+    GELU_TANH = 0x100
+    for mode in (0, 1, 2):  # the GELU flag changes no buffer
+        assert (L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, mode | GELU_TANH) ==
+                L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, mode))
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0x400) == 0
+    assert L.gf_linear_workspace_size(M, K, N, GELU_TANH) == 0  # other calls take no flag
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 2, 1, 4) > 0
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 1, 1, 4) == 0
 
@@ -120,6 +127,9 @@ def test_dconv1d_validation(L):
     assert call(C=512) == GF_ERR_SHAPE
     assert call(L=4094) == GF_ERR_SHAPE            # L % 4
     assert call(mode=5) == GF_ERR_MODE
+    assert call(mode=0x200) == GF_ERR_MODE         # unknown flag bit
+    assert call(mode=0x103) == GF_ERR_MODE         # tanh flag on an unknown precision mode
+    assert call(mode=0x100, C=48) == GF_ERR_SHAPE  # the flag passes; the shape does not
     assert call(C=96, mode=1) == GF_ERR_SHAPE      # bf16 k-blocks are 64 channels
     assert call(w=P[3] + 4) == GF_ERR_ALIGN
     assert call(wsb=5) == GF_ERR_WORKSPACE

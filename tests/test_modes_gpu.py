@@ -131,6 +131,17 @@ def test_dconv1d_modes(mode, B, C, L, dil):
     assert_close(out, ref, TOL[mode], f"dconv1d mode {mode}")
 
 
+@pytest.mark.parametrize("mode", [BF16, X3BF16])
+def test_dconv1d_modes_tanh_gelu(mode):
+    s = synth.DConv1dShape(B=2, C=128, L=260, dilation=3, padding=3)
+    d = synth.dconv1d_inputs(s, 650, affine="perturbed")
+    out = gf.gf_ln_gelu_dconv1d_res(T(d["x"]), T(d["ln_gamma"]), T(d["ln_beta"]), T(d["conv_w"]), T(d["conv_b"]),
+                                    s.dilation, s.padding, s.eps, mode=mode, gelu="tanh").cpu().numpy()
+    ref = oracle.ln_gelu_dconv1d_res(d["x"], d["ln_gamma"], d["ln_beta"], d["conv_w"], d["conv_b"], s.dilation,
+                                     s.padding, s.eps, gelu="tanh")
+    assert_close(out, ref, TOL[mode], f"dconv1d mode {mode} tanh GELU")
+
+
 def test_dconv1d_3xbf16_workload_sampled():
     s, seed = synth.WORKLOADS["ln_dconv1d_b32"]
     d = synth.dconv1d_inputs(s, seed)

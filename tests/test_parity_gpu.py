@@ -208,6 +208,21 @@ def test_dconv1d_small(B, C, L, dil):
     assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
 
 
+@pytest.mark.parametrize("B,C,L,dil", [(2, 64, 300, 4), (3, 256, 520, 2)])
+def test_dconv1d_tanh_gelu(B, C, L, dil):
+    # the tanh-approximate GELU variant (flag GF_FLAG_GELU_TANH)
+    s = synth.DConv1dShape(B=B, C=C, L=L, dilation=dil, padding=dil)
+    d = synth.dconv1d_inputs(s, 700 + L, affine="perturbed")
+    got = gf.gf_ln_gelu_dconv1d_res(T(d["x"]), T(d["ln_gamma"]), T(d["ln_beta"]), T(d["conv_w"]), T(d["conv_b"]),
+                                    s.dilation, s.padding, s.eps, gelu="tanh").cpu().numpy()
+    ref = oracle.ln_gelu_dconv1d_res(d["x"], d["ln_gamma"], d["ln_beta"], d["conv_w"], d["conv_b"], s.dilation,
+                                     s.padding, s.eps, gelu="tanh")
+    assert_close(got, ref, f"dconv1d tanh GELU {B}x{C}x{L}")
+    erf = oracle.ln_gelu_dconv1d_res(d["x"], d["ln_gamma"], d["ln_beta"], d["conv_w"], d["conv_b"], s.dilation,
+                                     s.padding, s.eps)
+    assert np.abs(got - erf).max() > 1e-4  # the variant is really the other GELU
+
+
 def test_dconv1d_kernel_size_5():
     s = synth.DConv1dShape(B=2, C=64, L=256, ksize=5, dilation=3, padding=6)
     got, ref = _dc_run(s, synth.dconv1d_inputs(s, 5, affine="perturbed"))
