@@ -444,6 +444,58 @@ def test_o4_torch_float64_cross_check():
     np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
 
 
+# Other kernel sizes, strides, paddings, channel counts and groups (the
+# module's constructor arguments on page Kimi-K2.6__l2_p60, turn 1)
+GENERAL_CT = [(3, 1, 1), (4, 2, 1), (5, 3, 2), (2, 2, 0), (3, 2, 0), (1, 1, 0), (4, 3, 3)]
+
+
+@pytest.mark.parametrize("k,s,p", GENERAL_CT)
+def test_o4_general_scatter_equals_zero_insert_and_torch(k, s, p):
+    r = rng(20 + 7 * k + s + p)
+    x = r.normal(size=(2, 3, 3, 4, 5))
+    w = r.normal(size=(3, 6, k, k, k))
+    b = r.normal(size=6)
+    a = oracle.conv_transpose3d_scatter(x, w, b, s, p)
+    assert a.shape[2:] == tuple(oracle.convt3d_out_size(i, k, s, p) for i in (3, 4, 5))
+    np.testing.assert_allclose(a, oracle.conv_transpose3d_zero_insert(x, w, b, s, p), rtol=1e-12, atol=1e-12)
+    ref = F.conv_transpose3d(_t(x), _t(w), _t(b), stride=s, padding=p)
+    np.testing.assert_allclose(a, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("k,s,p,Cout,G", [(4, 2, 1, 6, 3), (2, 3, 0, 4, 1), (3, 1, 1, 8, 8)])
+def test_o4_general_brute_force_tiny(k, s, p, Cout, G):
+    r = rng(30 + k + s + p + Cout)
+    N, Cin, D, H, W = 1, 2, 3, 2, 3
+    x = r.normal(size=(N, Cin, D, H, W))
+    w = r.normal(size=(Cin, Cout, k, k, k)) * 0.3
+    b = r.normal(size=Cout) * 0.1
+    gamma, beta = r.uniform(0.5, 1.5, Cout), r.normal(size=Cout) * 0.1
+    got = oracle.convt3d_swish_gn_hswish(x, w, b, gamma, beta, s, p, G)
+    OD, OH, OW = (oracle.convt3d_out_size(i, k, s, p) for i in (D, H, W))
+    assert min(OD, OH, OW) >= 1
+    td, th, tw = (_valid_taps_1d(I, O, k, s, p) for I, O in ((D, OD), (H, OH), (W, OW)))
+    sw = np.zeros((Cout, OD, OH, OW))
+    for co in range(Cout):
+        for od in range(OD):
+            for oh in range(OH):
+                for ow in range(OW):
+                    y = b[co]
+                    for ci in range(Cin):
+                        for (id_, kd) in td[od]:
+                            for (ih, kh) in th[oh]:
+                                for (iw, kw) in tw[ow]:
+                                    y += x[0, ci, id_, ih, iw] * w[ci, co, kd, kh, kw]
+                    sw[co, od, oh, ow] = y / (1 + math.exp(-y))
+    cg = Cout // G
+    for g in range(G):
+        vals = sw[g * cg:(g + 1) * cg].ravel()
+        mu = vals.sum() / vals.size
+        var = ((vals - mu) ** 2).sum() / vals.size
+        for c in range(g * cg, (g + 1) * cg):
+            h = (sw[c] - mu) / math.sqrt(var + 1e-5) * gamma[c] + beta[c]
+            np.testing.assert_allclose(got[0, c], h * np.clip(h + 3, 0, 6) / 6, rtol=1e-12, atol=1e-12)
+
+
 def test_o4_gn_invariants():
     r = rng(20)
     t = r.normal(size=(2, 8, 3, 4, 5)) * 0.05 + 0.02
