@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "convt3d_fused.cuh"
+#include "convt3d_general.h"
 #include "convt3d_tc.cuh"
 #include "host_common.h"
 #include "kernels_common.cuh"
@@ -511,7 +512,11 @@ extern "C" {
 
 size_t gf_convt3d_swish_gn_hswish_workspace_size(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H,
                                                  int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups) {
-  if (check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) != GF_OK) return 0;
+  if (check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) != GF_OK) {
+    // any other kernel size, stride, padding, channel counts or groups
+    CtGenShape g;
+    return ct_general_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups, &g) == GF_OK ? g.total : 0;
+  }
   if (Cin > 4) return ct_ws(N, D, H, W).total;
   // the single-kernel or the two-pass tensor-core path, chosen per device
   const size_t a = ct_tc_ws(N, D, H, W).total, c = cf_ws(N, D, H, W).total;
@@ -523,13 +528,30 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
                                      int64_t H, int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups,
                                      float eps, void* workspace, size_t workspace_bytes, void* stream) {
   if (!x || !w || !gamma || !beta || !out) return GF_ERR_NULL;
-  gf_status st = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups);
+  CtGenShape gen;
+  const bool fast = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) == GF_OK;
+  gf_status st = fast ? GF_OK : ct_general_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups, &gen);
   if (st != GF_OK) return st;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(w) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
       (b && !aligned16(b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
   const size_t need = gf_convt3d_swish_gn_hswish_workspace_size(N, Cin, Cout, D, H, W, k, stride, pad, groups);
+  if (!fast) {
+    if (!workspace) return GF_ERR_NULL;
+    if (workspace_bytes < need) return GF_ERR_WORKSPACE;
+    const Span gins[] = {{x, size_t(N) * Cin * D * H * W * 4},
+                         {w, size_t(Cin) * Cout * k * k * k * 4},
+                         {b, size_t(Cout) * 4},
+                         {gamma, size_t(Cout) * 4},
+                         {beta, size_t(Cout) * 4},
+                         {workspace, need}};
+    st = check_no_alias(Span{out, size_t(N) * Cout * gen.OD * gen.OH * gen.OW * 4}, gins, 6);
+    if (st != GF_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GF_OK) return st;
+    return launch_ct_general(gen, x, w, b, gamma, beta, out, eps, workspace, static_cast<cudaStream_t>(stream));
+  }
   if (!workspace) return GF_ERR_NULL;
   if (workspace_bytes < need) return GF_ERR_WORKSPACE;
   const size_t outb = size_t(N) * Cout * (2 * D - 1) * (2 * H - 1) * (2 * W - 1) * 4;
@@ -569,12 +591,29 @@ gf_status gf_convt3d_swish_gn_hswish_noalloc(const float* x, const float* w, con
                                              int64_t D, int64_t H, int64_t W, int32_t k, int32_t stride, int32_t pad,
                                              int32_t groups, float eps, void* stream) {
   if (!x || !w || !gamma || !beta || !out) return GF_ERR_NULL;
-  gf_status st = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups);
+  CtGenShape gen;
+  const bool fast = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) == GF_OK;
+  gf_status st = fast ? GF_OK : ct_general_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups, &gen);
   if (st != GF_OK) return st;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(w) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
       (b && !aligned16(b)))
     return GF_ERR_ALIGN;
+  if (!fast) {  // the general kernels, their workspace in the fixed scratch
+    if (gen.total > kCtNoAllocScratchBytes) return GF_ERR_WORKSPACE;
+    const Span gins[] = {{x, size_t(N) * Cin * D * H * W * 4},
+                         {w, size_t(Cin) * Cout * k * k * k * 4},
+                         {b, size_t(Cout) * 4},
+                         {gamma, size_t(Cout) * 4},
+                         {beta, size_t(Cout) * 4}};
+    st = check_no_alias(Span{out, size_t(N) * Cout * gen.OD * gen.OH * gen.OW * 4}, gins, 5);
+    if (st != GF_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != GF_OK) return st;
+    void* scratch = nullptr;
+    if ((st = ct_scratch_address(dev.device, &scratch)) != GF_OK) return st;
+    return launch_ct_general(gen, x, w, b, gamma, beta, out, eps, scratch, static_cast<cudaStream_t>(stream));
+  }
   const CtWs wl = ct_ws(N, D, H, W);
   if (wl.total > kCtNoAllocScratchBytes) return GF_ERR_WORKSPACE;  // beyond the fixed scratch
   const size_t outb = size_t(N) * Cout * (2 * D - 1) * (2 * H - 1) * (2 * W - 1) * 4;

@@ -228,8 +228,16 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
  *   x [N,Cin,D,H,W]; w [Cin,Cout,k,k,k] (nn.ConvTranspose3d layout);
  *   b [Cout] (may be NULL); gamma, beta [Cout];
  *   out [N,Cout,(D-1)s-2p+k, (H-1)s-2p+k, (W-1)s-2p+k].
- *   Supported: k == 3, stride == 2, pad == 1, Cin <= 8, Cout == 16,
- *   groups == 4; output_padding is 0.
+ *   Supported: 1 <= k <= 8, 1 <= stride <= 8, 0 <= pad <= 64 with every
+ *   output extent >= 1, 1 <= Cin, Cout <= 1024, Cout % groups == 0,
+ *   N <= 65535, fewer than 2^30 output voxels per sample; output_padding
+ *   is 0.
+ *
+ *   The pages' configuration (k == 3, stride == 2, pad == 1, Cout == 16,
+ *   groups == 4) with Cin <= 8 runs on specialized kernels (the tensor
+ *   cores for Cin <= 4, described next; the CUDA cores for 5..8); every
+ *   other shape on general CUDA-core kernels (gather form of the transposed
+ *   convolution, two passes, statistics in fp64).
  *
  *   With Cin <= 4 and at most (number of SMs + 1) tiles of 128 (h, w) cells
  *   per sample the call is one cooperative kernel (one CTA per SM, every CTA
@@ -261,7 +269,8 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
  * workspace.
  *
  * Same operator, arguments (minus workspace), supported shapes and result as
- * gf_convt3d_swish_gn_hswish.  The caller still owns and passes x, w, b,
+ * gf_convt3d_swish_gn_hswish (the pages' configuration on the CUDA-core
+ * two-pass kernels).  The caller still owns and passes x, w, b,
  * gamma, beta and out.  The scratch (the per-block GroupNorm sums and the
  * per-channel affine coefficients, gf_convt3d_swish_gn_hswish_workspace_size()
  * bytes) lives in a fixed array inside the library, 4 MiB

@@ -92,7 +92,13 @@ def test_workspace_sizes(L):
     assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0x400) == 0
     assert L.gf_linear_workspace_size(M, K, N, GELU_TANH) == 0  # other calls take no flag
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 2, 1, 4) > 0
-    assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 1, 1, 4) == 0
+    # other strides, kernel sizes, channel counts and groups take the general
+    # kernels: per (sample, channel, block) fp64 sums and per-channel
+    # coefficients
+    ws = L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 1, 1, 4)
+    assert ws >= 128 * 16 * 2 * 8 + 128 * 16 * 8
+    assert L.gf_convt3d_swish_gn_hswish_workspace_size(2, 12, 32, 4, 5, 6, 4, 3, 2, 8) > 0
+    assert L.gf_convt3d_swish_gn_hswish_workspace_size(2, 3, 16, 1, 1, 1, 1, 1, 1, 4) == 0  # empty output
 
 
 def test_lse_validation(L):
@@ -148,9 +154,17 @@ def test_convt3d_validation(L):
                                             a["Cout"], a["D"], a["H"], a["W"], a["k"], a["s"], a["p"], a["G"], a["eps"],
                                             a["ws"], a["wsb"], None)
     assert call(x=None) == GF_ERR_NULL
-    assert call(G=2) == GF_ERR_SHAPE
-    assert call(Cin=9) == GF_ERR_SHAPE
-    assert call(k=5) == GF_ERR_SHAPE
+    assert call(G=3) == GF_ERR_SHAPE               # 16 channels in 3 groups
+    assert call(G=0) == GF_ERR_SHAPE
+    assert call(Cin=2000) == GF_ERR_SHAPE
+    assert call(k=9) == GF_ERR_SHAPE               # kernel sizes 1..8
+    assert call(s=0) == GF_ERR_SHAPE
+    assert call(p=-1) == GF_ERR_SHAPE
+    assert call(D=1, k=1, s=1, p=1) == GF_ERR_SHAPE  # output extent (1-1)*1 - 2 + 1 < 1
+    assert call(N=70000, k=4) == GF_ERR_SHAPE       # general kernels: N <= 65535
+    assert call(k=4, wsb=8) == GF_ERR_WORKSPACE     # general kernels: the same checks
+    assert call(k=4, out=P[6]) == GF_ERR_ALIAS
+    assert call(k=4, w=P[1] + 8) == GF_ERR_ALIGN
     assert call(be=None) == GF_ERR_NULL
     assert call(g=P[3] + 4) == GF_ERR_ALIGN
     assert call(wsb=8) == GF_ERR_WORKSPACE

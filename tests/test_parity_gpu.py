@@ -274,6 +274,28 @@ def test_convt3d_small(N, Cin, D, H, W):
     assert_close(got, ref, f"convt3d {N}x{Cin}x{D}x{H}x{W}")
 
 
+# Shapes outside the pages' configuration (other kernel sizes, strides,
+# paddings, channel counts and groups; Cin > 8): the general CUDA-core kernels
+@pytest.mark.parametrize("N,Cin,Cout,G,k,st,pd,D,H,W", [
+    (2, 12, 16, 4, 3, 2, 1, 3, 5, 6), (2, 3, 8, 2, 3, 2, 1, 4, 6, 7), (1, 3, 32, 8, 4, 2, 1, 3, 4, 5),
+    (2, 2, 6, 3, 5, 3, 2, 3, 4, 4), (2, 4, 16, 4, 2, 2, 0, 5, 5, 6), (1, 3, 16, 4, 3, 1, 1, 6, 7, 8),
+    (3, 1, 4, 1, 1, 1, 0, 3, 3, 3), (1, 3, 16, 16, 3, 2, 0, 3, 4, 5), (1, 5, 12, 3, 8, 4, 3, 2, 3, 3),
+    (40, 2, 9, 3, 3, 2, 2, 2, 3, 4)])
+def test_convt3d_general(N, Cin, Cout, G, k, st, pd, D, H, W):
+    s = synth.ConvT3dShape(N=N, Cin=Cin, Cout=Cout, D=D, H=H, W=W, k=k, stride=st, pad=pd, groups=G)
+    got, ref = _ct_run(s, synth.convt3d_inputs(s, 900 + 10 * k + st + Cout))
+    assert_close(got, ref, f"convt3d general Cin {Cin} Cout {Cout}/{G} k{k} s{st} p{pd}")
+
+
+def test_convt3d_general_noalloc_matches_workspace_call():
+    s = synth.ConvT3dShape(N=2, Cin=3, Cout=8, D=4, H=5, W=6, k=4, stride=2, pad=1, groups=2)
+    d = synth.convt3d_inputs(s, 31)
+    args = (T(d["x"]), T(d["w"]), T(d["b"]), T(d["gamma"]), T(d["beta"]), s.stride, s.pad, s.groups, s.eps)
+    a = gf.gf_convt3d_swish_gn_hswish(*args).cpu()
+    b = gf.gf_convt3d_swish_gn_hswish_noalloc(*args).cpu()
+    assert torch.equal(a, b)
+
+
 def test_convt3d_uniform_inputs():
     s = synth.ConvT3dShape(N=2, D=6, H=12, W=12)
     got, ref = _ct_run(s, synth.convt3d_inputs(s, 77, x_dist="uniform01"))
