@@ -156,7 +156,7 @@ class Workload:
 
 class LinearGN(Workload):
     sources = Workload.sources + ("linear_ops.cu",)
-    kernel = "gemm_tc_kernel<256, OpTF32x3, LinearSrc, EpiSwishBiasGN>"
+    kernel = "gemm_tc_kernel<256, OpTF32x3, LinearSrc, EpiSwishBiasGNT<64>>"
 
     def __init__(self, M, name):
         from conv_activation_normalization_gb300 import synth
@@ -169,7 +169,7 @@ class LinearGN(Workload):
         self.config = {"workload": f"linear_swish_bias_groupnorm x[{s.M},{s.K}] W[{s.N},{s.K}] groups={s.groups}",
                        "M": s.M, "K": s.K, "N": s.N, "groups": s.groups, "eps": s.eps}
         bn = 256 if M >= 8192 else 64  # the library's tile width for this M (152 SMs)
-        self.kernel = f"gemm_tc_kernel<{bn}, OpTF32x3, LinearSrc, EpiSwishBiasGN>"
+        self.kernel = f"gemm_tc_kernel<{bn}, OpTF32x3, LinearSrc, EpiSwishBiasGNT<64>>"
         self.l2 = ("inputs larger than L2 (x 134 MB + out 537 MB per step vs 129 MB L2); no flush" if M >= 8192
                    else "L2 flushed between steps (a 256 MB buffer is written)")
 
