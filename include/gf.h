@@ -19,7 +19,11 @@
  *     matching *_workspace_size() query returns (256-byte aligned).  It may be
  *     NULL only when that size is 0.  Its contents on entry do not matter.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
- *     enqueued on it and the call returns without synchronising.
+ *     enqueued on it and the call returns without synchronising.  The device
+ *     entry points make only stream-ordered CUDA calls (kernel launches,
+ *     including cooperative ones, and async memsets), so a call can be
+ *     captured into a CUDA graph and replayed with the same arguments
+ *     (the host-buffer entry point, which waits on copies, cannot).
  *   - Arguments are validated before anything is launched; a rejected call
  *     launches nothing and returns a negative gf_status.  No C++ exception
  *     crosses this boundary.
