@@ -342,3 +342,42 @@ def test_dconv1d_offset_input_statistics():
     d["x"] = (d["x"] * np.float32(0.01) + np.float32(100.0)).astype(np.float32)
     got, ref = _dc_run(s, d)
     assert_close(got, ref, "dconv1d offset input")
+
+
+# ------------------------------------------------- CUDA graph capture
+def test_calls_replay_from_a_cuda_graph():
+    # every device entry point is stream-ordered and allocates nothing, so a
+    # captured call replays to the eager result bit for bit (the workspace
+    # comes from the binding's cache, filled by the eager calls)
+    s1, d1 = _lgn_case(300, 64, 256, 4, 5)
+    s2 = synth.LinearLSEShape(M=100, K=64, N=500)
+    d2 = synth.linear_lse_inputs(s2, 6)
+    s3 = synth.DConv1dShape(B=2, C=64, L=128, dilation=2, padding=2)
+    d3 = synth.dconv1d_inputs(s3, 7)
+    s4 = synth.ConvT3dShape(N=2, D=4, H=8, W=8)   # the single cooperative kernel
+    d4 = synth.convt3d_inputs(s4, 8)
+    s5 = synth.ConvT3dShape(N=2, Cout=8, groups=2, D=3, H=4, W=4, k=4)  # the general kernels
+    d5 = synth.convt3d_inputs(s5, 9)
+    # device inputs first: a capture may contain no host-to-device copy
+    g1 = [T(d1[k]) for k in ("x", "W", "b_lin", "bias", "gamma", "beta")]
+    g2 = [T(d2[k]) for k in ("x", "W", "b")]
+    g3 = [T(d3[k]) for k in ("x", "ln_gamma", "ln_beta", "conv_w", "conv_b")]
+    g4 = [T(d4[k]) for k in ("x", "w", "b", "gamma", "beta")]
+    g5 = [T(d5[k]) for k in ("x", "w", "b", "gamma", "beta")]
+    calls = [
+        lambda: gf.gf_linear_swish_bias_groupnorm(*g1, s1.groups, s1.eps),
+        lambda: gf.gf_linear_lse_act(*g2, s2.negative_slope),
+        lambda: gf.gf_ln_gelu_dconv1d_res(*g3, s3.dilation, s3.padding, s3.eps),
+        lambda: gf.gf_convt3d_swish_gn_hswish(*g4, s4.stride, s4.pad, s4.groups, s4.eps),
+        lambda: gf.gf_convt3d_swish_gn_hswish(*g5, s5.stride, s5.pad, s5.groups, s5.eps),
+    ]
+    for i, call in enumerate(calls):
+        ref = call().clone()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            out = call()
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"call {i}"
