@@ -140,15 +140,25 @@ class profile:
 _ws_cache: dict = {}
 
 
-def _workspace(device: torch.device, nbytes: int):
-    """Per-device cached scratch buffer (grown on demand)."""
+def _workspace(device: torch.device, nbytes: int, stream=None):
+    """Cached scratch buffer per (device, stream), grown on demand.  Calls on
+    one stream are ordered, so they can share one buffer; calls on different
+    streams get different buffers.  A buffer made for a stream other than
+    the current one is recorded on that stream, so that the allocator does
+    not hand its memory out again (after it is replaced) before the work
+    queued there is done."""
     if nbytes == 0:
         return None
-    key = device.index if device.index is not None else torch.cuda.current_device()
-    buf = _ws_cache.get(key)
-    if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        _ws_cache[key] = buf
+    index = device.index if device.index is not None else torch.cuda.current_device()
+    s = stream if stream is not None else torch.cuda.current_stream(index)
+    key = (index, s.cuda_stream)
+    with _lock:
+        buf = _ws_cache.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            if s.cuda_stream != torch.cuda.current_stream(index).cuda_stream:
+                buf.record_stream(s)
+            _ws_cache[key] = buf
     return buf
 
 
@@ -185,9 +195,9 @@ def _call(name, *args):
         raise GFError(st, name)
 
 
-def _ws_args(device, nbytes, workspace):
+def _ws_args(device, nbytes, workspace, stream=None):
     if workspace is None:
-        workspace = _workspace(device, nbytes)
+        workspace = _workspace(device, nbytes, stream)
     elif workspace.numel() * workspace.element_size() < nbytes:
         raise ValueError("workspace too small")
     return (None if workspace is None else workspace.data_ptr()), nbytes
@@ -203,7 +213,7 @@ def gf_linear(x, W, b=None, mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, 
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         nbytes = lib().gf_linear_workspace_size(M, K, N, mode)
-        wp, nb = _ws_args(dev, nbytes, workspace)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
         _call("gf_linear", _ptr(x), _ptr(W), _ptr(b), _ptr(out), M, K, N, mode, wp, nb, _stream_ptr(stream))
     return out
 
@@ -218,7 +228,7 @@ def gf_linear_swish_bias_groupnorm(x, W, b_lin, bias, gamma, beta, groups, eps=1
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         nbytes = lib().gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, groups, mode)
-        wp, nb = _ws_args(dev, nbytes, workspace)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
         _call("gf_linear_swish_bias_groupnorm", _ptr(x), _ptr(W), _ptr(b_lin), _ptr(bias), _ptr(gamma),
               _ptr(beta), _ptr(out), M, K, N, groups, eps, mode, wp, nb, _stream_ptr(stream))
     return out
@@ -266,7 +276,7 @@ def gf_linear_swish_bias_groupnorm_host(x_host, W, b_lin, bias, gamma, beta, gro
         out_host = torch.empty((M, N), dtype=torch.float32, pin_memory=x_host.is_pinned())
     with torch.cuda.device(dev):
         nbytes = lib().gf_linear_swish_bias_groupnorm_host_workspace_size(M, K, N, groups, mode, chunk_rows)
-        wp, nb = _ws_args(dev, nbytes, workspace)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
         _call("gf_linear_swish_bias_groupnorm_host", x_host.data_ptr(), _ptr(W), _ptr(b_lin), _ptr(bias),
               _ptr(gamma), _ptr(beta), out_host.data_ptr(), M, K, N, groups, eps, mode, chunk_rows, wp, nb,
               _stream_ptr(stream))
@@ -283,7 +293,7 @@ def gf_linear_lse_act(x, W, b, negative_slope=0.01, mode=GF_MODE_FP32_3XTF32, ou
         out = torch.empty((M, 1), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         nbytes = lib().gf_linear_lse_act_workspace_size(M, K, N, mode)
-        wp, nb = _ws_args(dev, nbytes, workspace)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
         _call("gf_linear_lse_act", _ptr(x), _ptr(W), _ptr(b), _ptr(out), M, K, N, negative_slope, mode, wp, nb,
               _stream_ptr(stream))
     return out
@@ -304,7 +314,7 @@ def gf_ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, paddi
         out = torch.empty_like(x)
     with torch.cuda.device(dev):
         nbytes = lib().gf_ln_gelu_dconv1d_res_workspace_size(B, C, L, ksize, mode)
-        wp, nb = _ws_args(dev, nbytes, workspace)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
         _call("gf_ln_gelu_dconv1d_res", _ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(conv_w), _ptr(conv_b),
               _ptr(out), B, C, L, ksize, dilation, padding, eps, mode, wp, nb, _stream_ptr(stream))
     return out
@@ -326,7 +336,7 @@ def gf_convt3d_swish_gn_hswish(x, w, b, gamma, beta, stride, pad, groups, eps=1e
         out = torch.empty(convt3d_out_shape(x.shape, Cout, k, stride, pad), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         nbytes = lib().gf_convt3d_swish_gn_hswish_workspace_size(N, Cin, Cout, D, H, W, k, stride, pad, groups)
-        wp, nb = _ws_args(dev, nbytes, workspace)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
         _call("gf_convt3d_swish_gn_hswish", _ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(out),
               N, Cin, Cout, D, H, W, k, stride, pad, groups, eps, wp, nb, _stream_ptr(stream))
     return out
