@@ -381,3 +381,24 @@ def test_calls_replay_from_a_cuda_graph():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, ref), f"call {i}"
+
+
+def test_calls_on_two_streams_use_separate_default_workspaces():
+    # the lo planes of x and W live in the workspace: two concurrent calls
+    # with different inputs would corrupt each other through a shared one
+    s, d = _lgn_case(2048, 512, 2048, 32, 21)
+    x2 = d["x"][::-1].copy()
+    rest = [T(d[k]) for k in ("W", "b_lin", "bias", "gamma", "beta")]
+    xa, xb = T(d["x"]), T(x2)
+    ref_a = gf.gf_linear_swish_bias_groupnorm(xa, *rest, s.groups, s.eps).clone()
+    ref_b = gf.gf_linear_swish_bias_groupnorm(xb, *rest, s.groups, s.eps).clone()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        with torch.cuda.stream(sa):
+            oa = gf.gf_linear_swish_bias_groupnorm(xa, *rest, s.groups, s.eps, stream=sa)
+        with torch.cuda.stream(sb):
+            ob = gf.gf_linear_swish_bias_groupnorm(xb, *rest, s.groups, s.eps, stream=sb)
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ref_a) and torch.equal(ob, ref_b)
