@@ -215,7 +215,7 @@ class LinearLSE(Workload):
     name = "linear_lse_m1024"
     metric = "fused Linear->logsumexp->LeakyReLU x2->GELU x2 TFLOP/s at x[1024,8192], W[8192,8192]"
     sources = Workload.sources + ("linear_ops.cu",)
-    kernel = "gemm_tc_kernel<224, OpTF32x3, LinearSrc, EpiLSEPartial>"  # 224-column tiles at 152 SMs
+    kernel = "gemm_tc_kernel<160, OpTF32x3, LinearSrc, EpiLSEPartial>"  # 160-column tiles (three stages)
     l2 = "inputs larger than L2 (W 268 MB per step vs 129 MB L2); no flush"
     chunk = 64
 

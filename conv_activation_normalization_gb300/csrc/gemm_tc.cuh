@@ -83,7 +83,9 @@ struct TileCfg {
   static constexpr int A_BYTES = kBM * 128;  // one plane of a 128-row tile
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = Op::kPlanes * (A_BYTES + B_BYTES);
-  static constexpr int STAGES_FIT = (208 * 1024) / STAGE_BYTES;
+  // stages within 220 KB (plus barriers and alignment: under the 227 KB a
+  // CTA may use)
+  static constexpr int STAGES_FIT = (220 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   // two accumulators, each starting on a multiple of TMEM_COLS / 2
   static constexpr int TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);

@@ -221,7 +221,7 @@ gf_status with_gn_epilogue(int gw, F&& f) {
 
 // Linear -> per-row (max, sum exp(y - max)) over the tile's BN columns,
 // written as one float2 partial per (row, n-block); columns are read 16 at a
-// time, so BN may be any multiple of 16 (the tile widths are 256 and 224).
+// time, so BN may be any multiple of 16 (the tile widths are 160, 224 and 256).
 struct EpiLSEPartial {
   static constexpr bool kFixedBN = true;  // the partials' layout follows the tile width
   struct Params {
@@ -328,17 +328,30 @@ namespace {
 
 constexpr int kBNLinear = 256;
 
-// Tile width of the LSE chain: 256 columns unless 224-column tiles fill the
-// SMs' waves noticeably better (e.g. 1024 x 8192: 256 tiles = 1.68 waves of
-// 152 SMs against 296 tiles = 1.95 waves).
-int lse_tile_width(int64_t M, int64_t N, int sm_count) {
+// Tile width of the LSE chain: 160, 224 or 256 columns, whichever gives the
+// least waves x per-tile time.  In the three-product modes a 160-column tile
+// fits three smem stages (two for 224 or 256), deep enough for the mainloop
+// to keep pace with W streaming from DRAM; with two stages it runs about
+// 15 % slower per column (1024 x 8192 x 8192: 160 -> 95 %, 224 -> 82 % of
+// the 3xTF32 peak, measured).  The one-product BF16 mode has four or more
+// stages at any width, and there the wider tiles win.
+constexpr int kLseWidths[3] = {160, 224, 256};
+int lse_tile_width(int64_t M, int64_t N, int sm_count, int32_t mode) {
   const int64_t mb = (M + 127) / 128;
-  auto eff = [&](int bn) {
+  int best = kLseWidths[0];
+  double best_t = 0.0;
+  for (int bn : kLseWidths) {
+    if (mode == GF_MODE_BF16 && bn == 160) continue;
     const int64_t tiles = mb * ((N + bn - 1) / bn);
     const int64_t waves = (tiles + sm_count - 1) / sm_count;
-    return double(tiles) / double(waves * sm_count) * (double(N) / double(((N + bn - 1) / bn) * bn));
-  };
-  return eff(224) > 1.05 * eff(256) ? 224 : 256;
+    const double depth = (mode == GF_MODE_BF16 || bn == 160) ? 1.0 : 0.85;
+    const double t = double(waves) * bn / depth;
+    if (best_t == 0.0 || t < best_t) {
+      best = bn;
+      best_t = t;
+    }
+  }
+  return best;
 }
 // Partials per row for a tile width: one per epilogue column half.
 int64_t lse_parts(int64_t N, int bn) { return (N + bn - 1) / bn * epi_halves(bn); }
@@ -431,16 +444,18 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
 // Tile width: 256 columns when that gives every SM at least one tile;
 // otherwise (small M) 128 or 64, trading per-tile efficiency for parallelism.
 // The LSE partials' layout follows the tile width, which lse_tile_width picks
-// (256 or 224 columns).
+// (160, 224 or 256 columns).
 template <class Op, class Epi>
 gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
                              int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
   if constexpr (Epi::kFixedBN) {
-    // the LSE partials: 256- or 224-column tiles, whichever fills the waves
-    // of SMs better (the caller sized the partials with lse_tile_width)
-    if (lse_tile_width(M, N, dev.sm_count) == 224)
-      return run_linear_gemm<224, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-    return run_linear_gemm<kBNLinear, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    // the LSE partials: the width lse_tile_width picks (the caller sized
+    // the partials with it)
+    switch (lse_tile_width(M, N, dev.sm_count, Op::kProducts == 1 ? GF_MODE_BF16 : GF_MODE_FP32_3XTF32)) {
+      case 160: return run_linear_gemm<160, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+      case 224: return run_linear_gemm<224, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+      default: return run_linear_gemm<kBNLinear, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    }
   } else {
     const int64_t mb = (M + kBM - 1) / kBM;
     // (the epilogue's groups must not straddle warps: Epi::kMinBN)
@@ -743,8 +758,8 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
 size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {
   if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
   // one (max, sum) partial per row and epilogue column half of each n-block,
-  // sized for the narrower of the two tile widths
-  const int64_t nb = lse_parts(N, 224);
+  // sized for the narrowest tile width
+  const int64_t nb = lse_parts(N, kLseWidths[0]);
   return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode) +
          align_up(size_t(M) * nb * sizeof(float2), 256);
 }
@@ -770,7 +785,7 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
   float2* part = reinterpret_cast<float2*>(ws + operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode));
   DeviceInfo dev;
   if ((st = current_device(&dev)) != GF_OK) return st;
-  const int nb = int(lse_parts(N, lse_tile_width(M, N, dev.sm_count)));
+  const int nb = int(lse_parts(N, lse_tile_width(M, N, dev.sm_count, mode)));
   EpiLSEPartial::Params ep{b, part, int(M), int(N), nb};
   // m-blocks fastest: the CTAs in flight share n-blocks, so each W tile is
   // fetched from HBM once and reused by every m-block from L2.

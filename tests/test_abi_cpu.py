@@ -81,9 +81,9 @@ def test_workspace_sizes(L):
     assert L.gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, 64, 3) == 0
     assert L.gf_linear_workspace_size(M, K, N, 0) == ws
     M, K, N = 1024, 8192, 8192
-    # one (max, sum) float2 per row and column half of each n-block, sized for
-    # the narrower (224-column) of the two tile widths
-    assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (-(-N // 224) * 2) * 8
+    # one (max, sum) float2 per row and column half of each n-block, sized
+    # for the narrowest (160-column) tile width
+    assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (-(-N // 160) * 2) * 8
     assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0) > 2 * 4 * 32 * 256 * 4096
     GELU_TANH = 0x100
     for mode in (0, 1, 2):  # the GELU flag changes no buffer
