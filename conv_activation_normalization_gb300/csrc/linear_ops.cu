@@ -203,19 +203,89 @@ struct EpiSwishBiasGNT {
   }
 };
 
-// Runs f(TypeTag<epilogue>) with the epilogue of group width gw.
+// Any other group width: the epilogue stores t = Swish(y + b_lin) + bias
+// and gn_rows_kernel normalises the rows in place afterwards (one more pass
+// over the output, instead of none).
+struct EpiSwishBiasStore {
+  static constexpr bool kFixedBN = false;
+  static constexpr int kMinBN = 64;
+  using Params = GNParams;
+  template <int BN>
+  __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
+    const int m = t.r0 + row;
+    const bool valid = m < p.M;
+    float* orow = p.out + size_t(m) * size_t(p.N);
+#pragma unroll 1
+    for (int g = 0; g < BN / 32; ++g) {
+      const int n0 = t.n0 + g * 32;
+      if (n0 >= p.N) break;  // uniform across the warp
+      uint32_t v[32];
+      GF_TMEM_LD32(taddr + uint32_t(g * 32), v);
+      GF_TMEM_WAIT32(v);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const int n = n0 + j;
+        const bool in0 = n < p.N, in1 = n + 1 < p.N;
+        const float b0 = p.b_lin && in0 ? __ldg(p.b_lin + n) : 0.f, b1 = p.b_lin && in1 ? __ldg(p.b_lin + n + 1) : 0.f;
+        const float2 sv = swish2(make_float2(__uint_as_float(v[j]) + b0, __uint_as_float(v[j + 1]) + b1));
+        if (valid && in0) orow[n] = sv.x + __ldg(p.bias + n);
+        if (valid && in1) orow[n + 1] = sv.y + __ldg(p.bias + n + 1);
+      }
+    }
+  }
+};
+
+// GroupNorm of each row of out[M][N] in place, groups of gw consecutive
+// columns: one block per row, one warp per group at a time, the group's
+// mean and centred second moment in two passes (fp32, lane-strided sums and
+// a shuffle tree), then (t - mean) rstd gamma + beta.
+__global__ void __launch_bounds__(256) gn_rows_kernel(float* __restrict__ out, const float* __restrict__ gamma,
+                                                      const float* __restrict__ beta, int N, int gw, float eps) {
+  float* row = out + size_t(blockIdx.x) * N;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const float inv = 1.f / float(gw);
+  for (int g = warp; g < N / gw; g += 8) {
+    float* v = row + size_t(g) * gw;
+    float s = 0.f;
+    for (int i = lane; i < gw; i += 32) s += v[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float mean = s * inv;
+    float q = 0.f;
+    for (int i = lane; i < gw; i += 32) {
+      const float d = v[i] - mean;
+      q = fmaf(d, d, q);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+    const float rstd = rsqrtf(q * inv + eps);
+    for (int i = lane; i < gw; i += 32) {
+      const int n = g * gw + i;
+      v[i] = fmaf((v[i] - mean) * rstd, __ldg(gamma + n), __ldg(beta + n));
+    }
+  }
+}
+
+// Runs f(TypeTag<epilogue>) with the fused epilogue of group width ep.gw
+// (16, 32, 64 or 128 columns), or with EpiSwishBiasStore followed by
+// gn_rows_kernel on stream s for any other width.
 template <class T>
 struct TypeTag {
   using type = T;
 };
 template <class F>
-gf_status with_gn_epilogue(int gw, F&& f) {
-  switch (gw) {
+gf_status with_gn_epilogue(const GNParams& ep, cudaStream_t s, F&& f) {
+  switch (ep.gw) {
     case 16: return f(TypeTag<EpiSwishBiasGNT<16>>{});
     case 32: return f(TypeTag<EpiSwishBiasGNT<32>>{});
     case 64: return f(TypeTag<EpiSwishBiasGNT<64>>{});
     case 128: return f(TypeTag<EpiSwishBiasGNT<128>>{});
-    default: return GF_ERR_SHAPE;
+    default: {
+      const gf_status st = f(TypeTag<EpiSwishBiasStore>{});
+      if (st != GF_OK) return st;
+      gn_rows_kernel<<<unsigned(ep.M), 256, 0, s>>>(ep.out, ep.gamma, ep.beta, ep.N, ep.gw, ep.eps);
+      return cuda_status(cudaGetLastError());
+    }
   }
 }
 
@@ -381,12 +451,9 @@ gf_status check_linear_shape(int64_t M, int64_t K, int64_t N, int32_t mode) {
   return GF_OK;
 }
 
-// GroupNorm group widths the epilogue handles: 16, 32, 64 or 128 columns.
-bool gn_width_ok(int64_t N, int32_t groups) {
-  if (groups < 1 || N % groups != 0) return false;
-  const int64_t w = N / groups;
-  return w == 16 || w == 32 || w == 64 || w == 128;
-}
+// GroupNorm groups: any count that divides N (groups of 16, 32, 64 or 128
+// columns run in the GEMM epilogue, other widths in a second kernel).
+bool gn_groups_ok(int64_t N, int32_t groups) { return groups >= 1 && N % groups == 0; }
 
 // Planes the GEMM reads for one operand: p[0] = hi (or the only operand),
 // p[1] = lo.
@@ -528,7 +595,7 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
   if (!x_planes || !W_planes || !bias || !gamma || !beta || !out) return GF_ERR_NULL;
   gf_status st = check_linear_shape(M, K, N, GF_MODE_FP32_3XTF32);
   if (st != GF_OK) return st;
-  if (!gn_width_ok(N, groups)) return GF_ERR_SHAPE;
+  if (!gn_groups_ok(N, groups)) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(x_planes) || !aligned16(W_planes) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       !aligned16(out) || (b_lin && !aligned16(b_lin)))
@@ -542,7 +609,7 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
   const Planes a{{x_planes, x_planes + size_t(M) * K}}, b{{W_planes, W_planes + size_t(N) * K}};
   const GNParams ep{b_lin, bias, gamma, beta, out, int(M), int(N), eps, int(N / groups)};
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return with_gn_epilogue(ep.gw, [&](auto tag) {
+  return with_gn_epilogue(ep, s, [&](auto tag) {
     return run_linear<typename decltype(tag)::type>(GF_MODE_FP32_3XTF32, dev, a, b, M, K, N, 0, ep, s);
   });
 }
@@ -555,7 +622,7 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
-  if (!gn_width_ok(N, groups)) return GF_ERR_SHAPE;
+  if (!gn_groups_ok(N, groups)) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(W) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       !aligned16(out) || (b_lin && !aligned16(b_lin)) || !aligned16(workspace))
@@ -572,7 +639,7 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
   // n-blocks fastest (m_fastest 0): the CTAs in flight share a few m-blocks
   // of x, while all of W stays resident in L2.
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return with_gn_epilogue(ep.gw, [&](auto tag) {
+  return with_gn_epilogue(ep, s, [&](auto tag) {
     return split_and_run<typename decltype(tag)::type>(mode, x, W, M, K, N, workspace, 0, ep, s);
   });
 }
@@ -645,7 +712,7 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
-  if (!gn_width_ok(N, groups) || chunk_rows < 0) return GF_ERR_SHAPE;
+  if (!gn_groups_ok(N, groups) || chunk_rows < 0) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(W) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       (b_lin && !aligned16(b_lin)) || !aligned16(workspace))
@@ -713,7 +780,7 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
       Planes xp{};
       const GNParams ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps, int(N / groups)};
       ok = prepare_operand(xd, rows, K, mode, ws + wl.xp[bi], dev, s, &xp) == GF_OK &&
-           with_gn_epilogue(ep.gw, [&](auto tag) {
+           with_gn_epilogue(ep, s, [&](auto tag) {
              return run_linear<typename decltype(tag)::type>(mode, dev, xp, wp, rows, K, N, 0, ep, s);
            }) == GF_OK &&
            cudaEventRecord(ev_comp[bi], s) == cudaSuccess;

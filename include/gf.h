@@ -127,8 +127,10 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
  *   x [M,K], W [N,K] (nn.Linear layout), b_lin/bias/gamma/beta [N], out [M,N].
  *   b_lin may be NULL (no linear bias).
  *   Supported: M >= 1, K >= 4 with K % 4 == 0 (K % 8 == 0 in the BF16 modes),
- *   N % groups == 0 and a group width N/groups of 16, 32, 64 or 128 (groups
- *   of 128 always run on 256-column tiles).
+ *   groups >= 1 with N % groups == 0.  Group widths N/groups of 16, 32, 64
+ *   and 128 run inside the GEMM epilogue (groups of 128 on 256-column
+ *   tiles); any other width stores t and normalises the rows in a second
+ *   kernel (one more pass over out).
  * ---------------------------------------------------------------------- */
 size_t gf_linear_swish_bias_groupnorm_workspace_size(int64_t M, int64_t K, int64_t N,
                                                      int32_t groups, int32_t mode);

@@ -55,9 +55,8 @@ def test_linear_gn_validation(L):
     assert _lgn(L, mode=0x100) == GF_ERR_MODE     # the GELU flag belongs to the Conv1d chain
     assert _lgn(L, K=1020, mode=1) == GF_ERR_SHAPE  # bf16 planes need K % 8
     assert _lgn(L, K=1020, mode=2) == GF_ERR_SHAPE
-    assert _lgn(L, groups=16) == GF_ERR_SHAPE      # group width 256 is not supported
-    assert _lgn(L, groups=512) == GF_ERR_SHAPE     # nor 8
-    assert _lgn(L, N=4032, groups=42) == GF_ERR_SHAPE  # nor 96
+    assert _lgn(L, groups=3) == GF_ERR_SHAPE       # groups must divide N
+    assert _lgn(L, groups=8192) == GF_ERR_SHAPE
     assert _lgn(L, groups=0) == GF_ERR_SHAPE
     assert _lgn(L, K=1022) == GF_ERR_SHAPE         # K % 4
     assert _lgn(L, M=0) == GF_ERR_SHAPE

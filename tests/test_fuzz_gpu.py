@@ -48,7 +48,7 @@ def _cases(seed, n, draw):
 
 def _lgn_case(r):
     mode = int(r.integers(0, 3))
-    gw = int(r.choice([16, 32, 64, 128]))
+    gw = int(r.choice([16, 32, 64, 128, 8, 48, 256, 320]))
     kq = 4 if mode == 0 else 8
     return dict(M=int(r.integers(1, 400)), K=kq * int(r.integers(1, 64)), gw=gw, groups=int(r.integers(1, 12)),
                 mode=mode, seed=int(r.integers(1 << 30)))

@@ -78,7 +78,7 @@ def test_linear_gn_modes(mode, M, K, N):
 
 
 @pytest.mark.parametrize("mode", [BF16, X3BF16])
-@pytest.mark.parametrize("M,K,N,gw", [(130, 40, 320, 16), (200, 64, 512, 128)])
+@pytest.mark.parametrize("M,K,N,gw", [(130, 40, 320, 16), (200, 64, 512, 128), (150, 64, 768, 256)])
 def test_linear_gn_modes_group_widths(mode, M, K, N, gw):
     s = synth.LinearGNShape(M=M, K=K, N=N, groups=N // gw)
     d = synth.linear_gn_inputs(s, 600 + gw)

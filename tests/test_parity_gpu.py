@@ -120,6 +120,16 @@ def test_linear_gn_group_widths(M, K, N, gw):
     assert_close(got, ref, f"linear_gn {M}x{K}x{N} groups of {gw}")
 
 
+# other group widths: t stored by the GEMM epilogue, rows normalised by a
+# second kernel (any width dividing N, including one group per row)
+@pytest.mark.parametrize("M,K,N,groups", [(130, 36, 512, 2), (200, 64, 4096, 16), (64, 32, 384, 4), (97, 40, 96, 12),
+                                          (33, 16, 1000, 5), (1, 4, 4096, 1), (129, 1024, 4096, 8)])
+def test_linear_gn_other_group_widths(M, K, N, groups):
+    s, d = _lgn_case(M, K, N, groups, 800 + N // groups)
+    got, ref = _lgn_run(s, d)
+    assert_close(got, ref, f"linear_gn {M}x{K}x{N} in {groups} groups of {N // groups}")
+
+
 def test_linear_gn_group_width_128_halves_differ():
     # a 128-column group whose halves have very different means: the merge of
     # the halves' (mean, M2) must carry the between-halves term
@@ -312,7 +322,7 @@ def test_convt3d_workload_sampled():
 
 # ------------------------------------------------- host-buffer pipeline
 @pytest.mark.parametrize("pinned,chunk,groups", [(True, 0, 8), (True, 200, 8), (False, 384, 8), (True, 200, 4),
-                                                 (True, 0, 16)])
+                                                 (True, 0, 16), (True, 200, 2)])
 def test_linear_gn_host_pipeline_matches_device_call(pinned, chunk, groups):
     # Rows are independent and each chunk runs the same kernels, so the
     # pipelined host-buffer call must reproduce the device call bit for bit.
