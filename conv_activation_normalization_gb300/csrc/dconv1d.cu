@@ -279,7 +279,7 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
 gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   if (B < 1 || C < 32 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
   // a k-block (BK channels of one tap) must not straddle two taps
-  if (C % (mode == GF_MODE_FP32_3XTF32 ? 32 : 64) || C > 256 || L % 4) return GF_ERR_SHAPE;
+  if (C % (mode == GF_MODE_FP32_3XTF32 ? 32 : 64) || C > 1024 || L % 4) return GF_ERR_SHAPE;
   if (B > 65535 || L > (int64_t(1) << 30)) return GF_ERR_SHAPE;
   return GF_OK;
 }

@@ -129,7 +129,7 @@ def test_dconv1d_validation(L):
     assert call(g=None) == GF_ERR_NULL
     assert call(p=3) == GF_ERR_SHAPE               # not length-preserving
     assert call(C=48) == GF_ERR_SHAPE              # C % 32
-    assert call(C=512) == GF_ERR_SHAPE
+    assert call(C=1056) == GF_ERR_SHAPE            # at most 1024 channels
     assert call(L=4094) == GF_ERR_SHAPE            # L % 4
     assert call(mode=5) == GF_ERR_MODE
     assert call(mode=0x200) == GF_ERR_MODE         # unknown flag bit

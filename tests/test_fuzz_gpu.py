@@ -88,7 +88,7 @@ def _dc_case(r):
     dil = int(r.integers(1, 6))
     if (ksize - 1) * dil % 2:
         dil += 1  # length-preserving padding needs an even span
-    return dict(B=int(r.integers(1, 4)), C=cq * int(r.integers(1, 256 // cq + 1)), L=4 * int(r.integers(1, 150)),
+    return dict(B=int(r.integers(1, 4)), C=cq * int(r.integers(1, 512 // cq + 1)), L=4 * int(r.integers(1, 150)),
                 ksize=ksize, dil=dil, mode=mode, gelu=str(r.choice(["erf", "tanh"])), seed=int(r.integers(1 << 30)))
 
 

@@ -233,6 +233,14 @@ def test_dconv1d_tanh_gelu(B, C, L, dil):
     assert np.abs(got - erf).max() > 1e-4  # the variant is really the other GELU
 
 
+@pytest.mark.parametrize("B,C,L,dil", [(2, 384, 260, 2), (1, 512, 200, 4), (1, 1024, 64, 1)])
+def test_dconv1d_wide(B, C, L, dil):
+    # more than 256 channels: the output channels span several 256-column tiles
+    s = synth.DConv1dShape(B=B, C=C, L=L, dilation=dil, padding=dil)
+    got, ref = _dc_run(s, synth.dconv1d_inputs(s, 950 + C, affine="perturbed"))
+    assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
+
+
 def test_dconv1d_kernel_size_5():
     s = synth.DConv1dShape(B=2, C=64, L=256, ksize=5, dilation=3, padding=6)
     got, ref = _dc_run(s, synth.dconv1d_inputs(s, 5, affine="perturbed"))
