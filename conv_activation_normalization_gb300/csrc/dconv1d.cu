@@ -141,17 +141,18 @@ __device__ __forceinline__ void store_planes4(void* planes, size_t plane_elems, 
   }
 }
 
-// grid (ceil(L/128), C/32, B), 256 threads: GELU(LayerNorm(x)) for a tile of
-// 32 channels x 128 positions, read as float4 along L (x, gamma, beta),
+// grid (ceil(L/128), Cp/32, B), 256 threads: GELU(LayerNorm(x)) for a tile
+// of 32 channels x 128 positions, read as float4 along L (x, gamma, beta),
 // transposed through shared memory and written 4 channels at a time to the
-// [B][L][C] operand planes.  L is a multiple of 4.  TANH: GELU's tanh
-// approximation instead of the erf form.
+// [B][L][Cp] operand planes; channels C .. Cp - 1 (the padding to a whole
+// number of k-blocks) are written as zeros.  L is a multiple of 4.  TANH:
+// GELU's tanh approximation instead of the erf form.
 template <int MODE, bool TANH>
 __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta,
                                                                   const float2* __restrict__ stats, void* planes,
-                                                                  int C, int L, int B) {
+                                                                  int C, int Cp, int L, int B) {
   __shared__ __align__(16) float tile[32][132];  // [channel][position]; 16-byte rows, 4-way reads
   const int l0 = blockIdx.x * 128, c0 = blockIdx.y * 32, b = blockIdx.z;
   const float2 st = stats[b];
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
     const int item = t + 256 * i, cc = item >> 5, q = item & 31;  // a warp: one channel, 128 positions
     const int l = l0 + 4 * q;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (l < L) {
+    if (l < L && c0 + cc < C) {
       const size_t cl = size_t(c0 + cc) * L + l;
       const float4 v = __ldcs(reinterpret_cast<const float4*>(xb + cl));
       const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + cl));
@@ -177,27 +178,29 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
     *reinterpret_cast<float4*>(&tile[cc][4 * q]) = a;
   }
   __syncthreads();
-  const size_t plane = size_t(B) * L * C;
+  const size_t plane = size_t(B) * L * Cp;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int item = t + 256 * i, pl = item >> 3, cq = item & 7;  // a warp: 4 positions x 32 channels
     const int l = l0 + pl;
     if (l < L)
-      store_planes4<MODE>(planes, plane, (size_t(b) * L + l) * C + c0 + 4 * cq,
+      store_planes4<MODE>(planes, plane, (size_t(b) * L + l) * Cp + c0 + 4 * cq,
                           make_float4(tile[4 * cq][pl], tile[4 * cq + 1][pl], tile[4 * cq + 2][pl],
                                       tile[4 * cq + 3][pl]));
   }
 }
 
-// W[co][ci][t] -> planes[Cout][ksize * C] with k = t * C + ci.
+// W[co][ci][t] -> planes[Cout][ksize * Cp] with k = t * Cp + ci, zeros for
+// the padding channels C .. Cp - 1.
 template <int MODE>
-__global__ void conv_weight_split_kernel(const float* __restrict__ w, void* planes, int Cout, int C, int ksize) {
-  const int64_t n = int64_t(Cout) * C * ksize;
+__global__ void conv_weight_split_kernel(const float* __restrict__ w, void* planes, int Cout, int C, int Cp,
+                                         int ksize) {
+  const int64_t n = int64_t(Cout) * ksize * Cp;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
-    const int t = int(i % ksize);
-    const int ci = int((i / ksize) % C);
-    const int64_t co = i / (int64_t(ksize) * C);
-    store_planes<MODE>(planes, size_t(n), size_t(co) * ksize * C + size_t(t) * C + ci, w[i]);
+    const int ci = int(i % Cp);
+    const int t = int((i / Cp) % ksize);
+    const int64_t co = i / (int64_t(ksize) * Cp);
+    store_planes<MODE>(planes, size_t(n), size_t(i), ci < C ? w[(co * C + ci) * ksize + t] : 0.f);
   }
 }
 
@@ -255,12 +258,20 @@ bool conv_mode_ok(int32_t mode) {
 // bytes per element of all operand planes together
 size_t plane_bytes(int32_t mode) { return mode == GF_MODE_FP32_3XTF32 ? 8 : (mode == GF_MODE_BF16 ? 2 : 4); }
 
+// Input channels padded to a whole number of k-blocks (32 fp32 or 64 bf16
+// channels), so that no k-block straddles two taps.
+int64_t padded_channels(int64_t C, int32_t mode) {
+  const int64_t q = mode == GF_MODE_FP32_3XTF32 ? 32 : 64;
+  return (C + q - 1) / q * q;
+}
+
 struct ConvWs {
   size_t part, stats, a_planes, w_planes, total;
   int chunks;
 };
 
 ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
+  const int64_t Cp = padded_channels(C, mode);
   ConvWs w{};
   w.chunks = int((C * L + kLnChunk - 1) / kLnChunk);
   size_t off = 0;
@@ -269,17 +280,17 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   w.stats = off;
   off += align_up(size_t(B) * sizeof(float2), 256);
   w.a_planes = off;
-  off += align_up(size_t(B) * L * C * plane_bytes(mode), 256);
+  off += align_up(size_t(B) * L * Cp * plane_bytes(mode), 256);
   w.w_planes = off;
-  off += align_up(size_t(C) * ksize * C * plane_bytes(mode), 256);
+  off += align_up(size_t(C) * ksize * Cp * plane_bytes(mode), 256);
   w.total = off;
   return w;
 }
 
 gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
-  if (B < 1 || C < 32 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
-  // a k-block (BK channels of one tap) must not straddle two taps
-  if (C % (mode == GF_MODE_FP32_3XTF32 ? 32 : 64) || C > 1024 || L % 4) return GF_ERR_SHAPE;
+  if (B < 1 || C < 1 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
+  (void)mode;  // any C: the operand planes pad the channels to whole k-blocks
+  if (C > 1024 || L % 4) return GF_ERR_SHAPE;
   if (B > 65535 || L > (int64_t(1) << 30)) return GF_ERR_SHAPE;
   return GF_OK;
 }
@@ -288,16 +299,17 @@ template <int MODE>
 void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
                          const float2* stats, void* a_planes, void* w_planes, int64_t B, int64_t C, int64_t L,
                          int32_t ksize, bool tanh_gelu, const DeviceInfo& dev, cudaStream_t s) {
-  const dim3 grid(unsigned((L + 127) / 128), unsigned(C / 32), unsigned(B));
+  const int64_t Cp = padded_channels(C, MODE);
+  const dim3 grid(unsigned((L + 127) / 128), unsigned(Cp / 32), unsigned(B));
   if (tanh_gelu)
-    ln_apply_gelu_split_kernel<MODE, true><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C), int(L),
-                                                                int(B));
+    ln_apply_gelu_split_kernel<MODE, true><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C),
+                                                                int(Cp), int(L), int(B));
   else
     ln_apply_gelu_split_kernel<MODE, false><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C),
-                                                                 int(L), int(B));
-  const int64_t n = C * C * ksize;
+                                                                 int(Cp), int(L), int(B));
+  const int64_t n = C * Cp * ksize;
   const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
-  conv_weight_split_kernel<MODE><<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), ksize);
+  conv_weight_split_kernel<MODE><<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), int(Cp), ksize);
 }
 
 template <class Op>
@@ -305,11 +317,12 @@ gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const vo
                            int64_t L, int32_t ksize, int32_t dilation, int32_t padding,
                            const EpiConvResidual::Params& ep, cudaStream_t s) {
   OperandMaps maps{};
-  const uint64_t da[3] = {uint64_t(C), uint64_t(L), uint64_t(B)};
+  const int64_t Cp = padded_channels(C, Op::kElem == 4 ? GF_MODE_FP32_3XTF32 : GF_MODE_BF16);
+  const uint64_t da[3] = {uint64_t(Cp), uint64_t(L), uint64_t(B)};
   const uint32_t ba[3] = {uint32_t(Op::kBK), uint32_t(kBM), 1};
-  const uint64_t db[2] = {uint64_t(ksize) * C, uint64_t(C)};
+  const uint64_t db[2] = {uint64_t(ksize) * Cp, uint64_t(C)};
   const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(kBNConv)};
-  const size_t a_plane = size_t(B) * L * C * Op::kElem, w_plane = size_t(C) * ksize * C * Op::kElem;
+  const size_t a_plane = size_t(B) * L * Cp * Op::kElem, w_plane = size_t(C) * ksize * Cp * Op::kElem;
   for (int p = 0; p < Op::kPlanes; ++p) {
     gf_status st = make_tmap(&maps.a[p], static_cast<const uint8_t*>(a_planes) + p * a_plane, Op::kElem, 3, da, ba);
     if (st != GF_OK) return st;
@@ -317,12 +330,12 @@ gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const vo
     if (st != GF_OK) return st;
   }
   ConvSrc src;
-  src.C = int(C);
+  src.C = int(Cp);  // channels per tap along K
   src.pad = padding;
   src.dil = dilation;
   src.num_jb = int((L + kBM - 1) / kBM);
   src.num_nb = int((C + kBNConv - 1) / kBNConv);
-  src.num_kb = int(ksize * C / Op::kBK);
+  src.num_kb = int(ksize * Cp / Op::kBK);
   src.bn = kBNConv;
   src.bk = Op::kBK;
   src.nsamples = int(B);

@@ -208,8 +208,9 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
  *
  *   x, out [B,C,L]; ln_gamma, ln_beta [C,L]; conv_w [C,C,ksize] (nn.Conv1d
  *   layout, cross-correlation); conv_b [C] (may be NULL).
- *   Supported: C % 32 == 0 (C % 64 == 0 in the BF16 modes), C <= 1024
- *   (output channels in tiles of 256),
+ *   Supported: 1 <= C <= 1024 (input channels padded to whole k-blocks of
+ *   32, or 64 in the BF16 modes, inside the workspace; output channels in
+ *   tiles of 256),
  *   L % 4 == 0, 1 <= ksize <= 16, dilation >= 1,
  *   2*padding == dilation*(ksize-1) (length-preserving, as the residual needs).
  * ---------------------------------------------------------------------- */

@@ -83,12 +83,11 @@ def test_fuzz_linear_lse(c):
 
 def _dc_case(r):
     mode = int(r.integers(0, 3))
-    cq = 32 if mode == 0 else 64
     ksize = int(r.choice([1, 2, 3, 4, 5, 7]))
     dil = int(r.integers(1, 6))
     if (ksize - 1) * dil % 2:
         dil += 1  # length-preserving padding needs an even span
-    return dict(B=int(r.integers(1, 4)), C=cq * int(r.integers(1, 512 // cq + 1)), L=4 * int(r.integers(1, 150)),
+    return dict(B=int(r.integers(1, 4)), C=int(r.integers(1, 513)), L=4 * int(r.integers(1, 150)),
                 ksize=ksize, dil=dil, mode=mode, gelu=str(r.choice(["erf", "tanh"])), seed=int(r.integers(1 << 30)))
 
 

@@ -120,7 +120,7 @@ def test_linear_lse_3xbf16_workload_sampled():
 
 
 @pytest.mark.parametrize("mode", [BF16, X3BF16])
-@pytest.mark.parametrize("B,C,L,dil", [(2, 64, 300, 4), (2, 256, 520, 2)])
+@pytest.mark.parametrize("B,C,L,dil", [(2, 64, 300, 4), (2, 256, 520, 2), (1, 96, 200, 2), (2, 40, 128, 1)])
 def test_dconv1d_modes(mode, B, C, L, dil):
     s = synth.DConv1dShape(B=B, C=C, L=L, dilation=dil, padding=dil)
     d = synth.dconv1d_inputs(s, 600 + L, affine="perturbed")

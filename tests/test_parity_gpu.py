@@ -241,6 +241,14 @@ def test_dconv1d_wide(B, C, L, dil):
     assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
 
 
+@pytest.mark.parametrize("B,C,L,dil", [(2, 48, 300, 4), (1, 100, 128, 2), (3, 1, 64, 1), (2, 33, 520, 3)])
+def test_dconv1d_unaligned_channels(B, C, L, dil):
+    # channel counts that are not whole k-blocks: zero-padded operand planes
+    s = synth.DConv1dShape(B=B, C=C, L=L, dilation=dil, padding=dil)
+    got, ref = _dc_run(s, synth.dconv1d_inputs(s, 970 + C, affine="perturbed"))
+    assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
+
+
 def test_dconv1d_kernel_size_5():
     s = synth.DConv1dShape(B=2, C=64, L=256, ksize=5, dilation=3, padding=6)
     got, ref = _dc_run(s, synth.dconv1d_inputs(s, 5, affine="perturbed"))
