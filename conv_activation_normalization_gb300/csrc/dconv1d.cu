@@ -37,7 +37,8 @@ __device__ __forceinline__ float sample_shift(const float* __restrict__ xs, int6
   return v / float(n_per_sample < 32 ? n_per_sample : 32);
 }
 
-// grid (chunks, B), 256 threads.  n_per_sample = C * L (a multiple of 4).
+// grid (chunks, B), 256 threads.  n_per_sample = C * L; float4 loads when it
+// is a multiple of 4 (every sample then starts 16-byte aligned), else scalar.
 // part[b][chunk] = (S1, S2) of the chunk's elements, in fp64.
 __global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict__ x, double2* __restrict__ part,
                                                          int64_t n_per_sample, int chunks) {
@@ -48,12 +49,20 @@ __global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict
   const int64_t end = begin + kLnChunk < n_per_sample ? begin + kLnChunk : n_per_sample;
   const float shift = sample_shift(xs, n_per_sample);
   float s1 = 0.f, s2 = 0.f;
+  if (n_per_sample % 4 == 0) {
 #pragma unroll 4
-  for (int64_t i = begin + 4 * threadIdx.x; i < end; i += 4 * blockDim.x) {
-    const float4 v = __ldcs(reinterpret_cast<const float4*>(xs + i));
-    const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
-    s1 += (d0 + d1) + (d2 + d3);
-    s2 += fmaf(d0, d0, d1 * d1) + fmaf(d2, d2, d3 * d3);
+    for (int64_t i = begin + 4 * threadIdx.x; i < end; i += 4 * blockDim.x) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(xs + i));
+      const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
+      s1 += (d0 + d1) + (d2 + d3);
+      s2 += fmaf(d0, d0, d1 * d1) + fmaf(d2, d2, d3 * d3);
+    }
+  } else {
+    for (int64_t i = begin + threadIdx.x; i < end; i += blockDim.x) {
+      const float d = __ldcs(xs + i) - shift;
+      s1 += d;
+      s2 = fmaf(d, d, s2);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -145,8 +154,9 @@ __device__ __forceinline__ void store_planes4(void* planes, size_t plane_elems, 
 // of 32 channels x 128 positions, read as float4 along L (x, gamma, beta),
 // transposed through shared memory and written 4 channels at a time to the
 // [B][L][Cp] operand planes; channels C .. Cp - 1 (the padding to a whole
-// number of k-blocks) are written as zeros.  L is a multiple of 4.  TANH:
-// GELU's tanh approximation instead of the erf form.
+// number of k-blocks) are written as zeros.  Loads are float4 when L is a
+// multiple of 4 (rows 16-byte aligned), else scalar.  TANH: GELU's tanh
+// approximation instead of the erf form.
 template <int MODE, bool TANH>
 __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ gamma,
@@ -165,9 +175,24 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (l < L && c0 + cc < C) {
       const size_t cl = size_t(c0 + cc) * L + l;
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(xb + cl));
-      const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + cl));
-      const float4 be = __ldg(reinterpret_cast<const float4*>(beta + cl));
+      float4 v, g, be;
+      if (L % 4 == 0) {
+        v = __ldcs(reinterpret_cast<const float4*>(xb + cl));
+        g = __ldg(reinterpret_cast<const float4*>(gamma + cl));
+        be = __ldg(reinterpret_cast<const float4*>(beta + cl));
+      } else {  // positions past L load as 0 and are not stored
+        float e[3][4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const bool in = l + k < L;
+          e[0][k] = in ? __ldcs(xb + cl + k) : 0.f;
+          e[1][k] = in ? __ldg(gamma + cl + k) : 0.f;
+          e[2][k] = in ? __ldg(beta + cl + k) : 0.f;
+        }
+        v = make_float4(e[0][0], e[0][1], e[0][2], e[0][3]);
+        g = make_float4(e[1][0], e[1][1], e[1][2], e[1][3]);
+        be = make_float4(e[2][0], e[2][1], e[2][2], e[2][3]);
+      }
       const float4 h = make_float4(fmaf((v.x - st.x) * st.y, g.x, be.x), fmaf((v.y - st.x) * st.y, g.y, be.y),
                                    fmaf((v.z - st.x) * st.y, g.z, be.z), fmaf((v.w - st.x) * st.y, g.w, be.w));
       if constexpr (TANH)
@@ -290,7 +315,7 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
 gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   if (B < 1 || C < 1 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
   (void)mode;  // any C: the operand planes pad the channels to whole k-blocks
-  if (C > 1024 || L % 4) return GF_ERR_SHAPE;
+  if (C > 1024) return GF_ERR_SHAPE;
   if (B > 65535 || L > (int64_t(1) << 30)) return GF_ERR_SHAPE;
   return GF_OK;
 }

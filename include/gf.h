@@ -211,7 +211,7 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
  *   Supported: 1 <= C <= 1024 (input channels padded to whole k-blocks of
  *   32, or 64 in the BF16 modes, inside the workspace; output channels in
  *   tiles of 256),
- *   L % 4 == 0, 1 <= ksize <= 16, dilation >= 1,
+ *   L >= 1, 1 <= ksize <= 16, dilation >= 1,
  *   2*padding == dilation*(ksize-1) (length-preserving, as the residual needs).
  * ---------------------------------------------------------------------- */
 size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize,

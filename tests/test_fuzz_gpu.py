@@ -87,7 +87,7 @@ def _dc_case(r):
     dil = int(r.integers(1, 6))
     if (ksize - 1) * dil % 2:
         dil += 1  # length-preserving padding needs an even span
-    return dict(B=int(r.integers(1, 4)), C=int(r.integers(1, 513)), L=4 * int(r.integers(1, 150)),
+    return dict(B=int(r.integers(1, 4)), C=int(r.integers(1, 513)), L=int(r.integers(1, 600)),
                 ksize=ksize, dil=dil, mode=mode, gelu=str(r.choice(["erf", "tanh"])), seed=int(r.integers(1 << 30)))
 
 

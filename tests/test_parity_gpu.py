@@ -249,6 +249,14 @@ def test_dconv1d_unaligned_channels(B, C, L, dil):
     assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
 
 
+@pytest.mark.parametrize("B,C,L,dil", [(2, 64, 301, 4), (1, 40, 7, 1), (3, 32, 1, 2), (1, 256, 4093, 4)])
+def test_dconv1d_any_length(B, C, L, dil):
+    # lengths that are not multiples of 4: scalar loads in the LayerNorm passes
+    s = synth.DConv1dShape(B=B, C=C, L=L, dilation=dil, padding=dil)
+    got, ref = _dc_run(s, synth.dconv1d_inputs(s, 990 + L, affine="perturbed"))
+    assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
+
+
 def test_dconv1d_kernel_size_5():
     s = synth.DConv1dShape(B=2, C=64, L=256, ksize=5, dilation=3, padding=6)
     got, ref = _dc_run(s, synth.dconv1d_inputs(s, 5, affine="perturbed"))
