@@ -157,47 +157,47 @@ struct EpiSwishBiasGNT {
       tmem_wait_st();
       tmem_load64(taddr, v);
       normalize_store(p, n0, 4, v, mu, rs, orow + n0, valid);
-      return;
-    }
+    } else {
 #pragma unroll 1
-    for (int g = 0; g < BN / 64; ++g) {
-      const int n0 = t.n0 + g * 64;
-      if (n0 >= p.N) break;  // uniform across the warp
-      // quarters inside the row (all four unless GW < 64 and N % 64 != 0)
-      const int nq = GW >= 64 ? 4 : min(4, (p.N - n0) / 16);
-      float v[64], q[4], mu[4], m2[4], rs[4];
-      tmem_load64(taddr + uint32_t(g * 64), v);
-      swish_bias(p, n0, nq, v, q);
-      if constexpr (GW == 64) {  // one group: one mean, one M2
-        float2 sum = make_float2(0.f, 0.f);
+      for (int g = 0; g < BN / 64; ++g) {
+        const int n0 = t.n0 + g * 64;
+        if (n0 >= p.N) break;  // uniform across the warp
+        // quarters inside the row (all four unless GW < 64 and N % 64 != 0)
+        const int nq = GW >= 64 ? 4 : min(4, (p.N - n0) / 16);
+        float v[64], q[4], mu[4], m2[4], rs[4];
+        tmem_load64(taddr + uint32_t(g * 64), v);
+        swish_bias(p, n0, nq, v, q);
+        if constexpr (GW == 64) {  // one group: one mean, one M2
+          float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sum.x += q[i];
-        const float mean = sum.x * (1.f / 64.f);
-        const float2 nmean = make_float2(-mean, -mean);
-        float2 acc = make_float2(0.f, 0.f);
+          for (int i = 0; i < 4; ++i) sum.x += q[i];
+          const float mean = sum.x * (1.f / 64.f);
+          const float2 nmean = make_float2(-mean, -mean);
+          float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          const float2 d = add2(make_float2(v[j], v[j + 1]), nmean);
-          acc = fma2(d, d, acc);
+          for (int j = 0; j < 64; j += 2) {
+            const float2 d = add2(make_float2(v[j], v[j + 1]), nmean);
+            acc = fma2(d, d, acc);
+          }
+          const float rstd = rsqrtf((acc.x + acc.y) * (1.f / 64.f) + p.eps);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            mu[i] = mean;
+            rs[i] = rstd;
+          }
+          normalize_store(p, n0, nq, v, mu, rs, orow + n0, valid);
+        } else {
+          constexpr float inv = 1.f / float(GW);  // a power of two: exact
+          float gs[4], gm2[4];
+          group_sums(q, gs);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mu[i] = gs[i] * inv;
+          quarter_m2(v, mu, m2);
+          group_sums(m2, gm2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rs[i] = rsqrtf(gm2[i] * inv + p.eps);
+          normalize_store(p, n0, nq, v, mu, rs, orow + n0, valid);
         }
-        const float rstd = rsqrtf((acc.x + acc.y) * (1.f / 64.f) + p.eps);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          mu[i] = mean;
-          rs[i] = rstd;
-        }
-        normalize_store(p, n0, nq, v, mu, rs, orow + n0, valid);
-      } else {
-        constexpr float inv = 1.f / float(GW);  // a power of two: exact
-        float gs[4], gm2[4];
-        group_sums(q, gs);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mu[i] = gs[i] * inv;
-        quarter_m2(v, mu, m2);
-        group_sums(m2, gm2);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rs[i] = rsqrtf(gm2[i] * inv + p.eps);
-        normalize_store(p, n0, nq, v, mu, rs, orow + n0, valid);
       }
     }
   }
@@ -432,7 +432,20 @@ bool mode_ok(int32_t mode) {
 
 // Bytes of one operand's pre-pass planes in the workspace: the lo plane
 // (3xTF32: hi is the raw tensor), bf16 hi (BF16) or bf16 hi + lo (3xBF16).
+// K padded to a whole number of 16-byte rows (4 fp32, 8 bf16 elements) for
+// the TMA: the pre-pass then writes every plane of the operand, zeros in
+// the padding columns.
+int64_t kpad(int64_t K, int32_t mode) {
+  const int64_t q = mode == GF_MODE_FP32_3XTF32 ? 4 : 8;
+  return (K + q - 1) / q * q;
+}
+
 size_t operand_ws_bytes(int64_t rows, int64_t K, int32_t mode) {
+  const int64_t Kp = kpad(K, mode);
+  if (Kp != K) {  // padded planes: fp32 hi + lo, bf16 hi, or bf16 hi + lo
+    const size_t n = size_t(rows) * size_t(Kp);
+    return align_up(n * (mode == GF_MODE_FP32_3XTF32 ? 8 : mode == GF_MODE_BF16 ? 2 : 4), 256);
+  }
   const size_t n = size_t(rows) * size_t(K);
   switch (mode) {
     case GF_MODE_FP32_3XTF32: return align_up(n * 4, 256);
@@ -442,10 +455,10 @@ size_t operand_ws_bytes(int64_t rows, int64_t K, int32_t mode) {
 }
 
 gf_status check_linear_shape(int64_t M, int64_t K, int64_t N, int32_t mode) {
-  if (M < 1 || K < 4 || N < 1) return GF_ERR_SHAPE;
-  // TMA row strides must be multiples of 16 bytes: K % 4 for fp32 rows,
-  // K % 8 for the bf16 planes.
-  if (K % (mode == GF_MODE_FP32_3XTF32 ? 4 : 8)) return GF_ERR_SHAPE;
+  if (M < 1 || K < 1 || N < 1) return GF_ERR_SHAPE;
+  // (a K that is not a whole number of 16-byte rows is padded by the
+  // pre-pass: kpad)
+  (void)mode;
   if (M > (int64_t(1) << 31) - 256 || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - 64)
     return GF_ERR_SHAPE;  // TMA coordinates are int32
   return GF_OK;
@@ -461,9 +474,52 @@ struct Planes {
   const void* p[2];
 };
 
-// Run the split pre-pass of one operand into `ws` and return its planes.
+// Every plane of an operand whose rows are K wide, written with rows Kp
+// wide (zeros in columns K .. Kp - 1): fp32 hi (the raw value) and lo in the
+// 3xTF32 mode, bf16 hi (and lo) in the BF16 modes.
+template <int MODE>
+__global__ void split_padded_kernel(const float* __restrict__ src, int64_t rows, int K, int Kp, void* planes) {
+  const size_t n = size_t(rows) * size_t(Kp);
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x) {
+    const size_t r = i / size_t(Kp);
+    const int k = int(i - r * size_t(Kp));
+    const float v = k < K ? __ldg(src + r * size_t(K) + size_t(k)) : 0.f;
+    if constexpr (MODE == GF_MODE_FP32_3XTF32) {
+      float* p = static_cast<float*>(planes);
+      p[i] = v;
+      p[n + i] = v - tf32_hi(v);
+    } else {
+      __nv_bfloat16* p = static_cast<__nv_bfloat16*>(planes);
+      const __nv_bfloat16 h = __float2bfloat16_rn(v);
+      p[i] = h;
+      if constexpr (MODE == GF_MODE_FP32_3XBF16) p[n + i] = __float2bfloat16_rn(v - __bfloat162float(h));
+    }
+  }
+}
+
+// Run the split pre-pass of one operand into `ws` and return its planes
+// (rows kpad(K, mode) wide).
 gf_status prepare_operand(const float* src, int64_t rows, int64_t K, int32_t mode, void* ws, const DeviceInfo& dev,
                           cudaStream_t s, Planes* out) {
+  const int64_t Kp = kpad(K, mode);
+  if (Kp != K) {
+    const size_t n = size_t(rows) * size_t(Kp);
+    const size_t esz = mode == GF_MODE_FP32_3XTF32 ? 4 : 2;
+    out->p[0] = ws;
+    out->p[1] = mode == GF_MODE_BF16 ? nullptr : static_cast<uint8_t*>(ws) + n * esz;
+    const int blocks = split_blocks((n + 3) / 4, dev.sm_count);
+    switch (mode) {
+      case GF_MODE_FP32_3XTF32:
+        split_padded_kernel<GF_MODE_FP32_3XTF32><<<blocks, 256, 0, s>>>(src, rows, int(K), int(Kp), ws);
+        break;
+      case GF_MODE_BF16:
+        split_padded_kernel<GF_MODE_BF16><<<blocks, 256, 0, s>>>(src, rows, int(K), int(Kp), ws);
+        break;
+      default:
+        split_padded_kernel<GF_MODE_FP32_3XBF16><<<blocks, 256, 0, s>>>(src, rows, int(K), int(Kp), ws);
+    }
+    return cuda_status(cudaGetLastError());
+  }
   const size_t n = size_t(rows) * size_t(K);
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
@@ -559,7 +615,7 @@ gf_status split_and_run(int32_t mode, const float* x, const float* W, int64_t M,
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   if ((st = prepare_operand(x, M, K, mode, w8, dev, s, &a)) != GF_OK) return st;
   if ((st = prepare_operand(W, N, K, mode, w8 + operand_ws_bytes(M, K, mode), dev, s, &b)) != GF_OK) return st;
-  return run_linear<Epi>(mode, dev, a, b, M, K, N, m_fastest, ep, s);
+  return run_linear<Epi>(mode, dev, a, b, M, kpad(K, mode), N, m_fastest, ep, s);
 }
 
 }  // namespace
@@ -595,6 +651,7 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
   if (!x_planes || !W_planes || !bias || !gamma || !beta || !out) return GF_ERR_NULL;
   gf_status st = check_linear_shape(M, K, N, GF_MODE_FP32_3XTF32);
   if (st != GF_OK) return st;
+  if (K % 4) return GF_ERR_SHAPE;  // the caller's planes are read with K-wide rows
   if (!gn_groups_ok(N, groups)) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
   if (!aligned16(x_planes) || !aligned16(W_planes) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
@@ -781,7 +838,7 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
       const GNParams ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps, int(N / groups)};
       ok = prepare_operand(xd, rows, K, mode, ws + wl.xp[bi], dev, s, &xp) == GF_OK &&
            with_gn_epilogue(ep, s, [&](auto tag) {
-             return run_linear<typename decltype(tag)::type>(mode, dev, xp, wp, rows, K, N, 0, ep, s);
+             return run_linear<typename decltype(tag)::type>(mode, dev, xp, wp, rows, kpad(K, mode), N, 0, ep, s);
            }) == GF_OK &&
            cudaEventRecord(ev_comp[bi], s) == cudaSuccess;
     }

@@ -107,7 +107,8 @@ gf_status gf_profile_end(int32_t* calls, float* total_ms);
  * The contraction step shared by the two Linear chains (nn.Linear / addmm,
  * page Kimi-K2.6__l2_p37 turn 1 and page Kimi-K2.6__l2_p64 turn 1), exposed
  * so that it can be checked on its own.  x [M,K], W [N,K], b [N] (may be
- * NULL), out [M,N].  Supported: M >= 1, K >= 4 with K % 4 == 0, N >= 1.
+ * NULL), out [M,N].  Supported: M, K, N >= 1 (a K that is not a multiple of
+ * 4 fp32 / 8 bf16 elements is zero-padded in the workspace's operand planes).
  * With integer-valued x and W (|v| <= 2^11) and |out| < 2^24 the result is
  * exact.
  * ---------------------------------------------------------------------- */
@@ -126,7 +127,7 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
  *
  *   x [M,K], W [N,K] (nn.Linear layout), b_lin/bias/gamma/beta [N], out [M,N].
  *   b_lin may be NULL (no linear bias).
- *   Supported: M >= 1, K >= 4 with K % 4 == 0 (K % 8 == 0 in the BF16 modes),
+ *   Supported: M, K >= 1 (K padded as for gf_linear),
  *   groups >= 1 with N % groups == 0.  Group widths N/groups of 16, 32, 64
  *   and 128 run inside the GEMM epilogue (groups of 128 on 256-column
  *   tiles); any other width stores t and normalises the rows in a second
@@ -143,7 +144,8 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
 /* The same operator on operands already split for the tensor cores (see
  * gf_tf32_split): x_planes [2][M][K], W_planes [2][N][K].  It launches the
  * fused GEMM kernel alone, so a caller can split a weight once and reuse it.
- * Same shapes, checks and result as gf_linear_swish_bias_groupnorm. */
+ * Same checks and result as gf_linear_swish_bias_groupnorm; K must be a
+ * multiple of 4 (the planes' rows are read as they are). */
 gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const float* W_planes,
                                                 const float* b_lin, const float* bias,
                                                 const float* gamma, const float* beta, float* out,
@@ -187,7 +189,7 @@ gf_status gf_tf32_split(const float* src, float* planes, int64_t n, void* stream
  *   out[m]  = gelu(gelu(a)),    gelu(v) = v * Phi(v)   (exact, erf form)
  *
  *   x [M,K], W [N,K], b [N] (may be NULL), out [M,1].
- *   Supported: M >= 1, K >= 4 with K % 4 == 0, N >= 1.
+ *   Supported: M, K, N >= 1 (K padded as for gf_linear).
  * ---------------------------------------------------------------------- */
 size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode);
 gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, float* out,

@@ -49,8 +49,7 @@ def _cases(seed, n, draw):
 def _lgn_case(r):
     mode = int(r.integers(0, 3))
     gw = int(r.choice([16, 32, 64, 128, 8, 48, 256, 320]))
-    kq = 4 if mode == 0 else 8
-    return dict(M=int(r.integers(1, 400)), K=kq * int(r.integers(1, 64)), gw=gw, groups=int(r.integers(1, 12)),
+    return dict(M=int(r.integers(1, 400)), K=int(r.integers(1, 512)), gw=gw, groups=int(r.integers(1, 12)),
                 mode=mode, seed=int(r.integers(1 << 30)))
 
 
@@ -67,8 +66,7 @@ def test_fuzz_linear_gn(c):
 
 def _lse_case(r):
     mode = int(r.integers(0, 3))
-    kq = 4 if mode == 0 else 8
-    return dict(M=int(r.integers(1, 300)), K=kq * int(r.integers(1, 64)), N=int(r.integers(1, 1500)), mode=mode,
+    return dict(M=int(r.integers(1, 300)), K=int(r.integers(1, 512)), N=int(r.integers(1, 1500)), mode=mode,
                 seed=int(r.integers(1 << 30)))
 
 

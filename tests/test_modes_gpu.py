@@ -42,7 +42,7 @@ def assert_close(got, ref, tol, what=""):
 
 
 @pytest.mark.parametrize("mode", [BF16, X3BF16])
-@pytest.mark.parametrize("M,K,N", [(128, 64, 256), (300, 104, 520), (257, 1024, 4096)])
+@pytest.mark.parametrize("M,K,N", [(128, 64, 256), (300, 104, 520), (257, 1024, 4096), (70, 37, 130), (9, 5, 3)])
 def test_linear_integer_exact(mode, M, K, N):
     r = np.random.default_rng(M + K + mode)
     x = r.integers(-15, 16, size=(M, K)).astype(np.float32)

@@ -47,7 +47,8 @@ def assert_close(got, ref, what=""):
 
 
 # ------------------------------------------------------------ contraction
-@pytest.mark.parametrize("M,K,N", [(128, 32, 256), (300, 100, 520), (1, 4, 1), (257, 1024, 4096)])
+@pytest.mark.parametrize("M,K,N", [(128, 32, 256), (300, 100, 520), (1, 4, 1), (257, 1024, 4096), (70, 37, 130),
+                                   (5, 1, 7)])
 def test_linear_integer_exact(M, K, N):
     r = np.random.default_rng(M * 7 + K)
     x = r.integers(-15, 16, size=(M, K)).astype(np.float32)
@@ -140,6 +141,14 @@ def test_linear_gn_group_width_128_halves_differ():
     assert_close(got, ref, "linear_gn groups of 128, shifted halves")
 
 
+@pytest.mark.parametrize("M,K,N", [(130, 37, 256), (64, 1, 128), (200, 1023, 512)])
+def test_linear_gn_unaligned_k(M, K, N):
+    # K not a whole number of 16-byte rows: the pre-pass pads every plane
+    s, d = _lgn_case(M, K, N, N // 64, 850 + K)
+    got, ref = _lgn_run(s, d)
+    assert_close(got, ref, f"linear_gn {M}x{K}x{N}")
+
+
 def test_linear_gn_no_linear_bias_and_constant_group():
     s, d = _lgn_case(64, 64, 256, 4, 7)
     d["W"][:64] = 0.0      # group 0: t = swish(0) + bias = bias, varies per channel
@@ -182,6 +191,13 @@ def _lse_run(s, d, rows=None):
 def test_linear_lse_small(M, K, N):
     s = synth.LinearLSEShape(M=M, K=K, N=N)
     got, ref = _lse_run(s, synth.linear_lse_inputs(s, 200 + M))
+    assert_close(got, ref, f"lse {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("M,K,N", [(100, 3, 300), (129, 1001, 2048)])
+def test_linear_lse_unaligned_k(M, K, N):
+    s = synth.LinearLSEShape(M=M, K=K, N=N)
+    got, ref = _lse_run(s, synth.linear_lse_inputs(s, 860 + K))
     assert_close(got, ref, f"lse {M}x{K}x{N}")
 
 
