@@ -37,9 +37,10 @@ __device__ __forceinline__ float sample_shift(const float* __restrict__ xs, int6
   return v / float(n_per_sample < 32 ? n_per_sample : 32);
 }
 
-// grid (chunks, B), 256 threads.  n_per_sample = C * L; float4 loads when it
-// is a multiple of 4 (every sample then starts 16-byte aligned), else scalar.
-// part[b][chunk] = (S1, S2) of the chunk's elements, in fp64.
+// grid (chunks, B), 256 threads.  n_per_sample = C * L; VEC: float4 loads
+// (n_per_sample a multiple of 4, so every sample starts 16-byte aligned),
+// else scalar.  part[b][chunk] = (S1, S2) of the chunk's elements, in fp64.
+template <bool VEC>
 __global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict__ x, double2* __restrict__ part,
                                                          int64_t n_per_sample, int chunks) {
   __shared__ double2 red[8];
@@ -49,7 +50,7 @@ __global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict
   const int64_t end = begin + kLnChunk < n_per_sample ? begin + kLnChunk : n_per_sample;
   const float shift = sample_shift(xs, n_per_sample);
   float s1 = 0.f, s2 = 0.f;
-  if (n_per_sample % 4 == 0) {
+  if constexpr (VEC) {
 #pragma unroll 4
     for (int64_t i = begin + 4 * threadIdx.x; i < end; i += 4 * blockDim.x) {
       const float4 v = __ldcs(reinterpret_cast<const float4*>(xs + i));
@@ -154,10 +155,10 @@ __device__ __forceinline__ void store_planes4(void* planes, size_t plane_elems, 
 // of 32 channels x 128 positions, read as float4 along L (x, gamma, beta),
 // transposed through shared memory and written 4 channels at a time to the
 // [B][L][Cp] operand planes; channels C .. Cp - 1 (the padding to a whole
-// number of k-blocks) are written as zeros.  Loads are float4 when L is a
-// multiple of 4 (rows 16-byte aligned), else scalar.  TANH: GELU's tanh
-// approximation instead of the erf form.
-template <int MODE, bool TANH>
+// number of k-blocks) are written as zeros.  VEC: float4 loads (L a multiple
+// of 4, rows 16-byte aligned), else scalar.  TANH: GELU's tanh approximation
+// instead of the erf form.
+template <int MODE, bool TANH, bool VEC>
 __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* __restrict__ x,
                                                                   const float* __restrict__ gamma,
                                                                   const float* __restrict__ beta,
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
     if (l < L && c0 + cc < C) {
       const size_t cl = size_t(c0 + cc) * L + l;
       float4 v, g, be;
-      if (L % 4 == 0) {
+      if constexpr (VEC) {
         v = __ldcs(reinterpret_cast<const float4*>(xb + cl));
         g = __ldg(reinterpret_cast<const float4*>(gamma + cl));
         be = __ldg(reinterpret_cast<const float4*>(beta + cl));
@@ -326,12 +327,19 @@ void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_
                          int32_t ksize, bool tanh_gelu, const DeviceInfo& dev, cudaStream_t s) {
   const int64_t Cp = padded_channels(C, MODE);
   const dim3 grid(unsigned((L + 127) / 128), unsigned(Cp / 32), unsigned(B));
-  if (tanh_gelu)
-    ln_apply_gelu_split_kernel<MODE, true><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C),
-                                                                int(Cp), int(L), int(B));
+  const int c = int(C), cp = int(Cp), l = int(L), b = int(B);
+  const bool vec = L % 4 == 0;
+  if (tanh_gelu && vec)
+    ln_apply_gelu_split_kernel<MODE, true, true><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, c, cp, l, b);
+  else if (tanh_gelu)
+    ln_apply_gelu_split_kernel<MODE, true, false><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, c, cp, l,
+                                                                       b);
+  else if (vec)
+    ln_apply_gelu_split_kernel<MODE, false, true><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, c, cp, l,
+                                                                       b);
   else
-    ln_apply_gelu_split_kernel<MODE, false><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, int(C),
-                                                                 int(Cp), int(L), int(B));
+    ln_apply_gelu_split_kernel<MODE, false, false><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, c, cp,
+                                                                        l, b);
   const int64_t n = C * Cp * ksize;
   const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
   conv_weight_split_kernel<MODE><<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), int(Cp), ksize);
@@ -421,7 +429,10 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   void* a_planes = ws + wl.a_planes;
   void* w_planes = ws + wl.w_planes;
 
-  ln_partial_kernel<<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
+  if ((C * L) % 4 == 0)
+    ln_partial_kernel<true><<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
+  else
+    ln_partial_kernel<false><<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
   ln_finalize_kernel<<<unsigned(B), 256, 0, s>>>(x, part, stats, C * L, wl.chunks, eps);
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
