@@ -627,8 +627,7 @@ extern "C" {
 
 size_t gf_linear_swish_bias_groupnorm_workspace_size(int64_t M, int64_t K, int64_t N, int32_t groups,
                                                      int32_t mode) {
-  (void)groups;
-  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || !gn_groups_ok(N, groups)) return 0;
   return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode);
 }
 
@@ -750,8 +749,8 @@ HostWs host_ws(int64_t chunk, int64_t K, int64_t N, int32_t mode) {
 
 size_t gf_linear_swish_bias_groupnorm_host_workspace_size(int64_t M, int64_t K, int64_t N, int32_t groups,
                                                           int32_t mode, int64_t chunk_rows) {
-  (void)groups;
-  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || chunk_rows < 0) return 0;
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || !gn_groups_ok(N, groups) || chunk_rows < 0)
+    return 0;
   if (chunk_rows == 0) {
     DeviceInfo dev;
     if (current_device(&dev) != GF_OK) return 0;
