@@ -383,6 +383,24 @@ def test_linear_gn_host_pipeline_matches_device_call(pinned, chunk, groups):
     assert_close(oh.numpy(), ref64, "host pipeline")
 
 
+def test_linear_gn_host_pipeline_unaligned_k_and_row_kernel():
+    # a K that is not a whole number of 16-byte rows (padded planes per
+    # chunk) and a group width that takes the second row kernel
+    s, d = _lgn_case(700, 37, 768, 3, 4343)
+    dev = {k: T(d[k]) for k in ("W", "b_lin", "bias", "gamma", "beta")}
+    ref = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), dev["W"], dev["b_lin"], dev["bias"], dev["gamma"],
+                                            dev["beta"], s.groups, s.eps).cpu()
+    xh = torch.from_numpy(d["x"]).pin_memory()
+    oh = torch.full((s.M, s.N), float("nan"), dtype=torch.float32, pin_memory=True)
+    gf.gf_linear_swish_bias_groupnorm_host(xh, dev["W"], dev["b_lin"], dev["bias"], dev["gamma"], dev["beta"],
+                                           s.groups, s.eps, out_host=oh, chunk_rows=256)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(oh, ref)
+    ref64 = oracle.linear_swish_bias_groupnorm(d["x"], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"],
+                                               s.groups, s.eps)
+    assert_close(oh.numpy(), ref64, "host pipeline, K = 37, groups of 256")
+
+
 @pytest.mark.gpu
 def test_dconv1d_offset_input_statistics():
     # mean 100, std 0.01: the LayerNorm statistics must not lose the variance
