@@ -1,6 +1,12 @@
 // ConvTranspose3d(k 3, stride 2, pad 1) -> Swish -> GroupNorm -> HardSwish
 //                                               (page Kimi-K2.6__l2_p60)
 //
+// This file holds the entry points (which send every other kernel size,
+// stride, padding, channel count or group count to convt3d_general.cu) and
+// the CUDA-core kernels of the pages' configuration for 4 < Cin <= 8 and the
+// no-workspace entry point; Cin <= 4 runs on the tensor cores
+// (convt3d_tc.cuh, convt3d_fused.cuh).
+//
 // Sub-pixel (phase) form of the transposed convolution.  Output index o
 // along one dimension is o = 2 i - 1 + k; splitting o into a cell q and a
 // phase p (o = 2q + p):

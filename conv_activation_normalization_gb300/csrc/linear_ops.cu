@@ -2,8 +2,10 @@
 //   gf_linear_swish_bias_groupnorm   (page Kimi-K2.6__l2_p37)
 //   gf_linear_lse_act                (page Kimi-K2.6__l2_p64)
 // Both run a hi/lo split pre-pass on x and W, then one persistent tcgen05
-// 3xTF32 GEMM whose epilogue does the rest of the chain on the accumulator
-// tile in registers; the logsumexp chain adds a tiny per-row merge kernel.
+// GEMM (3xTF32, BF16 or 3xBF16) whose epilogue does the rest of the chain
+// on the accumulator tile in registers; the logsumexp chain adds a tiny
+// per-row merge kernel, and GroupNorm groups other than 16-128 columns wide
+// a per-row normalisation kernel.
 #include <cmath>
 
 #include "gemm_tc.cuh"
