@@ -180,6 +180,20 @@ def _check(*ts):
     return dev
 
 
+def _shape(t, shape, name):
+    """Raise unless t (if given) has exactly this shape: the sizes passed to
+    the library come from the leading operands, so every other tensor must
+    agree with them or the kernels would read or write past its end."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _numel(t, n, name):
+    """Raise unless t (if given) holds exactly n elements (any shape)."""
+    if t is not None and t.numel() != n:
+        raise ValueError(f"{name} holds {t.numel()} elements, expected {n}")
+
+
 def _ptr(t):
     return None if t is None else t.data_ptr()
 
@@ -195,6 +209,11 @@ def _call(name, *args):
         raise GFError(st, name)
 
 
+def _gn_vectors(N, b_lin, bias, gamma, beta):
+    for t, name in ((b_lin, "b_lin"), (bias, "bias"), (gamma, "gamma"), (beta, "beta")):
+        _numel(t, N, name)
+
+
 def _ws_args(device, nbytes, workspace, stream=None):
     if workspace is None:
         workspace = _workspace(device, nbytes, stream)
@@ -206,9 +225,12 @@ def _ws_args(device, nbytes, workspace, stream=None):
 # -------------------------------------------------------------- the ABI
 def gf_linear(x, W, b=None, mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None):
     """out[M, N] = x @ W.T + b (the contraction step alone)."""
-    dev = _check(x, W, b, out)
     M, K = x.shape
     N = W.shape[0]
+    _shape(W, (N, K), "W")
+    _numel(b, N, "b")
+    _shape(out, (M, N), "out")
+    dev = _check(x, W, b, out)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -221,9 +243,12 @@ def gf_linear(x, W, b=None, mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, 
 def gf_linear_swish_bias_groupnorm(x, W, b_lin, bias, gamma, beta, groups, eps=1e-5,
                                    mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None):
     """out[M, N] = GroupNorm(groups)(swish(x @ W.T + b_lin) + bias) * gamma + beta."""
-    dev = _check(x, W, b_lin, bias, gamma, beta, out)
     M, K = x.shape
     N = W.shape[0]
+    _shape(W, (N, K), "W")
+    _gn_vectors(N, b_lin, bias, gamma, beta)
+    _shape(out, (M, N), "out")
+    dev = _check(x, W, b_lin, bias, gamma, beta, out)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -236,6 +261,7 @@ def gf_linear_swish_bias_groupnorm(x, W, b_lin, bias, gamma, beta, groups, eps=1
 
 def gf_tf32_split(src, planes=None, stream=None):
     """planes[0] = src with the 13 low mantissa bits cleared, planes[1] = src - planes[0]."""
+    _shape(planes, (2,) + tuple(src.shape), "planes")
     dev = _check(src, planes)
     if planes is None:
         planes = torch.empty((2,) + tuple(src.shape), dtype=torch.float32, device=dev)
@@ -247,9 +273,13 @@ def gf_tf32_split(src, planes=None, stream=None):
 def gf_linear_swish_bias_groupnorm_planes(x_planes, W_planes, b_lin, bias, gamma, beta, groups, eps=1e-5, out=None,
                                           stream=None):
     """gf_linear_swish_bias_groupnorm on pre-split operands (x_planes [2,M,K], W_planes [2,N,K])."""
-    dev = _check(x_planes, W_planes, b_lin, bias, gamma, beta, out)
     _, M, K = x_planes.shape
     N = W_planes.shape[1]
+    _shape(x_planes, (2, M, K), "x_planes")
+    _shape(W_planes, (2, N, K), "W_planes")
+    _gn_vectors(N, b_lin, bias, gamma, beta)
+    _shape(out, (M, N), "out")
+    dev = _check(x_planes, W_planes, b_lin, bias, gamma, beta, out)
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -266,12 +296,15 @@ def gf_linear_swish_bias_groupnorm_host(x_host, W, b_lin, bias, gamma, beta, gro
     Chunks of rows are copied in, computed and copied out in an overlapped
     pipeline.  Enqueues and returns; synchronise the stream before reading
     out_host."""
+    M, K = x_host.shape
+    N = W.shape[0]
+    _shape(W, (N, K), "W")
+    _gn_vectors(N, b_lin, bias, gamma, beta)
+    _shape(out_host, (M, N), "out_host")
     dev = _check(W, b_lin, bias, gamma, beta)
     for t in (x_host, out_host):
         if t is not None and (t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
             raise ValueError("host tensors must be contiguous float32 CPU tensors")
-    M, K = x_host.shape
-    N = W.shape[0]
     if out_host is None:
         out_host = torch.empty((M, N), dtype=torch.float32, pin_memory=x_host.is_pinned())
     with torch.cuda.device(dev):
@@ -286,9 +319,12 @@ def gf_linear_swish_bias_groupnorm_host(x_host, W, b_lin, bias, gamma, beta, gro
 def gf_linear_lse_act(x, W, b, negative_slope=0.01, mode=GF_MODE_FP32_3XTF32, out=None, workspace=None,
                       stream=None):
     """out[M, 1] = gelu(gelu(lrelu(lrelu(logsumexp(x @ W.T + b, dim=1)))))."""
-    dev = _check(x, W, b, out)
     M, K = x.shape
     N = W.shape[0]
+    _shape(W, (N, K), "W")
+    _numel(b, N, "b")
+    _numel(out, M, "out")
+    dev = _check(x, W, b, out)
     if out is None:
         out = torch.empty((M, 1), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -307,9 +343,14 @@ def gf_ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, paddi
         raise ValueError("gelu must be 'erf' or 'tanh'")
     if gelu == "tanh":
         mode |= GF_FLAG_GELU_TANH
-    dev = _check(x, ln_gamma, ln_beta, conv_w, conv_b, out)
     B, C, L = x.shape
     ksize = conv_w.shape[2]
+    _shape(conv_w, (C, C, ksize), "conv_w")
+    _numel(ln_gamma, C * L, "ln_gamma")
+    _numel(ln_beta, C * L, "ln_beta")
+    _numel(conv_b, C, "conv_b")
+    _shape(out, (B, C, L), "out")
+    dev = _check(x, ln_gamma, ln_beta, conv_w, conv_b, out)
     if out is None:
         out = torch.empty_like(x)
     with torch.cuda.device(dev):
@@ -326,12 +367,22 @@ def convt3d_out_shape(x_shape, Cout, k, stride, pad):
     return (N, Cout, f(D), f(H), f(W))
 
 
+def _convt3d_shapes(x, w, b, gamma, beta, out, stride, pad):
+    Cin, Cout, k = x.shape[1], w.shape[1], w.shape[2]
+    _shape(w, (Cin, Cout, k, k, k), "w")
+    _numel(b, Cout, "b")
+    _numel(gamma, Cout, "gamma")
+    _numel(beta, Cout, "beta")
+    _shape(out, convt3d_out_shape(x.shape, Cout, k, stride, pad), "out")
+
+
 def gf_convt3d_swish_gn_hswish(x, w, b, gamma, beta, stride, pad, groups, eps=1e-5, out=None, workspace=None,
                                stream=None):
     """out = hardswish(GroupNorm(groups)(swish(conv_transpose3d(x, w, b, stride, pad))))."""
-    dev = _check(x, w, b, gamma, beta, out)
     N, Cin, D, H, W = x.shape
     Cout, k = w.shape[1], w.shape[2]
+    _convt3d_shapes(x, w, b, gamma, beta, out, stride, pad)
+    dev = _check(x, w, b, gamma, beta, out)
     if out is None:
         out = torch.empty(convt3d_out_shape(x.shape, Cout, k, stride, pad), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
@@ -347,9 +398,10 @@ def gf_convt3d_swish_gn_hswish_noalloc(x, w, b, gamma, beta, stride, pad, groups
     give the library device scratch memory; the library's own fixed scratch
     (gf_convt3d_noalloc_scratch_limit() bytes per device) is used instead.
     Calls that overlap on the GPU race on that scratch."""
-    dev = _check(x, w, b, gamma, beta, out)
     N, Cin, D, H, W = x.shape
     Cout, k = w.shape[1], w.shape[2]
+    _convt3d_shapes(x, w, b, gamma, beta, out, stride, pad)
+    dev = _check(x, w, b, gamma, beta, out)
     if out is None:
         out = torch.empty(convt3d_out_shape(x.shape, Cout, k, stride, pad), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
