@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -502,7 +503,8 @@ def run_ours(wl, args):
             torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    ms_total = sum(a.elapsed_time(b) for a, b in evs)
+    per_step = sorted(a.elapsed_time(b) for a, b in evs)
+    ms_total = sum(per_step)
     ms_total, kern_ms = reduce_over_ranks([ms_total, prof.mean_ms], device=dev)
     ms_step = ms_total / steps
     value = job_value(wl.work_per_step(), ws, ms_step, wl.scale())
@@ -603,9 +605,21 @@ def run_ours(wl, args):
                 "config": dict(wl.config, l2=wl.l2, parallelism=f"replicas x{ws}" if ws > 1 else "single GPU",
                                launch=launch, **({"mode": MODES[MODE][1]} if wl.bound == "tensor" else {})),
                 "e2e": e2e, "gpu_launches": launches * steps, "roofline": roofline, "cpu_baseline": cpu,
+                "step_ms": step_percentiles(per_step),
                 "other_modes": other,
                 "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
+
+
+def step_percentiles(ms):
+    """Median, 10th and 90th percentile of the per-step times (rank 0's
+    steps; nearest-rank percentiles of the sorted list)."""
+    ms = sorted(ms)
+    if not ms:
+        return None
+    at = lambda q: ms[min(len(ms) - 1, max(0, math.ceil(q * len(ms)) - 1))]  # noqa: E731
+    return {"median": round(statistics.median(ms), 4), "p10": round(at(0.1), 4), "p90": round(at(0.9), 4),
+            "n": len(ms)}
 
 
 def cpu_baseline(wl, d, budget_s=12.0):
