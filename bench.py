@@ -622,6 +622,26 @@ def step_percentiles(ms):
             "n": len(ms)}
 
 
+def host_threads():
+    """Threads the oracle's BLAS calls run on: the BLAS pool's size where
+    threadpoolctl can read it, else the first thread-count variable that
+    OpenBLAS honours (torchrun sets OMP_NUM_THREADS=1), capped by the CPU
+    affinity mask."""
+    n = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_info
+        pools = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        if pools:
+            return max(1, min(n, max(pools)))
+    except Exception:  # not installed: fall back on the environment
+        pass
+    for v in ("OPENBLAS_NUM_THREADS", "GOTO_NUM_THREADS", "OMP_NUM_THREADS"):
+        s = os.environ.get(v, "").strip()
+        if s.isdigit() and int(s) > 0:
+            return min(n, int(s))
+    return n
+
+
 def cpu_baseline(wl, d, budget_s=12.0):
     """The fp64 oracle, as it stands, on a bounded sample of the workload."""
     t0 = time.perf_counter()
@@ -631,7 +651,7 @@ def cpu_baseline(wl, d, budget_s=12.0):
         i += 1
     dt = time.perf_counter() - t0
     v = wl.work_per_step() * frac / dt / wl.scale()
-    return {"value": round(v, 6), "unit": wl.unit, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+    return {"value": round(v, 6), "unit": wl.unit, "cores": host_threads(), "kind": "oracle",
             "sample": f"{frac * 100:.1f}% of one step of the same workload ({i} chunks of {wl.chunk} "
                       f"{'rows' if 'linear' in wl.name else 'samples'}), fp64 numpy/scipy with BLAS threads at "
                       f"their default, {dt:.1f} s"}
@@ -651,7 +671,7 @@ def run_reference(wl, args):
             f += wl.oracle_chunk(d, i, wl.chunk)
         return f
 
-    for _ in range(min(args.warmup, 1)):
+    for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     frac = 0.0
@@ -660,7 +680,7 @@ def run_reference(wl, args):
     steps = args.steps or 3
     dt = (time.perf_counter() - t0) / steps
     v = wl.work_per_step() * frac / dt / wl.scale()
-    cores = len(os.sched_getaffinity(0))
+    cores = host_threads()
     sample = f"{frac * 100:.2f}% of the workload per step ({n_chunks} chunk(s) of {wl.chunk}), fp64 numpy oracle"
     line = {"metric": wl.metric, "value": round(v, 6), "unit": wl.unit, "n_gpus": ws, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",

@@ -91,3 +91,20 @@ def algo_bytes(name, work):
         B, C, L = 32, 256, 4096
         return 4 * (2 * B * C * L + 2 * C * C * 3 + 2 * B * C * L)
     return work  # convt3d: x once + out once
+
+
+def test_host_threads_follow_the_blas_pool_or_the_environment(monkeypatch):
+    import sys
+    n = len(os.sched_getaffinity(0))
+    assert 1 <= bench.host_threads() <= n
+    # without threadpoolctl (as on hosts that lack it) the variables decide, in OpenBLAS's order
+    monkeypatch.setitem(sys.modules, "threadpoolctl", None)
+    for v in ("OPENBLAS_NUM_THREADS", "GOTO_NUM_THREADS", "OMP_NUM_THREADS"):
+        monkeypatch.delenv(v, raising=False)
+    assert bench.host_threads() == n
+    monkeypatch.setenv("OMP_NUM_THREADS", "1")  # what torchrun sets
+    assert bench.host_threads() == 1
+    monkeypatch.setenv("OPENBLAS_NUM_THREADS", "2")
+    assert bench.host_threads() == min(n, 2)
+    monkeypatch.setenv("OPENBLAS_NUM_THREADS", "100000")
+    assert bench.host_threads() == n
