@@ -171,3 +171,52 @@ def test_device_status_signature(L):
     # the argument is optional; the call itself needs a device, so only the
     # ctypes signature is checked here
     assert L.gf_device_status.argtypes == [ctypes.POINTER(ctypes.c_int32)]
+
+
+def _header_text():
+    import re
+    return re.sub(r"/\*.*?\*/", "", open(binding.HEADER_PATH).read(), flags=re.S)
+
+
+def test_binding_constants_match_the_header():
+    import re
+    defs = {m.group(1): int(m.group(2), 0) for m in
+            re.finditer(r"#define\s+(GF_[A-Z0-9_]+)\s+(-?(?:0x[0-9a-fA-F]+|\d+))\b", _header_text())}
+    for name in ("GF_MODE_FP32_3XTF32", "GF_MODE_BF16", "GF_MODE_FP32_3XBF16", "GF_FLAG_GELU_TANH"):
+        assert getattr(binding, name) == defs[name], name
+    for name, v in (("GF_OK", GF_OK), ("GF_ERR_NULL", GF_ERR_NULL), ("GF_ERR_SHAPE", GF_ERR_SHAPE),
+                    ("GF_ERR_ALIGN", GF_ERR_ALIGN), ("GF_ERR_ALIAS", GF_ERR_ALIAS),
+                    ("GF_ERR_WORKSPACE", GF_ERR_WORKSPACE), ("GF_ERR_MODE", GF_ERR_MODE)):
+        assert defs[name] == v, name
+
+
+def test_binding_signatures_match_the_header_prototypes():
+    """Each ctypes signature has the prototype's parameter count, and each
+    parameter the ctypes type of its C type (pointers as pointers, int64_t,
+    int32_t/gf_status, float, size_t), as has the return type."""
+    import re
+    protos = {}
+    for m in re.finditer(r"([A-Za-z_][\w \*]*?)\b(gf_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", _header_text()):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        ps = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        protos[name] = (ret, ps)
+    assert set(protos) == set(binding.header_functions())
+
+    def kind(c):
+        c = " ".join(c.split())
+        if "*" in c:
+            return "ptr"
+        base = c.replace("const ", "").split()[0]
+        return {"int64_t": "i64", "int32_t": "i32", "gf_status": "i32", "float": "f32", "size_t": "size"}[base]
+
+    def ckind(t):
+        if t in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+            return "ptr"
+        return {ctypes.c_int64: "i64", ctypes.c_int32: "i32", ctypes.c_float: "f32", ctypes.c_size_t: "size"}[t]
+
+    for name, (ret, ps) in protos.items():
+        res, args = binding._SIGS[name]
+        assert len(args) == len(ps), (name, len(args), len(ps))
+        for i, (p, a) in enumerate(zip(ps, args)):
+            assert kind(p) == ckind(a), (name, i, p, a)
+        assert kind(ret) == ckind(res), (name, ret, res)
