@@ -25,7 +25,7 @@ def _f64(a):
 def silu(v):
     """Swish / SiLU: ``v * sigmoid(v)`` with ``sigmoid(v) = 1 / (1 + e^-v)``.
 
-    Page Kimi-K2.6__l2_p37, turn 1 (the model applies ``sigmoid(x) * x``);
+    Page Kimi-K2.6__l2_p37, turn 1 (the model multiplies its input by its sigmoid);
     page Kimi-K2.6__l2_p60, turn 1 (swish before the GroupNorm).
     For v below about -709, e^-v overflows to inf and the quotient is the
     correct limit -0.
@@ -280,8 +280,8 @@ def conv_transpose3d_zero_insert(x, w, b, stride, pad):
 def group_norm_nc(t, groups, gamma=None, beta=None, eps=1e-5):
     """GroupNorm of t[N, C, *spatial]: per sample and group of C/groups
     contiguous channels times all spatial positions; biased variance; per-channel
-    affine (page Kimi-K2.6__l2_p60, turn 1: "GroupNorm groups contiguous
-    channels", 4 channels per group)."""
+    affine (page Kimi-K2.6__l2_p60, turn 1: each group is a run of adjacent
+    channels, 4 of the 16 here)."""
     t = _f64(t)
     N, C = t.shape[:2]
     if C % groups:
