@@ -1,8 +1,10 @@
 """Build libgf.so in-tree: one nvcc process per translation unit, in parallel,
-then a shared-library link.  sm_103a only."""
+then a shared-library link.  sm_103a only.  Concurrent builds (several test
+processes) take turns through an exclusive lock on a file beside the library."""
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import glob
 import os
 import shutil
@@ -14,6 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgf.so")
+LOCK = os.path.join(PKG, ".libgf.build.lock")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
@@ -37,14 +40,27 @@ def _compile(src, obj, verbose):
     return r.stderr if verbose else ""
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+def _up_to_date(srcs):
     deps = srcs + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
         [os.path.join(ROOT, "include", "gf.h"), __file__]
-    if not force and os.path.exists(LIB):
-        t = os.path.getmtime(LIB)
-        if all(os.path.getmtime(d) <= t for d in deps):
+    if not os.path.exists(LIB):
+        return False
+    t = os.path.getmtime(LIB)
+    return all(os.path.getmtime(d) <= t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    if not force and _up_to_date(srcs):
+        return LIB
+    with open(LOCK, "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)  # released when the file closes
+        if not force and _up_to_date(srcs):  # another process built it meanwhile
             return LIB
+        return _build_locked(srcs, verbose)
+
+
+def _build_locked(srcs, verbose):
     os.makedirs(BUILD, exist_ok=True)
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
     logs = []
