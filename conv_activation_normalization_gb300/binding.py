@@ -162,6 +162,17 @@ def _workspace(device: torch.device, nbytes: int, stream=None):
     return buf
 
 
+def release_workspaces() -> int:
+    """Drop the cached workspace buffers (all devices and streams) and return
+    how many there were.  Safe while work that uses them is still queued:
+    each buffer was allocated on, or recorded on, the stream it serves, so
+    torch's allocator does not reuse its memory before that work is done."""
+    with _lock:
+        n = len(_ws_cache)
+        _ws_cache.clear()
+    return n
+
+
 def _check(*ts):
     dev = None
     for t in ts:

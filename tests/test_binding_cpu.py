@@ -2,7 +2,8 @@
 derives from the leading operands, before any device or library call: the C
 entry points take only sizes and pointers, so a short bias or a W with the
 wrong K would otherwise be read past its end.  CPU tensors suffice: the shape
-checks come first, and tensors of the right shapes then fail the CUDA check."""
+checks come first, and tensors of the right shapes then fail the CUDA check.
+Also: the cached default workspaces are dropped on request."""
 import pytest
 import torch
 
@@ -79,3 +80,11 @@ def test_convt3d_shapes(fn):
     assert gf.convt3d_out_shape(x.shape, Cout, k, 2, 1) == (2, 8, 7, 9, 11)
     _raises("out has shape", fn, **ok, out=z(2, 8, 8, 9, 11))
     _raises("CUDA", fn, **{**ok, "b": None}, out=z(2, 8, 7, 9, 11))
+
+
+def test_release_workspaces_empties_the_cache():
+    gf.release_workspaces()
+    gf._ws_cache[(0, 0)] = z(4)  # stands in for a cached buffer (no device needed)
+    gf._ws_cache[(0, 1)] = z(4)
+    assert gf.release_workspaces() == 2
+    assert gf._ws_cache == {} and gf.release_workspaces() == 0
