@@ -162,7 +162,10 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
  * staging buffers in the workspace.  Returns once everything is enqueued;
  * out_host is complete when `stream` reaches that point (synchronise it
  * before reading).  Workspace: the matching *_host_workspace_size() query.
- * The internal streams and events are created and released by each call. */
+ * The internal streams and events are created and released by each call.
+ * A GF_ERR_CUDA returned after work was enqueued leaves copies already queued
+ * on the internal streams running: synchronise the device before reusing
+ * x_host, out_host or the workspace. */
 size_t gf_linear_swish_bias_groupnorm_host_workspace_size(int64_t M, int64_t K, int64_t N,
                                                           int32_t groups, int32_t mode,
                                                           int64_t chunk_rows);
