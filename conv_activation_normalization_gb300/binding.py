@@ -24,6 +24,7 @@ GF_MODE_FP32_3XTF32 = 0
 GF_MODE_BF16 = 1
 GF_MODE_FP32_3XBF16 = 2
 GF_FLAG_GELU_TANH = 0x100  # OR'd into the Conv1d chain's mode: tanh-approximate GELU
+GF_CHAIN_GROUPNORM, GF_CHAIN_LSE, GF_CHAIN_LINEAR = 0, 1, 2  # gf_linear_tile_width's chains
 
 _lib = None
 _lock = threading.Lock()
@@ -36,6 +37,9 @@ _SIGS = {
     "gf_device_status": (_I32, [ctypes.POINTER(ctypes.c_int32)]),
     "gf_profile_begin": (_I32, [_I32]),
     "gf_profile_end": (_I32, [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_float)]),
+    "gf_measure_tensor_rate": (_I32, [_I32, _I32, _I32, ctypes.POINTER(ctypes.c_double)]),
+    "gf_linear_tile_width": (_I32, [_I32, _I64, _I64, _I32, _I32, _I32]),
+    "gf_testing_host_pipeline_trace": (_I32, [_I64, _I32, ctypes.c_char_p, _SZ]),
     "gf_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
     "gf_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
     "gf_linear_swish_bias_groupnorm_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
@@ -57,6 +61,8 @@ _SIGS = {
     "gf_convt3d_swish_gn_hswish": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I32,
                                           _I32, _I32, _I32, _F, _P, _SZ, _P]),
     "gf_convt3d_noalloc_scratch_limit": (_SZ, []),
+    "gf_convt3d_swish_gn_hswish_noalloc_scratch_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I64, _I32, _I32,
+                                                              _I32, _I32]),
     "gf_convt3d_swish_gn_hswish_noalloc": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
                                                   _I32, _I32, _I32, _I32, _F, _P]),
 }
@@ -89,6 +95,30 @@ def header_functions() -> list[str]:
     text = open(HEADER_PATH).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(gf_[a-z0-9_]+)\s*\(", text)))
+
+
+def linear_tile_width(chain: int, M: int, N: int, groups: int, mode: int, sm_count: int) -> int:
+    """The GEMM tile width the Linear chains' dispatch picks (host arithmetic
+    only; 0 for invalid arguments)."""
+    return lib().gf_linear_tile_width(chain, M, N, groups, mode, sm_count)
+
+
+def measure_tensor_rate(kind: str, iters: int = 4096, repeats: int = 5) -> float:
+    """The tensor pipe's measured dense rate in TFLOP/s for kind "tf32" or
+    "bf16" (gf_measure_tensor_rate; synchronises)."""
+    out = ctypes.c_double(0.0)
+    st = lib().gf_measure_tensor_rate({"tf32": 0, "bf16": 1}[kind], iters, repeats, ctypes.byref(out))
+    if st != 0:
+        raise GFError(st, "gf_measure_tensor_rate")
+    return out.value
+
+
+def host_pipeline_trace(nchunks: int, fail_at: int = -1) -> tuple[int, str]:
+    """(status, steps) of the host-buffer pipeline's schedule run against a
+    recorder that fails at step fail_at (-1: none).  No device is touched."""
+    buf = ctypes.create_string_buffer(64 * (3 * nchunks + 4))
+    st = lib().gf_testing_host_pipeline_trace(nchunks, fail_at, buf, len(buf))
+    return st, buf.value.decode()
 
 
 def status_string(status: int) -> str:

@@ -31,7 +31,40 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                    CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+unsigned long long g_status_ctx[kMaxDevices];
+
+template <class F>
+bool driver_entry(const char* name, F* fn) {
+  if (*fn) return true;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !p)
+    return false;
+  *fn = reinterpret_cast<F>(p);
+  return true;
+}
 }  // namespace
+
+gf_status current_context_id(unsigned long long* id) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!driver_entry("cuCtxGetCurrent", &g_ctx_current) || !driver_entry("cuCtxGetId", &g_ctx_id))
+      return GF_ERR_CUDA;
+  }
+  // make the current device's primary context current on this thread (the
+  // runtime creates contexts lazily; cudaSetDevice initialises it)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return GF_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return GF_ERR_CUDA;
+  return g_ctx_id(ctx, id) == CUDA_SUCCESS ? GF_OK : GF_ERR_CUDA;
+}
 
 gf_status current_device(DeviceInfo* info) {
   int dev = 0;
@@ -58,11 +91,14 @@ gf_status current_device(DeviceInfo* info) {
 uint32_t* device_status_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned long long ctx = 0;
+  if (current_context_id(&ctx) != GF_OK) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[dev]) {
+  if (!g_status_ptr[dev] || g_status_ctx[dev] != ctx) {  // looked up again in a new context
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
     g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    g_status_ctx[dev] = ctx;
   }
   return g_status_ptr[dev];
 }

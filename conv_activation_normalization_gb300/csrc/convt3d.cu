@@ -492,22 +492,57 @@ constexpr size_t kCtNoAllocScratchBytes = size_t(4) << 20;
 static __device__ __align__(256) unsigned char g_ct_noalloc_scratch[kCtNoAllocScratchBytes];
 
 namespace {
+// An empty batch (N = 0): the arguments other than the batch are checked as
+// for a batch of one (x and out may be NULL), then nothing is launched.
+gf_status ct_empty_batch(const float* x, const float* w, const float* b, const float* gamma, const float* beta,
+                         const float* out, int64_t Cin, int64_t Cout, int64_t D, int64_t H, int64_t W, int32_t k,
+                         int32_t stride, int32_t pad, int32_t groups, float eps) {
+  if (!w || !gamma || !beta) return GF_ERR_NULL;
+  CtGenShape gen;
+  if (check_ct_shape(1, Cin, Cout, D, H, W, k, stride, pad, groups) != GF_OK &&
+      ct_general_shape(1, Cin, Cout, D, H, W, k, stride, pad, groups, &gen) != GF_OK)
+    return GF_ERR_SHAPE;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
+      (b && !aligned16(b)))
+    return GF_ERR_ALIGN;
+  return GF_OK;
+}
+
 std::mutex g_ct_scratch_mu;
 void* g_ct_scratch_addr[64];
+unsigned long long g_ct_scratch_ctx[64];
 
 // Device address of g_ct_noalloc_scratch on the current device, looked up once
-// per device.  In host code the array's name is only a host-side stand-in, so
-// the kernels must be given this address instead.
+// per device and context.  In host code the array's name is only a host-side
+// stand-in, so the kernels must be given this address instead.  The cached
+// address is tied to the context it was looked up in (its unique id): after
+// the context is destroyed and recreated (cudaDeviceReset) the module is
+// loaded afresh and the address is looked up again.
 gf_status ct_scratch_address(int device, void** addr) {
   if (device < 0 || device >= 64) return GF_ERR_CUDA;
+  unsigned long long ctx = 0;
+  if (current_context_id(&ctx) != GF_OK) return GF_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_ct_scratch_mu);
-  if (!g_ct_scratch_addr[device]) {
+  if (!g_ct_scratch_addr[device] || g_ct_scratch_ctx[device] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_ct_noalloc_scratch) != cudaSuccess || !p) return GF_ERR_CUDA;
     g_ct_scratch_addr[device] = p;
+    g_ct_scratch_ctx[device] = ctx;
   }
   *addr = g_ct_scratch_addr[device];
   return GF_OK;
+}
+
+// Scratch bytes the no-workspace call needs for a shape (0: shape rejected):
+// the CUDA-core two-pass kernels' partials and coefficients for the pages'
+// configuration, the general kernels' workspace for every other shape.
+size_t ct_noalloc_scratch_bytes(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H, int64_t W, int32_t k,
+                                int32_t stride, int32_t pad, int32_t groups) {
+  if (N == 0) return 0;
+  if (check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) == GF_OK) return ct_ws(N, D, H, W).total;
+  CtGenShape g;
+  return ct_general_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups, &g) == GF_OK ? g.total : 0;
 }
 }  // namespace
 }  // namespace gf
@@ -518,6 +553,7 @@ extern "C" {
 
 size_t gf_convt3d_swish_gn_hswish_workspace_size(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H,
                                                  int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups) {
+  if (N == 0) return 0;  // an empty batch launches nothing
   if (check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) != GF_OK) {
     // any other kernel size, stride, padding, channel counts or groups
     CtGenShape g;
@@ -533,6 +569,7 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
                                      const float* beta, float* out, int64_t N, int64_t Cin, int64_t Cout, int64_t D,
                                      int64_t H, int64_t W, int32_t k, int32_t stride, int32_t pad, int32_t groups,
                                      float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  if (N == 0) return ct_empty_batch(x, w, b, gamma, beta, out, Cin, Cout, D, H, W, k, stride, pad, groups, eps);
   if (!x || !w || !gamma || !beta || !out) return GF_ERR_NULL;
   CtGenShape gen;
   const bool fast = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) == GF_OK;
@@ -592,10 +629,17 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
 
 size_t gf_convt3d_noalloc_scratch_limit(void) { return kCtNoAllocScratchBytes; }
 
+size_t gf_convt3d_swish_gn_hswish_noalloc_scratch_size(int64_t N, int64_t Cin, int64_t Cout, int64_t D, int64_t H,
+                                                       int64_t W, int32_t k, int32_t stride, int32_t pad,
+                                                       int32_t groups) {
+  return ct_noalloc_scratch_bytes(N, Cin, Cout, D, H, W, k, stride, pad, groups);
+}
+
 gf_status gf_convt3d_swish_gn_hswish_noalloc(const float* x, const float* w, const float* b, const float* gamma,
                                              const float* beta, float* out, int64_t N, int64_t Cin, int64_t Cout,
                                              int64_t D, int64_t H, int64_t W, int32_t k, int32_t stride, int32_t pad,
                                              int32_t groups, float eps, void* stream) {
+  if (N == 0) return ct_empty_batch(x, w, b, gamma, beta, out, Cin, Cout, D, H, W, k, stride, pad, groups, eps);
   if (!x || !w || !gamma || !beta || !out) return GF_ERR_NULL;
   CtGenShape gen;
   const bool fast = check_ct_shape(N, Cin, Cout, D, H, W, k, stride, pad, groups) == GF_OK;
@@ -605,8 +649,9 @@ gf_status gf_convt3d_swish_gn_hswish_noalloc(const float* x, const float* w, con
   if (!aligned16(x) || !aligned16(w) || !aligned16(gamma) || !aligned16(beta) || !aligned16(out) ||
       (b && !aligned16(b)))
     return GF_ERR_ALIGN;
+  if (ct_noalloc_scratch_bytes(N, Cin, Cout, D, H, W, k, stride, pad, groups) > kCtNoAllocScratchBytes)
+    return GF_ERR_WORKSPACE;  // beyond the fixed scratch
   if (!fast) {  // the general kernels, their workspace in the fixed scratch
-    if (gen.total > kCtNoAllocScratchBytes) return GF_ERR_WORKSPACE;
     const Span gins[] = {{x, size_t(N) * Cin * D * H * W * 4},
                          {w, size_t(Cin) * Cout * k * k * k * 4},
                          {b, size_t(Cout) * 4},
@@ -621,7 +666,6 @@ gf_status gf_convt3d_swish_gn_hswish_noalloc(const float* x, const float* w, con
     return launch_ct_general(gen, x, w, b, gamma, beta, out, eps, scratch, static_cast<cudaStream_t>(stream));
   }
   const CtWs wl = ct_ws(N, D, H, W);
-  if (wl.total > kCtNoAllocScratchBytes) return GF_ERR_WORKSPACE;  // beyond the fixed scratch
   const size_t outb = size_t(N) * Cout * (2 * D - 1) * (2 * H - 1) * (2 * W - 1) * 4;
   const Span ins[] = {{x, size_t(N) * Cin * D * H * W * 4},
                       {w, size_t(Cin) * Cout * 27 * 4},

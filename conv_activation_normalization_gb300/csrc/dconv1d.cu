@@ -313,8 +313,10 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   return w;
 }
 
+// B = 0 (an empty batch) passes: the entry point then returns GF_OK without
+// launching anything.
 gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
-  if (B < 1 || C < 1 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
+  if (B < 0 || C < 1 || L < 1 || ksize < 1 || ksize > 16) return GF_ERR_SHAPE;
   (void)mode;  // any C: the operand planes pad the channels to whole k-blocks
   if (C > 1024) return GF_ERR_SHAPE;
   if (B > 65535 || L > (int64_t(1) << 30)) return GF_ERR_SHAPE;
@@ -369,6 +371,7 @@ gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const vo
   src.num_jb = int((L + kBM - 1) / kBM);
   src.num_nb = int((C + kBNConv - 1) / kBNConv);
   src.num_kb = int(ksize * Cp / Op::kBK);
+  src.kb_chunk = src.num_kb;
   src.bn = kBNConv;
   src.bk = Op::kBK;
   src.nsamples = int(B);
@@ -385,7 +388,7 @@ extern "C" {
 size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t mode) {
   if (mode & ~(GF_FLAG_GELU_TANH | 0xff)) return 0;
   mode &= 0xff;
-  if (!conv_mode_ok(mode) || check_conv_shape(B, C, L, ksize, mode) != GF_OK) return 0;
+  if (!conv_mode_ok(mode) || check_conv_shape(B, C, L, ksize, mode) != GF_OK || B == 0) return 0;
   return conv_ws(B, C, L, ksize, mode).total;
 }
 
@@ -393,7 +396,8 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
                                  const float* conv_b, float* out, int64_t B, int64_t C, int64_t L, int32_t ksize,
                                  int32_t dilation, int32_t padding, float eps, int32_t mode, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  if (!x || !ln_gamma || !ln_beta || !conv_w || !out) return GF_ERR_NULL;
+  // (an empty batch, B = 0, may pass NULL for x and out)
+  if ((B && (!x || !out)) || !ln_gamma || !ln_beta || !conv_w) return GF_ERR_NULL;
   if (mode & ~(GF_FLAG_GELU_TANH | 0xff)) return GF_ERR_MODE;
   const bool tanh_gelu = (mode & GF_FLAG_GELU_TANH) != 0;
   mode &= 0xff;
@@ -406,6 +410,7 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   if (!aligned16(x) || !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(conv_w) || !aligned16(out) ||
       (conv_b && !aligned16(conv_b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
+  if (B == 0) return GF_OK;
   const ConvWs wl = conv_ws(B, C, L, ksize, mode);
   if (!workspace) return GF_ERR_NULL;
   if (workspace_bytes < wl.total) return GF_ERR_WORKSPACE;

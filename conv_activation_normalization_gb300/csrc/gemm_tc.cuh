@@ -36,6 +36,20 @@
 //
 // The operand source (a plain [rows, K] matrix, or the implicit-GEMM view of
 // a dilated Conv1d) and the epilogue are template policies.
+//
+// Chunked accumulation (epi_chunked below): the tensor core adds
+// each MMA's products into the fp32 accumulator with truncation, which over a
+// long K loop of same-signed products (all-positive operands, say) becomes a
+// bias that grows with K^2: -0.32 on sums of about 2048 at K = 8192, against
+// an fp32 rounding error of about 1e-3.  Such epilogues take the tile's K loop
+// in chunks of kb_chunk k-blocks, each accumulated from zero into the two
+// TMEM accumulators in turn; the epilogue warps add each finished chunk into
+// a running total kept in TMEM columns beside the accumulators (fp32 adds
+// with round-to-nearest), so the bias grows only with K * chunk length, and
+// hand the total of the earlier chunks to the epilogue with the last chunk.
+// The accumulator of the next chunk fills while the last one is being added,
+// as it does across tiles.  This needs BN + BN / halves <= ACC_STRIDE
+// columns (160-column tiles: 240 of 256).
 #pragma once
 
 #include <cstdint>
@@ -112,9 +126,29 @@ struct Tile {
   int b, r0, n0, nb;
 };
 
+// Whether the epilogue takes its accumulator in chunks (for this operand mode
+// and BNW epilogue columns per thread): epilogues that declare
+// chunked<Op, BNW>() and say so.
+template <class Epi, class = void>
+struct HasChunked {
+  static constexpr bool value = false;
+};
+template <class Epi>
+struct HasChunked<Epi, decltype(void(&Epi::template apply_last<64>))> {
+  static constexpr bool value = true;
+};
+template <class Epi, class Op, int BN>
+__host__ __device__ constexpr bool epi_chunked() {
+  if constexpr (HasChunked<Epi>::value)
+    return Epi::template chunked<Op>() && BN + BN / epi_halves(BN) <= TileCfg<BN, Op>::ACC_STRIDE;
+  else
+    return false;
+}
+
 // A = [M][K] planes (2-D maps {K, M}, box {BK, 128}), B = [N][K] planes.
 struct LinearSrc {
   int num_mb, num_nb, num_kb, bn, bk;
+  int kb_chunk;   // k-blocks per accumulation chunk (chunked epilogues only)
   int m_fastest;  // tile order: consecutive tiles share an n-block (1) or an m-block (0)
   __device__ __forceinline__ int num_tiles() const { return num_mb * num_nb; }
   __device__ __forceinline__ Tile tile(int t) const {
@@ -150,6 +184,7 @@ struct LinearSrc {
 struct ConvSrc {
   int C, pad, dil;
   int num_jb, num_nb, num_kb, bn, bk, nsamples;
+  int kb_chunk;   // k-blocks per accumulation chunk (chunked epilogues only)
   __device__ __forceinline__ int num_tiles() const { return nsamples * num_jb * num_nb; }
   __device__ __forceinline__ Tile tile(int t) const {
     const int nb = t % num_nb;
@@ -221,6 +256,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = src.num_tiles();
+  // k-blocks per accumulation chunk: the whole K loop unless the epilogue
+  // adds chunks (both the MMA issuer and the epilogue count chunks with it)
+  constexpr bool kChunked = epi_chunked<Epi, Op, BN>();
+  const int kb_chunk = kChunked && src.kb_chunk > 0 ? src.kb_chunk : src.num_kb;
 
   // smem address of plane p of A / B in stage s
   auto a_addr = [&](int s, int p) { return smem_u32(smem + s * Cfg::STAGE_BYTES + p * Cfg::A_BYTES); };
@@ -270,44 +309,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok && !*abort_flag; t += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1)) {
-          ok = false;
-          break;
+      // the MMAs of one k-block into accumulator d; the first of a chunk
+      // overwrites it
+      auto mma_kblock = [&](uint32_t d, bool chunk_start) {
+        const uint32_t a_hi = a_addr(stage, 0), b_hi = b_addr(stage, 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t off = uint32_t(kk * 32);  // one MMA K-step = 32 bytes of the row
+          const uint32_t accumulate = !chunk_start || kk != 0;
+          if constexpr (Op::kProducts == 3) {
+            const uint32_t a_lo = a_addr(stage, 1), b_lo = b_addr(stage, 1);
+            Op::mma(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, accumulate);
+            Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
+            Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
+          } else {
+            Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, accumulate);
+          }
         }
-        tc_fence_after();
-        const uint32_t d = tmem_base + uint32_t(acc * Cfg::ACC_STRIDE);
-        for (int kb = 0; kb < src.num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase)) {
+        mma_commit(&empty[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      };
+      for (int t = blockIdx.x; t < num_tiles && ok && !*abort_flag; t += gridDim.x) {
+        if constexpr (kChunked) {
+          uint32_t d = 0;
+          // kc: k-block index within the current accumulation chunk
+          for (int kb = 0, kc = 0; kb < src.num_kb; ++kb) {
+            if (kc == 0) {  // a chunk starts: take the next accumulator
+              if (!mbar_wait(&tempty[acc], acc_phase ^ 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              d = tmem_base + uint32_t(acc * Cfg::ACC_STRIDE);
+            }
+            if (!mbar_wait(&full[stage], phase)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_kblock(d, kc == 0);
+            if (++kc == kb_chunk || kb == src.num_kb - 1) {  // the chunk (or the tile) is done
+              kc = 0;
+              mma_commit(&tfull[acc]);
+              if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+              }
+            }
+          }
+          if (!ok) break;
+        } else {
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_hi = a_addr(stage, 0), b_hi = b_addr(stage, 0);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t off = uint32_t(kk * 32);  // one MMA K-step = 32 bytes of the row
-            const uint32_t first = (kb | kk) != 0;
-            if constexpr (Op::kProducts == 3) {
-              const uint32_t a_lo = a_addr(stage, 1), b_lo = b_addr(stage, 1);
-              Op::mma(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, first);
-              Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
-              Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
-            } else {
-              Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, first);
+          const uint32_t d = tmem_base + uint32_t(acc * Cfg::ACC_STRIDE);
+          for (int kb = 0; kb < src.num_kb; ++kb) {
+            if (!mbar_wait(&full[stage], phase)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+            mma_kblock(d, kb == 0);
           }
-          mma_commit(&empty[stage]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
+          if (!ok) break;
+          mma_commit(&tfull[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
           }
-        }
-        if (!ok) break;
-        mma_commit(&tfull[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1;
         }
       }
       if (!ok) {
@@ -328,26 +402,78 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     // narrow tiles (H == 1): the second set of epilogue warps idles
-    for (int t = blockIdx.x; half < H && t < num_tiles; t += gridDim.x) {
-      const Tile tile = src.tile(t);
-      bool ok = mbar_wait(&tfull[acc], acc_phase);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok || __any_sync(0xffffffffu, *abort_flag)) {
-        if (!ok) {
-          record_error(status, GF_DEV_WAIT_TIMEOUT);
-          *abort_flag = 1;
+    if constexpr (kChunked) {
+      // running total of the tile's earlier chunks: TMEM columns
+      // half * ACC_STRIDE + BN .. + BNW - 1 of this warp's lanes
+      const int nchunks = (src.num_kb + kb_chunk - 1) / kb_chunk;
+      const uint32_t tot = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(half * Cfg::ACC_STRIDE + BN);
+      bool failed = false;
+      for (int t = blockIdx.x; half < H && t < num_tiles && !failed; t += gridDim.x) {
+        const Tile tile = src.tile(t);
+        const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
+        for (int c = 0; c < nchunks; ++c) {
+          bool ok = mbar_wait(&tfull[acc], acc_phase);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok || __any_sync(0xffffffffu, *abort_flag)) {
+            if (!ok) {
+              record_error(status, GF_DEV_WAIT_TIMEOUT);
+              *abort_flag = 1;
+            }
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr =
+              tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * Cfg::ACC_STRIDE + half * BNW);
+          if (c < nchunks - 1) {
+#pragma unroll 1
+            for (int j = 0; j < BNW; j += 16) {
+              uint32_t r[16], q[16];
+              GF_TMEM_LD16(taddr + uint32_t(j), r);
+              if (c > 0) GF_TMEM_LD16(tot + uint32_t(j), q);
+              GF_TMEM_WAIT16(r);
+              if (c > 0) {
+                GF_TMEM_WAIT16(q);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(q[i]) + __uint_as_float(r[i]));
+              }
+              GF_TMEM_ST16(tot + uint32_t(j), r);
+            }
+            tmem_wait_st();  // the next chunk reads the total back
+          } else {
+            Epi::template apply_last<BNW>(ep, taddr, tot, part, row, c > 0);
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1;
+          }
         }
-        break;
       }
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * Cfg::ACC_STRIDE + half * BNW);
-      const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
-      Epi::template apply<BNW>(ep, taddr, part, row);
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1;
+    } else {
+      for (int t = blockIdx.x; half < H && t < num_tiles; t += gridDim.x) {
+        const Tile tile = src.tile(t);
+        bool ok = mbar_wait(&tfull[acc], acc_phase);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok || __any_sync(0xffffffffu, *abort_flag)) {
+          if (!ok) {
+            record_error(status, GF_DEV_WAIT_TIMEOUT);
+            *abort_flag = 1;
+          }
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr =
+            tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * Cfg::ACC_STRIDE + half * BNW);
+        const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
+        Epi::template apply<BNW>(ep, taddr, part, row);
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
     }
   }

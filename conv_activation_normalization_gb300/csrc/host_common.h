@@ -43,6 +43,12 @@ gf_status current_device(DeviceInfo* info);
 // Device address of the library's status word on the current device.
 uint32_t* device_status_word();
 
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context.  A
+// device address looked up with cudaGetSymbolAddress is cached together with
+// this id and looked up again when the id changes (a context that was
+// destroyed and recreated, e.g. by cudaDeviceReset, reloads the module).
+gf_status current_context_id(unsigned long long* id);
+
 gf_status cuda_status(cudaError_t e);
 
 // TMA ---------------------------------------------------------------------

@@ -7,6 +7,8 @@
 // per-row merge kernel, and GroupNorm groups other than 16-128 columns wide
 // a per-row normalisation kernel.
 #include <cmath>
+#include <cstdio>
+#include <cstring>
 
 #include "gemm_tc.cuh"
 #include "host_common.h"
@@ -40,6 +42,7 @@ struct EpiSwishBiasGNT {
   // narrowest tile whose epilogue warps own whole groups: a 128-column group
   // takes a warp's whole half of a 256-column tile
   static constexpr int kMinBN = GW == 128 ? 256 : 64;
+  static constexpr int kTileGW = GW;  // the group width the tile-width rule sees
   using Params = GNParams;
 
   // t = Swish(y + b_lin) + bias over the 64 columns n0.., in place; q[i] =
@@ -211,6 +214,7 @@ struct EpiSwishBiasGNT {
 struct EpiSwishBiasStore {
   static constexpr bool kFixedBN = false;
   static constexpr int kMinBN = 64;
+  static constexpr int kTileGW = 0;
   using Params = GNParams;
   template <int BN>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
@@ -291,16 +295,45 @@ gf_status with_gn_epilogue(const GNParams& ep, cudaStream_t s, F&& f) {
   }
 }
 
-// Linear -> per-row (max, sum exp(y - max)) over the tile's BN columns,
-// written as one float2 partial per (row, n-block); columns are read 16 at a
-// time, so BN may be any multiple of 16 (the tile widths are 160, 224 and 256).
+// Linear -> per-row (max, sum exp(y - max)) over the tile's columns, written
+// as one float2 partial per (row, epilogue column half); columns are read 16
+// at a time and merged online, so BN may be any multiple of 16 (the tile
+// widths are 160, 224 and 256).
+//
+// The chain's K is long (8192 in the pages' problem), so in the
+// three-product modes the accumulator is taken in chunks of kChunkK
+// (chunked(), see gemm_tc.cuh): the kernel keeps the running total of the
+// earlier chunks in spare TMEM columns and hands it to apply_last with the
+// last chunk.  The one-product BF16 mode (3e-2 tolerance) reads its single
+// chunk with apply.
 struct EpiLSEPartial {
   static constexpr bool kFixedBN = true;  // the partials' layout follows the tile width
+  static constexpr int kChunkK = 512;     // K elements per accumulation chunk
+  template <class Op>
+  __host__ __device__ static constexpr bool chunked() {
+    return Op::kProducts == 3;
+  }
   struct Params {
     const float* b;  // may be null
     float2* part;    // [M][n_blocks]: one per row and epilogue column range
     int M, N, n_blocks;
   };
+  // v[j] (+ bias, -inf past N) of one 16-column piece folded into (mx, s)
+  __device__ __forceinline__ static void merge_piece(const Params& p, int n0, float (&v)[16], float& mx, float& s) {
+    float cm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int n = n0 + j;
+      const float bj = (p.b && n < p.N) ? __ldg(p.b + n) : 0.f;
+      v[j] = n < p.N ? v[j] + bj : -INFINITY;
+      cm = fmaxf(cm, v[j]);
+    }
+    const float nm = fmaxf(mx, cm);
+    s *= __expf(mx - nm);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s += __expf(v[j] - nm);
+    mx = nm;
+  }
   template <int BN>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
     static_assert(BN % 16 == 0, "16-column pieces");
@@ -314,19 +347,37 @@ struct EpiLSEPartial {
       GF_TMEM_LD16(taddr + uint32_t(g * 16), r);
       GF_TMEM_WAIT16(r);
       float v[16];
-      float cm = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int n = n0 + j;
-        const float bj = (p.b && n < p.N) ? __ldg(p.b + n) : 0.f;
-        v[j] = n < p.N ? __uint_as_float(r[j]) + bj : -INFINITY;
-        cm = fmaxf(cm, v[j]);
+      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+      merge_piece(p, n0, v, mx, s);
+    }
+    if (m < p.M) p.part[size_t(m) * p.n_blocks + t.nb] = make_float2(mx, s);
+  }
+  // the last chunk at taddr plus, when `earlier`, the earlier chunks' total
+  // at tot (both TMEM addresses of the thread's lane)
+  template <int BN>
+  __device__ __forceinline__ static void apply_last(const Params& p, uint32_t taddr, uint32_t tot, const Tile& t,
+                                                    int row, bool earlier) {
+    const int m = t.r0 + row;
+    float mx = -INFINITY, s = 0.f;
+#pragma unroll 1
+    for (int g = 0; g < BN / 16; ++g) {
+      const int n0 = t.n0 + g * 16;
+      if (n0 >= p.N) break;  // uniform across the warp
+      uint32_t r[16], q[16];
+      GF_TMEM_LD16(taddr + uint32_t(g * 16), r);
+      if (earlier) GF_TMEM_LD16(tot + uint32_t(g * 16), q);
+      GF_TMEM_WAIT16(r);
+      float v[16];
+      if (earlier) {
+        GF_TMEM_WAIT16(q);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(q[j]) + __uint_as_float(r[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
       }
-      const float nm = fmaxf(mx, cm);
-      s *= __expf(mx - nm);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) s += __expf(v[j] - nm);
-      mx = nm;
+      merge_piece(p, n0, v, mx, s);
     }
     if (m < p.M) p.part[size_t(m) * p.n_blocks + t.nb] = make_float2(mx, s);
   }
@@ -341,6 +392,7 @@ struct EpiStore {
     int M, N;
   };
   static constexpr int kMinBN = 64;
+  static constexpr int kTileGW = 0;
   template <int BN>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row) {
     const int m = t.r0 + row;
@@ -400,24 +452,24 @@ namespace {
 
 constexpr int kBNLinear = 256;
 
-// Tile width of the LSE chain: 160, 224 or 256 columns, whichever gives the
-// least waves x per-tile time.  In the three-product modes a 160-column tile
-// fits three smem stages (two for 224 or 256), deep enough for the mainloop
-// to keep pace with W streaming from DRAM; with two stages it runs about
-// 15 % slower per column (1024 x 8192 x 8192: 160 -> 95 %, 224 -> 82 % of
-// the 3xTF32 peak, measured).  The one-product BF16 mode has four or more
-// stages at any width, and there the wider tiles win.
+// Tile width of the LSE chain.  In the three-product modes 160 columns: the
+// tile fits three smem stages (two for 224 or 256), deep enough for the
+// mainloop to keep pace with W streaming from DRAM (1024 x 8192 x 8192: 95 %
+// of the 3xTF32 peak against 82 % with 224-column tiles and two stages), and
+// its chunked accumulation finds room for the running totals in TMEM.
+// The one-product BF16 mode has four or more stages at any width and no
+// chunking; there 224 or 256 columns, whichever gives fewer waves x per-tile
+// time.
 constexpr int kLseWidths[3] = {160, 224, 256};
 int lse_tile_width(int64_t M, int64_t N, int sm_count, int32_t mode) {
+  if (mode != GF_MODE_BF16) return 160;
   const int64_t mb = (M + 127) / 128;
-  int best = kLseWidths[0];
+  int best = 224;
   double best_t = 0.0;
-  for (int bn : kLseWidths) {
-    if (mode == GF_MODE_BF16 && bn == 160) continue;
+  for (int bn : {224, 256}) {
     const int64_t tiles = mb * ((N + bn - 1) / bn);
     const int64_t waves = (tiles + sm_count - 1) / sm_count;
-    const double depth = (mode == GF_MODE_BF16 || bn == 160) ? 1.0 : 0.85;
-    const double t = double(waves) * bn / depth;
+    const double t = double(waves) * bn;
     if (best_t == 0.0 || t < best_t) {
       best = bn;
       best_t = t;
@@ -427,6 +479,25 @@ int lse_tile_width(int64_t M, int64_t N, int sm_count, int32_t mode) {
 }
 // Partials per row for a tile width: one per epilogue column half.
 int64_t lse_parts(int64_t N, int bn) { return (N + bn - 1) / bn * epi_halves(bn); }
+
+// The GEMM tile width (columns per CTA tile) of a call: for the logsumexp
+// chain the width lse_tile_width picks; otherwise 256 columns when that gives
+// every SM at least one tile, else 128 or 64 (small M), trading per-tile
+// efficiency for parallelism; a fused 128-column GroupNorm group (gw = 128)
+// always takes 256-column tiles (a warp's half-tile is one group).  gw is the
+// fused epilogue's group width, 0 for the other epilogues.  The dispatch and
+// gf_linear_tile_width both use this function.
+int linear_tile_width(bool lse, int64_t M, int64_t N, int gw, int32_t mode, int sm_count) {
+  if (lse) return lse_tile_width(M, N, sm_count, mode);
+  if (gw == 128) return 256;
+  const int64_t mb = (M + kBM - 1) / kBM;
+  if (mb * ((N + 255) / 256) >= sm_count) return 256;
+  if (mb * ((N + 127) / 128) >= sm_count) return 128;
+  return 64;
+}
+
+// Group widths the GEMM epilogue normalises itself (others: gn_rows_kernel).
+bool gn_fused_width(int64_t gw) { return gw == 16 || gw == 32 || gw == 64 || gw == 128; }
 
 bool mode_ok(int32_t mode) {
   return mode == GF_MODE_FP32_3XTF32 || mode == GF_MODE_BF16 || mode == GF_MODE_FP32_3XBF16;
@@ -456,8 +527,10 @@ size_t operand_ws_bytes(int64_t rows, int64_t K, int32_t mode) {
   }
 }
 
+// M = 0 (an empty batch) passes: the entry points then return GF_OK
+// without launching anything.
 gf_status check_linear_shape(int64_t M, int64_t K, int64_t N, int32_t mode) {
-  if (M < 1 || K < 1 || N < 1) return GF_ERR_SHAPE;
+  if (M < 0 || K < 1 || N < 1) return GF_ERR_SHAPE;
   // (a K that is not a whole number of 16-byte rows is padded by the
   // pre-pass: kpad)
   (void)mode;
@@ -559,6 +632,10 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
   src.num_mb = int((M + kBM - 1) / kBM);
   src.num_nb = int((N + BN - 1) / BN);
   src.num_kb = int((K + Op::kBK - 1) / Op::kBK);
+  if constexpr (epi_chunked<Epi, Op, BN>())
+    src.kb_chunk = Epi::kChunkK / Op::kBK;  // (kChunkK is a multiple of kBK in every mode)
+  else
+    src.kb_chunk = src.num_kb;
   src.bn = BN;
   src.bk = Op::kBK;
   src.m_fastest = m_fastest;
@@ -566,32 +643,27 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
   return launch_gemm<BN, Op, LinearSrc, Epi>(dev, maps, src, tiles, ep, stream);
 }
 
-// Tile width: 256 columns when that gives every SM at least one tile;
-// otherwise (small M) 128 or 64, trading per-tile efficiency for parallelism.
-// The LSE partials' layout follows the tile width, which lse_tile_width picks
-// (160, 224 or 256 columns).
+// Runs the GEMM at the tile width linear_tile_width picks.  The LSE
+// partials' layout follows the tile width (the caller sized them with the
+// same function); a fused epilogue's groups must not straddle warps
+// (Epi::kMinBN).
 template <class Op, class Epi>
 gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
                              int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
+  const int32_t mode = Op::kProducts == 1 ? GF_MODE_BF16 : GF_MODE_FP32_3XTF32;  // (only BF16 or not matters)
   if constexpr (Epi::kFixedBN) {
-    // the LSE partials: the width lse_tile_width picks (the caller sized
-    // the partials with it)
-    switch (lse_tile_width(M, N, dev.sm_count, Op::kProducts == 1 ? GF_MODE_BF16 : GF_MODE_FP32_3XTF32)) {
+    switch (linear_tile_width(true, M, N, 0, mode, dev.sm_count)) {
       case 160: return run_linear_gemm<160, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
       case 224: return run_linear_gemm<224, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
       default: return run_linear_gemm<kBNLinear, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
     }
+  } else if constexpr (Epi::kMinBN > 128) {
+    return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
   } else {
-    const int64_t mb = (M + kBM - 1) / kBM;
-    // (the epilogue's groups must not straddle warps: Epi::kMinBN)
-    if constexpr (Epi::kMinBN > 128) {
-      return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-    } else {
-      if (mb * ((N + 255) / 256) >= dev.sm_count)
-        return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-      if (mb * ((N + 127) / 128) >= dev.sm_count)
-        return run_linear_gemm<128, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
-      return run_linear_gemm<64, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+    switch (linear_tile_width(false, M, N, Epi::kTileGW, mode, dev.sm_count)) {
+      case 256: return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+      case 128: return run_linear_gemm<128, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
+      default: return run_linear_gemm<64, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
     }
   }
 }
@@ -627,9 +699,23 @@ using namespace gf;
 
 extern "C" {
 
+int32_t gf_linear_tile_width(int32_t chain, int64_t M, int64_t N, int32_t groups, int32_t mode, int32_t sm_count) {
+  if (!mode_ok(mode) || sm_count < 1 || M < 0 || N < 1) return 0;
+  switch (chain) {
+    case GF_CHAIN_GROUPNORM: {
+      if (!gn_groups_ok(N, groups)) return 0;
+      const int64_t gw = N / groups;
+      return linear_tile_width(false, M, N, gn_fused_width(gw) ? int(gw) : 0, mode, sm_count);
+    }
+    case GF_CHAIN_LSE: return linear_tile_width(true, M, N, 0, mode, sm_count);
+    case GF_CHAIN_LINEAR: return linear_tile_width(false, M, N, 0, mode, sm_count);
+    default: return 0;
+  }
+}
+
 size_t gf_linear_swish_bias_groupnorm_workspace_size(int64_t M, int64_t K, int64_t N, int32_t groups,
                                                      int32_t mode) {
-  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || !gn_groups_ok(N, groups)) return 0;
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || !gn_groups_ok(N, groups) || M == 0) return 0;
   return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode);
 }
 
@@ -649,7 +735,8 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
                                                 const float* bias, const float* gamma, const float* beta, float* out,
                                                 int64_t M, int64_t K, int64_t N, int32_t groups, float eps,
                                                 void* stream) {
-  if (!x_planes || !W_planes || !bias || !gamma || !beta || !out) return GF_ERR_NULL;
+  // (an empty batch, M = 0, may pass NULL for x_planes and out)
+  if ((M && (!x_planes || !out)) || !W_planes || !bias || !gamma || !beta) return GF_ERR_NULL;
   gf_status st = check_linear_shape(M, K, N, GF_MODE_FP32_3XTF32);
   if (st != GF_OK) return st;
   if (K % 4) return GF_ERR_SHAPE;  // the caller's planes are read with K-wide rows
@@ -658,6 +745,7 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
   if (!aligned16(x_planes) || !aligned16(W_planes) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       !aligned16(out) || (b_lin && !aligned16(b_lin)))
     return GF_ERR_ALIGN;
+  if (M == 0) return GF_OK;
   const Span ins[] = {{x_planes, size_t(M) * K * 8}, {W_planes, size_t(N) * K * 8}, {b_lin, size_t(N) * 4},
                       {bias, size_t(N) * 4},         {gamma, size_t(N) * 4},         {beta, size_t(N) * 4}};
   st = check_no_alias(Span{out, size_t(M) * N * 4}, ins, 6);
@@ -676,7 +764,7 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
                                          const float* gamma, const float* beta, float* out, int64_t M,
                                          int64_t K, int64_t N, int32_t groups, float eps, int32_t mode,
                                          void* workspace, size_t workspace_bytes, void* stream) {
-  if (!x || !W || !bias || !gamma || !beta || !out) return GF_ERR_NULL;
+  if ((M && (!x || !out)) || !W || !bias || !gamma || !beta) return GF_ERR_NULL;
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
@@ -685,6 +773,7 @@ gf_status gf_linear_swish_bias_groupnorm(const float* x, const float* W, const f
   if (!aligned16(x) || !aligned16(W) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       !aligned16(out) || (b_lin && !aligned16(b_lin)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
+  if (M == 0) return GF_OK;  // an empty batch: nothing to compute
   const size_t need = gf_linear_swish_bias_groupnorm_workspace_size(M, K, N, groups, mode);
   if (!workspace) return GF_ERR_NULL;
   if (workspace_bytes < need) return GF_ERR_WORKSPACE;
@@ -747,11 +836,160 @@ HostWs host_ws(int64_t chunk, int64_t K, int64_t N, int32_t mode) {
   return w;
 }
 
+// The host-buffer pipeline's schedule, kept apart from the CUDA calls that
+// carry it out (HostPipeOps), so that its error path can be run without a
+// GPU.  Chunk i uses staging buffer i % 2: its copy-in waits until the
+// compute of chunk i - 2 has read that buffer, its compute waits for its own
+// copy-in and for the copy-out of chunk i - 2 (same output buffer), its
+// copy-out waits for its compute.  Every step returns false when one of its
+// CUDA calls fails; then nothing more is enqueued and drain() blocks until
+// the copies already queued on the internal streams have finished, so that
+// none of them touches the caller's host buffers after the call returns.
+struct HostPipeOps {
+  virtual bool setup() = 0;                  // the weight's operand planes, on the caller's stream
+  virtual bool copy_in(int64_t i, int buf) = 0;
+  virtual bool compute(int64_t i, int buf) = 0;
+  virtual bool copy_out(int64_t i, int buf) = 0;
+  virtual bool join() = 0;                   // the caller's stream waits for the last copy-outs
+  virtual void drain() = 0;                  // error path: wait for everything already queued
+  virtual ~HostPipeOps() = default;
+};
+
+gf_status run_host_pipeline(HostPipeOps& ops, int64_t nchunks) {
+  bool ok = ops.setup();
+  for (int64_t i = 0; ok && i < nchunks; ++i) {
+    const int buf = int(i & 1);
+    ok = ops.copy_in(i, buf) && ops.compute(i, buf) && ops.copy_out(i, buf);
+  }
+  if (ok) ok = ops.join();
+  if (!ok) ops.drain();
+  return ok ? GF_OK : GF_ERR_CUDA;
+}
+
+// The CUDA side: two internal copy streams and the events that order the
+// three stages, created by the call and released at its end (their resources
+// go once the enqueued work completes).
+struct CudaHostPipe final : HostPipeOps {
+  // inputs of the call
+  const float* x_host;
+  float* out_host;
+  const float *W, *b_lin, *bias, *gamma, *beta;
+  int64_t M, K, N, chunk;
+  int32_t groups, mode;
+  float eps;
+  uint8_t* ws;
+  HostWs wl;
+  DeviceInfo dev;
+  cudaStream_t s;
+  // owned
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
+  Planes wp{};
+
+  bool create() {
+    bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < 2; ++i)
+      ok = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+    return ok;
+  }
+  ~CudaHostPipe() override {
+    for (int i = 0; i < 2; ++i) {
+      if (ev_in[i]) cudaEventDestroy(ev_in[i]);
+      if (ev_comp[i]) cudaEventDestroy(ev_comp[i]);
+      if (ev_out[i]) cudaEventDestroy(ev_out[i]);
+    }
+    if (ev_start) cudaEventDestroy(ev_start);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+  }
+  int64_t rows_of(int64_t i) const { return (M - i * chunk) < chunk ? (M - i * chunk) : chunk; }
+
+  bool setup() override {
+    // the copy streams start after everything already queued on `stream`
+    return cudaEventRecord(ev_start, s) == cudaSuccess && cudaStreamWaitEvent(s_in, ev_start, 0) == cudaSuccess &&
+           cudaStreamWaitEvent(s_out, ev_start, 0) == cudaSuccess &&
+           prepare_operand(W, N, K, mode, ws + wl.w_planes, dev, s, &wp) == GF_OK;
+  }
+  bool copy_in(int64_t i, int buf) override {
+    float* xd = reinterpret_cast<float*>(ws + wl.x[buf]);
+    return cudaStreamWaitEvent(s_in, ev_comp[buf], 0) == cudaSuccess &&
+           cudaMemcpyAsync(xd, x_host + size_t(i * chunk) * K, size_t(rows_of(i)) * K * 4, cudaMemcpyHostToDevice,
+                           s_in) == cudaSuccess &&
+           cudaEventRecord(ev_in[buf], s_in) == cudaSuccess;
+  }
+  bool compute(int64_t i, int buf) override {
+    if (cudaStreamWaitEvent(s, ev_in[buf], 0) != cudaSuccess || cudaStreamWaitEvent(s, ev_out[buf], 0) != cudaSuccess)
+      return false;
+    const int64_t rows = rows_of(i);
+    const float* xd = reinterpret_cast<const float*>(ws + wl.x[buf]);
+    float* od = reinterpret_cast<float*>(ws + wl.out[buf]);
+    Planes xp{};
+    const GNParams ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps, int(N / groups)};
+    return prepare_operand(xd, rows, K, mode, ws + wl.xp[buf], dev, s, &xp) == GF_OK &&
+           with_gn_epilogue(ep, s, [&](auto tag) {
+             return run_linear<typename decltype(tag)::type>(mode, dev, xp, wp, rows, kpad(K, mode), N, 0, ep, s);
+           }) == GF_OK &&
+           cudaEventRecord(ev_comp[buf], s) == cudaSuccess;
+  }
+  bool copy_out(int64_t i, int buf) override {
+    const float* od = reinterpret_cast<const float*>(ws + wl.out[buf]);
+    return cudaStreamWaitEvent(s_out, ev_comp[buf], 0) == cudaSuccess &&
+           cudaMemcpyAsync(out_host + size_t(i * chunk) * N, od, size_t(rows_of(i)) * N * 4, cudaMemcpyDeviceToHost,
+                           s_out) == cudaSuccess &&
+           cudaEventRecord(ev_out[buf], s_out) == cudaSuccess;
+  }
+  bool join() override {
+    return cudaStreamWaitEvent(s, ev_out[0], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev_out[1], 0) == cudaSuccess;
+  }
+  void drain() override {
+    // blocks until the internal streams are idle (their copies wait on the
+    // computes they depend on, so those finish too)
+    if (s_in) cudaStreamSynchronize(s_in);
+    if (s_out) cudaStreamSynchronize(s_out);
+  }
+};
+
+// A stand-in for the CUDA side that records each step and fails at a chosen
+// one (gf_testing_host_pipeline_trace).
+struct TraceHostPipe final : HostPipeOps {
+  int fail_at;  // index of the step that fails (-1: none)
+  int step = 0;
+  char* buf;
+  size_t cap, len = 0;
+  TraceHostPipe(int f, char* b, size_t c) : fail_at(f), buf(b), cap(c) {
+    if (buf && cap) buf[0] = 0;
+  }
+  void put(const char* name, int64_t i) {
+    char item[48];
+    const int n = i < 0 ? std::snprintf(item, sizeof item, "%s%s", len ? " " : "", name)
+                        : std::snprintf(item, sizeof item, "%s%s%lld", len ? " " : "", name, (long long)i);
+    if (buf && n > 0 && len + size_t(n) < cap) {
+      std::memcpy(buf + len, item, size_t(n) + 1);
+      len += size_t(n);
+    }
+  }
+  bool next(const char* name, int64_t i) {
+    put(name, i);
+    return step++ != fail_at;
+  }
+  bool setup() override { return next("setup", -1); }
+  bool copy_in(int64_t i, int) override { return next("in", i); }
+  bool compute(int64_t i, int) override { return next("compute", i); }
+  bool copy_out(int64_t i, int) override { return next("out", i); }
+  bool join() override { return next("join", -1); }
+  void drain() override { put("drain", -1); }
+};
+
 }  // namespace
 
 size_t gf_linear_swish_bias_groupnorm_host_workspace_size(int64_t M, int64_t K, int64_t N, int32_t groups,
                                                           int32_t mode, int64_t chunk_rows) {
-  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || !gn_groups_ok(N, groups) || chunk_rows < 0)
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || !gn_groups_ok(N, groups) || chunk_rows < 0 ||
+      M == 0)
     return 0;
   if (chunk_rows == 0) {
     DeviceInfo dev;
@@ -766,7 +1004,7 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
                                               float* out_host, int64_t M, int64_t K, int64_t N, int32_t groups,
                                               float eps, int32_t mode, int64_t chunk_rows, void* workspace,
                                               size_t workspace_bytes, void* stream) {
-  if (!x_host || !W || !bias || !gamma || !beta || !out_host) return GF_ERR_NULL;
+  if ((M && (!x_host || !out_host)) || !W || !bias || !gamma || !beta) return GF_ERR_NULL;
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
@@ -775,6 +1013,7 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
   if (!aligned16(W) || !aligned16(bias) || !aligned16(gamma) || !aligned16(beta) ||
       (b_lin && !aligned16(b_lin)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
+  if (M == 0) return GF_OK;
   DeviceInfo dev;
   if ((st = current_device(&dev)) != GF_OK) return st;
   const int64_t chunk = chunk_rows == 0 ? host_chunk_rows(M, N, dev.sm_count) : (chunk_rows < M ? chunk_rows : M);
@@ -785,90 +1024,49 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
                       {gamma, size_t(N) * 4}, {beta, size_t(N) * 4}};
   if ((st = check_no_alias(Span{workspace, wl.total}, ins, 5)) != GF_OK) return st;
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // Copy streams and the events that order the three stages; destroyed at
-  // the end of the call (their resources are released once the enqueued work
-  // completes).
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
-  auto cleanup = [&]() {
-    for (int i = 0; i < 2; ++i) {
-      if (ev_in[i]) cudaEventDestroy(ev_in[i]);
-      if (ev_comp[i]) cudaEventDestroy(ev_comp[i]);
-      if (ev_out[i]) cudaEventDestroy(ev_out[i]);
-    }
-    if (ev_start) cudaEventDestroy(ev_start);
-    if (s_in) cudaStreamDestroy(s_in);
-    if (s_out) cudaStreamDestroy(s_out);
-  };
-  bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
-  for (int i = 0; ok && i < 2; ++i)
-    ok = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&ev_out[i], cudaEventDisableTiming) == cudaSuccess;
-  if (!ok) {
-    cleanup();
-    return GF_ERR_CUDA;
-  }
+  CudaHostPipe pipe;
+  pipe.x_host = x_host;
+  pipe.out_host = out_host;
+  pipe.W = W;
+  pipe.b_lin = b_lin;
+  pipe.bias = bias;
+  pipe.gamma = gamma;
+  pipe.beta = beta;
+  pipe.M = M;
+  pipe.K = K;
+  pipe.N = N;
+  pipe.chunk = chunk;
+  pipe.groups = groups;
+  pipe.mode = mode;
+  pipe.eps = eps;
+  pipe.ws = static_cast<uint8_t*>(workspace);
+  pipe.wl = wl;
+  pipe.dev = dev;
+  pipe.s = static_cast<cudaStream_t>(stream);
+  if (!pipe.create()) return GF_ERR_CUDA;  // nothing enqueued yet
+  return run_host_pipeline(pipe, (M + chunk - 1) / chunk);
+}
 
-  // The copy streams start after everything already queued on `stream`.
-  ok = cudaEventRecord(ev_start, s) == cudaSuccess && cudaStreamWaitEvent(s_in, ev_start, 0) == cudaSuccess &&
-       cudaStreamWaitEvent(s_out, ev_start, 0) == cudaSuccess;
-  Planes wp{};
-  if (ok) ok = prepare_operand(W, N, K, mode, ws + wl.w_planes, dev, s, &wp) == GF_OK;
-  const int64_t nchunks = (M + chunk - 1) / chunk;
-  for (int64_t i = 0; ok && i < nchunks; ++i) {
-    const int bi = int(i & 1);
-    const int64_t r0 = i * chunk, rows = (M - r0) < chunk ? (M - r0) : chunk;
-    float* xd = reinterpret_cast<float*>(ws + wl.x[bi]);
-    float* od = reinterpret_cast<float*>(ws + wl.out[bi]);
-    // stage 1: x rows in (after the compute that last read this buffer)
-    ok = cudaStreamWaitEvent(s_in, ev_comp[bi], 0) == cudaSuccess &&
-         cudaMemcpyAsync(xd, x_host + size_t(r0) * K, size_t(rows) * K * 4, cudaMemcpyHostToDevice, s_in) ==
-             cudaSuccess &&
-         cudaEventRecord(ev_in[bi], s_in) == cudaSuccess;
-    // stage 2: split + fused GEMM on the caller's stream (after the copy-out
-    // that last read this output buffer)
-    if (ok)
-      ok = cudaStreamWaitEvent(s, ev_in[bi], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev_out[bi], 0) == cudaSuccess;
-    if (ok) {
-      Planes xp{};
-      const GNParams ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps, int(N / groups)};
-      ok = prepare_operand(xd, rows, K, mode, ws + wl.xp[bi], dev, s, &xp) == GF_OK &&
-           with_gn_epilogue(ep, s, [&](auto tag) {
-             return run_linear<typename decltype(tag)::type>(mode, dev, xp, wp, rows, kpad(K, mode), N, 0, ep, s);
-           }) == GF_OK &&
-           cudaEventRecord(ev_comp[bi], s) == cudaSuccess;
-    }
-    // stage 3: out rows back
-    if (ok)
-      ok = cudaStreamWaitEvent(s_out, ev_comp[bi], 0) == cudaSuccess &&
-           cudaMemcpyAsync(out_host + size_t(r0) * N, od, size_t(rows) * N * 4, cudaMemcpyDeviceToHost, s_out) ==
-               cudaSuccess &&
-           cudaEventRecord(ev_out[bi], s_out) == cudaSuccess;
-  }
-  // The caller's stream completes only after the last copy-out.
-  if (ok) ok = cudaStreamWaitEvent(s, ev_out[0], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev_out[1], 0) == cudaSuccess;
-  cleanup();
-  return ok ? GF_OK : GF_ERR_CUDA;
+gf_status gf_testing_host_pipeline_trace(int64_t nchunks, int32_t fail_at, char* trace, size_t trace_bytes) {
+  if (nchunks < 0) return GF_ERR_SHAPE;
+  TraceHostPipe pipe(fail_at, trace, trace_bytes);
+  return run_host_pipeline(pipe, nchunks);
 }
 
 size_t gf_linear_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {
-  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || M == 0) return 0;
   return operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode);
 }
 
 gf_status gf_linear(const float* x, const float* W, const float* b, float* out, int64_t M, int64_t K, int64_t N,
                     int32_t mode, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!x || !W || !out) return GF_ERR_NULL;
+  if ((M && (!x || !out)) || !W) return GF_ERR_NULL;
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
   if (!aligned16(x) || !aligned16(W) || !aligned16(out) || (b && !aligned16(b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
+  if (M == 0) return GF_OK;
   const size_t need = gf_linear_workspace_size(M, K, N, mode);
   if (!workspace) return GF_ERR_NULL;
   if (workspace_bytes < need) return GF_ERR_WORKSPACE;
@@ -881,7 +1079,7 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
 }
 
 size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode) {
-  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK) return 0;
+  if (!mode_ok(mode) || check_linear_shape(M, K, N, mode) != GF_OK || M == 0) return 0;
   // one (max, sum) partial per row and epilogue column half of each n-block,
   // sized for the narrowest tile width
   const int64_t nb = lse_parts(N, kLseWidths[0]);
@@ -892,13 +1090,14 @@ size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t
 gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, float* out, int64_t M, int64_t K,
                             int64_t N, float negative_slope, int32_t mode, void* workspace, size_t workspace_bytes,
                             void* stream) {
-  if (!x || !W || !out) return GF_ERR_NULL;
+  if ((M && (!x || !out)) || !W) return GF_ERR_NULL;
   if (!mode_ok(mode)) return GF_ERR_MODE;
   gf_status st = check_linear_shape(M, K, N, mode);
   if (st != GF_OK) return st;
   if (!std::isfinite(negative_slope)) return GF_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(W) || !aligned16(out) || (b && !aligned16(b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
+  if (M == 0) return GF_OK;
   const size_t need = gf_linear_lse_act_workspace_size(M, K, N, mode);
   if (!workspace) return GF_ERR_NULL;
   if (workspace_bytes < need) return GF_ERR_WORKSPACE;
@@ -910,7 +1109,7 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
   float2* part = reinterpret_cast<float2*>(ws + operand_ws_bytes(M, K, mode) + operand_ws_bytes(N, K, mode));
   DeviceInfo dev;
   if ((st = current_device(&dev)) != GF_OK) return st;
-  const int nb = int(lse_parts(N, lse_tile_width(M, N, dev.sm_count, mode)));
+  const int nb = int(lse_parts(N, linear_tile_width(true, M, N, 0, mode, dev.sm_count)));
   EpiLSEPartial::Params ep{b, part, int(M), int(N), nb};
   // m-blocks fastest: the CTAs in flight share n-blocks, so each W tile is
   // fetched from HBM once and reused by every m-block from L2.

@@ -99,6 +99,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return kSleep ? mbar_wait_slow_sleep(bar, parity) : mbar_wait_slow(bar, parity);
 }
 
+// The same bounded wait, entirely inline: for a caller that holds many live
+// registers across the wait (a call to the out-of-line slow path would have
+// to save them to local memory).
+__device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -38,6 +38,24 @@ def _uniform(rng, shape, lo, hi):
     return a
 
 
+def _draw_x(rng, shape, dist):
+    if dist == "normal":
+        return _normal(rng, shape)
+    if dist == "uniform01":
+        return _uniform(rng, shape, 0.0, 1.0)
+    raise ValueError(dist)
+
+
+def _draw_w(rng, shape, dist, bound):
+    if dist == "default":
+        return _uniform(rng, shape, -bound, bound)
+    if dist == "normal":
+        return _normal(rng, shape)
+    if dist == "uniform01":
+        return _uniform(rng, shape, 0.0, 1.0)
+    raise ValueError(dist)
+
+
 # --------------------------------------------------------------- recipes
 @dataclasses.dataclass(frozen=True)
 class LinearGNShape:
@@ -49,13 +67,19 @@ class LinearGNShape:
     eps: float = 1e-5
 
 
-def linear_gn_inputs(shape: LinearGNShape, seed: int):
+def linear_gn_inputs(shape: LinearGNShape, seed: int, x_dist: str = "normal", w_dist: str = "default"):
     """x ~ N(0,1); W, b_lin ~ U(+-1/sqrt(K)); bias ~ N(0,1);
-    gamma ~ U(0.5, 1.5); beta ~ N(0, 0.1).  Drawn in that order."""
+    gamma ~ U(0.5, 1.5); beta ~ N(0, 0.1).  Drawn in that order.
+
+    Stress variants: ``x_dist="uniform01"`` draws x ~ U[0,1) (the torch.rand
+    inputs that page Kimi-K2.6__l2_p37 reasons about in turn 1);
+    ``w_dist="normal"`` draws W ~ N(0,1) (that page's other assumption in the
+    same turn), ``w_dist="uniform01"`` W ~ U[0,1) (page Kimi-K2.6__l2_p64's
+    all-uniform case, turn 1).  b_lin keeps its default distribution."""
     r = _rng(seed)
     bound = 1.0 / math.sqrt(shape.K)
-    x = _normal(r, (shape.M, shape.K))
-    W = _uniform(r, (shape.N, shape.K), -bound, bound)
+    x = _draw_x(r, (shape.M, shape.K), x_dist)
+    W = _draw_w(r, (shape.N, shape.K), w_dist, bound)
     b_lin = _uniform(r, (shape.N,), -bound, bound)
     bias = _normal(r, (shape.N,))
     gamma = _uniform(r, (shape.N,), 0.5, 1.5)
@@ -72,14 +96,25 @@ class LinearLSEShape:
     negative_slope: float = 0.01
 
 
-def linear_lse_inputs(shape: LinearLSEShape, seed: int, bias_shift: float = 0.0):
+def linear_lse_inputs(shape: LinearLSEShape, seed: int, bias_shift: float = 0.0, dist: str = "default"):
     """x ~ N(0,1); W, b ~ U(+-1/sqrt(K)), drawn in that order.  ``bias_shift``
-    adds a constant to b (used to reach the negative LeakyReLU branch)."""
+    adds a constant to b (used to reach the negative LeakyReLU branch).
+
+    ``dist="uniform01"`` draws x, W and b ~ U[0,1) instead: the all-uniform
+    case page Kimi-K2.6__l2_p64 reasons about in turn 1, where every logit is
+    a sum of K products of mean 1/4, so logsumexp lands in the thousands."""
     r = _rng(seed)
     bound = 1.0 / math.sqrt(shape.K)
-    x = _normal(r, (shape.M, shape.K))
-    W = _uniform(r, (shape.N, shape.K), -bound, bound)
-    b = _uniform(r, (shape.N,), -bound, bound)
+    if dist == "default":
+        x = _normal(r, (shape.M, shape.K))
+        W = _uniform(r, (shape.N, shape.K), -bound, bound)
+        b = _uniform(r, (shape.N,), -bound, bound)
+    elif dist == "uniform01":
+        x = _uniform(r, (shape.M, shape.K), 0.0, 1.0)
+        W = _uniform(r, (shape.N, shape.K), 0.0, 1.0)
+        b = _uniform(r, (shape.N,), 0.0, 1.0)
+    else:
+        raise ValueError(dist)
     if bias_shift:
         b += np.float32(bias_shift)
     return dict(x=x, W=W, b=b)

@@ -27,6 +27,12 @@
  *   - Arguments are validated before anything is launched; a rejected call
  *     launches nothing and returns a negative gf_status.  No C++ exception
  *     crosses this boundary.
+ *   - An empty batch (M = 0 for the Linear chains, B = 0 for the Conv1d
+ *     chain, N = 0 for the ConvTranspose3d chain) is valid: the other sizes
+ *     are still checked, the batch-sized pointers (x and out) may then be
+ *     NULL, the workspace queries return 0, and the call launches nothing
+ *     and returns GF_OK, as the pages' PyTorch modules return an empty
+ *     output for an empty batch.
  *   - `out` must not overlap any input or the workspace (GF_ERR_ALIAS).
  *   - Device-side errors (a bounded wait inside a kernel that ran out) are
  *     recorded in a device status word; gf_device_status() reads it.
@@ -77,6 +83,11 @@ typedef int32_t gf_status;
  * erf form.  Other calls reject it (GF_ERR_MODE). */
 #define GF_FLAG_GELU_TANH 0x100
 
+/* Chains whose GEMM tile width gf_linear_tile_width reports. */
+#define GF_CHAIN_GROUPNORM 0  /* gf_linear_swish_bias_groupnorm (and _planes, _host) */
+#define GF_CHAIN_LSE       1  /* gf_linear_lse_act                                    */
+#define GF_CHAIN_LINEAR    2  /* gf_linear                                            */
+
 /* Version of this ABI (bumped on any signature change). */
 int32_t gf_abi_version(void);
 
@@ -101,13 +112,23 @@ gf_status gf_device_status(int32_t* device_bits);
 gf_status gf_profile_begin(int32_t max_calls);
 gf_status gf_profile_end(int32_t* calls, float* total_ms);
 
+/* Measures the tensor pipe's dense rate on this GPU: one CTA per SM issues
+ * tcgen05.mma instructions back to back (128 x 256 fp32 accumulator in TMEM,
+ * operands already in shared memory, nothing loaded or stored) for `iters`
+ * rounds of four K-steps, kind 0 = kind::tf32, 1 = kind::f16 with BF16
+ * operands.  Launches once to warm up, then `repeats` times on an internal
+ * stream, waits for them, and writes the best rate in TFLOP/s (2 M N K per
+ * instruction) into *tflops.  A measurement utility (it synchronises), not
+ * part of any operator.  Supported: 1 <= iters <= 65536, 1 <= repeats <= 100. */
+gf_status gf_measure_tensor_rate(int32_t kind, int32_t iters, int32_t repeats, double* tflops);
+
 /* ------------------------------------------------------------------------
  * Linear alone: out[m,n] = sum_k x[m,k] * W[n,k] + b[n]
  *
  * The contraction step shared by the two Linear chains (nn.Linear / addmm,
  * page Kimi-K2.6__l2_p37 turn 1 and page Kimi-K2.6__l2_p64 turn 1), exposed
  * so that it can be checked on its own.  x [M,K], W [N,K], b [N] (may be
- * NULL), out [M,N].  Supported: M, K, N >= 1 (a K that is not a multiple of
+ * NULL), out [M,N].  Supported: M >= 0, K, N >= 1 (a K that is not a multiple of
  * 4 fp32 / 8 bf16 elements is zero-padded in the workspace's operand planes).
  * With integer-valued x and W (|v| <= 2^11) and |out| < 2^24 the result is
  * exact.
@@ -127,7 +148,7 @@ gf_status gf_linear(const float* x, const float* W, const float* b, float* out, 
  *
  *   x [M,K], W [N,K] (nn.Linear layout), b_lin/bias/gamma/beta [N], out [M,N].
  *   b_lin may be NULL (no linear bias).
- *   Supported: M, K >= 1 (K padded as for gf_linear),
+ *   Supported: M >= 0, K >= 1 (K padded as for gf_linear),
  *   groups >= 1 with N % groups == 0.  Group widths N/groups of 16, 32, 64
  *   and 128 run inside the GEMM epilogue (groups of 128 on 256-column
  *   tiles); any other width stores t and normalises the rows in a second
@@ -163,9 +184,11 @@ gf_status gf_linear_swish_bias_groupnorm_planes(const float* x_planes, const flo
  * out_host is complete when `stream` reaches that point (synchronise it
  * before reading).  Workspace: the matching *_host_workspace_size() query.
  * The internal streams and events are created and released by each call.
- * A GF_ERR_CUDA returned after work was enqueued leaves copies already queued
- * on the internal streams running: synchronise the device before reusing
- * x_host, out_host or the workspace. */
+ * If a CUDA call fails after work was enqueued, the call stops enqueuing,
+ * blocks until the copies already queued on its internal streams have
+ * finished (and the computes they wait on), then returns GF_ERR_CUDA: no copy
+ * of this call reads x_host or writes out_host after it returns, and rows
+ * whose chunks were not reached are left as they were. */
 size_t gf_linear_swish_bias_groupnorm_host_workspace_size(int64_t M, int64_t K, int64_t N,
                                                           int32_t groups, int32_t mode,
                                                           int64_t chunk_rows);
@@ -175,6 +198,26 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
                                               int32_t groups, float eps, int32_t mode,
                                               int64_t chunk_rows, void* workspace,
                                               size_t workspace_bytes, void* stream);
+
+/* The GEMM tile width (output columns per CTA tile: 64, 128 or 256, or
+ * 160, 224 or 256 for GF_CHAIN_LSE) that the chain's dispatch picks for a
+ * call of M rows and N output columns in `mode` (for GF_CHAIN_GROUPNORM with
+ * `groups` groups; ignored otherwise) on a GPU with sm_count SMs.  Pure host
+ * arithmetic (no device call), the same function the dispatch uses; 0 for
+ * invalid arguments.  Lets tests check that every kernel variant the dispatch
+ * can reach is exercised. */
+int32_t gf_linear_tile_width(int32_t chain, int64_t M, int64_t N, int32_t groups, int32_t mode,
+                             int32_t sm_count);
+
+/* Testing hook of the host-buffer pipeline's schedule: runs the schedule of
+ * gf_linear_swish_bias_groupnorm_host for nchunks chunks with the CUDA calls
+ * replaced by a recorder, making step number fail_at (counted from 0; -1:
+ * none) fail as a failed CUDA call would.  Writes the steps taken, separated
+ * by spaces ("setup in0 compute0 out0 ... join", "drain" after a failure),
+ * into trace (NUL-terminated, truncated to trace_bytes) and returns the
+ * status the real call would return.  Touches no device. */
+gf_status gf_testing_host_pipeline_trace(int64_t nchunks, int32_t fail_at, char* trace,
+                                         size_t trace_bytes);
 
 /* Splits n fp32 values (n % 4 == 0) into the two planes the 3xTF32
  * contraction reads: planes[0][i] = src[i] with its 13 low mantissa bits
@@ -192,7 +235,7 @@ gf_status gf_tf32_split(const float* src, float* planes, int64_t n, void* stream
  *   out[m]  = gelu(gelu(a)),    gelu(v) = v * Phi(v)   (exact, erf form)
  *
  *   x [M,K], W [N,K], b [N] (may be NULL), out [M,1].
- *   Supported: M, K, N >= 1 (K padded as for gf_linear).
+ *   Supported: M >= 0, K, N >= 1 (K padded as for gf_linear).
  * ---------------------------------------------------------------------- */
 size_t gf_linear_lse_act_workspace_size(int64_t M, int64_t K, int64_t N, int32_t mode);
 gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, float* out,
@@ -282,25 +325,31 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
  * workspace.
  *
  * Same operator, arguments (minus workspace), supported shapes and result as
- * gf_convt3d_swish_gn_hswish (the pages' configuration on the CUDA-core
- * two-pass kernels).  The caller still owns and passes x, w, b,
- * gamma, beta and out.  The scratch (the per-block GroupNorm sums and the
- * per-channel affine coefficients, gf_convt3d_swish_gn_hswish_workspace_size()
- * bytes) lives in a fixed array inside the library, 4 MiB
- * (gf_convt3d_noalloc_scratch_limit()) on every GPU that loads the library,
- * held until the process exits.  Shapes that need more return
- * GF_ERR_WORKSPACE before anything is launched.  No call allocates: the
- * entry point calls no cudaMalloc, cudaFree or allocating library routine.
+ * gf_convt3d_swish_gn_hswish (up to rounding: the pages' configuration runs
+ * on the CUDA-core two-pass kernels here, not on the tensor-core kernels the
+ * workspace entry point uses for Cin <= 4).  The caller still owns and passes
+ * x, w, b, gamma, beta and out.  The scratch (the per-block GroupNorm sums and
+ * the per-channel affine coefficients) lives in a fixed array inside the
+ * library, 4 MiB (gf_convt3d_noalloc_scratch_limit()) on every GPU that loads
+ * the library, held until the process exits.  The bytes a shape needs are
+ * what gf_convt3d_swish_gn_hswish_noalloc_scratch_size() returns (NOT the
+ * workspace entry point's query, whose kernels differ); shapes that need more
+ * than the limit return GF_ERR_WORKSPACE before anything is launched.  No call
+ * allocates: the entry point calls no cudaMalloc, cudaFree or allocating
+ * library routine.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call on a device uses the same array and leaves its
- * contents behind; the kernels overwrite all of it that they read, so nothing
- * needs clearing between calls.  Two calls whose kernels overlap on the GPU
- * (different streams, no ordering between them) race on the array: order
- * them, e.g. by issuing them on one stream.
+ * device and CUDA context, with that device current); make that first call
+ * before any stream capture.  Every call on a device uses the same array and
+ * leaves its contents behind; the kernels overwrite all of it that they read,
+ * so nothing needs clearing between calls.  Two calls whose kernels overlap
+ * on the GPU (different streams, no ordering between them) race on the
+ * array: order them, e.g. by issuing them on one stream.
  * ---------------------------------------------------------------------- */
 size_t gf_convt3d_noalloc_scratch_limit(void);
+size_t gf_convt3d_swish_gn_hswish_noalloc_scratch_size(int64_t N, int64_t Cin, int64_t Cout,
+                                                       int64_t D, int64_t H, int64_t W, int32_t k,
+                                                       int32_t stride, int32_t pad, int32_t groups);
 gf_status gf_convt3d_swish_gn_hswish_noalloc(const float* x, const float* w, const float* b,
                                              const float* gamma, const float* beta, float* out,
                                              int64_t N, int64_t Cin, int64_t Cout, int64_t D,

@@ -17,6 +17,7 @@ def L():
 
 
 GF_OK, GF_ERR_NULL, GF_ERR_SHAPE, GF_ERR_ALIGN, GF_ERR_ALIAS, GF_ERR_WORKSPACE, GF_ERR_MODE = 0, -1, -2, -3, -4, -5, -6
+GF_ERR_CUDA = -7
 
 # Fake, 256-byte aligned, far-apart "device addresses" (never dereferenced:
 # every call below fails validation first).
@@ -57,7 +58,7 @@ def test_linear_gn_validation(L):
     assert _lgn(L, groups=8192) == GF_ERR_SHAPE
     assert _lgn(L, groups=0) == GF_ERR_SHAPE
     assert _lgn(L, K=0) == GF_ERR_SHAPE
-    assert _lgn(L, M=0) == GF_ERR_SHAPE
+    assert _lgn(L, M=-1) == GF_ERR_SHAPE
     assert _lgn(L, eps=float("nan")) == GF_ERR_SHAPE
     assert _lgn(L, eps=-1.0) == GF_ERR_SHAPE
     assert _lgn(L, x=P[0] + 4) == GF_ERR_ALIGN
@@ -220,3 +221,116 @@ def test_binding_signatures_match_the_header_prototypes():
         for i, (p, a) in enumerate(zip(ps, args)):
             assert kind(p) == ckind(a), (name, i, p, a)
         assert kind(ret) == ckind(res), (name, ret, res)
+
+
+# ------------------------------------------------------------ empty batches
+def test_empty_batches_launch_nothing(L):
+    # M / B / N = 0 is an empty batch: GF_OK before any device call (so it
+    # passes here, without a GPU), NULL x and out allowed, workspace query 0;
+    # the other arguments are still checked
+    assert L.gf_linear_swish_bias_groupnorm_workspace_size(0, 1024, 4096, 64, 0) == 0
+    assert _lgn(L, M=0, x=None, out=None, ws=None, wsb=0) == GF_OK
+    assert _lgn(L, M=0, groups=3, ws=None, wsb=0) == GF_ERR_SHAPE
+    assert _lgn(L, M=0, W=None, ws=None, wsb=0) == GF_ERR_NULL
+    assert _lgn(L, M=0, mode=7, ws=None, wsb=0) == GF_ERR_MODE
+    assert L.gf_linear(None, P[1], None, None, 0, 64, 128, 0, None, 0, None) == GF_OK
+    assert L.gf_linear_workspace_size(0, 64, 128, 0) == 0
+    assert L.gf_linear_lse_act(None, P[1], P[2], None, 0, 64, 128, 0.01, 0, None, 0, None) == GF_OK
+    assert L.gf_linear_lse_act(None, P[1], P[2], None, 0, 64, 0, 0.01, 0, None, 0, None) == GF_ERR_SHAPE
+    assert L.gf_linear_lse_act_workspace_size(0, 64, 128, 0) == 0
+    assert L.gf_linear_swish_bias_groupnorm_planes(None, P[1], P[2], P[3], P[4], P[5], None, 0, 64, 256, 4, 1e-5,
+                                                   None) == GF_OK
+    assert L.gf_linear_swish_bias_groupnorm_host(None, P[1], P[2], P[3], P[4], P[5], None, 0, 64, 256, 4, 1e-5, 0, 0,
+                                                 None, 0, None) == GF_OK
+    assert L.gf_linear_swish_bias_groupnorm_host_workspace_size(0, 64, 256, 4, 0, 0) == 0
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(0, 256, 4096, 3, 0) == 0
+    assert L.gf_ln_gelu_dconv1d_res(None, P[1], P[2], P[3], P[4], None, 0, 256, 4096, 3, 4, 4, 1e-5, 0, None, 0,
+                                    None) == GF_OK
+    assert L.gf_ln_gelu_dconv1d_res(None, P[1], P[2], P[3], P[4], None, 0, 256, 4096, 3, 4, 3, 1e-5, 0, None, 0,
+                                    None) == GF_ERR_SHAPE
+    for k, s, p, G in ((3, 2, 1, 4), (4, 3, 2, 8)):
+        assert L.gf_convt3d_swish_gn_hswish_workspace_size(0, 3, 16, 16, 32, 32, k, s, p, G) == 0
+        assert L.gf_convt3d_swish_gn_hswish(None, P[1], P[2], P[3], P[4], None, 0, 3, 16, 16, 32, 32, k, s, p, G,
+                                            1e-5, None, 0, None) == GF_OK
+        assert L.gf_convt3d_swish_gn_hswish_noalloc(None, P[1], P[2], P[3], P[4], None, 0, 3, 16, 16, 32, 32, k, s,
+                                                    p, G, 1e-5, None) == GF_OK
+    assert L.gf_convt3d_swish_gn_hswish(None, P[1], P[2], P[3], P[4], None, 0, 3, 16, 16, 32, 32, 3, 2, 1, 3,
+                                        1e-5, None, 0, None) == GF_ERR_SHAPE  # 16 channels in 3 groups
+    assert L.gf_convt3d_swish_gn_hswish(None, P[1], P[2], P[3], P[4], None, -1, 3, 16, 16, 32, 32, 3, 2, 1, 4,
+                                        1e-5, None, 0, None) != GF_OK
+
+
+# ------------------------------------------------- dispatch tile widths
+def test_tile_width_rule(L):
+    GN, LSE, LIN = binding.GF_CHAIN_GROUPNORM, binding.GF_CHAIN_LSE, binding.GF_CHAIN_LINEAR
+    tw = L.gf_linear_tile_width
+    # 256 columns once every SM gets a tile; else 128; else 64 (152 SMs)
+    assert tw(GN, 32768, 4096, 64, 0, 152) == 256
+    assert tw(GN, 2432, 2048, 32, 0, 152) == 256       # 19 m-blocks x 8 = 152 tiles
+    assert tw(GN, 2304, 2048, 32, 0, 152) == 128       # 18 x 8 = 144 < 152
+    assert tw(GN, 1024, 4096, 64, 1, 152) == 128
+    assert tw(GN, 256, 4096, 64, 0, 152) == 64
+    assert tw(GN, 256, 4096, 32, 2, 152) == 256        # groups of 128: always 256-column tiles
+    assert tw(GN, 256, 4096, 2, 0, 152) == 64          # groups of 2048: the row kernel's width rule
+    assert tw(GN, 256, 4096, 3, 0, 152) == 0           # 3 does not divide 4096
+    assert tw(LIN, 256, 4096, 0, 0, 152) == 64
+    # logsumexp: 160 columns in the three-product modes (three smem stages,
+    # room in TMEM for the chunked accumulation's totals); the BF16 mode 224
+    # or 256, whichever needs fewer waves
+    assert tw(LSE, 1024, 8192, 0, 0, 152) == 160
+    assert tw(LSE, 1024, 8192, 0, 2, 152) == 160
+    assert tw(LSE, 128, 30000, 0, 0, 152) == 160
+    assert tw(LSE, 1024, 8192, 0, 1, 152) == 224
+    assert tw(LSE, 512, 8960, 0, 1, 152) == 256
+    assert tw(GN, 256, 4096, 64, 9, 152) == 0          # unknown mode
+    assert tw(7, 256, 4096, 64, 0, 152) == 0           # unknown chain
+    assert tw(GN, 256, 4096, 64, 0, 0) == 0
+
+
+# -------------------------------------- host pipeline schedule and errors
+def test_host_pipeline_schedule(L):
+    st, tr = binding.host_pipeline_trace(3)
+    assert st == GF_OK
+    assert tr == "setup in0 compute0 out0 in1 compute1 out1 in2 compute2 out2 join"
+    st, tr = binding.host_pipeline_trace(0)
+    assert st == GF_OK and tr == "setup join"
+
+
+@pytest.mark.parametrize("fail_at", range(0, 11))
+def test_host_pipeline_error_path_drains(L, fail_at):
+    # a failing step stops the schedule at once and the call waits for the
+    # copies already queued (drain) before it returns GF_ERR_CUDA, so none of
+    # them can touch the caller's host buffers after the return
+    st, tr = binding.host_pipeline_trace(3, fail_at)
+    steps = tr.split()
+    assert st == GF_ERR_CUDA
+    assert steps[-1] == "drain"
+    assert len(steps) == fail_at + 2          # the steps up to the failing one, then drain
+    assert "join" not in steps[:-1] or fail_at == 10
+
+
+# ------------------------------------------------ no-workspace scratch
+def test_noalloc_scratch_query_agrees_with_accept_reject(L):
+    """The no-workspace call accepts a shape exactly when
+    gf_convt3d_swish_gn_hswish_noalloc_scratch_size() is within the limit
+    (accepted calls get past validation and then fail here only for want of
+    a device)."""
+    limit = L.gf_convt3d_noalloc_scratch_limit()
+    shapes = [(128, 3, 16, 16, 32, 32, 3, 2, 1, 4),    # the pages' workload: its own kernels' scratch is small
+              (1, 3, 16, 4, 5, 6, 3, 2, 1, 4), (4000, 3, 16, 16, 32, 32, 3, 2, 1, 4), (2000, 3, 16, 16, 32, 32, 3, 2, 1, 4),
+              (3, 6, 16, 16, 32, 32, 3, 2, 1, 4), (2, 3, 8, 4, 5, 6, 4, 2, 1, 2), (3000, 3, 8, 4, 5, 6, 4, 2, 1, 2),
+              (64, 2, 32, 30, 30, 30, 3, 1, 1, 8)]
+    seen = set()
+    for sh in shapes:
+        need = L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(*sh)
+        assert need > 0, sh
+        st = L.gf_convt3d_swish_gn_hswish_noalloc(P[0], P[1], P[2], P[3], P[4], P[5], *sh, 1e-5, None)
+        assert (st == GF_ERR_WORKSPACE) == (need > limit), (sh, need, st)
+        seen.add(need > limit)
+    assert seen == {True, False}
+    # the headline workload needs far less than the workspace entry point's
+    # query reports (that one sizes the tensor-core kernels)
+    need = L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(*shapes[0])
+    assert need <= limit < L.gf_convt3d_swish_gn_hswish_workspace_size(*shapes[0])
+    assert L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(0, 3, 16, 16, 32, 32, 3, 2, 1, 4) == 0
+    assert L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(1, 3, 16, 16, 32, 32, 3, 2, 1, 3) == 0

@@ -170,6 +170,35 @@ def test_linear_gn_workload_m32768_sampled():
     assert_close(got, ref, "linear_gn M=32768 (sampled rows)")
 
 
+@pytest.mark.parametrize("w_dist", ["default", "normal"])
+def test_linear_gn_uniform01_inputs(w_dist):
+    # x ~ U[0,1) (torch.rand inputs), with the module's default weights or
+    # W ~ N(0,1): page Kimi-K2.6__l2_p37, turn 1, reasons about both
+    s = synth.LinearGNShape(M=130, K=1024, N=4096)
+    d = synth.linear_gn_inputs(s, 13, x_dist="uniform01", w_dist=w_dist)
+    got, ref = _lgn_run(s, d)
+    assert_close(got, ref, f"linear_gn U[0,1) x, {w_dist} W")
+
+
+def test_linear_gn_all_uniform_inputs():
+    # x and W ~ U[0,1) (page Kimi-K2.6__l2_p64's all-uniform case): every y is
+    # about 256 = K/4, and the tensor core's truncating fp32 accumulation
+    # biases it by about -5e-3 (a few 1e-4 apart between channels).  GroupNorm
+    # cancels the common part; the rest, over a group spread of about 5,
+    # stays within 1e-4 in the 3xBF16 mode (half the accumulation steps) and
+    # within 2e-4 in the 3xTF32 mode, whose 256-column tiles leave no TMEM for
+    # the chunked accumulation the logsumexp chain uses
+    s = synth.LinearGNShape(M=130, K=1024, N=4096)
+    d = synth.linear_gn_inputs(s, 13, x_dist="uniform01", w_dist="uniform01")
+    ref = oracle.linear_swish_bias_groupnorm(d["x"], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"], s.groups,
+                                             s.eps)
+    for mode, tol in ((2, 1e-4), (0, 2e-4)):
+        got = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), T(d["b_lin"]), T(d["bias"]), T(d["gamma"]),
+                                                T(d["beta"]), s.groups, s.eps, mode=mode).cpu().numpy()
+        err = np.abs(got.astype(np.float64) - ref)
+        assert np.all(err <= tol + tol * np.abs(ref)), (mode, float(err.max()))
+
+
 def test_linear_gn_deterministic():
     s, d = _lgn_case(512, 256, 1024, 16, 3)
     a = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), T(d["b_lin"]), T(d["bias"]), T(d["gamma"]),
@@ -207,6 +236,21 @@ def test_linear_lse_negative_branch():
     got, ref = _lse_run(s, d)
     assert np.all(ref < 0)
     assert_close(got, ref, "lse negative branch")
+
+
+def test_linear_lse_uniform01_inputs():
+    # x, W, b ~ U[0,1): every logit is a sum of 8192 products of mean 1/4,
+    # so logsumexp is about 2100 and the tiles' maxima differ by tens; the
+    # (max, sum exp) merge rescales across them (page Kimi-K2.6__l2_p64,
+    # turn 1, reasons about exactly this input)
+    s = synth.LinearLSEShape(M=160, K=8192, N=8192)
+    d = synth.linear_lse_inputs(s, 12, dist="uniform01")
+    got, ref = _lse_run(s, d)
+    assert ref.min() > 1500
+    assert_close(got, ref, "lse U[0,1) inputs")
+    # the same in the 3xBF16 mode (chunked accumulation too)
+    got = gf.gf_linear_lse_act(T(d["x"]), T(d["W"]), T(d["b"]), s.negative_slope, mode=2).cpu().numpy()
+    assert_close(got, ref, "lse U[0,1) inputs, 3xbf16")
 
 
 def test_linear_lse_workload_sampled():

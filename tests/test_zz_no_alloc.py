@@ -11,12 +11,11 @@ point gf_convt3d_swish_gn_hswish on the same inputs, within the parity
 tolerance used everywhere else (1e-4 abs + 1e-4 rel).  The file is named to be
 collected last.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from conv_activation_normalization_gb300 import binding as gf
 from conv_activation_normalization_gb300 import synth
 
@@ -56,11 +55,62 @@ def test_noalloc_matches_workspace_entry_point_two_calls(L):
     assert gf.gf_device_status() == 0
 
 
+def _close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - ref)
+    bad = ~(err <= ATOL + RTOL * np.abs(ref))
+    assert not bad.any(), f"{what}: {int(bad.sum())}/{bad.size} outside tolerance; max err {np.nanmax(err):.3g}"
+
+
+@pytest.mark.parametrize("shape", [dict(N=5, D=6, H=13, W=40), dict(N=2, Cin=6, D=3, H=9, W=17),
+                                   dict(N=2, Cin=3, Cout=8, D=4, H=5, W=6, k=4, stride=2, pad=1, groups=2)])
+def test_noalloc_matches_oracle(L, shape):
+    # the pages' configuration (Cin 3 and 6: the CUDA-core two-pass kernels)
+    # and a general shape, against the fp64 oracle itself
+    s = synth.ConvT3dShape(**shape)
+    d = synth.convt3d_inputs(s, 911 + s.N)
+    t = {k: torch.from_numpy(v).cuda() for k, v in d.items()}
+    out = gf.gf_convt3d_swish_gn_hswish_noalloc(t["x"], t["w"], t["b"], t["gamma"], t["beta"], s.stride, s.pad,
+                                                s.groups, s.eps)
+    ref = oracle.convt3d_swish_gn_hswish(d["x"], d["w"], d["b"], d["gamma"], d["beta"], s.stride, s.pad, s.groups,
+                                         s.eps)
+    _close(out.cpu().numpy(), ref, f"noalloc {shape}")
+    assert gf.gf_device_status() == 0
+
+
+def test_noalloc_full_workload_sampled_and_allocates_nothing(L):
+    # N = 128 (the benchmark workload): 0.53 MB of scratch, within the 4 MiB
+    # array; samples 0, 63 and 127 against the oracle.  After one warm-up
+    # call, a second call changes neither torch's allocated bytes nor the
+    # device's free memory.
+    s, seed = synth.WORKLOADS["convt3d_n128"]
+    need = L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(s.N, s.Cin, s.Cout, s.D, s.H, s.W, s.k, s.stride,
+                                                             s.pad, s.groups)
+    assert 0 < need <= L.gf_convt3d_noalloc_scratch_limit()
+    d = synth.convt3d_inputs(s, seed)
+    t = {k: torch.from_numpy(v).cuda() for k, v in d.items()}
+    out = torch.empty(gf.convt3d_out_shape(d["x"].shape, s.Cout, s.k, s.stride, s.pad), dtype=torch.float32,
+                      device="cuda")
+    assert _noalloc(L, t, s, out) == 0  # warm-up: the kernels are loaded
+    torch.cuda.synchronize()
+    alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+    out.fill_(float("nan"))
+    assert _noalloc(L, t, s, out) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+    idx = np.array([0, 63, 127])
+    ref = oracle.convt3d_swish_gn_hswish(d["x"][idx], d["w"], d["b"], d["gamma"], d["beta"], s.stride, s.pad,
+                                         s.groups, s.eps)
+    _close(out[idx].cpu().numpy(), ref, "noalloc full workload (samples 0, 63, 127)")
+    assert gf.gf_device_status() == 0
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch(L):
     limit = L.gf_convt3d_noalloc_scratch_limit()
     assert limit == 4 << 20
     s = synth.ConvT3dShape(N=4000)
-    need = L.gf_convt3d_swish_gn_hswish_workspace_size(s.N, s.Cin, s.Cout, s.D, s.H, s.W, 3, 2, 1, 4)
+    need = L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(s.N, s.Cin, s.Cout, s.D, s.H, s.W, 3, 2, 1, 4)
     assert need > limit
     # validation fails before any pointer is touched, so placeholders suffice
     p = [0x7F0000000000 + i * (1 << 36) for i in range(6)]
