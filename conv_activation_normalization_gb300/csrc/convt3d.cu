@@ -403,10 +403,12 @@ gf_status launch_ct_fused(const CfParams& prm, int grid, cudaStream_t s) {
   return cuda_status(e);
 }
 
-// The single-kernel path needs every CTA resident (one per SM) and a sample
-// of at most grid + 1 tiles (see convt3d_fused.cuh).
+// The single-kernel path needs every CTA resident (one per SM), a sample of at
+// most grid + 1 tiles (see convt3d_fused.cuh) and 16 channel volumes of a
+// sample within 32-bit element offsets.
 template <int CIN>
-bool ct_fused_fits(int P, int grid, int device) {
+bool ct_fused_fits(int P, int grid, int device, uint64_t plane) {
+  if (16 * plane >= (uint64_t(1) << 32)) return false;
   int coop = 0, blocks = 0;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, device) != cudaSuccess || !coop) return false;
   if (cudaFuncSetAttribute(convt3d_fused_kernel<CIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCfSmem) !=
@@ -423,7 +425,8 @@ gf_status launch_ct_tensor_core(const float* x, const float* w, const float* b, 
                                 void* ws, const DeviceInfo& dev, cudaStream_t s) {
   const int bpp = int((H * W + 127) / 128), P = int(D) * bpp, num_tiles = int(N) * P;
   const int grid = num_tiles < dev.sm_count ? num_tiles : dev.sm_count;
-  if (ct_fused_fits<CIN>(P, grid, dev.device)) {
+  const uint64_t plane = uint64_t(2 * D - 1) * uint64_t(2 * H - 1) * uint64_t(2 * W - 1);
+  if (ct_fused_fits<CIN>(P, grid, dev.device, plane)) {
     const CfWs cw = cf_ws(N, D, H, W);
     uint8_t* base = static_cast<uint8_t*>(ws);
     if (cudaMemsetAsync(base + cw.done, 0, cw.part - cw.done, s) != cudaSuccess) return GF_ERR_CUDA;
@@ -447,7 +450,11 @@ gf_status launch_ct_tensor_core(const float* x, const float* w, const float* b, 
     p.div_bpp = make_fastdiv(uint32_t(bpp));
     p.div_w = make_fastdiv(uint32_t(W));
     p.inv_count = 1.0 / (double(kCT_COUT / kCT_G) * double(2 * D - 1) * double(2 * H - 1) * double(2 * W - 1));
-    p.eps = eps;
+    // the kernel's statistics are of s' = s log2 e (see convt3d_fused.cuh)
+    p.eps = float(double(eps) * double(kLog2e) * double(kLog2e));
+    p.plane = uint32_t(plane);
+    p.OHW = int((2 * H - 1) * (2 * W - 1));
+    p.OW = int(2 * W - 1);
     return launch_ct_fused<CIN>(p, grid, s);
   }
   const CtTcWs wl = ct_tc_ws(N, D, H, W);

@@ -13,9 +13,10 @@
 //                (tcgen05.st); the tile's per-group (sum s, sum s^2) go to
 //                the tile's own slot in global memory and the sample's
 //                counter of finished tiles is incremented;
-//   round r + 3  (first thing in the round) once all tiles of t's sample
-//                are counted, the CTA sums their slots in fp64, turns the
-//                totals into the per-channel affine (A, B) and writes tile t,
+//   round r + 3  (first thing in the round) once all tiles of t's sample are
+//                counted, the CTA sums their slots (in a fixed order,
+//                double-float arithmetic), turns the totals into the
+//                per-channel affine (A, B) and writes tile t,
 //                HardSwish(A s + B), straight from TMEM; that frees buffer
 //                r % 4 for the MMAs of tile r + 4.
 //
@@ -27,15 +28,25 @@
 // r + 1 .. r + 3 and the MMA's target r + 4.  The host uses the two-pass
 // kernels when a sample has more tiles than that.
 //
-// Roles (736 threads):
-//   warps 0-3    producers, warp 4 TMEM owner and MMA issuer (as in the
-//                two-pass kernel, with 4 accumulator buffers);
+// The weights (and the conv bias) are scaled by log2 e when the B tile is
+// built, so the accumulator holds u = y log2 e and the Swish needs no scaling
+// multiply: s' = u / (1 + 2^-u) = s log2 e.  GroupNorm of s' with
+// eps (log2 e)^2 is exactly GroupNorm of s with eps (a common scale of the
+// values and of sqrt(eps) cancels).
+//
+// Roles (768 threads):
+//   warps 0-3    producers (thread = cell: gathers, A rows, and the cell's
+//                record: output offset and which of its phases exist), warp 4
+//                TMEM owner and MMA issuer (as in the two-pass kernel, with 4
+//                accumulator buffers);
 //   warp 5       publisher: per round, sums the epilogue warps' partial sums
 //                into the tile's slot and counts the tile for its sample;
-//   warp 6       coefficients: per tile, waits (bounded) until every tile of
-//                the tile's sample is counted, reduces the sample's slots and
-//                writes the tile's 16 (A, A, B, B) into a shared slot;
-//   warps 7-22   epilogue: warp (7 + e) owns TMEM lane quadrant (warp % 4)
+//   warps 6-7    coefficients, alternate tiles: waits (bounded) until every
+//                tile of the tile's sample is counted, reduces the sample's
+//                slots and writes the tile's 16 (A, A, B, B) into a shared
+//                slot (two warps, so that one's reduction latency does not
+//                limit the round rate);
+//   warps 8-23   epilogue: warp (8 + e) owns TMEM lane quadrant (warp % 4)
 //                and the 32 columns of chunk e / 4 (output phases
 //                pd = chunk / 2, ph = chunk % 2, 16 channels x both pw); per
 //                round it writes the tile from three rounds earlier and does
@@ -48,19 +59,22 @@ namespace gf {
 
 constexpr int kCfEpiWarps = 16;
 constexpr int kCfPubWarp = 5;
-constexpr int kCfCoefWarp = 6;
-constexpr int kCfEpiWarp0 = 7;
+constexpr int kCfCoefWarp0 = 6;   // and 7
+constexpr int kCfCoefWarps = 2;
+constexpr int kCfEpiWarp0 = 8;
 constexpr int kCfThreads = (kCfEpiWarp0 + kCfEpiWarps) * 32;
 constexpr int kCfBufs = 4;                          // TMEM tile buffers of 128 columns
 constexpr int kCfLag = 3;                           // rounds between a tile's statistics and its output
 constexpr int kCfCoefFloats = 16 * 4;               // per buffer: 16 channels x (A, A, B, B)
 constexpr int kCfPartFloats = kCfEpiWarps * 8;      // per round: 8 sums per epilogue warp
-// per buffer and epilogue thread: the tile's output offset with the two
-// in-volume flags in bits 62 and 63, written with the statistics work and
-// read back three rounds later for the output
-constexpr int kCfDecBytes = kCfBufs * kCfEpiWarps * 32 * 8;
+constexpr float kLog2e = 1.4426950408889634f;
+// The producers run at most kCtTcStages tiles ahead of the MMAs, which run at
+// most kCfBufs tiles ahead of the output of a tile: the records of the last
+// 8 tiles cover that.
+static_assert(kCtRecSlots >= kCtTcStages + kCfBufs, "record ring too short");
+constexpr int kCfRecBytes = kCtRecSlots * 128 * 8;
 constexpr int kCfSmem = kCtTcStages * kCtTcStageBytes + kCtTcBBytes + kCfBufs * kCfCoefFloats * 4 +
-                        2 * kCfPartFloats * 4 + kCfDecBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+                        2 * kCfPartFloats * 4 + kCfRecBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 
 struct CfParams {
   const float* x;
@@ -69,7 +83,7 @@ struct CfParams {
   const float* gamma;
   const float* beta;
   float* out;
-  float* part;        // [num_tiles][8]: per tile and group g, (sum s, sum s^2) at 2g, 2g + 1
+  float* part;        // [num_tiles][8]: per tile and group g, (sum s', sum s'^2) at 2g, 2g + 1
   uint32_t* done;     // [N]: tiles of the sample whose slot is written; zero at launch
   int N, D, H, W;
   int bpp;            // tiles per (n, qd) plane: ceil(H*W / 128)
@@ -77,12 +91,14 @@ struct CfParams {
   int rounds;         // ceil(num_tiles / gridDim.x)
   FastDiv div_dp, div_bpp, div_w;  // by D * bpp (tiles per sample), bpp and W
   double inv_count;   // 1 / elements per (sample, group)
-  float eps;
+  float eps;          // GroupNorm eps x (log2 e)^2 (the statistics are of s')
+  uint32_t plane;     // output elements per (sample, channel); 16 * plane < 2^32
+  int OHW, OW;
 };
 
-// Wait until `need` tiles of a sample are counted; false after the time
-// limit.  Every lane polls with acquire loads, so each lane's later reads see
-// the slots written before the increments.
+// Wait until *cnt reaches `need`; false after the time limit.  Every lane
+// polls with acquire loads, so each lane's later reads see what was written
+// before the flag was raised.
 __device__ __forceinline__ bool cf_wait_count(const uint32_t* cnt, uint32_t need) {
   if (ld_acquire_gpu(cnt) >= need) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -119,11 +135,71 @@ __device__ __forceinline__ void df_mul(float hi, float lo, float f, float& ph, f
   pl = __fadd_rn(__fmaf_rn(hi, f, -ph), __fmul_rn(lo, f));
 }
 
+// The whole warp: sum the P tile slots of sample n (8 floats each) in a fixed
+// order in double-float arithmetic and write the sample's per-channel affine
+// A = gamma rsqrt(var + eps), B = beta - mean A, as (A, A, B, B), to
+// coef[lane] (lane c < 16: channel c, group c / 4).  gam, bet: this lane's
+// channel's gamma, beta.
+__device__ __forceinline__ void cf_sample_coefs(const CfParams& p, int n, int P, int lane, float gam, float bet,
+                                                float4* coef) {
+  constexpr uint32_t kFull = 0xffffffffu;
+  // lane l sums the float4 halves (l & 1) of tiles l / 2, l / 2 + 16, ...
+  // (loads of a batch in flight together), then lanes of equal parity combine
+  const float4* sp = reinterpret_cast<const float4*>(p.part + size_t(n) * P * 8);
+  float h[4] = {0.f, 0.f, 0.f, 0.f}, l[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i0 = 0; i0 < 2 * P; i0 += 8 * 32) {
+    float4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      v[j] = i < 2 * P ? __ldcg(sp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      df_add(h[0], l[0], v[j].x);
+      df_add(h[1], l[1], v[j].y);
+      df_add(h[2], l[2], v[j].z);
+      df_add(h[3], l[3], v[j].w);
+    }
+  }
+#pragma unroll
+  for (int o = 2; o < 32; o <<= 1)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float h2 = __shfl_xor_sync(kFull, h[c], o), l2 = __shfl_xor_sync(kFull, l[c], o);
+      df_add2(h[c], l[c], h2, l2);
+    }
+  // lane 0 holds groups 0-1 as (s, s^2, s, s^2), lane 1 groups 2-3; channel
+  // lane c < 16 takes group c / 4 from lane c / 8
+  const int src = (lane >> 3) & 1, k = ((lane >> 2) & 1) * 2;
+  float sh[4], sl[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    sh[c] = __shfl_sync(kFull, h[c], src);
+    sl[c] = __shfl_sync(kFull, l[c], src);
+  }
+  if (lane < 16) {
+    const float inv = float(p.inv_count);
+    float mh, ml, qh, ql, ph, pl, vh, ve;
+    df_mul(k ? sh[2] : sh[0], k ? sl[2] : sl[0], inv, mh, ml);  // mean
+    df_mul(k ? sh[3] : sh[1], k ? sl[3] : sl[1], inv, qh, ql);  // E[s^2]
+    // mean^2 = mh^2 + 2 mh ml (+ ml^2, below the precision kept)
+    ph = __fmul_rn(mh, mh);
+    pl = __fadd_rn(__fmaf_rn(mh, mh, -ph), __fmul_rn(2.f * mh, ml));
+    two_sum(qh, -ph, vh, ve);
+    const float var = fmaxf(__fadd_rn(vh, __fadd_rn(ve, __fsub_rn(ql, pl))), 0.f);
+    const float A = gam * rsqrtf(var + p.eps);
+    const float B = bet - __fadd_rn(mh, ml) * A;
+    coef[lane] = make_float4(A, A, B, B);
+  }
+}
+
 // One round of an epilogue warp: the output of an earlier tile (OUT) and the
-// statistics work of the new tile (P1), interleaved channel by channel, a few
-// columns at a time, so that the Swish of one and the stores of the other
-// overlap.  Columns 2 co + pw of the warp's chunk are channel co at width
-// phase pw.
+// statistics work of the new tile (P1), interleaved piece by piece (8
+// columns = 4 channels = one group), so that the Swish of one and the stores
+// of the other overlap.  Columns 2 co + pw of the warp's chunk are channel co
+// at width phase pw.  gs / gq collect, per group, the (pw 0, pw 1) sums of s'
+// and s'^2 over every cell; the caller masks out the phases that do not exist.
 struct CfOutSide {
   uint32_t taddr;     // TMEM address of the warp's 32 columns (Swish values)
   float* oc;          // output of channel 0, width phase 0
@@ -131,21 +207,15 @@ struct CfOutSide {
   bool pv0, pv1;      // the width-phase-0 / 1 outputs lie inside the volume
   uint64_t* tempty;   // released once the columns are read
 };
-struct CfStatSide {
-  uint32_t taddr;     // TMEM address of the warp's 32 columns (accumulator)
-  float2 m;           // 1 / 0 per width phase: inside the volume or not
-};
 
 template <bool OUT, bool P1, int K>
-__device__ __forceinline__ void cf_round(const CfOutSide& o, const CfStatSide& q, const float* bias, size_t plane,
+__device__ __forceinline__ void cf_round(const CfOutSide& o, uint32_t q_taddr, const float* bias, uint32_t plane,
                                          int lane, float2 (&gs)[4], float2 (&gq)[4]) {
-  float* oc = o.oc;
-  // columns in pieces of kPiece (TMEM loads of 8 keep the registers down)
   constexpr int kPiece = 8;
 #pragma unroll
   for (int part = 0; part < 32 / kPiece; ++part) {
     uint32_t ry[kPiece], rz[kPiece];
-    if constexpr (P1) GF_TMEM_LD8(q.taddr + uint32_t(part * kPiece), ry);
+    if constexpr (P1) GF_TMEM_LD8(q_taddr + uint32_t(part * kPiece), ry);
     if constexpr (OUT) GF_TMEM_LD8(o.taddr + uint32_t(part * kPiece), rz);
     if constexpr (P1) GF_TMEM_WAIT8(ry);
     if constexpr (OUT) {
@@ -158,24 +228,30 @@ __device__ __forceinline__ void cf_round(const CfOutSide& o, const CfStatSide& q
     }
 #pragma unroll
     for (int j = 0; j < kPiece / 2; ++j) {
-      const int co = part * (kPiece / 2) + j;
+      const int co = part * (kPiece / 2) + j;  // (co >> 2 == part: a piece is one group)
       if constexpr (P1) {
-        float2 y = make_float2(__uint_as_float(ry[2 * j]), __uint_as_float(ry[2 * j + 1]));
-        if constexpr (K == 32) {  // no padding column: the bias is added here
+        float2 u = make_float2(__uint_as_float(ry[2 * j]), __uint_as_float(ry[2 * j + 1]));
+        if constexpr (K == 32) {  // no padding column: the (scaled) bias is added here
           if (bias) {
-            const float b = __ldg(bias + co);
-            y = add2(y, make_float2(b, b));
+            const float b = __ldg(bias + co) * kLog2e;
+            u = add2(u, make_float2(b, b));
           }
         }
-        // outputs outside the volume are zeroed before Swish (Swish(0) = 0)
-        const float2 sv = swish2(mul2(y, q.m));
-        gs[co >> 2] = add2(gs[co >> 2], sv);
-        gq[co >> 2] = fma2(sv, sv, gq[co >> 2]);
+        // s' = u / (1 + 2^-u)
+        const float2 d = add2(make_float2(ex2_approx(-u.x), ex2_approx(-u.y)), make_float2(1.f, 1.f));
+        const float2 sv = mul2(u, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+        if (j == 0) {
+          gs[part] = sv;
+          gq[part] = mul2(sv, sv);
+        } else {
+          gs[part] = add2(gs[part], sv);
+          gq[part] = fma2(sv, sv, gq[part]);
+        }
         ry[2 * j] = __float_as_uint(sv.x);
         ry[2 * j + 1] = __float_as_uint(sv.y);
       }
       if constexpr (OUT) {
-        // GroupNorm affine A s + B, then HardSwish h sat(h / 6 + 1/2); the
+        // GroupNorm affine A s' + B, then HardSwish h sat(h / 6 + 1/2); the
         // pair's two outputs are adjacent in memory
         const float2 sv = make_float2(__uint_as_float(rz[2 * j]), __uint_as_float(rz[2 * j + 1]));
         const float4 ab = reinterpret_cast<const float4*>(o.cf)[co];  // a broadcast read
@@ -183,12 +259,12 @@ __device__ __forceinline__ void cf_round(const CfOutSide& o, const CfStatSide& q
         // (f32x2 FMAs have no saturating form)
         const float2 v = mul2(h, make_float2(__saturatef(fmaf(h.x, 1.f / 6.f, 0.5f)),
                                              __saturatef(fmaf(h.y, 1.f / 6.f, 0.5f))));
+        float* oc = o.oc + co * plane;  // (16 * plane < 2^32)
         if (o.pv0) __stcs(oc, v.x);
         if (o.pv1) __stcs(oc + 1, v.y);
-        oc += plane;
       }
     }
-    if constexpr (P1) GF_TMEM_ST8(q.taddr + uint32_t(part * kPiece), ry);
+    if constexpr (P1) GF_TMEM_ST8(q_taddr + uint32_t(part * kPiece), ry);
   }
 }
 
@@ -200,8 +276,8 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
   uint8_t* b_tile = smem + kCtTcStages * kCtTcStageBytes;          // [hi, lo]
   float* coef_s = reinterpret_cast<float*>(b_tile + kCtTcBBytes);  // [kCfBufs][16][4]
   float* part_s = coef_s + kCfBufs * kCfCoefFloats;                // [2][kCfEpiWarps][8]
-  uint64_t* dec_s = reinterpret_cast<uint64_t*>(part_s + 2 * kCfPartFloats);  // [kCfBufs][warps][32]
-  uint64_t* full = dec_s + kCfBufs * kCfEpiWarps * 32;
+  uint64_t* rec_s = reinterpret_cast<uint64_t*>(part_s + 2 * kCfPartFloats);  // [kCtRecSlots][128]
+  uint64_t* full = rec_s + kCtRecSlots * 128;
   uint64_t* empty = full + kCtTcStages;
   uint64_t* tfull = empty + kCtTcStages;  // accumulator of buffer b written by the MMAs
   uint64_t* tempty = tfull + kCfBufs;     // buffer b written out, free for the MMAs
@@ -209,14 +285,14 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
   uint64_t* cempty = cfull + kCfBufs;     // coefficient slot b read
   uint64_t* pfull = cempty + kCfBufs;     // [2] partial sums of the round written
   uint64_t* pempty = pfull + 2;           // [2] partial sums consumed
-  uint64_t* drain = pempty + 2;
+  uint64_t* rfull = pempty + 2;           // [kCtRecSlots] the tile's cell records written
+  uint64_t* drain = rfull + kCtRecSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   constexpr int K = 8 * CIN;
   constexpr uint32_t kFull = 0xffffffffu;
-  const int HW = p.H * p.W;
   const int G = int(gridDim.x);
 
   if (threadIdx.x == 0) {
@@ -234,11 +310,12 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
       mbar_init(&pfull[i], kCfEpiWarps);
       mbar_init(&pempty[i], 1);
     }
+    for (int i = 0; i < kCtRecSlots; ++i) mbar_init(&rfull[i], kCtTcProducerThreads / 32);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  ct_fill_tiles<CIN>(p.w, p.bias, a_ring, b_tile);
+  ct_fill_tiles<CIN>(p.w, p.bias, a_ring, b_tile, kLog2e);
   fence_proxy_async_smem();
   if (warp == kCtTcMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kCfBufs * 128);
@@ -256,11 +333,12 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
 
   if (warp < 4) {
     // ------------------------------------------------------------ producers
-    ct_produce<CIN>(p, a_ring, full, empty, abort_flag, status);
+    const CtRecords rec{rec_s, rfull, uint64_t(p.plane), p.OHW, p.OW};
+    ct_produce<CIN, true>(p, a_ring, full, empty, abort_flag, status, rec);
   } else if (warp == kCtTcMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0)
-      ct_mma<kCfBufs>(p, tmem_base, a_ring, b_tile, full, empty, tfull, tempty, drain, abort_flag, status);
+      ct_mma<kCfBufs, CIN>(p, tmem_base, a_ring, b_tile, full, empty, tfull, tempty, drain, abort_flag, status);
     __syncwarp();
   } else if (warp == kCfPubWarp) {
     // ----------------------------------------------------------- publisher
@@ -272,7 +350,7 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
         break;
       float v = 0.f;
       if (t < p.num_tiles && lane < 8) {
-        // value v = lane: sum s (even) or sum s^2 (odd) of group lane / 2
+        // value v = lane: sum s' (even) or sum s'^2 (odd) of group lane / 2
         const float* ps = part_s + (r & 1) * kCfPartFloats + lane;
 #pragma unroll
         for (int e = 0; e < kCfEpiWarps; ++e) v += ps[e * 8];
@@ -293,12 +371,14 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
       if (lane == 0)
         for (int n = 0; n < p.N; ++n) atomicAdd(p.done + n, 1u << 20);
     }
-  } else if (warp == kCfCoefWarp) {
+  } else if (warp < kCfEpiWarp0) {
     // -------------------------------------------------------- coefficients
-    // lane c < 16: channel c's GroupNorm affine
+    // warp kCfCoefWarp0 + i takes the tiles of rounds i, i + 2, ...; lane
+    // c < 16: channel c's GroupNorm affine
+    const int ci = warp - kCfCoefWarp0;
     const float gam = lane < 16 ? __ldg(p.gamma + lane) : 0.f, bet = lane < 16 ? __ldg(p.beta + lane) : 0.f;
     const int P = int(p.div_dp.d);
-    for (int rt = 0; rt < p.rounds; ++rt) {
+    for (int rt = ci; rt < p.rounds; rt += kCfCoefWarps) {
       const int t = blockIdx.x + rt * G;
       if (t >= p.num_tiles) break;
       const int slot = rt % kCfBufs, n = fdiv(t, p.div_dp);
@@ -307,56 +387,7 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
         fail();
         break;
       }
-      // the sample's P slots of 8 floats: lane l sums the float4 halves
-      // (l & 1) of tiles l / 2, l / 2 + 16, ... (loads of a batch in flight
-      // together), then lanes of equal parity combine; all sums double-float
-      const float4* sp = reinterpret_cast<const float4*>(p.part + size_t(n) * P * 8);
-      float h[4] = {0.f, 0.f, 0.f, 0.f}, l[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int i0 = 0; i0 < 2 * P; i0 += 8 * 32) {
-        float4 v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int i = i0 + lane + 32 * j;
-          v[j] = i < 2 * P ? __ldcg(sp + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          df_add(h[0], l[0], v[j].x);
-          df_add(h[1], l[1], v[j].y);
-          df_add(h[2], l[2], v[j].z);
-          df_add(h[3], l[3], v[j].w);
-        }
-      }
-#pragma unroll
-      for (int o = 2; o < 32; o <<= 1)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float h2 = __shfl_xor_sync(kFull, h[c], o), l2 = __shfl_xor_sync(kFull, l[c], o);
-          df_add2(h[c], l[c], h2, l2);
-        }
-      // lane 0 holds groups 0-1 as (s, s^2, s, s^2), lane 1 groups 2-3;
-      // channel lane c < 16 takes group c / 4 from lane c / 8
-      const int src = (lane >> 3) & 1, k = ((lane >> 2) & 1) * 2;
-      float sh[4], sl[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        sh[c] = __shfl_sync(kFull, h[c], src);
-        sl[c] = __shfl_sync(kFull, l[c], src);
-      }
-      if (lane < 16) {
-        const float inv = float(p.inv_count);
-        float mh, ml, qh, ql, ph, pl, vh, ve;
-        df_mul(k ? sh[2] : sh[0], k ? sl[2] : sl[0], inv, mh, ml);  // mean
-        df_mul(k ? sh[3] : sh[1], k ? sl[3] : sl[1], inv, qh, ql);  // E[s^2]
-        // mean^2 = mh^2 + 2 mh ml (+ ml^2, below the precision kept)
-        ph = __fmul_rn(mh, mh);
-        pl = __fadd_rn(__fmaf_rn(mh, mh, -ph), __fmul_rn(2.f * mh, ml));
-        two_sum(qh, -ph, vh, ve);
-        const float var = fmaxf(__fadd_rn(vh, __fadd_rn(ve, __fsub_rn(ql, pl))), 0.f);
-        const float A = gam * rsqrtf(var + p.eps);
-        const float B = bet - __fadd_rn(mh, ml) * A;
-        reinterpret_cast<float4*>(coef_s + slot * kCfCoefFloats)[lane] = make_float4(A, A, B, B);
-      }
+      cf_sample_coefs(p, n, P, lane, gam, bet, reinterpret_cast<float4*>(coef_s + slot * kCfCoefFloats));
       __syncwarp();
       if (lane == 0) mbar_arrive(&cfull[slot]);
     }
@@ -364,11 +395,14 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
     // ------------------------------------------------------------ epilogue
     const int e = warp - kCfEpiWarp0;
     const int quad = warp & 3, chunk = e >> 2;
-    const int pd = chunk >> 1, hh = chunk & 1;  // depth and height phase of the warp's columns
+    const int pd = chunk >> 1, ph = chunk & 1;  // depth and height phase of the warp's columns
     const int row = quad * 32 + lane;
-    const int OD = 2 * p.D - 1, OH = 2 * p.H - 1, OW = 2 * p.W - 1;
-    const int OHW = OH * OW;
-    const size_t plane = size_t(OD) * OHW;
+    // record flags that make the warp's width-phase-0 / 1 outputs exist: the
+    // cell (bit 0), depth phase pd (bit 1), height phase ph (bit 2), width
+    // phase 1 (bit 3)
+    const uint32_t m0 = 1u | (uint32_t(pd) << 1) | (uint32_t(ph) << 2), m1 = m0 | 8u;
+    const uint32_t phase_off = uint32_t(pd) * uint32_t(p.OHW) + uint32_t(ph) * uint32_t(p.OW);
+    constexpr uint64_t kOffMask = (uint64_t(1) << 56) - 1;
     const uint32_t lane_base = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(chunk * 32);
     for (int r = 0; r < p.rounds + kCfLag; ++r) {
       if (__any_sync(kFull, *abort_flag)) break;
@@ -376,7 +410,6 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
       const int ro = r - kCfLag, to = blockIdx.x + ro * G, tp = blockIdx.x + r * G;
       const bool has_out = r >= kCfLag && to < p.num_tiles, has_p1 = r < p.rounds && tp < p.num_tiles;
       CfOutSide o{};
-      CfStatSide q{};
       int ob = 0;
       if (has_out) {
         ob = ro % kCfBufs;
@@ -384,11 +417,14 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
           fail();
           break;
         }
-        const uint64_t dv = dec_s[(ob * kCfEpiWarps + e) * 32 + lane];
-        o.pv0 = (dv >> 62) & 1;
-        o.pv1 = dv >> 63;
+        // (this thread read the record in round ro, after its barrier; the
+        // slot is not rewritten before this tile's buffer is released)
+        const uint64_t rv = rec_s[(ro % kCtRecSlots) * 128 + row];
+        const uint32_t fl = uint32_t(rv >> 56);
+        o.pv0 = (fl & m0) == m0;
+        o.pv1 = (fl & m1) == m1;
         o.taddr = lane_base + uint32_t(ob * 128);
-        o.oc = p.out + (dv & ((uint64_t(1) << 62) - 1));
+        o.oc = p.out + ((rv & kOffMask) + phase_off);
         o.cf = coef_s + ob * kCfCoefFloats;
         o.tempty = &tempty[ob];
       }
@@ -396,49 +432,45 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
         fail();
         break;
       }
+      uint32_t q_taddr = 0;
+      float mx = 0.f, my = 0.f;  // the new tile's width phase 0 / 1 outputs exist (1) or not (0)
       if (has_p1) {
         const int buf = r % kCfBufs;
-        if (!__all_sync(kFull, mbar_wait<true>(&tfull[buf], (r / kCfBufs) & 1))) {
+        if (!__all_sync(kFull, mbar_wait<true>(&rfull[r % kCtRecSlots], (r / kCtRecSlots) & 1)) ||
+            !__all_sync(kFull, mbar_wait<true>(&tfull[buf], (r / kCfBufs) & 1))) {
           fail();
           break;
         }
         tc_fence_after();
-        const CtTile tl = ct_tile(p, tp);
-        const int qd = tl.qd, c = tl.c0 + row;
-        const bool cv = c < HW;
-        const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
-        const bool pv0 = cv && ct_phase_ok(pd * 4 + hh * 2, qd, qh, qw, p.D, p.H, p.W);
-        const bool pv1 = cv && ct_phase_ok(pd * 4 + hh * 2 + 1, qd, qh, qw, p.D, p.H, p.W);
-        q.taddr = lane_base + uint32_t(buf * 128);
-        q.m = make_float2(pv0 ? 1.f : 0.f, pv1 ? 1.f : 0.f);
-        // for the output of this tile three rounds later
-        const uint64_t off =
-            uint64_t(tl.n) * 16 * plane + uint64_t((2 * qd + pd) * OHW + (2 * qh + hh) * OW + 2 * qw);
-        dec_s[(buf * kCfEpiWarps + e) * 32 + lane] = off | (uint64_t(pv0) << 62) | (uint64_t(pv1) << 63);
+        const uint32_t fl = uint32_t(rec_s[(r % kCtRecSlots) * 128 + row] >> 56);
+        mx = (fl & m0) == m0 ? 1.f : 0.f;
+        my = (fl & m1) == m1 ? 1.f : 0.f;
+        q_taddr = lane_base + uint32_t(buf * 128);
       }
+      // this thread's Swish values of the previous round are in TMEM before
+      // any of them is read back (three rounds on)
+      tmem_wait_st();
       float2 gs[4], gq[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) gs[g] = gq[g] = make_float2(0.f, 0.f);
       if (has_out && has_p1)
-        cf_round<true, true, K>(o, q, p.bias, plane, lane, gs, gq);
+        cf_round<true, true, K>(o, q_taddr, p.bias, p.plane, lane, gs, gq);
       else if (has_out)
-        cf_round<true, false, K>(o, q, p.bias, plane, lane, gs, gq);
+        cf_round<true, false, K>(o, q_taddr, p.bias, p.plane, lane, gs, gq);
       else if (has_p1)
-        cf_round<false, true, K>(o, q, p.bias, plane, lane, gs, gq);
+        cf_round<false, true, K>(o, q_taddr, p.bias, p.plane, lane, gs, gq);
       if (has_out) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&cempty[ob]);
       }
       if (has_p1) {
-        // reduce-scatter of the 8 sums over the warp's 32 lanes (9
-        // shuffles): afterwards lane l holds the full sum of value
-        // v = 4*b4 + 2*b3 + b2 (b_i = bit i of l), value v being gs[v/2]
-        // (even v) or gq[v/2] (odd v)
+        // the cell's existing phases only, then a reduce-scatter of the 8 sums
+        // over the warp's 32 lanes (9 shuffles): afterwards lane l holds the
+        // full sum of value v = 4*b4 + 2*b3 + b2 (b_i = bit i of l), value v
+        // being the sum s' (even v) or s'^2 (odd v) of group v / 2
         float rs[8];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          rs[2 * g] = gs[g].x + gs[g].y;
-          rs[2 * g + 1] = gq[g].x + gq[g].y;
+          rs[2 * g] = fmaf(gs[g].y, my, gs[g].x * mx);
+          rs[2 * g + 1] = fmaf(gq[g].y, my, gq[g].x * mx);
         }
         {
           const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
@@ -463,7 +495,6 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
           rs[0] += __shfl_xor_sync(kFull, rs[0], 1);
         }
         if ((lane & 3) == 0) part_s[(r & 1) * kCfPartFloats + e * 8 + (lane >> 2)] = rs[0];
-        tmem_wait_st();
       }
       if (r < p.rounds) {
         __syncwarp();
@@ -472,6 +503,7 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
     }
   }
 
+  if (warp >= kCfEpiWarp0) tmem_wait_st();
   tc_fence_before();
   __syncthreads();
   if (warp == kCtTcMmaWarp) {

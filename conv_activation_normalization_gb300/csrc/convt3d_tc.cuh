@@ -21,11 +21,11 @@
 //
 // Roles (5 + kCtTcEpiWarps warps, one CTA per SM, persistent over tiles of
 // 128 cells that run along the flattened (qh, qw) plane of one (n, qd)):
-//   warps 0-3   producers: thread r gathers cell r's 8*Cin inputs with
-//               cp.async straight into the A hi row of a ring stage (128-byte
-//               swizzle computed by hand), several tiles in flight; once a
-//               tile has landed it writes the lo row, fence.proxy.async, and
-//               each warp arrives once;
+//   warps 0-3   producers: thread r gathers cell r's 8*Cin inputs (coalesced
+//               loads per warp, the neighbouring width position by shuffle)
+//               and writes the hi and lo rows of a ring stage (128-byte
+//               swizzle computed by hand), fence.proxy.async, and each warp
+//               arrives once;
 //   warp 4      TMEM owner; one thread issues the 12 MMAs of a tile into one
 //               of kCtTcAccBufs 128-column accumulators and commits;
 //   warps 5-    epilogue: warp (5 + e) reads TMEM lane quadrant (warp % 4)
@@ -56,7 +56,6 @@ constexpr int kCtTcMmaWarp = 4;
 constexpr int kCtTcEpiWarp0 = 5;
 constexpr int kCtTcEpiThreads = kCtTcEpiWarps * 32;
 constexpr int kCtTcStages = 4;
-constexpr int kCtTcGatherDepth = kCtTcStages - 1;  // tiles whose input gathers are in flight
 constexpr int kCtTcAccBufs = 2;  // TMEM accumulators of 128 columns
 constexpr int kCtTcTmemCols = kCtTcAccBufs * 128 <= 256 ? 256 : 512;
 constexpr int kCtTcPlane = 128 * 128;              // one 128-row x 128-byte tile
@@ -122,12 +121,14 @@ __device__ __forceinline__ bool ct_phase_ok(int p, int qd, int qh, int qw, int D
   return ((p >> 2) == 0 || qd < D - 1) && (((p >> 1) & 1) == 0 || qh < H - 1) && ((p & 1) == 0 || qw < W - 1);
 }
 
-// The weights tile B (hi/lo, rows in accumulator-column order) and the K
-// padding of every A ring row: 1 in column K of the hi plane (so the GEMM
-// adds the bias column of B) and zeros elsewhere.  All threads of the CTA
-// take part; the caller fences and synchronises.
+// The weights tile B (hi/lo, rows in accumulator-column order), its values
+// multiplied by `scale`, and the K padding of every A ring row: 1 in column K
+// of the hi plane (so the GEMM adds the bias column of B, scaled too) and
+// zeros elsewhere.  All threads of the CTA take part; the caller fences and
+// synchronises.
 template <int CIN>
-__device__ __forceinline__ void ct_fill_tiles(const float* w, const float* bias, uint8_t* a_ring, uint8_t* b_tile) {
+__device__ __forceinline__ void ct_fill_tiles(const float* w, const float* bias, uint8_t* a_ring, uint8_t* b_tile,
+                                              float scale = 1.f) {
   constexpr int K = 8 * CIN;
   for (int i = threadIdx.x; i < 128 * 32; i += blockDim.x) {
     const int row = i / 32, k = i % 32;  // row = (pd*2 + ph)*32 + co*2 + pw
@@ -147,6 +148,7 @@ __device__ __forceinline__ void ct_fill_tiles(const float* w, const float* bias,
       const int tap = (kd * 3 + kh) * 3 + kw;
       if (used) v = __ldg(w + (size_t(ci) * 16 + co) * 27 + tap);
     }
+    v *= scale;
     *reinterpret_cast<float*>(b_tile + sw128_offset(row, k)) = v;
     *reinterpret_cast<float*>(b_tile + kCtTcPlane + sw128_offset(row, k)) = v - tf32_hi(v);
   }
@@ -158,50 +160,44 @@ __device__ __forceinline__ void ct_fill_tiles(const float* w, const float* bias,
   }
 }
 
-// Producer warps 0-3 (thread r = cell row r of the tile).
-template <int CIN, class Prm>
+// Per-cell record of a tile for the output side of the single-kernel path
+// (CtRecords): the element index of the cell's first output
+// (n, co 0, 2 qd, 2 qh, 2 qw) in bits 0-55 and in bits 56-59 whether the cell
+// exists (cv) and whether its second phase exists along depth (vd), height
+// (vh) and width (vw).
+constexpr int kCtRecSlots = 8;  // tiles whose records are kept (see convt3d_fused.cuh)
+struct CtRecords {
+  uint64_t* ring;     // [kCtRecSlots][128] in shared memory
+  uint64_t* full;     // [kCtRecSlots] mbarriers: one arrival per producer warp
+  uint64_t plane;     // output elements per (sample, channel)
+  int OHW, OW;
+};
+
+// Producer warps 0-3: thread r gathers the 8 Cin inputs of cell r of the tile
+// into row r of the A operand (hi = the raw values, lo = value - TF32 part),
+// warp w holding 32 consecutive cells.  For each (ci, depth offset a, height
+// offset b) every lane loads the input at its own width position qw (one
+// coalesced load per warp) and takes the one at qw + 1 from the next lane,
+// which holds cell (qh, qw + 1) whenever qw + 1 < W; the last lane loads it
+// itself.  Inputs outside the volume are zero.  Once its 32 rows (and, with
+// RECORDS, the cells' records) are written the warp arrives on the stage's
+// full barrier (and the record slot's).
+template <int CIN, bool RECORDS, class Prm>
 __device__ __forceinline__ void ct_produce(const Prm& p, uint8_t* a_ring, uint64_t* full, uint64_t* empty,
-                                           volatile uint32_t* abort_flag, uint32_t* status) {
+                                           volatile uint32_t* abort_flag, uint32_t* status, const CtRecords& rec) {
   constexpr int K = 8 * CIN;
+  constexpr uint32_t kFull = 0xffffffffu;
   const int lane = threadIdx.x % 32;
-  const int HW = p.H * p.W;
-  // The gathers of up to kCtTcGatherDepth tiles are in flight at once:
-  // thread r copies cell r's inputs straight into the A hi plane of a ring
-  // stage with 4-byte cp.async (zero-filled outside the input), and once a
-  // tile's copies have landed it writes the lo plane from them and marks
-  // the stage full.
   const int r = threadIdx.x;  // cell row of the tile
-  int istage = 0, fstage = 0, pending = 0;
-  uint32_t iphase = 0;
-  auto finish_oldest = [&]() {
-    uint8_t* a_hi = a_ring + fstage * kCtTcStageBytes;
-    uint8_t* a_lo = a_hi + kCtTcPlane;
-#pragma unroll
-    for (int ch = 0; ch < K / 4; ++ch) {
-      const uint32_t off = sw128_offset(r, ch * 4);
-      const float4 v = *reinterpret_cast<const float4*>(a_hi + off);
-      *reinterpret_cast<float4*>(a_lo + off) =
-          make_float4(v.x - tf32_hi(v.x), v.y - tf32_hi(v.y), v.z - tf32_hi(v.z), v.w - tf32_hi(v.w));
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&full[fstage]);
-    if (++fstage == kCtTcStages) fstage = 0;
-    --pending;
-  };
-  for (int t = blockIdx.x;; t += gridDim.x) {
-    // decisions are warp-uniform: the warp arrives once for all its lanes
-    bool more = t < p.num_tiles && !__any_sync(0xffffffffu, *abort_flag);
-    if (more && !__all_sync(0xffffffffu, mbar_wait<true>(&empty[istage], iphase ^ 1))) {
+  const int HW = p.H * p.W;
+  const size_t sD = size_t(HW), sC = size_t(p.D) * sD;  // strides of a depth slice and an input channel
+  int stage = 0, count = 0;
+  uint32_t phase = 0;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++count) {
+    if (__any_sync(kFull, *abort_flag)) break;
+    if (!__all_sync(kFull, mbar_wait<true>(&empty[stage], phase ^ 1))) {
       record_error(status, GF_DEV_WAIT_TIMEOUT);
       *abort_flag = 1;
-      more = false;
-    }
-    if (!more) {
-      // drain: every issued tile is completed and marked full, so the MMA
-      // issuer never waits on a stage that will not fill
-      cp_async_wait<0>();
-      while (pending > 0) finish_oldest();
       break;
     }
     const CtTile tl = ct_tile(p, t);
@@ -209,33 +205,58 @@ __device__ __forceinline__ void ct_produce(const Prm& p, uint8_t* a_ring, uint64
     const bool cv = c < HW;
     const int qh = cv ? fdiv(c, p.div_w) : 0, qw = cv ? c - qh * p.W : 0;
     const bool vd = qd + 1 < p.D, vh = qh + 1 < p.H, vw = qw + 1 < p.W;
-    const float* xc = p.x + (size_t(n) * CIN * p.D + qd) * HW + size_t(qh) * p.W + qw;
-    const uint32_t a_hi = smem_u32(a_ring + istage * kCtTcStageBytes);
+    const float* xb = p.x + (size_t(n) * CIN * p.D + qd) * sD + size_t(qh) * p.W + qw;
+    float v[K];  // the A row in k order: k = pos * CIN + ci, pos = 4 a + 2 b + (width offset)
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int pos = k / CIN, ci = k % CIN;
-      const int a = pos >> 2, b = (pos >> 1) & 1, cc = pos & 1;
-      const bool ok = cv && (a == 0 || vd) && (b == 0 || vh) && (cc == 0 || vw);
-      const float* src = ok ? xc + size_t(ci) * p.D * HW + a * HW + b * p.W + cc : p.x;
-      cp_async4(a_hi + sw128_offset(r, k), src, ok ? 4u : 0u);
+    for (int ci = 0; ci < CIN; ++ci)
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const bool ok = cv && (a == 0 || vd) && (b == 0 || vh);
+          const float* src = xb + ci * sC + a * sD + b * p.W;
+          const float v0 = ok ? __ldg(src) : 0.f;
+          const float own = (ok && vw && lane == 31) ? __ldg(src + 1) : 0.f;
+          const float nb = __shfl_down_sync(kFull, v0, 1);
+          v[(4 * a + 2 * b) * CIN + ci] = v0;
+          v[(4 * a + 2 * b + 1) * CIN + ci] = vw ? (lane == 31 ? own : nb) : 0.f;
+        }
+    uint8_t* a_hi = a_ring + stage * kCtTcStageBytes;
+    uint8_t* a_lo = a_hi + kCtTcPlane;
+#pragma unroll
+    for (int ch = 0; ch < K / 4; ++ch) {
+      const float4 h = make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+      const uint32_t off = sw128_offset(r, ch * 4);
+      *reinterpret_cast<float4*>(a_hi + off) = h;
+      *reinterpret_cast<float4*>(a_lo + off) =
+          make_float4(h.x - tf32_hi(h.x), h.y - tf32_hi(h.y), h.z - tf32_hi(h.z), h.w - tf32_hi(h.w));
     }
-    cp_async_commit();
-    ++pending;
-    if (++istage == kCtTcStages) {
-      istage = 0;
-      iphase ^= 1;
+    if constexpr (RECORDS) {
+      const uint64_t base = cv ? (uint64_t(n) * 16) * rec.plane + uint64_t(2 * qd) * uint64_t(rec.OHW) +
+                                     uint64_t(2 * qh) * uint64_t(rec.OW) + uint64_t(2 * qw)
+                               : 0;
+      const uint64_t flags = uint64_t(cv) | (uint64_t(vd) << 1) | (uint64_t(vh) << 2) | (uint64_t(vw) << 3);
+      rec.ring[(count % kCtRecSlots) * 128 + r] = base | (flags << 56);
     }
-    if (pending == kCtTcGatherDepth) {
-      cp_async_wait<kCtTcGatherDepth - 1>();
-      finish_oldest();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&full[stage]);
+      if constexpr (RECORDS) mbar_arrive(&rec.full[count % kCtRecSlots]);
+    }
+    if (++stage == kCtTcStages) {
+      stage = 0;
+      phase ^= 1;
     }
   }
 }
 
-// The MMA issuer (one thread): per tile 12 MMAs (3xTF32 over 4 k-steps of 8)
-// into TMEM accumulator (tile count % NBUF), then commits to the ring stage's
-// empty barrier and the accumulator's full barrier.
-template <int NBUF, class Prm>
+// The MMA issuer (one thread): per tile the 3xTF32 MMAs of the k-steps of 8
+// that hold data (the K = 8 Cin inputs, and the bias column when K < 32:
+// lo x hi only where A's lo plane can be non-zero, k < K) into TMEM
+// accumulator (tile count % NBUF), then commits to the ring stage's empty
+// barrier and the accumulator's full barrier.
+template <int NBUF, int CIN = 4, class Prm>
 __device__ __forceinline__ void ct_mma(const Prm& p, uint32_t tmem_base, uint8_t* a_ring, uint8_t* b_tile,
                                        uint64_t* full, uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
                                        uint64_t* drain, volatile uint32_t* abort_flag, uint32_t* status) {
@@ -253,10 +274,14 @@ __device__ __forceinline__ void ct_mma(const Prm& p, uint32_t tmem_base, uint8_t
     tc_fence_after();
     const uint32_t d = tmem_base + uint32_t(acc * 128);
     const uint32_t a_hi = smem_u32(a_ring + stage * kCtTcStageBytes), a_lo = a_hi + kCtTcPlane;
+    constexpr int K = 8 * CIN;
+    constexpr int kSteps = K < 32 ? (K + 1 + 7) / 8 : 4;  // k-steps holding inputs or the bias column
+    constexpr int kLoSteps = (K + 7) / 8;                // k-steps where A's lo plane can be non-zero
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < kSteps; ++kk) {
       const uint32_t off = uint32_t(kk * 32);
-      mma_tf32(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, kk != 0);
+      if (kk < kLoSteps)
+        mma_tf32(d, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, kk != 0);
       mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
       mma_tf32(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
     }
@@ -325,11 +350,11 @@ __global__ void __launch_bounds__(kCtTcThreads, 1) convt3d_tc_kernel(const CtTcP
 
   if (warp < 4) {
     // ------------------------------------------------------------ producers
-    ct_produce<CIN>(p, a_ring, full, empty, abort_flag, status);
+    ct_produce<CIN, false>(p, a_ring, full, empty, abort_flag, status, CtRecords{});
   } else if (warp == kCtTcMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0)
-      ct_mma<kCtTcAccBufs>(p, tmem_base, a_ring, b_tile, full, empty, tfull, tempty, drain, abort_flag, status);
+      ct_mma<kCtTcAccBufs, CIN>(p, tmem_base, a_ring, b_tile, full, empty, tfull, tempty, drain, abort_flag, status);
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue

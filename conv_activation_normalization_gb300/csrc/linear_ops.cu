@@ -308,7 +308,7 @@ gf_status with_gn_epilogue(const GNParams& ep, cudaStream_t s, F&& f) {
 // chunk with apply.
 struct EpiLSEPartial {
   static constexpr bool kFixedBN = true;  // the partials' layout follows the tile width
-  static constexpr int kChunkK = 512;     // K elements per accumulation chunk
+  static constexpr int kChunkK = 1024;    // K elements per accumulation chunk
   template <class Op>
   __host__ __device__ static constexpr bool chunked() {
     return Op::kProducts == 3;
