@@ -287,6 +287,32 @@ class DConv1d(Workload):
         gf.gf_ln_gelu_dconv1d_res(t["x"] if x is None else x, t["ln_gamma"], t["ln_beta"], t["conv_w"], t["conv_b"],
                                   s.dilation, s.padding, s.eps, mode=MODES[MODE][0], out=t["out"])
 
+    def extra_measure(self, gf, t, stream):
+        """The same step with GF_FLAG_FUSED_PRODUCER (LayerNorm and GELU inside
+        the GEMM, no activation planes in the workspace), eager calls."""
+        import torch
+        s = self.shape
+        call = lambda: gf.gf_ln_gelu_dconv1d_res(t["x"], t["ln_gamma"], t["ln_beta"], t["conv_w"], t["conv_b"],  # noqa
+                                                 s.dilation, s.padding, s.eps, out=t["out"], fused_producer=True)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        n = 10
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        lib = gf.lib()
+        ws_planes = lib.gf_ln_gelu_dconv1d_res_workspace_size(s.B, s.C, s.L, s.ksize, s.dilation, 0)
+        ws_fused = lib.gf_ln_gelu_dconv1d_res_workspace_size(s.B, s.C, s.L, s.ksize, s.dilation, gf.GF_FLAG_FUSED_PRODUCER)
+        return {"fused_producer": {"flag": "GF_FLAG_FUSED_PRODUCER", "ms_per_step": round(ms, 4),
+                                   "value": round(self.work_per_step() / (ms * 1e-3) / self.scale(), 3),
+                                   "unit": self.unit, "steps": n, "launch": "eager",
+                                   "workspace_bytes": int(ws_fused), "default_workspace_bytes": int(ws_planes)}}
+
     def oracle_chunk(self, d, i, chunk):
         import oracle
         s = self.shape
@@ -666,7 +692,7 @@ def measure_other_workloads(args):
             out[n] = None
             continue
         keep = ("metric", "value", "unit", "ms_per_step", "steps", "roofline", "e2e", "cpu_baseline", "clocks",
-                "step_ms", "noalloc")
+                "step_ms", "noalloc", "fused_producer")
         out[n] = {k: line[k] for k in keep if k in line}
         out[n]["workload"] = line["config"]["workload"]
         out[n]["launch"] = line["config"]["launch"]

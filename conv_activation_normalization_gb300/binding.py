@@ -24,6 +24,7 @@ GF_MODE_FP32_3XTF32 = 0
 GF_MODE_BF16 = 1
 GF_MODE_FP32_3XBF16 = 2
 GF_FLAG_GELU_TANH = 0x100  # OR'd into the Conv1d chain's mode: tanh-approximate GELU
+GF_FLAG_FUSED_PRODUCER = 0x200  # OR'd into the Conv1d chain's mode: LayerNorm + GELU inside the GEMM
 GF_CHAIN_GROUPNORM, GF_CHAIN_LSE, GF_CHAIN_LINEAR = 0, 1, 2  # gf_linear_tile_width's chains
 
 _lib = None
@@ -53,7 +54,7 @@ _SIGS = {
                                                    _I64, _P, _SZ, _P]),
     "gf_linear_lse_act_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
     "gf_linear_lse_act": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _F, _I32, _P, _SZ, _P]),
-    "gf_ln_gelu_dconv1d_res_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32]),
+    "gf_ln_gelu_dconv1d_res_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32, _I32]),
     "gf_ln_gelu_dconv1d_res": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _F, _I32,
                                       _P, _SZ, _P]),
     "gf_convt3d_swish_gn_hswish_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I64, _I32, _I32, _I32,
@@ -377,13 +378,18 @@ def gf_linear_lse_act(x, W, b, negative_slope=0.01, mode=GF_MODE_FP32_3XTF32, ou
 
 
 def gf_ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, padding, eps=1e-5,
-                           mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None, gelu="erf"):
+                           mode=GF_MODE_FP32_3XTF32, out=None, workspace=None, stream=None, gelu="erf",
+                           fused_producer=False):
     """out = conv1d(gelu(layer_norm(x, [C, L])), dilation, padding) + x.
-    gelu: "erf" (exact) or "tanh" (the tanh approximation)."""
+    gelu: "erf" (exact) or "tanh" (the tanh approximation).  fused_producer:
+    LayerNorm + GELU inside the GEMM (no activation planes in the
+    workspace; slower)."""
     if gelu not in ("erf", "tanh"):
         raise ValueError("gelu must be 'erf' or 'tanh'")
     if gelu == "tanh":
         mode |= GF_FLAG_GELU_TANH
+    if fused_producer:
+        mode |= GF_FLAG_FUSED_PRODUCER
     B, C, L = x.shape
     ksize = conv_w.shape[2]
     _shape(conv_w, (C, C, ksize), "conv_w")
@@ -395,7 +401,7 @@ def gf_ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, paddi
     if out is None:
         out = torch.empty_like(x)
     with torch.cuda.device(dev):
-        nbytes = lib().gf_ln_gelu_dconv1d_res_workspace_size(B, C, L, ksize, mode)
+        nbytes = lib().gf_ln_gelu_dconv1d_res_workspace_size(B, C, L, ksize, dilation, mode)
         wp, nb = _ws_args(dev, nbytes, workspace, stream)
         _call("gf_ln_gelu_dconv1d_res", _ptr(x), _ptr(ln_gamma), _ptr(ln_beta), _ptr(conv_w), _ptr(conv_b),
               _ptr(out), B, C, L, ksize, dilation, padding, eps, mode, wp, nb, _stream_ptr(stream))

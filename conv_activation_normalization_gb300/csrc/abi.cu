@@ -212,7 +212,7 @@ gf_status gf_profile_end(int32_t* calls, float* total_ms) {
 }
 
 
-int32_t gf_abi_version(void) { return 1; }
+int32_t gf_abi_version(void) { return 2; }
 
 const char* gf_status_string(gf_status s) {
   switch (s) {

@@ -13,6 +13,18 @@
 //      with the TMA unit's zero fill supplying the padding; its epilogue adds
 //      the conv bias and the residual x and stores out[b][co][j] (32
 //      consecutive j per warp, so every store is a full 128-byte line).
+//
+// With GF_FLAG_FUSED_PRODUCER (3xTF32 mode, taps spanning at most 92
+// positions) steps 3-5 are one kernel instead (LnConvSrc): converter warps
+// inside the GEMM apply LayerNorm and GELU to raw x while they build each
+// stage's A operand, so the activation planes are never written and the
+// workspace shrinks from 8 B per activation to the statistics and weight
+// planes; steps 1, 2 and a weight split remain.  It is the slower path on
+// the benchmark workload (0.46 against 0.32 ms per call): the window of
+// activations it computes per tile and channel block cannot be
+// double-buffered within the shared memory the two 96 KB stages leave, so
+// its LayerNorm/GELU work does not overlap the MMAs, and the planes path
+// stays the default.
 #include <cmath>
 
 #include "gemm_tc.cuh"
@@ -230,6 +242,182 @@ __global__ void conv_weight_split_kernel(const float* __restrict__ w, void* plan
   }
 }
 
+// Operand source of the fused LayerNorm -> GELU -> dilated Conv1d GEMM (3xTF32
+// mode): rows are output positions j of one sample, columns output channels,
+// and the reduction runs over channel blocks cb of 32 (outer) and taps t
+// (inner), k-block kb = cb * ksize + t; the weight planes are laid out in that
+// order (conv_weight_split_cb_kernel).  Warp 0 loads only the weights (B);
+// five converter warps build A.  Per tile and channel block they compute the
+// activation a = GELU((x - mean) rstd gamma + beta) once for the window of
+// positions l = j0 - pad + p, p < 128 + (ksize - 1) dil (zero outside
+// [0, L): the conv's padding), into shared memory (128-byte rows of 32
+// channels, 16-byte chunks swizzled by row; the window starts at the 4-aligned
+// position at or before j0 - pad, `shift` rows earlier), then four of them
+// copy, for each tap, window rows shift + t dil .. + 127 into the stage's A
+// planes (hi = the value, which the tensor core truncates; lo = value - its
+// TF32 part).  A window task is 4 positions x 4 channels: x, gamma and beta
+// each read as 4 float4 (all 12 loads issued before any arithmetic), so that
+// many loads are in flight per thread.
+template <bool TANH>
+struct LnConvSrc {
+  static constexpr int kConverterWarps = 5;
+  static constexpr int kArrivingWarps = 4;                      // the copying warps: one A row per thread
+  static constexpr int kMaxWindow = 220;                        // positions: 128 + (ksize - 1) dil <= 220
+  static constexpr int kScratchBytes = (kMaxWindow + 4) * 128;  // + the alignment shift
+  const float* x;
+  const float* gamma;
+  const float* beta;
+  const float2* stats;  // [B] (mean, rstd)
+  int C, Cp, L, pad, dil, ksize;
+  int num_jb, num_nb, num_kb, bn, bk, nsamples;
+  int kb_chunk;
+  int ncb;      // Cp / 32
+  int wrows;    // 128 + (ksize - 1) dil
+  __device__ __forceinline__ int num_tiles() const { return nsamples * num_jb * num_nb; }
+  __device__ __forceinline__ Tile tile(int t) const {
+    const int nb = t % num_nb;
+    const int r = t / num_nb;
+    const int jb = r % num_jb;
+    const int b = r / num_jb;
+    return Tile{b, jb * kBM, nb * bn, nb};
+  }
+  template <int PLANES>
+  __device__ __forceinline__ void load(const OperandMaps& m, uint64_t* bar, const uint32_t*, const uint32_t* sb,
+                                       const Tile& t, int kb) const {
+#pragma unroll
+    for (int p = 0; p < PLANES; ++p) tma_load_2d(sb[p], &m.b[p], bar, kb * bk, t.n0);
+  }
+  // byte offset of 16-byte chunk q of row r in a 128-byte-row swizzled tile
+  __device__ __forceinline__ static uint32_t chunk_off(int r, int q) {
+    return uint32_t(r) * 128u + ((uint32_t(q) ^ uint32_t(r & 7)) << 4);
+  }
+  __device__ __forceinline__ static float act(float h) { return TANH ? gelu_tanh(h) : gelu_erf(h); }
+
+  // one window task: positions pos0 .. pos0 + 3 (window rows row0 .. row0 + 3)
+  // x channels c0 .. c0 + 3 of the sample at xb
+  __device__ __forceinline__ void window_task(const float* xb, float2 st, int pos0, int row0, int c0,
+                                              uint8_t* win) const {
+    const bool vec = (L & 3) == 0 && pos0 >= 0 && pos0 + 3 < L;  // whole float4s inside the row
+    float4 xv[4], gv[4], bv[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int ci = c0 + c;
+      xv[c] = gv[c] = bv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ci < C) {
+        const int64_t o = int64_t(ci) * L + pos0;
+        if (vec) {
+          xv[c] = __ldg(reinterpret_cast<const float4*>(xb + o));
+          gv[c] = __ldg(reinterpret_cast<const float4*>(gamma + o));
+          bv[c] = __ldg(reinterpret_cast<const float4*>(beta + o));
+        } else {
+          float e[3][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const bool in = pos0 + i >= 0 && pos0 + i < L;
+            e[0][i] = in ? __ldg(xb + o + i) : 0.f;
+            e[1][i] = in ? __ldg(gamma + o + i) : 0.f;
+            e[2][i] = in ? __ldg(beta + o + i) : 0.f;
+          }
+          xv[c] = make_float4(e[0][0], e[0][1], e[0][2], e[0][3]);
+          gv[c] = make_float4(e[1][0], e[1][1], e[1][2], e[1][3]);
+          bv[c] = make_float4(e[2][0], e[2][1], e[2][2], e[2][3]);
+        }
+      }
+    }
+    float a[4][4];  // [position][channel]
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const bool cin = c0 + c < C;
+      const float xs[4] = {xv[c].x, xv[c].y, xv[c].z, xv[c].w}, gs[4] = {gv[c].x, gv[c].y, gv[c].z, gv[c].w},
+                  bs[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool in = cin && pos0 + i >= 0 && pos0 + i < L;
+        a[i][c] = in ? act(fmaf((xs[i] - st.x) * st.y, gs[i], bs[i])) : 0.f;
+      }
+    }
+    const int q = (c0 & 31) >> 2;  // the 16-byte chunk of the channels
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(win + chunk_off(row0 + i, q)) = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
+  }
+
+  template <class Op>
+  __device__ void convert(const ConvCtx& c) const {
+    static_assert(Op::kind == MmaKind::TF32 && Op::kProducts == 3, "the fused path is the 3xTF32 mode");
+    constexpr uint32_t kFull = 0xffffffffu;
+    constexpr int kThreads = kConverterWarps * 32;
+    const int ct = int(threadIdx.x) - kGemmThreads;  // 0 .. kThreads - 1
+    const int lane = ct & 31;
+    const bool copier = ct < 128;                     // A row ct of each stage
+    uint8_t* win = c.scratch;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < c.num_tiles; t += gridDim.x) {
+      const Tile tl = tile(t);
+      const float2 st = stats[tl.b];
+      const float* xb = x + size_t(tl.b) * size_t(C) * size_t(L);
+      const int l0 = tl.r0 - pad;          // the first position any tap reads
+      const int la = (l0 >> 2) << 2;       // rounded down to a multiple of 4 (floor, also for l0 < 0)
+      const int shift = l0 - la;
+      const int quads = (wrows + shift + 3) >> 2;
+      for (int cb = 0; cb < ncb; ++cb) {
+        bar_sync(1, kThreads);  // the previous block's copies are done with the window
+        for (int task = ct; task < quads * 8; task += kThreads) {
+          const int qd = task >> 3, cq = task & 7;  // position quad, channel quartet
+          window_task(xb, st, la + 4 * qd, 4 * qd, cb * 32 + 4 * cq, win);
+        }
+        bar_sync(1, kThreads);  // the window is complete
+        if (!copier) continue;
+        for (int tap = 0; tap < ksize; ++tap) {
+          if (__any_sync(kFull, *c.abort_flag)) return;
+          if (!__all_sync(kFull, mbar_wait<true>(&c.empty[stage], phase ^ 1))) {
+            record_error(c.status, GF_DEV_WAIT_TIMEOUT);
+            *c.abort_flag = 1;
+            return;
+          }
+          uint8_t* a_hi = c.stages + stage * c.stage_bytes;
+          uint8_t* a_lo = a_hi + c.a_bytes / 2;
+          const int src_row = ct + shift + tap * dil;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 h = *reinterpret_cast<const float4*>(win + chunk_off(src_row, q));
+            const uint32_t off = chunk_off(ct, q);
+            *reinterpret_cast<float4*>(a_hi + off) = h;
+            *reinterpret_cast<float4*>(a_lo + off) =
+                make_float4(h.x - tf32_hi(h.x), h.y - tf32_hi(h.y), h.z - tf32_hi(h.z), h.w - tf32_hi(h.w));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c.full[stage]);
+          if (++stage == c.nstages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  }
+};
+
+// W[co][ci][t] -> planes[Cout][ksize * Cp] in the fused GEMM's k order:
+// k = (cb * ksize + t) * 32 + (ci - 32 cb), cb = ci / 32, zeros for the padding
+// channels C .. Cp - 1 (3xTF32 planes: the value and value - its TF32 part).
+__global__ void conv_weight_split_cb_kernel(const float* __restrict__ w, float* planes, int Cout, int C, int Cp,
+                                            int ksize) {
+  const int64_t n = int64_t(Cout) * ksize * Cp;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t co = i / (int64_t(ksize) * Cp);
+    const int k = int(i - co * (int64_t(ksize) * Cp));
+    const int kb = k / 32, c = k % 32;
+    const int cb = kb / ksize, t = kb % ksize;
+    const int ci = cb * 32 + c;
+    const float v = ci < C ? w[(co * C + ci) * ksize + t] : 0.f;
+    planes[i] = v;
+    planes[n + i] = v - tf32_hi(v);
+  }
+}
+
 // Epilogue: out[b][co][j] = acc + conv_b[co] + x[b][co][j].
 struct EpiConvResidual {
   static constexpr bool kFixedBN = true;
@@ -294,11 +482,20 @@ int64_t padded_channels(int64_t C, int32_t mode) {
 struct ConvWs {
   size_t part, stats, a_planes, w_planes, total;
   int chunks;
+  bool fused;  // the single GEMM with converter warps: no activation planes
 };
 
-ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
+// The fused LayerNorm/GELU/Conv1d GEMM (GF_FLAG_FUSED_PRODUCER) runs in the
+// 3xTF32 mode when the taps' window (128 + (ksize - 1) dilation positions)
+// fits its scratch.
+bool conv_fused_fits(int64_t ksize, int64_t dilation) {
+  return (ksize - 1) * dilation <= LnConvSrc<false>::kMaxWindow - 128;
+}
+
+ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode, bool fused) {
   const int64_t Cp = padded_channels(C, mode);
   ConvWs w{};
+  w.fused = fused;
   w.chunks = int((C * L + kLnChunk - 1) / kLnChunk);
   size_t off = 0;
   w.part = off;
@@ -306,7 +503,7 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode) {
   w.stats = off;
   off += align_up(size_t(B) * sizeof(float2), 256);
   w.a_planes = off;
-  off += align_up(size_t(B) * L * Cp * plane_bytes(mode), 256);
+  if (!fused) off += align_up(size_t(B) * L * Cp * plane_bytes(mode), 256);
   w.w_planes = off;
   off += align_up(size_t(C) * ksize * Cp * plane_bytes(mode), 256);
   w.total = off;
@@ -378,6 +575,46 @@ gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const vo
   const int64_t tiles = int64_t(B) * src.num_jb * src.num_nb;
   return launch_gemm<kBNConv, Op, ConvSrc, EpiConvResidual>(dev, maps, src, tiles, ep, s);
 }
+// The fused LayerNorm -> GELU -> dilated Conv1d GEMM (3xTF32): weight planes
+// in the channel-block-major k order, A built by the converter warps.
+template <bool TANH>
+gf_status launch_conv_fused(const DeviceInfo& dev, const float* x, const float* ln_gamma, const float* ln_beta,
+                            const float2* stats, const float* w_planes, int64_t B, int64_t C, int64_t L,
+                            int32_t ksize, int32_t dilation, int32_t padding, const EpiConvResidual::Params& ep,
+                            cudaStream_t s) {
+  using Op = OpTF32x3;
+  OperandMaps maps{};
+  const int64_t Cp = padded_channels(C, GF_MODE_FP32_3XTF32);
+  const uint64_t db[2] = {uint64_t(ksize) * Cp, uint64_t(C)};
+  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(kBNConv)};
+  const size_t w_plane = size_t(C) * ksize * Cp;
+  for (int p = 0; p < Op::kPlanes; ++p) {
+    const gf_status st = make_tmap(&maps.b[p], w_planes + p * w_plane, Op::kElem, 2, db, bb);
+    if (st != GF_OK) return st;
+  }
+  LnConvSrc<TANH> src{};
+  src.x = x;
+  src.gamma = ln_gamma;
+  src.beta = ln_beta;
+  src.stats = stats;
+  src.C = int(C);
+  src.Cp = int(Cp);
+  src.L = int(L);
+  src.pad = padding;
+  src.dil = dilation;
+  src.ksize = ksize;
+  src.num_jb = int((L + kBM - 1) / kBM);
+  src.num_nb = int((C + kBNConv - 1) / kBNConv);
+  src.num_kb = int(ksize * Cp / Op::kBK);
+  src.bn = kBNConv;
+  src.bk = Op::kBK;
+  src.nsamples = int(B);
+  src.kb_chunk = src.num_kb;
+  src.ncb = int(Cp / 32);
+  src.wrows = 128 + (ksize - 1) * dilation;
+  const int64_t tiles = int64_t(B) * src.num_jb * src.num_nb;
+  return launch_gemm<kBNConv, Op, LnConvSrc<TANH>, EpiConvResidual>(dev, maps, src, tiles, ep, s);
+}
 }  // namespace
 }  // namespace gf
 
@@ -385,11 +622,14 @@ using namespace gf;
 
 extern "C" {
 
-size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t mode) {
-  if (mode & ~(GF_FLAG_GELU_TANH | 0xff)) return 0;
+size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t dilation,
+                                             int32_t mode) {
+  if (mode & ~(GF_FLAG_GELU_TANH | GF_FLAG_FUSED_PRODUCER | 0xff)) return 0;
+  const bool fused = (mode & GF_FLAG_FUSED_PRODUCER) != 0;
   mode &= 0xff;
-  if (!conv_mode_ok(mode) || check_conv_shape(B, C, L, ksize, mode) != GF_OK || B == 0) return 0;
-  return conv_ws(B, C, L, ksize, mode).total;
+  if (!conv_mode_ok(mode) || check_conv_shape(B, C, L, ksize, mode) != GF_OK || B == 0 || dilation < 1) return 0;
+  if (fused && (mode != GF_MODE_FP32_3XTF32 || !conv_fused_fits(ksize, dilation))) return 0;
+  return conv_ws(B, C, L, ksize, mode, fused).total;
 }
 
 gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
@@ -398,20 +638,22 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
                                  size_t workspace_bytes, void* stream) {
   // (an empty batch, B = 0, may pass NULL for x and out)
   if ((B && (!x || !out)) || !ln_gamma || !ln_beta || !conv_w) return GF_ERR_NULL;
-  if (mode & ~(GF_FLAG_GELU_TANH | 0xff)) return GF_ERR_MODE;
+  if (mode & ~(GF_FLAG_GELU_TANH | GF_FLAG_FUSED_PRODUCER | 0xff)) return GF_ERR_MODE;
   const bool tanh_gelu = (mode & GF_FLAG_GELU_TANH) != 0;
+  const bool fused = (mode & GF_FLAG_FUSED_PRODUCER) != 0;
   mode &= 0xff;
-  if (!conv_mode_ok(mode)) return GF_ERR_MODE;
+  if (!conv_mode_ok(mode) || (fused && mode != GF_MODE_FP32_3XTF32)) return GF_ERR_MODE;
   gf_status st = check_conv_shape(B, C, L, ksize, mode);
   if (st != GF_OK) return st;
   if (dilation < 1 || padding < 0 || int64_t(2) * padding != int64_t(dilation) * (ksize - 1)) return GF_ERR_SHAPE;
   if (int64_t(dilation) * (ksize - 1) > (int64_t(1) << 30)) return GF_ERR_SHAPE;
   if (!(eps >= 0.f) || !std::isfinite(eps)) return GF_ERR_SHAPE;
+  if (fused && !conv_fused_fits(ksize, dilation)) return GF_ERR_SHAPE;
   if (!aligned16(x) || !aligned16(ln_gamma) || !aligned16(ln_beta) || !aligned16(conv_w) || !aligned16(out) ||
       (conv_b && !aligned16(conv_b)) || !aligned16(workspace))
     return GF_ERR_ALIGN;
   if (B == 0) return GF_OK;
-  const ConvWs wl = conv_ws(B, C, L, ksize, mode);
+  const ConvWs wl = conv_ws(B, C, L, ksize, mode, fused);
   if (!workspace) return GF_ERR_NULL;
   if (workspace_bytes < wl.total) return GF_ERR_WORKSPACE;
   const size_t xb = size_t(B) * C * L * 4;
@@ -439,6 +681,22 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   else
     ln_partial_kernel<false><<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
   ln_finalize_kernel<<<unsigned(B), 256, 0, s>>>(x, part, stats, C * L, wl.chunks, eps);
+  EpiConvResidual::Params ep{conv_b, x, out, int(C), int(L)};
+  if (wl.fused) {
+    // weights split once into the fused GEMM's k order; LayerNorm + GELU are
+    // applied inside the GEMM
+    const int64_t Cp = padded_channels(C, mode);
+    const int64_t n = C * Cp * ksize;
+    const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
+    conv_weight_split_cb_kernel<<<blocks, 256, 0, s>>>(conv_w, static_cast<float*>(w_planes), int(C), int(C),
+                                                       int(Cp), ksize);
+    if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
+    return tanh_gelu ? launch_conv_fused<true>(dev, x, ln_gamma, ln_beta, stats, static_cast<const float*>(w_planes),
+                                               B, C, L, ksize, dilation, padding, ep, s)
+                     : launch_conv_fused<false>(dev, x, ln_gamma, ln_beta, stats,
+                                                static_cast<const float*>(w_planes), B, C, L, ksize, dilation,
+                                                padding, ep, s);
+  }
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
       launch_conv_prepass<GF_MODE_FP32_3XTF32>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,
@@ -453,7 +711,6 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
                                                ksize, tanh_gelu, dev, s);
   }
   if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
-  EpiConvResidual::Params ep{conv_b, x, out, int(C), int(L)};
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
       return launch_conv_gemm<OpTF32x3>(dev, a_planes, w_planes, B, C, L, ksize, dilation, padding, ep, s);

@@ -16,7 +16,7 @@
 //   OpBF16x1  one BF16 product (the BF16 mode).
 // All modes accumulate in fp32 in TMEM.
 //
-// Roles (one CTA per SM, 320 threads):
+// Roles (one CTA per SM, 320 threads, plus a source's converter warps):
 //   warp 0      one thread issues TMA loads of a k-block's operand tiles (one
 //               or two planes of A and of B) into a ring of smem stages
 //               (full/empty mbarriers);
@@ -35,7 +35,12 @@
 // swizzle, so one MMA K-step is always 32 bytes of the row.
 //
 // The operand source (a plain [rows, K] matrix, or the implicit-GEMM view of
-// a dilated Conv1d) and the epilogue are template policies.
+// a dilated Conv1d) and the epilogue are template policies.  A source may
+// build the A operand itself instead of loading it (kConverterWarps > 0):
+// then warp 0 loads only B, and that many more warps (after the epilogue
+// warps) write each stage's A planes with ordinary shared-memory stores
+// (fence.proxy.async, then one arrival per warp on the stage's full
+// barrier), using kScratchBytes of shared memory of their own.
 //
 // Chunked accumulation (epi_chunked below): the tensor core adds
 // each MMA's products into the fp32 accumulator with truncation, which over a
@@ -92,20 +97,21 @@ using OpTF32x3 = MmaOp<MmaKind::TF32, 3>;
 using OpBF16x3 = MmaOp<MmaKind::BF16, 3>;
 using OpBF16x1 = MmaOp<MmaKind::BF16, 1>;
 
-template <int BN, class Op>
+template <int BN, class Op, int EXTRA = 0>
 struct TileCfg {
   static constexpr int A_BYTES = kBM * 128;  // one plane of a 128-row tile
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = Op::kPlanes * (A_BYTES + B_BYTES);
-  // stages within 220 KB (plus barriers and alignment: under the 227 KB a
-  // CTA may use)
-  static constexpr int STAGES_FIT = (220 * 1024) / STAGE_BYTES;
+  // stages within 220 KB less the source's own scratch (plus barriers and
+  // alignment: under the 227 KB a CTA may use)
+  static constexpr int STAGES_FIT = (220 * 1024 - EXTRA) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   // two accumulators, each starting on a multiple of TMEM_COLS / 2
   static constexpr int TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int ACC_STRIDE = TMEM_COLS / 2;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int EXTRA_BYTES = EXTRA;  // after the barriers
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + EXTRA + 1024;
   static_assert(STAGES >= 2, "need at least two smem stages");
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
                 "TMEM allocation must be a power of two >= 32 columns");
@@ -118,6 +124,37 @@ struct TileCfg {
 struct OperandMaps {
   CUtensorMap a[2];
   CUtensorMap b[2];
+};
+
+// Converter warps of a source (0: TMA loads A) and their shared scratch.
+template <class Src, class = void>
+struct SrcConv {
+  static constexpr int warps = 0;
+  static constexpr int arrivals = 0;
+  static constexpr int scratch = 0;
+};
+template <class Src>
+struct SrcConv<Src, decltype(void(Src::kConverterWarps))> {
+  static constexpr int warps = Src::kConverterWarps;
+  static constexpr int arrivals = Src::kArrivingWarps;  // converter warps that arrive on a stage's full barrier
+  static constexpr int scratch = Src::kScratchBytes;
+};
+template <class Src>
+__host__ __device__ constexpr int gemm_threads() {
+  return kGemmThreads + 32 * SrcConv<Src>::warps;
+}
+
+// What the converter warps of a source get from the kernel: the stage ring
+// and its barriers, the abort flag and status word, and their scratch.
+struct ConvCtx {
+  uint8_t* stages;       // stage s at stages + s * stage_bytes: A planes, then B planes
+  int stage_bytes, a_bytes, nstages;
+  uint64_t* full;
+  uint64_t* empty;
+  volatile uint32_t* abort_flag;
+  uint32_t* status;
+  uint8_t* scratch;
+  int num_tiles;
 };
 
 // One output tile: rows r0..r0+127 of sample b (b = 0 for a plain GEMM),
@@ -209,10 +246,11 @@ struct ConvSrc {
 };
 
 template <int BN, class Op, class Src, class Epi>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<Src>(), 1)
     gemm_tc_kernel(const __grid_constant__ OperandMaps maps, const Src src, const typename Epi::Params ep,
                    uint32_t* status) {
-  using Cfg = TileCfg<BN, Op>;
+  constexpr int kConv = SrcConv<Src>::warps;
+  using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch>;
   constexpr int S = Cfg::STAGES;
   constexpr int P = Op::kPlanes;
   extern __shared__ uint8_t smem_raw[];
@@ -224,13 +262,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  uint8_t* scratch = smem + S * Cfg::STAGE_BYTES + Cfg::BAR_BYTES;  // the converters' (kConv > 0)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + SrcConv<Src>::arrivals);  // the TMA thread (and the converter warps)
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -286,7 +325,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             sa[p] = a_addr(stage, p);
             sb[p] = b_addr(stage, p);
           }
-          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+          mbar_arrive_expect_tx(&full[stage], kConv ? P * Cfg::B_BYTES : Cfg::STAGE_BYTES);
           src.template load<P>(maps, &full[stage], sa, sb, tile, kb);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -393,6 +432,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(drain, 0)) record_error(status, GF_DEV_WAIT_TIMEOUT);
     }
     __syncwarp();
+  } else if (warp >= 2 + kEpiWarps) {
+    // ---------------------------------------------------------- converters
+    if constexpr (kConv > 0) {
+      const ConvCtx c{smem, Cfg::STAGE_BYTES, P * Cfg::A_BYTES, S, full, empty, abort_flag, status, scratch,
+                      num_tiles};
+      src.template convert<Op>(c);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     constexpr int H = epi_halves(BN), BNW = BN / H;
@@ -492,13 +538,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int BN, class Op, class Src, class Epi>
 gf_status launch_gemm(const DeviceInfo& dev, const OperandMaps& maps, const Src& src, int64_t tiles,
                       const typename Epi::Params& ep, cudaStream_t stream) {
-  using Cfg = TileCfg<BN, Op>;
+  using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch>;
   const int grid = int(tiles < dev.sm_count ? tiles : dev.sm_count);
   auto kern = gemm_tc_kernel<BN, Op, Src, Epi>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return GF_ERR_CUDA;
   profile_mark_begin(stream);
-  kern<<<grid, kGemmThreads, Cfg::SMEM_BYTES, stream>>>(maps, src, ep, device_status_word());
+  kern<<<grid, gemm_threads<Src>(), Cfg::SMEM_BYTES, stream>>>(maps, src, ep, device_status_word());
   profile_mark_end(stream);
   return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
 }

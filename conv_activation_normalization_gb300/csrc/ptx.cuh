@@ -113,6 +113,12 @@ __device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity)
   }
 }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a
+// multiple of 32): the warps of one role synchronise without the others.
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -83,6 +83,16 @@ typedef int32_t gf_status;
  * erf form.  Other calls reject it (GF_ERR_MODE). */
 #define GF_FLAG_GELU_TANH 0x100
 
+/* Flag OR'd into the mode of gf_ln_gelu_dconv1d_res (and its workspace
+ * query), 3xTF32 mode only: LayerNorm and GELU are applied inside the conv
+ * GEMM while it builds its operand tiles (page Kimi-K2.6__l2_p5 turn 2 fuses
+ * them into the loading step), so the workspace holds no activation planes:
+ * about 2 MB instead of 8 B per activation (270 MB for x[32,256,4096]).  It is
+ * slower than the default (about 0.46 against 0.32 ms per call on that
+ * workload) and needs (ksize - 1) * dilation <= 92 (else GF_ERR_SHAPE; other
+ * modes: GF_ERR_MODE).  Results equal the default path's up to rounding. */
+#define GF_FLAG_FUSED_PRODUCER 0x200
+
 /* Chains whose GEMM tile width gf_linear_tile_width reports. */
 #define GF_CHAIN_GROUPNORM 0  /* gf_linear_swish_bias_groupnorm (and _planes, _host) */
 #define GF_CHAIN_LSE       1  /* gf_linear_lse_act                                    */
@@ -261,9 +271,11 @@ gf_status gf_linear_lse_act(const float* x, const float* W, const float* b, floa
  *   tiles of 256),
  *   L >= 1, 1 <= ksize <= 16, dilation >= 1,
  *   2*padding == dilation*(ksize-1) (length-preserving, as the residual needs).
+ *   The workspace query takes the dilation and the mode with its flags: the
+ *   size depends on whether GF_FLAG_FUSED_PRODUCER is given.
  * ---------------------------------------------------------------------- */
 size_t gf_ln_gelu_dconv1d_res_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize,
-                                             int32_t mode);
+                                             int32_t dilation, int32_t mode);
 gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const float* ln_beta,
                                  const float* conv_w, const float* conv_b, float* out,
                                  int64_t B, int64_t C, int64_t L, int32_t ksize, int32_t dilation,

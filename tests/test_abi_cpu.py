@@ -31,7 +31,7 @@ def test_exports_every_header_symbol(L):
     for n in names:
         assert hasattr(L, n), n
         assert n in binding._SIGS, f"binding lacks a signature for {n}"
-    assert L.gf_abi_version() == 1
+    assert L.gf_abi_version() == 2
 
 
 def test_status_strings(L):
@@ -82,12 +82,26 @@ def test_workspace_sizes(L):
     # one (max, sum) float2 per row and column half of each n-block, sized
     # for the narrowest (160-column) tile width
     assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (-(-N // 160) * 2) * 8
-    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0) > 2 * 4 * 32 * 256 * 4096
+    # the default keeps activation planes (8 B per activation in the
+    # 3xTF32 mode); GF_FLAG_FUSED_PRODUCER (3xTF32, taps within 92
+    # positions) only the LayerNorm partials, statistics and weight planes
+    FUSED = 0x200
+    planes = L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, 0)
+    assert planes > 2 * 4 * 32 * 256 * 4096
+    fused = L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, FUSED)
+    assert 2 * 4 * 256 * 256 * 3 <= fused < 4 << 20
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 46, FUSED) == fused
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 47, FUSED) == 0  # taps span 94 > 92
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, FUSED | 1) == 0  # 3xTF32 only
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, 2) > 2 * 2 * 32 * 256 * 4096
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0, 0) == 0  # dilation >= 1
     GELU_TANH = 0x100
     for mode in (0, 1, 2):  # the GELU flag changes no buffer
-        assert (L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, mode | GELU_TANH) ==
-                L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, mode))
-    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 0x400) == 0
+        for dil in (4, 64):
+            assert (L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, dil, mode | GELU_TANH) ==
+                    L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, dil, mode))
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, 0x400) == 0
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, 0x800) == 0
     assert L.gf_linear_workspace_size(M, K, N, GELU_TANH) == 0  # other calls take no flag
     assert L.gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 2, 1, 4) > 0
     # other strides, kernel sizes, channel counts and groups take the general
@@ -122,7 +136,8 @@ def test_dconv1d_validation(L):
                  mode=0, ws=P[6], wsb=None)
         a.update(kw)
         if a["wsb"] is None:
-            a["wsb"] = L.gf_ln_gelu_dconv1d_res_workspace_size(a["B"], a["C"], a["L"], a["k"], a["mode"])
+            a["wsb"] = L.gf_ln_gelu_dconv1d_res_workspace_size(a["B"], a["C"], a["L"], a["k"], max(a["d"], 1),
+                                                               a["mode"])
         return L.gf_ln_gelu_dconv1d_res(a["x"], a["g"], a["b"], a["w"], a["cb"], a["out"], a["B"], a["C"], a["L"],
                                         a["k"], a["d"], a["p"], a["eps"], a["mode"], a["ws"], a["wsb"], None)
     assert call(g=None) == GF_ERR_NULL
@@ -131,7 +146,9 @@ def test_dconv1d_validation(L):
     assert call(C=1056) == GF_ERR_SHAPE            # at most 1024 channels
     assert call(L=0) == GF_ERR_SHAPE
     assert call(mode=5) == GF_ERR_MODE
-    assert call(mode=0x200) == GF_ERR_MODE         # unknown flag bit
+    assert call(mode=0x400) == GF_ERR_MODE         # unknown flag bit
+    assert call(mode=0x201) == GF_ERR_MODE         # the fused producer is 3xTF32 only
+    assert call(mode=0x200, d=47, p=47) == GF_ERR_SHAPE  # taps span 94 > 92
     assert call(mode=0x103) == GF_ERR_MODE         # tanh flag on an unknown precision mode
     assert call(mode=0x100, L=0) == GF_ERR_SHAPE   # the flag passes; the shape does not
     assert call(w=P[3] + 4) == GF_ERR_ALIGN
@@ -183,7 +200,8 @@ def test_binding_constants_match_the_header():
     import re
     defs = {m.group(1): int(m.group(2), 0) for m in
             re.finditer(r"#define\s+(GF_[A-Z0-9_]+)\s+(-?(?:0x[0-9a-fA-F]+|\d+))\b", _header_text())}
-    for name in ("GF_MODE_FP32_3XTF32", "GF_MODE_BF16", "GF_MODE_FP32_3XBF16", "GF_FLAG_GELU_TANH"):
+    for name in ("GF_MODE_FP32_3XTF32", "GF_MODE_BF16", "GF_MODE_FP32_3XBF16", "GF_FLAG_GELU_TANH",
+                 "GF_FLAG_FUSED_PRODUCER", "GF_CHAIN_GROUPNORM", "GF_CHAIN_LSE", "GF_CHAIN_LINEAR"):
         assert getattr(binding, name) == defs[name], name
     for name, v in (("GF_OK", GF_OK), ("GF_ERR_NULL", GF_ERR_NULL), ("GF_ERR_SHAPE", GF_ERR_SHAPE),
                     ("GF_ERR_ALIGN", GF_ERR_ALIGN), ("GF_ERR_ALIAS", GF_ERR_ALIAS),
@@ -243,7 +261,7 @@ def test_empty_batches_launch_nothing(L):
     assert L.gf_linear_swish_bias_groupnorm_host(None, P[1], P[2], P[3], P[4], P[5], None, 0, 64, 256, 4, 1e-5, 0, 0,
                                                  None, 0, None) == GF_OK
     assert L.gf_linear_swish_bias_groupnorm_host_workspace_size(0, 64, 256, 4, 0, 0) == 0
-    assert L.gf_ln_gelu_dconv1d_res_workspace_size(0, 256, 4096, 3, 0) == 0
+    assert L.gf_ln_gelu_dconv1d_res_workspace_size(0, 256, 4096, 3, 4, 0) == 0
     assert L.gf_ln_gelu_dconv1d_res(None, P[1], P[2], P[3], P[4], None, 0, 256, 4096, 3, 4, 4, 1e-5, 0, None, 0,
                                     None) == GF_OK
     assert L.gf_ln_gelu_dconv1d_res(None, P[1], P[2], P[3], P[4], None, 0, 256, 4096, 3, 4, 3, 1e-5, 0, None, 0,

@@ -20,7 +20,7 @@ static int fails = 0;
 #define EXPECT(cond) do { if (!(cond)) { printf("FAIL line %d: %s\n", __LINE__, #cond); ++fails; } } while (0)
 
 int main(void) {
-  EXPECT(gf_abi_version() == 1);
+  EXPECT(gf_abi_version() == 2);
   EXPECT(strcmp(gf_status_string(GF_OK), "ok") == 0 || strlen(gf_status_string(GF_OK)) > 0);
   EXPECT(strlen(gf_status_string(GF_ERR_SHAPE)) > 0);
   /* NULL pointers are rejected before anything touches a device */
@@ -36,7 +36,7 @@ int main(void) {
   EXPECT(gf_linear_swish_bias_groupnorm_workspace_size(32768, 1024, 4096, 64, GF_MODE_FP32_3XTF32) ==
          (size_t)4 * (32768 * 1024 + 4096 * 1024));
   EXPECT(gf_linear_swish_bias_groupnorm_workspace_size(32768, 1024, 4096, 3, GF_MODE_FP32_3XTF32) == 0);
-  EXPECT(gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, GF_MODE_FP32_3XTF32 | GF_FLAG_GELU_TANH) > 0);
+  EXPECT(gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, GF_MODE_FP32_3XTF32 | GF_FLAG_GELU_TANH) > 0);
   EXPECT(gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 3, 2, 1, 4) > 0);
   EXPECT(gf_convt3d_swish_gn_hswish_workspace_size(128, 3, 16, 16, 32, 32, 9, 2, 1, 4) == 0);
   printf("%s\n", fails ? "failed" : "ok");
@@ -55,7 +55,7 @@ def _compiler(name):
 @pytest.mark.parametrize("lang,cc,std", [("c", "gcc", "-std=c99"), ("c++", "g++", "-std=c++17")])
 def test_header_compiles_strictly(tmp_path, lang, cc, std):
     src = tmp_path / ("h.c" if lang == "c" else "h.cpp")
-    src.write_text('#include "gf.h"\nint main(void) { return gf_abi_version() == 1 ? 0 : 1; }\n')
+    src.write_text('#include "gf.h"\nint main(void) { return gf_abi_version() == 2 ? 0 : 1; }\n')
     r = subprocess.run([_compiler(cc), std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
                         "-I", INCLUDE, str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr

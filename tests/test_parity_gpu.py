@@ -317,6 +317,47 @@ def test_dconv1d_any_length(B, C, L, dil):
     assert_close(got, ref, f"dconv1d {B}x{C}x{L} d{dil}")
 
 
+@pytest.mark.parametrize("B,C,L,k,dil,gelu", [(2, 64, 300, 3, 46, "erf"), (2, 64, 300, 3, 4, "erf"),
+                                              (1, 32, 4, 3, 4, "erf"), (3, 256, 520, 3, 2, "tanh"),
+                                              (2, 40, 262, 5, 23, "erf"), (1, 300, 200, 3, 46, "erf"),
+                                              (3, 20, 131, 3, 1, "tanh"), (2, 33, 301, 3, 3, "erf"),
+                                              (1, 1024, 64, 3, 1, "erf")])
+def test_dconv1d_fused_producer(B, C, L, k, dil, gelu):
+    # GF_FLAG_FUSED_PRODUCER: LayerNorm + GELU inside the GEMM's operand
+    # build; taps spanning up to 92 positions ((k - 1) dil = 92 is the widest
+    # window), any channel count and length (scalar loads when L % 4 != 0)
+    s = synth.DConv1dShape(B=B, C=C, L=L, ksize=k, dilation=dil, padding=dil * (k - 1) // 2)
+    d = synth.dconv1d_inputs(s, 1100 + dil + C, affine="perturbed")
+    got = gf.gf_ln_gelu_dconv1d_res(T(d["x"]), T(d["ln_gamma"]), T(d["ln_beta"]), T(d["conv_w"]), T(d["conv_b"]),
+                                    s.dilation, s.padding, s.eps, gelu=gelu, fused_producer=True).cpu().numpy()
+    ref = oracle.ln_gelu_dconv1d_res(d["x"], d["ln_gamma"], d["ln_beta"], d["conv_w"], d["conv_b"], s.dilation,
+                                     s.padding, s.eps, gelu=gelu)
+    assert_close(got, ref, f"dconv1d fused producer {B}x{C}x{L} k{k} d{dil} {gelu}")
+
+
+def test_dconv1d_fused_producer_workload_sampled():
+    s, seed = synth.WORKLOADS["ln_dconv1d_b32"]
+    d = synth.dconv1d_inputs(s, seed)
+    got = gf.gf_ln_gelu_dconv1d_res(T(d["x"]), T(d["ln_gamma"]), T(d["ln_beta"]), T(d["conv_w"]), T(d["conv_b"]),
+                                    s.dilation, s.padding, s.eps, fused_producer=True).cpu().numpy()
+    idx = np.array([0, 31])
+    ref = oracle.ln_gelu_dconv1d_res(d["x"][idx], d["ln_gamma"], d["ln_beta"], d["conv_w"], d["conv_b"], s.dilation,
+                                     s.padding, s.eps)
+    assert_close(got[idx], ref, "dconv1d fused producer, full workload (samples 0, 31)")
+
+
+def test_dconv1d_fused_producer_rejects_wide_taps_and_other_modes():
+    s = synth.DConv1dShape(B=1, C=32, L=300, ksize=3, dilation=47, padding=47)
+    d = synth.dconv1d_inputs(s, 5)
+    args = [T(d[k]) for k in ("x", "ln_gamma", "ln_beta", "conv_w", "conv_b")]
+    with pytest.raises(gf.GFError) as e:
+        gf.gf_ln_gelu_dconv1d_res(*args, s.dilation, s.padding, s.eps, fused_producer=True)
+    assert e.value.status == -2  # GF_ERR_SHAPE: (k - 1) dilation = 94 > 92
+    with pytest.raises(gf.GFError) as e:
+        gf.gf_ln_gelu_dconv1d_res(*args, 4, 4, s.eps, mode=1, fused_producer=True)
+    assert e.value.status == -6  # GF_ERR_MODE: the 3xTF32 mode only
+
+
 def test_dconv1d_kernel_size_5():
     s = synth.DConv1dShape(B=2, C=64, L=256, ksize=5, dilation=3, padding=6)
     got, ref = _dc_run(s, synth.dconv1d_inputs(s, 5, affine="perturbed"))
