@@ -104,7 +104,7 @@ uint32_t* device_status_word() {
 }
 
 gf_status make_tmap(CUtensorMap* map, const void* base, int elem_bytes, int rank, const uint64_t* dims,
-                    const uint32_t* box) {
+                    const uint32_t* box, int swizzle_bytes) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode) {
@@ -117,7 +117,8 @@ gf_status make_tmap(CUtensorMap* map, const void* base, int elem_bytes, int rank
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
   }
-  if (rank < 1 || rank > 5 || (elem_bytes != 4 && elem_bytes != 2) || box[0] * uint32_t(elem_bytes) != 128)
+  if (rank < 1 || rank > 5 || (elem_bytes != 4 && elem_bytes != 2) || (swizzle_bytes != 128 && swizzle_bytes != 64) ||
+      box[0] * uint32_t(elem_bytes) != uint32_t(swizzle_bytes))
     return GF_ERR_SHAPE;
   cuuint64_t gdim[5], gstride[4];
   cuuint32_t bdim[5], estride[5];
@@ -132,7 +133,8 @@ gf_status make_tmap(CUtensorMap* map, const void* base, int elem_bytes, int rank
   const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUresult r = g_encode(map, dt, cuuint32_t(rank), const_cast<void*>(base),
                               gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GF_OK : GF_ERR_CUDA;
 }

@@ -97,22 +97,26 @@ using OpTF32x3 = MmaOp<MmaKind::TF32, 3>;
 using OpBF16x3 = MmaOp<MmaKind::BF16, 3>;
 using OpBF16x1 = MmaOp<MmaKind::BF16, 1>;
 
+constexpr int kMaxDynSmem = 227 * 1024;  // dynamic shared memory one CTA may use
+
 template <int BN, class Op, int EXTRA = 0>
 struct TileCfg {
   static constexpr int A_BYTES = kBM * 128;  // one plane of a 128-row tile
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = Op::kPlanes * (A_BYTES + B_BYTES);
-  // stages within 220 KB less the source's own scratch (plus barriers and
-  // alignment: under the 227 KB a CTA may use)
-  static constexpr int STAGES_FIT = (220 * 1024 - EXTRA) / STAGE_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int EXTRA_BYTES = EXTRA;  // after the barriers
+  // as many stages (up to 8) as fit beside the barriers, the source's and
+  // the epilogue's scratch and the 1024-byte alignment slack in the 227 KB
+  // of shared memory a CTA may use
+  static constexpr int STAGES_FIT = (kMaxDynSmem - BAR_BYTES - 1024 - EXTRA) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   // two accumulators, each starting on a multiple of TMEM_COLS / 2
   static constexpr int TMEM_COLS = 2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512);
   static constexpr int ACC_STRIDE = TMEM_COLS / 2;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int EXTRA_BYTES = EXTRA;  // after the barriers
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + EXTRA + 1024;
   static_assert(STAGES >= 2, "need at least two smem stages");
+  static_assert(SMEM_BYTES <= kMaxDynSmem, "over the shared memory a CTA may use");
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
                 "TMEM allocation must be a power of two >= 32 columns");
   // epilogue halves of BN / 2 columns are read in pieces of 16
@@ -141,27 +145,13 @@ struct SrcConv<Src, decltype(void(Src::kConverterWarps))> {
   static constexpr int arrivals = Src::kArrivingWarps;  // converter warps that arrive on a stage's full barrier
   static constexpr int scratch = Src::kScratchBytes;
 };
-// Per-column parameter vectors an epilogue has staged in shared memory for
-// each tile (0: none): kParamVectors vectors of the tile's columns, which the
-// epilogue warps of a column half copy in (one float4 per thread and vector
-// at most) before they run the epilogue on the half, so that the epilogue
-// reads them with shared-memory loads instead of one global load per 4
-// columns per thread (which, beside the output stores, fills the global
-// load/store queue).
-template <class Epi, class = void>
-struct EpiParams {
-  static constexpr int vectors = 0;
-};
-template <class Epi>
-struct EpiParams<Epi, decltype(void(Epi::kParamVectors))> {
-  static constexpr int vectors = Epi::kParamVectors;
-};
-// Epilogues that can write their output as 32-row x 32-column fp32 boxes,
-// staged in shared memory and sent by TMA stores (kTmaStore), do so in the
-// one-plane operand mode.  There the MMAs are fast enough that the plain
-// path's stores bound the kernel: a thread owns a row, so each warp store
-// instruction touches 32 rows' cache lines.  (The three-product modes are
-// bound by their MMAs, and their larger stages leave no room for the boxes.)
+// Epilogues that can write their output as boxes of 32 rows x 16 fp32
+// columns, staged in shared memory and sent by TMA stores (kTmaStore), do so
+// in the one-plane operand mode.  There the MMAs are fast enough that the
+// plain path's stores bound the kernel: a thread owns a row, so each warp
+// store instruction touches 32 rows' cache lines.  (The three-product modes
+// are bound by their MMAs, and their larger stages leave no room for the
+// boxes.)
 template <class Epi, class = void>
 struct EpiTma {
   static constexpr bool value = false;
@@ -174,19 +164,16 @@ template <class Epi, class Op>
 __host__ __device__ constexpr bool epi_tma_store() {
   return EpiTma<Epi>::value && Op::kPlanes == 1;
 }
-constexpr int kStoreBoxFloats = 32 * 32;
-template <class Epi, class Op, int BN>
+constexpr int kStoreBoxFloats = 32 * 16;  // 2 KB: a row is 64 bytes (64-byte swizzle)
+template <class Epi, class Op>
 __host__ __device__ constexpr int epi_smem_bytes() {
-  // the parameters of two tiles (alternating), both halves; then, 1024-byte
-  // aligned, two box buffers per epilogue warp
-  return 2 * EpiParams<Epi>::vectors * BN * 4 +
-         (epi_tma_store<Epi, Op>() ? 1024 + kEpiWarps * 2 * kStoreBoxFloats * 4 : 0);
+  // two box buffers per epilogue warp, 1024-byte aligned
+  return epi_tma_store<Epi, Op>() ? 1024 + kEpiWarps * 2 * kStoreBoxFloats * 4 : 0;
 }
 
 // An epilogue warp's output path through TMA stores: its two box buffers
-// (1024-byte aligned, 4 KB each, used in turn), the output's tensor map, the
-// first output row of the warp's 32 rows, and the number of boxes the warp
-// has stored so far (which buffer is next).
+// (used in turn), the output's tensor map, the first output row of the
+// warp's 32 rows, and the number of boxes the warp has stored so far.
 struct BoxStore {
   float* buf;
   const CUtensorMap* map;
@@ -194,7 +181,7 @@ struct BoxStore {
   uint32_t n;
 };
 
-template <class Src>
+template <class Src, class Epi, class Op, int BN>
 __host__ __device__ constexpr int gemm_threads() {
   return kGemmThreads + 32 * SrcConv<Src>::warps;
 }
@@ -301,11 +288,11 @@ struct ConvSrc {
 };
 
 template <int BN, class Op, class Src, class Epi>
-__global__ void __launch_bounds__(gemm_threads<Src>(), 1)
+__global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
     gemm_tc_kernel(const __grid_constant__ OperandMaps maps, const Src src, const typename Epi::Params ep,
                    uint32_t* status) {
   constexpr int kConv = SrcConv<Src>::warps;
-  using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op, BN>()>;
+  using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op>()>;
   constexpr int S = Cfg::STAGES;
   constexpr int P = Op::kPlanes;
   extern __shared__ uint8_t smem_raw[];
@@ -315,11 +302,11 @@ __global__ void __launch_bounds__(gemm_threads<Src>(), 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* psync = drain + 1;  // [2] per column half: its warps' parameter copies done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(psync + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint8_t* scratch = smem + S * Cfg::STAGE_BYTES + Cfg::BAR_BYTES;  // the converters' (kConv > 0)
-  float* epi_par = reinterpret_cast<float*>(scratch + SrcConv<Src>::scratch);  // staged column parameters
+  float* boxes = reinterpret_cast<float*>(  // the epilogue's TMA-store boxes
+      (reinterpret_cast<uintptr_t>(scratch + SrcConv<Src>::scratch) + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -334,7 +321,6 @@ __global__ void __launch_bounds__(gemm_threads<Src>(), 1)
       mbar_init(&tempty[a], 128 * epi_halves(BN));  // every thread of the active epilogue warps
     }
     mbar_init(drain, 1);
-    for (int h = 0; h < 2; ++h) mbar_init(&psync[h], 4);  // one arrival per epilogue warp of the half
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -559,12 +545,9 @@ __global__ void __launch_bounds__(gemm_threads<Src>(), 1)
       constexpr bool kTma = epi_tma_store<Epi, Op>();
       BoxStore st{};
       if constexpr (kTma) {
-        const uintptr_t boxes =
-            (reinterpret_cast<uintptr_t>(epi_par + 2 * EpiParams<Epi>::vectors * BN) + 1023) & ~uintptr_t(1023);
-        st.buf = reinterpret_cast<float*>(boxes) + (warp - 2) * 2 * kStoreBoxFloats;
+        st.buf = boxes + (warp - 2) * 2 * kStoreBoxFloats;
         st.map = &maps.c;
       }
-      int tcount = 0;  // tiles this half has done (parameter buffer parity)
       for (int t = blockIdx.x; half < H && t < num_tiles; t += gridDim.x) {
         const Tile tile = src.tile(t);
         bool ok = mbar_wait(&tfull[acc], acc_phase);
@@ -580,27 +563,9 @@ __global__ void __launch_bounds__(gemm_threads<Src>(), 1)
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * Cfg::ACC_STRIDE + half * BNW);
         const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
-        if constexpr (EpiParams<Epi>::vectors > 0) {
-          // stage the half's column parameters in the buffer of this tile's
-          // parity (the other one may still be read for the previous tile),
-          // then wait (bounded) until the half's four warps have copied theirs
-          constexpr int V = EpiParams<Epi>::vectors;
-          float* sp = epi_par + ((tcount & 1) * H + half) * V * BNW;
-          const int th = (warp - 2 - 4 * half) * 32 + lane;
-          for (int i = th; i < V * BNW / 4; i += 128) {
-            const int v = i / (BNW / 4), c4 = i % (BNW / 4);
-            reinterpret_cast<float4*>(sp)[i] = Epi::param4(ep, v, part.n0 + 4 * c4);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&psync[half]);
-          if (!__all_sync(0xffffffffu, mbar_wait_inline(&psync[half], uint32_t(tcount & 1)))) {
-            record_error(status, GF_DEV_WAIT_TIMEOUT);
-            *abort_flag = 1;
-            break;
-          }
-          ++tcount;
+        if constexpr (EpiTma<Epi>::value) {
           st.y = part.r0 + quad * 32;
-          Epi::template apply<BNW, kTma>(ep, taddr, part, row, sp, st);
+          Epi::template apply<BNW, kTma>(ep, taddr, part, row, st);
         } else {
           Epi::template apply<BNW>(ep, taddr, part, row);
         }
@@ -632,13 +597,13 @@ __global__ void __launch_bounds__(gemm_threads<Src>(), 1)
 template <int BN, class Op, class Src, class Epi>
 gf_status launch_gemm(const DeviceInfo& dev, const OperandMaps& maps, const Src& src, int64_t tiles,
                       const typename Epi::Params& ep, cudaStream_t stream) {
-  using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op, BN>()>;
+  using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op>()>;
   const int grid = int(tiles < dev.sm_count ? tiles : dev.sm_count);
   auto kern = gemm_tc_kernel<BN, Op, Src, Epi>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return GF_ERR_CUDA;
   profile_mark_begin(stream);
-  kern<<<grid, gemm_threads<Src>(), Cfg::SMEM_BYTES, stream>>>(maps, src, ep, device_status_word());
+  kern<<<grid, gemm_threads<Src, Epi, Op, BN>(), Cfg::SMEM_BYTES, stream>>>(maps, src, ep, device_status_word());
   profile_mark_end(stream);
   return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
 }

@@ -53,11 +53,11 @@ gf_status cuda_status(cudaError_t e);
 
 // TMA ---------------------------------------------------------------------
 // Tiled tensor map of fp32 (elem_bytes 4) or bf16 (elem_bytes 2) data with
-// 128-byte swizzle and zero fill out of bounds.  dims[0] is the contiguous
-// dimension; strides are derived from a dense layout; box[0] * elem_bytes
-// must be 128.
+// 128-byte swizzle (or 64-byte, swizzle_bytes = 64) and zero fill out of
+// bounds.  dims[0] is the contiguous dimension; strides are derived from a
+// dense layout; box[0] * elem_bytes must equal the swizzle span.
 gf_status make_tmap(CUtensorMap* map, const void* base, int elem_bytes, int rank, const uint64_t* dims,
-                    const uint32_t* box);
+                    const uint32_t* box, int swizzle_bytes = 128);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

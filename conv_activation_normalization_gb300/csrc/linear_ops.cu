@@ -18,15 +18,15 @@ namespace gf {
 
 // ------------------------------------------------------------- epilogues
 // Linear -> Swish -> +bias -> GroupNorm on a 128 x BN accumulator tile; one
-// thread owns one row.  The four per-column vectors (b_lin, bias, gamma,
-// beta) of the tile's columns are staged in shared memory by the kernel
-// (kParamVectors, param4) and read from there: sp[v * BN + column].  A group is gw consecutive columns (gw = 16, 32, 64 or
+// thread owns one row.  A group is gw consecutive columns (gw = 16, 32, 64 or
 // 128).  Columns are handled 64 at a time: the mean and the (two-pass,
 // biased) variance of each 16-column quarter's group are formed in the
 // thread's registers.  A 128-column group spans two such halves: the first
 // half's t is parked in TMEM (over its accumulator), the halves' (mean, M2)
 // are merged with the pairwise update of Chan, Golub and LeVeque, and the
-// first half is read back for its output.
+// first half is read back for its output.  The output goes out with plain
+// stores, or (TMA) as boxes of 32 rows x 16 columns written to shared memory
+// and sent by TMA stores.
 struct GNParams {
   const float* b_lin;  // may be null
   const float* bias;
@@ -45,24 +45,14 @@ struct EpiSwishBiasGNT {
   // takes a warp's whole half of a 256-column tile
   static constexpr int kMinBN = GW == 128 ? 256 : 64;
   static constexpr int kTileGW = GW;  // the group width the tile-width rule sees
-  static constexpr int kParamVectors = 4;  // b_lin, bias, gamma, beta
   static constexpr bool kTmaStore = true;  // the output may go out as TMA-stored boxes
   using Params = GNParams;
-
-  // columns n .. n + 3 of parameter vector v (0 past N; b_lin may be null)
-  __device__ __forceinline__ static float4 param4(const Params& p, int v, int n) {
-    const float* src = v == 0 ? p.b_lin : v == 1 ? p.bias : v == 2 ? p.gamma : p.beta;
-    if (!src || n >= p.N) return make_float4(0.f, 0.f, 0.f, 0.f);
-    return __ldg(reinterpret_cast<const float4*>(src + n));  // (N is a multiple of 16 here)
-  }
 
   // t = Swish(y + b_lin) + bias over the 64 columns n0.., in place; q[i] =
   // sum of quarter i's t.  Quarters from nq on lie past the last column
   // (N is a multiple of the group width, so only when GW < 64) and are left
   // alone.
-  // sp: the staged parameters of these 64 columns (vector v at v * BN)
-  template <int BN>
-  __device__ __forceinline__ static void swish_bias(const float* sp, int nq, float (&v)[64], float (&q)[4]) {
+  __device__ __forceinline__ static void swish_bias(const Params& p, int n0, int nq, float (&v)[64], float (&q)[4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       q[i] = 0.f;
@@ -70,8 +60,8 @@ struct EpiSwishBiasGNT {
       float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 16 * i; j < 16 * i + 16; j += 4) {
-        const float4 bl = *reinterpret_cast<const float4*>(sp + j);
-        const float4 bb = *reinterpret_cast<const float4*>(sp + BN + j);
+        const float4 bl = p.b_lin ? __ldg(reinterpret_cast<const float4*>(p.b_lin + n0 + j)) : make_float4(0, 0, 0, 0);
+        const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + n0 + j));
         const float2 a = add2(swish2(add2(make_float2(v[j], v[j + 1]), make_float2(bl.x, bl.y))),
                               make_float2(bb.x, bb.y));
         const float2 c = add2(swish2(add2(make_float2(v[j + 2], v[j + 3]), make_float2(bl.z, bl.w))),
@@ -107,18 +97,17 @@ struct EpiSwishBiasGNT {
       m2[i] = acc.x + acc.y;
     }
   }
-  // (t - mu) rstd gamma + beta over the 64 columns of the row at sp (the
+  // (t - mu) rstd gamma + beta over the 64 columns n0.. of the row (the
   // first nq quarters)
-  template <int BN>
-  __device__ __forceinline__ static void normalize_store(const float* sp, int nq, const float (&v)[64],
+  __device__ __forceinline__ static void normalize_store(const Params& p, int n0, int nq, const float (&v)[64],
                                                          const float (&mu)[4], const float (&rstd)[4], float* orow,
                                                          bool valid) {
 #pragma unroll
     for (int j = 0; j < 64; j += 4) {
       if (j / 16 >= nq) break;  // uniform across the warp
       const float2 nm = make_float2(-mu[j / 16], -mu[j / 16]), r2 = make_float2(rstd[j / 16], rstd[j / 16]);
-      const float4 ga = *reinterpret_cast<const float4*>(sp + 2 * BN + j);
-      const float4 be = *reinterpret_cast<const float4*>(sp + 3 * BN + j);
+      const float4 ga = __ldg(reinterpret_cast<const float4*>(p.gamma + n0 + j));
+      const float4 be = __ldg(reinterpret_cast<const float4*>(p.beta + n0 + j));
       const float2 a = fma2(mul2(add2(make_float2(v[j], v[j + 1]), nm), r2), make_float2(ga.x, ga.y),
                             make_float2(be.x, be.y));
       const float2 c = fma2(mul2(add2(make_float2(v[j + 2], v[j + 3]), nm), r2), make_float2(ga.z, ga.w),
@@ -126,61 +115,64 @@ struct EpiSwishBiasGNT {
       if (valid) __stcs(reinterpret_cast<float4*>(orow + j), make_float4(a.x, a.y, c.x, c.y));
     }
   }
-  // The same values for columns J0 .. J0 + 31 of the 64, sent as one box:
-  // lane l writes its row into row l of a 128-byte-swizzled box (16-byte
-  // piece c of row l at piece c ^ (l & 7): a warp's 16-byte writes hit
-  // distinct banks in each group of 8 lanes), then lane 0 stores the box at
-  // output column x + J0, row st.y (rows past M and columns past N are not
-  // written).  A buffer is rewritten once the store issued from it two boxes
-  // earlier has read it.
-  template <int BN, int J0>
-  __device__ __forceinline__ static void normalize_box(const float* sp, int nq, const float (&v)[64],
-                                                       const float (&mu)[4], const float (&rstd)[4], BoxStore& st,
-                                                       int x) {
-    if (J0 / 16 >= nq) return;  // the box lies past the last column (uniform across the warp)
+  // The same values for quarter J0 / 16 (columns n0 + J0 ..  + 15), sent as
+  // one box: lane l writes its row's 64 bytes into row l of a box with the
+  // 64-byte swizzle (16-byte piece c of row l at piece c ^ ((l >> 1) & 3):
+  // the warp's 16-byte writes hit distinct banks in each group of 8 lanes),
+  // then lane 0 stores the box at output column n0 + J0, row st.y (rows past
+  // M are not written).  The values are formed first; the buffer, used two
+  // boxes earlier, is rewritten once that box's store has read it.
+  template <int J0>
+  __device__ __forceinline__ static void normalize_box(const Params& p, int n0, const float (&v)[64], float mu,
+                                                       float rstd, BoxStore& st) {
     const int lane = int(threadIdx.x & 31);
+    const float2 nm = make_float2(-mu, -mu), r2 = make_float2(rstd, rstd);
+    float4 o[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = J0 + 4 * c;
+      const float4 ga = __ldg(reinterpret_cast<const float4*>(p.gamma + n0 + j));
+      const float4 be = __ldg(reinterpret_cast<const float4*>(p.beta + n0 + j));
+      const float2 a = fma2(mul2(add2(make_float2(v[j], v[j + 1]), nm), r2), make_float2(ga.x, ga.y),
+                            make_float2(be.x, be.y));
+      const float2 d = fma2(mul2(add2(make_float2(v[j + 2], v[j + 3]), nm), r2), make_float2(ga.z, ga.w),
+                            make_float2(be.z, be.w));
+      o[c] = make_float4(a.x, a.y, d.x, d.y);
+    }
     float* b = st.buf + (st.n & 1) * kStoreBoxFloats;
     if (st.n >= 2) {
       if (lane == 0) bulk_wait_read<1>();
       __syncwarp();
     }
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int j = J0 + 4 * c;
-      if (j / 16 >= nq) break;  // uniform across the warp
-      const float2 nm = make_float2(-mu[j / 16], -mu[j / 16]), r2 = make_float2(rstd[j / 16], rstd[j / 16]);
-      const float4 ga = *reinterpret_cast<const float4*>(sp + 2 * BN + j);
-      const float4 be = *reinterpret_cast<const float4*>(sp + 3 * BN + j);
-      const float2 a = fma2(mul2(add2(make_float2(v[j], v[j + 1]), nm), r2), make_float2(ga.x, ga.y),
-                            make_float2(be.x, be.y));
-      const float2 d = fma2(mul2(add2(make_float2(v[j + 2], v[j + 3]), nm), r2), make_float2(ga.z, ga.w),
-                            make_float2(be.z, be.w));
-      *reinterpret_cast<float4*>(b + lane * 32 + ((c ^ (lane & 7)) << 2)) = make_float4(a.x, a.y, d.x, d.y);
-    }
+    for (int c = 0; c < 4; ++c) *reinterpret_cast<float4*>(b + lane * 16 + ((c ^ ((lane >> 1) & 3)) << 2)) = o[c];
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(st.map, smem_u32(b), x + J0, st.y);
+      tma_store_2d(st.map, smem_u32(b), n0 + J0, st.y);
       bulk_commit();
     }
     ++st.n;
   }
-  // normalised output of the 64 columns starting at output column x (row
-  // pointer orow + x ... for the plain stores)
-  template <int BN, bool TMA>
-  __device__ __forceinline__ static void emit(const float* sp, int nq, const float (&v)[64], const float (&mu)[4],
-                                              const float (&rstd)[4], float* orow, bool valid, BoxStore& st, int x) {
+  // the normalised 64 columns n0.. (their first nq quarters) of the row:
+  // boxes (TMA) or plain stores
+  template <bool TMA>
+  __device__ __forceinline__ static void emit(const Params& p, int n0, int nq, const float (&v)[64],
+                                              const float (&mu)[4], const float (&rstd)[4], float* orow, bool valid,
+                                              BoxStore& st) {
     if constexpr (TMA) {
-      normalize_box<BN, 0>(sp, nq, v, mu, rstd, st, x);
-      normalize_box<BN, 32>(sp, nq, v, mu, rstd, st, x);
+      normalize_box<0>(p, n0, v, mu[0], rstd[0], st);
+      if (nq > 1) normalize_box<16>(p, n0, v, mu[1], rstd[1], st);  // (nq uniform across the warp)
+      if (nq > 2) normalize_box<32>(p, n0, v, mu[2], rstd[2], st);
+      if (nq > 3) normalize_box<48>(p, n0, v, mu[3], rstd[3], st);
     } else {
-      normalize_store<BN>(sp, nq, v, mu, rstd, orow + x, valid);
+      normalize_store(p, n0, nq, v, mu, rstd, orow, valid);
     }
   }
 
   template <int BN, bool TMA>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row,
-                                               const float* sp, BoxStore& st) {
+                                               BoxStore& st) {
     const int m = t.r0 + row;
     const bool valid = m < p.M;
     float* orow = p.out + size_t(m) * size_t(p.N);
@@ -191,7 +183,7 @@ struct EpiSwishBiasGNT {
       float v[64], q[4], mu[4], m2[4], rs[4];
       // first half: t and its (mean, M2); t parked over the accumulator
       tmem_load64(taddr, v);
-      swish_bias<BN>(sp, 4, v, q);
+      swish_bias(p, n0, 4, v, q);
       const float mean0 = (q[0] + q[1] + q[2] + q[3]) * (1.f / 64.f);
 #pragma unroll
       for (int i = 0; i < 4; ++i) mu[i] = mean0;
@@ -209,7 +201,7 @@ struct EpiSwishBiasGNT {
       }
       // second half
       tmem_load64(taddr + 64, v);
-      swish_bias<BN>(sp + 64, 4, v, q);
+      swish_bias(p, n0 + 64, 4, v, q);
       const float mean1 = (q[0] + q[1] + q[2] + q[3]) * (1.f / 64.f);
 #pragma unroll
       for (int i = 0; i < 4; ++i) mu[i] = mean1;
@@ -224,10 +216,10 @@ struct EpiSwishBiasGNT {
         mu[i] = mean;
         rs[i] = rstd;
       }
-      emit<BN, TMA>(sp + 64, 4, v, mu, rs, orow, valid, st, n0 + 64);
+      emit<TMA>(p, n0 + 64, 4, v, mu, rs, orow + n0 + 64, valid, st);
       tmem_wait_st();
       tmem_load64(taddr, v);
-      emit<BN, TMA>(sp, 4, v, mu, rs, orow, valid, st, n0);
+      emit<TMA>(p, n0, 4, v, mu, rs, orow + n0, valid, st);
     } else {
 #pragma unroll 1
       for (int g = 0; g < BN / 64; ++g) {
@@ -237,7 +229,7 @@ struct EpiSwishBiasGNT {
         const int nq = GW >= 64 ? 4 : min(4, (p.N - n0) / 16);
         float v[64], q[4], mu[4], m2[4], rs[4];
         tmem_load64(taddr + uint32_t(g * 64), v);
-        swish_bias<BN>(sp + g * 64, nq, v, q);
+        swish_bias(p, n0, nq, v, q);
         if constexpr (GW == 64) {  // one group: one mean, one M2
           float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
@@ -256,7 +248,7 @@ struct EpiSwishBiasGNT {
             mu[i] = mean;
             rs[i] = rstd;
           }
-          emit<BN, TMA>(sp + g * 64, nq, v, mu, rs, orow, valid, st, n0);
+          emit<TMA>(p, n0, nq, v, mu, rs, orow + n0, valid, st);
         } else {
           constexpr float inv = 1.f / float(GW);  // a power of two: exact
           float gs[4], gm2[4];
@@ -267,7 +259,7 @@ struct EpiSwishBiasGNT {
           group_sums(m2, gm2);
 #pragma unroll
           for (int i = 0; i < 4; ++i) rs[i] = rsqrtf(gm2[i] * inv + p.eps);
-          emit<BN, TMA>(sp + g * 64, nq, v, mu, rs, orow, valid, st, n0);
+          emit<TMA>(p, n0, nq, v, mu, rs, orow + n0, valid, st);
         }
       }
     }
@@ -694,10 +686,10 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
     st = make_tmap(&maps.b[p], b.p[p], Op::kElem, 2, db, bb);
     if (st != GF_OK) return st;
   }
-  if constexpr (epi_tma_store<Epi, Op>()) {  // the output, in the epilogue's 32 x 32 boxes
+  if constexpr (epi_tma_store<Epi, Op>()) {  // the output, in the epilogue's boxes of 32 rows x 16 columns
     const uint64_t dc[2] = {uint64_t(N), uint64_t(M)};
-    const uint32_t bc[2] = {32u, 32u};
-    const gf_status st = make_tmap(&maps.c, ep.out, 4, 2, dc, bc);
+    const uint32_t bc[2] = {16u, 32u};
+    const gf_status st = make_tmap(&maps.c, ep.out, 4, 2, dc, bc, 64);
     if (st != GF_OK) return st;
   }
   LinearSrc src;
