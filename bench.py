@@ -640,7 +640,7 @@ def run_ours(wl, args, quiet=False):
                                      "kernel_ms": round(pm.mean_ms, 4)}}
         MODE = base_mode
 
-    extra = wl.extra_measure(gf, t, stream) if hasattr(wl, "extra_measure") else None
+    extra = wl.extra_measure(gf, t, stream) if hasattr(wl, "extra_measure") and not args.no_extras else None
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu:
@@ -815,6 +815,8 @@ def main():
     ap.add_argument("--no-other-modes", action="store_true")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="headline run only: skip measuring the other four workloads")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="profiling: skip the extra entry points timed beside a workload (no-workspace, fused producer)")
     ap.add_argument("--eager", action="store_true", help="time one library call per step instead of graph replays")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-chunks", type=int, default=1)
