@@ -40,7 +40,6 @@ _SIGS = {
     "gf_profile_end": (_I32, [ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_float)]),
     "gf_measure_tensor_rate": (_I32, [_I32, _I32, _I32, ctypes.POINTER(ctypes.c_double)]),
     "gf_linear_tile_width": (_I32, [_I32, _I64, _I64, _I32, _I32, _I32]),
-    "gf_linear_gn_split_k": (_I32, [_I64, _I64, _I64, _I32, _I32, _I32]),
     "gf_testing_host_pipeline_trace": (_I32, [_I64, _I32, ctypes.c_char_p, _SZ]),
     "gf_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I32]),
     "gf_linear": (_I32, [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _SZ, _P]),
@@ -103,12 +102,6 @@ def linear_tile_width(chain: int, M: int, N: int, groups: int, mode: int, sm_cou
     """The GEMM tile width the Linear chains' dispatch picks (host arithmetic
     only; 0 for invalid arguments)."""
     return lib().gf_linear_tile_width(chain, M, N, groups, mode, sm_count)
-
-
-def linear_gn_split_k(M: int, K: int, N: int, groups: int, mode: int, sm_count: int) -> int:
-    """CTAs per tile that split the K loop of the Linear->GroupNorm GEMM (1: no
-    split; host arithmetic only; 0 for invalid arguments)."""
-    return lib().gf_linear_gn_split_k(M, K, N, groups, mode, sm_count)
 
 
 def measure_tensor_rate(kind: str, iters: int = 4096, repeats: int = 5) -> float:

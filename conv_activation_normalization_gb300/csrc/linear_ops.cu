@@ -46,7 +46,6 @@ struct EpiSwishBiasGNT {
   static constexpr int kMinBN = GW == 128 ? 256 : 64;
   static constexpr int kTileGW = GW;  // the group width the tile-width rule sees
   static constexpr bool kTmaStore = true;  // the output may go out as TMA-stored boxes
-  static constexpr bool kSplitK = GW <= 64;  // the split-K cluster kernel can run it
   using Params = GNParams;
 
   // t = Swish(y + b_lin) + bias over the 64 columns n0.., in place; q[i] =
@@ -171,47 +170,6 @@ struct EpiSwishBiasGNT {
     }
   }
 
-  // The rest of the epilogue on 64 accumulator columns n0.. of the row (v,
-  // raw; GW <= 64): Swish + bias, the groups' mean and variance, the
-  // normalised output (the first nq quarters).
-  template <bool TMA>
-  __device__ __forceinline__ static void finish64(const Params& p, int n0, int nq, float (&v)[64], float* orow,
-                                                  bool valid, BoxStore& st) {
-    float q[4], mu[4], m2[4], rs[4];
-    swish_bias(p, n0, nq, v, q);
-    if constexpr (GW == 64) {  // one group: one mean, one M2
-      float2 sum = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sum.x += q[i];
-      const float mean = sum.x * (1.f / 64.f);
-      const float2 nmean = make_float2(-mean, -mean);
-      float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 64; j += 2) {
-        const float2 d = add2(make_float2(v[j], v[j + 1]), nmean);
-        acc = fma2(d, d, acc);
-      }
-      const float rstd = rsqrtf((acc.x + acc.y) * (1.f / 64.f) + p.eps);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mu[i] = mean;
-        rs[i] = rstd;
-      }
-      emit<TMA>(p, n0, nq, v, mu, rs, orow, valid, st);
-    } else {
-      constexpr float inv = 1.f / float(GW);  // a power of two: exact
-      float gs[4], gm2[4];
-      group_sums(q, gs);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mu[i] = gs[i] * inv;
-      quarter_m2(v, mu, m2);
-      group_sums(m2, gm2);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) rs[i] = rsqrtf(gm2[i] * inv + p.eps);
-      emit<TMA>(p, n0, nq, v, mu, rs, orow, valid, st);
-    }
-  }
-
   template <int BN, bool TMA>
   __device__ __forceinline__ static void apply(const Params& p, uint32_t taddr, const Tile& t, int row,
                                                BoxStore& st) {
@@ -269,256 +227,44 @@ struct EpiSwishBiasGNT {
         if (n0 >= p.N) break;  // uniform across the warp
         // quarters inside the row (all four unless GW < 64 and N % 64 != 0)
         const int nq = GW >= 64 ? 4 : min(4, (p.N - n0) / 16);
-        float v[64];
+        float v[64], q[4], mu[4], m2[4], rs[4];
         tmem_load64(taddr + uint32_t(g * 64), v);
-        finish64<TMA>(p, n0, nq, v, orow + n0, valid, st);
+        swish_bias(p, n0, nq, v, q);
+        if constexpr (GW == 64) {  // one group: one mean, one M2
+          float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) sum.x += q[i];
+          const float mean = sum.x * (1.f / 64.f);
+          const float2 nmean = make_float2(-mean, -mean);
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 64; j += 2) {
+            const float2 d = add2(make_float2(v[j], v[j + 1]), nmean);
+            acc = fma2(d, d, acc);
+          }
+          const float rstd = rsqrtf((acc.x + acc.y) * (1.f / 64.f) + p.eps);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            mu[i] = mean;
+            rs[i] = rstd;
+          }
+          emit<TMA>(p, n0, nq, v, mu, rs, orow + n0, valid, st);
+        } else {
+          constexpr float inv = 1.f / float(GW);  // a power of two: exact
+          float gs[4], gm2[4];
+          group_sums(q, gs);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mu[i] = gs[i] * inv;
+          quarter_m2(v, mu, m2);
+          group_sums(m2, gm2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) rs[i] = rsqrtf(gm2[i] * inv + p.eps);
+          emit<TMA>(p, n0, nq, v, mu, rs, orow + n0, valid, st);
+        }
       }
     }
   }
 };
-
-// ---------------------------------------------------------------- split-K
-// Linear -> Swish -> bias -> GroupNorm for few rows.  With one 64-column tile
-// per CTA each CTA streams the whole K loop of its operands through a
-// latency-bound stage ring; here the K loop is split over the kCsplit CTAs of
-// a thread-block cluster instead, each multiplying a 128 x 256 tile over its
-// share of K into TMEM (a quarter of the operand bytes per CTA).  Each CTA
-// parks its partial accumulator in its shared memory as four 64-column
-// quarters (over its operand stages, whose loads and MMAs are done by then),
-// and once every CTA of the cluster has parked, sends quarter j to CTA j with
-// the bulk-copy engine (the copies complete as transaction bytes on the
-// receiver's mbarrier).  CTA j sums its own quarter and the three it received
-// and runs the GroupNorm epilogue on them: groups of at most 64 columns stay
-// within a quarter.  Hand-offs between CTAs are mbarriers with bounded waits;
-// the cluster barrier runs only once, after the barriers are initialised.
-constexpr int kCsplit = 4;
-constexpr int kSkBN = 256;
-constexpr int kSkQuarterFloats = kBM * (kSkBN / kCsplit);   // 128 rows x 64 columns
-constexpr int kSkPartBytes = kCsplit * kSkQuarterFloats * 4;  // the parked partial, 128 KB
-constexpr int kSkRecvBytes = (kCsplit - 1) * kSkQuarterFloats * 4;  // quarters received from the peers
-
-// Offset (in floats) of column c (0..63) of row r in a parked quarter: rows of
-// 64 floats whose 16-byte pieces are permuted (piece i at i ^ (r & 7)), so
-// that the 16-byte accesses of 8 consecutive rows hit distinct banks.
-__device__ __forceinline__ int sk_offset(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 7))) << 2) + (c & 3); }
-
-template <class Op, int GW>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_splitk_gn_kernel(const __grid_constant__ OperandMaps maps, const LinearSrc src, const GNParams ep,
-                          int kb_per_split, uint32_t* status) {
-  using Epi = EpiSwishBiasGNT<GW>;
-  using Cfg = TileCfg<kSkBN, Op>;
-  constexpr int S = Cfg::STAGES;
-  constexpr int P = Op::kPlanes;
-  constexpr int kData = S * Cfg::STAGE_BYTES > kSkPartBytes + kSkRecvBytes ? S * Cfg::STAGE_BYTES
-                                                                          : kSkPartBytes + kSkRecvBytes;
-  constexpr uint32_t kFull = 0xffffffffu;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* part = reinterpret_cast<float*>(smem);                  // [4][128 x 64], after the K loop
-  float* recv = reinterpret_cast<float*>(smem + kSkPartBytes);  // [3][128 x 64] from the peers
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kData);
-  uint64_t* empty = full + S;
-  uint64_t* tfull = empty + S;
-  uint64_t* ready = tfull + 1;  // every CTA of the cluster has parked its partial (kCsplit x 256 arrivals)
-  uint64_t* rbar = ready + 1;   // the three quarters sent to this CTA have landed (transaction bytes)
-  uint64_t* done = rbar + 1;    // the three peers have received this CTA's quarters (3 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t rank = cluster_ctarank();
-  const Tile tile = src.tile(int(blockIdx.y));
-  const int kb0 = int(rank) * kb_per_split;
-  const int nkb = max(0, min(kb_per_split, src.num_kb - kb0));  // this CTA's k-blocks (0 leaves a zero partial)
-
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < S; ++st) {
-      mbar_init(&full[st], 1);
-      mbar_init(&empty[st], 1);
-    }
-    mbar_init(tfull, 1);
-    mbar_init(ready, kCsplit * 32 * kEpiWarps);
-    mbar_init(rbar, 1);
-    mbar_init(done, kCsplit - 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(rbar, uint32_t(kSkRecvBytes));  // the phase ends when all three quarters have landed
-  }
-  if (warp == 0 && lane == 0) {
-#pragma unroll
-    for (int pl = 0; pl < P; ++pl) {
-      prefetch_tmap(&maps.a[pl]);
-      prefetch_tmap(&maps.b[pl]);
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kSkBN);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  cluster_sync_all();  // every CTA's barriers are initialised before any arrives on a peer's
-  const uint32_t tmem_base = *tmem_slot;
-  auto a_addr = [&](int st, int pl) { return smem_u32(smem + st * Cfg::STAGE_BYTES + pl * Cfg::A_BYTES); };
-  auto b_addr = [&](int st, int pl) {
-    return smem_u32(smem + st * Cfg::STAGE_BYTES + P * Cfg::A_BYTES + pl * Cfg::B_BYTES);
-  };
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int i = 0; i < nkb; ++i) {
-        if (!mbar_wait(&empty[stage], phase ^ 1)) {
-          record_error(status, GF_DEV_WAIT_TIMEOUT);
-          break;
-        }
-        uint32_t sa[2], sb[2];
-#pragma unroll
-        for (int pl = 0; pl < P; ++pl) {
-          sa[pl] = a_addr(stage, pl);
-          sb[pl] = b_addr(stage, pl);
-        }
-        mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-        src.template load<P>(maps, &full[stage], sa, sb, tile, kb0 + i);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && nkb > 0) {
-      constexpr uint32_t idesc = Op::template idesc<kSkBN>();
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int i = 0; i < nkb; ++i) {
-        if (!mbar_wait(&full[stage], phase)) {
-          record_error(status, GF_DEV_WAIT_TIMEOUT);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a_hi = a_addr(stage, 0), b_hi = b_addr(stage, 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t off = uint32_t(kk * 32);  // one MMA K-step = 32 bytes of the row
-          const uint32_t accumulate = i != 0 || kk != 0;
-          if constexpr (Op::kProducts == 3) {
-            const uint32_t a_lo = a_addr(stage, 1), b_lo = b_addr(stage, 1);
-            Op::mma(tmem_base, sdesc_kmajor_sw128(a_lo + off), sdesc_kmajor_sw128(b_hi + off), idesc, accumulate);
-            Op::mma(tmem_base, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_lo + off), idesc, 1u);
-            Op::mma(tmem_base, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, 1u);
-          } else {
-            Op::mma(tmem_base, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, accumulate);
-          }
-        }
-        mma_commit(&empty[stage]);
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-      mma_commit(tfull);  // (also after a failed wait: it completes once the issued MMAs have)
-    }
-    __syncwarp();
-  } else {
-    // ---------------------------------------- epilogue, part 1: park the partial
-    const int quad = warp & 3, half = (warp - 2) >> 2;
-    const int row = quad * 32 + lane;
-    bool ok = true;
-    if (nkb > 0) {
-      ok = __all_sync(kFull, mbar_wait(tfull, 0));
-      if (!ok) record_error(status, GF_DEV_WAIT_TIMEOUT);
-      tc_fence_after();
-    }
-#pragma unroll 1
-    for (int c = 0; c < kSkBN / 2; c += 64) {  // quarter 2 half + c / 64 of the tile
-      float v[64];
-      if (nkb > 0 && ok) {
-        tmem_load64(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(half * (kSkBN / 2) + c), v);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 64; ++j) v[j] = 0.f;
-      }
-      float* q = part + (2 * half + c / 64) * kSkQuarterFloats;
-#pragma unroll
-      for (int j = 0; j < 64; j += 4)
-        *reinterpret_cast<float4*>(q + sk_offset(row, j)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-    }
-    fence_proxy_async_smem();  // the bulk copies (async proxy) read what these stores wrote
-    // this thread's rows and columns are parked (and this CTA's operand
-    // stages, where its peers' quarters land, are free): tell every CTA
-#pragma unroll
-    for (int r = 0; r < kCsplit; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(ready), uint32_t(r)));
-  }
-  tc_fence_before();
-  __syncthreads();  // the TMEM reads are done
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kSkBN);
-  }
-  if (warp == 6) {
-    // once every CTA has parked, quarter j of this CTA's partial goes to CTA j
-    // (into slot `rank` less one past j's own).  A warp of its own, waiting
-    // as a whole: the receiving warps below spin on the copies' arrival, and
-    // a lane of theirs could not be relied on to be scheduled while its warp
-    // mates spin.
-    if (__all_sync(kFull, mbar_wait_cluster(ready, 0))) {
-      if (lane == 0) {
-#pragma unroll 1
-        for (int j = 0; j < kCsplit; ++j) {
-          if (j == int(rank)) continue;
-          const int slot = int(rank) < j ? int(rank) : int(rank) - 1;
-          bulk_copy_s2c(mapa_shared(smem_u32(recv + slot * kSkQuarterFloats), uint32_t(j)),
-                        smem_u32(part + j * kSkQuarterFloats), uint32_t(kSkQuarterFloats * 4),
-                        mapa_shared(smem_u32(rbar), uint32_t(j)));
-        }
-      }
-    } else {
-      record_error(status, GF_DEV_WAIT_TIMEOUT);
-    }
-  }
-  if (warp >= 2 && warp < 6) {
-    // ------------------------------- epilogue, part 2: column quarter `rank`
-    const int row = (warp - 2) * 32 + lane;  // (any warp may take any row: the data is in shared memory now)
-    const bool ok = __all_sync(kFull, mbar_wait(rbar, 0));
-    if (!ok) record_error(status, GF_DEV_WAIT_TIMEOUT);
-    float v[64];
-    {
-      const float* own = part + int(rank) * kSkQuarterFloats;
-#pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        float4 x = *reinterpret_cast<const float4*>(own + sk_offset(row, j));
-#pragma unroll
-        for (int s3 = 0; s3 < kCsplit - 1; ++s3) {
-          const float4 y = *reinterpret_cast<const float4*>(recv + s3 * kSkQuarterFloats + sk_offset(row, j));
-          x = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
-        }
-        v[j] = x.x;
-        v[j + 1] = x.y;
-        v[j + 2] = x.z;
-        v[j + 3] = x.w;
-      }
-    }
-    // the quarters the peers sent have landed: their senders may leave
-    if (warp == 2 && lane == 0) {
-#pragma unroll 1
-      for (int j = 0; j < kCsplit; ++j)
-        if (j != int(rank)) mbar_arrive_cluster(mapa_shared(smem_u32(done), uint32_t(j)));
-    }
-    const int n0 = tile.n0 + int(rank) * (kSkBN / kCsplit), m = tile.r0 + row;
-    if (ok && n0 < ep.N) {  // (uniform across the warp)
-      const int nq = GW >= 64 ? 4 : min(4, (ep.N - n0) / 16);
-      BoxStore st{};
-      Epi::template finish64<false>(ep, n0, nq, v, ep.out + size_t(m) * size_t(ep.N) + n0, m < ep.M, st);
-    }
-    // no CTA leaves while its quarters may still be in flight to a peer
-    if (warp == 2 && !__all_sync(kFull, mbar_wait_cluster(done, 0))) record_error(status, GF_DEV_WAIT_TIMEOUT);
-  }
-}
 
 // Any other group width: the epilogue stores t = Swish(y + b_lin) + bias
 // and gn_rows_kernel normalises the rows in place afterwards (one more pass
@@ -811,21 +557,6 @@ int linear_tile_width(bool lse, int64_t M, int64_t N, int gw, int32_t mode, int 
 // Group widths the GEMM epilogue normalises itself (others: gn_rows_kernel).
 bool gn_fused_width(int64_t gw) { return gw == 16 || gw == 32 || gw == 64 || gw == 128; }
 
-// CTAs that split the K loop of a Linear -> GroupNorm tile (the cluster
-// kernel), or 1: when even 64-column tiles leave part of the GPU idle, the
-// 4-CTA clusters of 256-column tiles fit in one wave, the groups fit in a
-// 64-column quarter, and every CTA gets at least two k-blocks.
-// gf_linear_gn_split_k and the dispatch both use this function.
-int gn_split_k(int64_t M, int64_t K, int64_t N, int64_t gw, int32_t mode, int sm_count) {
-  if (gw != 16 && gw != 32 && gw != 64) return 1;
-  const int64_t mb = (M + kBM - 1) / kBM;
-  if (mb * ((N + 63) / 64) >= sm_count) return 1;
-  if (mb * ((N + kSkBN - 1) / kSkBN) * kCsplit > sm_count) return 1;
-  const int64_t bk = mode == GF_MODE_FP32_3XTF32 ? 32 : 64;  // k-block: one 128-byte row of the operand planes
-  if ((K + bk - 1) / bk < 2 * kCsplit) return 1;
-  return kCsplit;
-}
-
 bool mode_ok(int32_t mode) {
   return mode == GF_MODE_FP32_3XTF32 || mode == GF_MODE_BF16 || mode == GF_MODE_FP32_3XBF16;
 }
@@ -976,71 +707,6 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
   return launch_gemm<BN, Op, LinearSrc, Epi>(dev, maps, src, tiles, ep, stream);
 }
 
-// The split-K cluster kernel on 128 x 256 tiles: grid (kCsplit, tiles),
-// clusters of kCsplit CTAs along x.
-template <class Op, int GW>
-gf_status run_splitk_gn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K, int64_t N,
-                        const GNParams& ep, cudaStream_t stream) {
-  (void)dev;
-  using Cfg = TileCfg<kSkBN, Op>;
-  constexpr int kData = Cfg::STAGES * Cfg::STAGE_BYTES > kSkPartBytes + kSkRecvBytes
-                            ? Cfg::STAGES * Cfg::STAGE_BYTES
-                            : kSkPartBytes + kSkRecvBytes;
-  constexpr int kSmem = kData + Cfg::BAR_BYTES + 1024;  // (+ 1024-byte alignment slack)
-  static_assert(kSmem <= kMaxDynSmem, "over the shared memory a CTA may use");
-  OperandMaps maps{};
-  const uint64_t da[2] = {uint64_t(K), uint64_t(M)};
-  const uint32_t ba[2] = {uint32_t(Op::kBK), uint32_t(kBM)};
-  const uint64_t db[2] = {uint64_t(K), uint64_t(N)};
-  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(kSkBN)};
-  for (int p = 0; p < Op::kPlanes; ++p) {
-    gf_status st = make_tmap(&maps.a[p], a.p[p], Op::kElem, 2, da, ba);
-    if (st != GF_OK) return st;
-    st = make_tmap(&maps.b[p], b.p[p], Op::kElem, 2, db, bb);
-    if (st != GF_OK) return st;
-  }
-  LinearSrc src;
-  src.num_mb = int((M + kBM - 1) / kBM);
-  src.num_nb = int((N + kSkBN - 1) / kSkBN);
-  src.num_kb = int((K + Op::kBK - 1) / Op::kBK);
-  src.kb_chunk = src.num_kb;
-  src.bn = kSkBN;
-  src.bk = Op::kBK;
-  src.m_fastest = 0;
-  const int kb_per_split = (src.num_kb + kCsplit - 1) / kCsplit;
-  auto kern = gemm_splitk_gn_kernel<Op, GW>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
-    return GF_ERR_CUDA;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(kCsplit, unsigned(src.num_mb * src.num_nb), 1);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCsplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) return GF_ERR_CUDA;
-  profile_mark_begin(stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, src, ep, kb_per_split, device_status_word());
-  profile_mark_end(stream);
-  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
-}
-
-// Epilogues the split-K cluster kernel can run (kSplitK)
-template <class Epi, class = void>
-struct EpiSplitK {
-  static constexpr bool value = false;
-};
-template <class Epi>
-struct EpiSplitK<Epi, decltype(void(Epi::kSplitK))> {
-  static constexpr bool value = Epi::kSplitK;
-};
-
 // Runs the GEMM at the tile width linear_tile_width picks.  The LSE
 // partials' layout follows the tile width (the caller sized them with the
 // same function); a fused epilogue's groups must not straddle warps
@@ -1049,11 +715,6 @@ template <class Op, class Epi>
 gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
                              int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
   const int32_t mode = Op::kProducts == 1 ? GF_MODE_BF16 : GF_MODE_FP32_3XTF32;  // (only BF16 or not matters)
-  if constexpr (EpiSplitK<Epi>::value) {
-    const int32_t kmode = Op::kBK == 32 ? GF_MODE_FP32_3XTF32 : GF_MODE_BF16;  // (only the k-block width matters)
-    if (gn_split_k(M, K, N, Epi::kTileGW, kmode, dev.sm_count) > 1)
-      return run_splitk_gn<Op, Epi::kTileGW>(dev, a, b, M, K, N, ep, stream);
-  }
   if constexpr (Epi::kFixedBN) {
     switch (linear_tile_width(true, M, N, 0, mode, dev.sm_count)) {
       case 160: return run_linear_gemm<160, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
@@ -1114,11 +775,6 @@ int32_t gf_linear_tile_width(int32_t chain, int64_t M, int64_t N, int32_t groups
     case GF_CHAIN_LINEAR: return linear_tile_width(false, M, N, 0, mode, sm_count);
     default: return 0;
   }
-}
-
-int32_t gf_linear_gn_split_k(int64_t M, int64_t K, int64_t N, int32_t groups, int32_t mode, int32_t sm_count) {
-  if (!mode_ok(mode) || sm_count < 1 || M < 0 || K < 1 || N < 1 || !gn_groups_ok(N, groups)) return 0;
-  return gn_split_k(M, K, N, N / groups, mode, sm_count);
 }
 
 size_t gf_linear_swish_bias_groupnorm_workspace_size(int64_t M, int64_t K, int64_t N, int32_t groups,

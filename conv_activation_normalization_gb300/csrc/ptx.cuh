@@ -113,68 +113,6 @@ __device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity)
   }
 }
 
-// ------------------------------------------------------------ thread-block clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// the shared::cluster address of this CTA's shared variable at `addr` in the
-// cluster's CTA `rank`
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// arrive on an mbarrier of any CTA of the cluster (release at cluster scope:
-// this thread's earlier writes are visible to whoever completes the wait)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-// the bounded wait on this CTA's mbarrier with acquire at cluster scope (the
-// arrivals came from other CTAs of the cluster)
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i) {
-      uint32_t ok;
-      asm volatile(
-          "{\n\t.reg .pred p;\n\t"
-          "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-          "selp.u32 %0, 1, 0, p;\n\t}"
-          : "=r"(ok)
-          : "r"(smem_u32(bar)), "r"(parity)
-          : "memory");
-      if (ok) return true;
-    }
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-// bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
-// from this CTA's shared memory to a cluster CTA's, completing as
-// transaction bytes on that CTA's mbarrier
-__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                              uint32_t bar_cluster) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst_cluster),
-               "r"(src), "r"(bytes), "r"(bar_cluster)
-               : "memory");
-}
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
-  return v;
-}
-// Every thread of every CTA of the cluster (a hardware barrier, so only where
-// all threads are sure to arrive: no thread leaves the kernel before it).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads (a
 // multiple of 32): the warps of one role synchronise without the others.
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {

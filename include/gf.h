@@ -219,20 +219,6 @@ gf_status gf_linear_swish_bias_groupnorm_host(const float* x_host, const float* 
 int32_t gf_linear_tile_width(int32_t chain, int64_t M, int64_t N, int32_t groups, int32_t mode,
                              int32_t sm_count);
 
-/* Whether gf_linear_swish_bias_groupnorm (and _planes, _host per chunk)
- * splits the K loop of a tile over the CTAs of a thread-block cluster for a
- * call of M rows, K inputs and N outputs with `groups` groups in `mode` on a
- * GPU with sm_count SMs: the number of CTAs per tile (4), or 1 when it runs
- * the one-CTA tiles gf_linear_tile_width reports.  It splits when even
- * 64-column tiles would leave SMs idle (few rows), the 4-CTA clusters of
- * 256-column tiles fit in one wave, the group width is 16, 32 or 64 and each
- * CTA gets at least two k-blocks (32 inputs in the 3xTF32 mode, 64 in the
- * others).  The four partial sums of a tile meet in distributed shared memory
- * and each CTA normalises a quarter of the tile's columns.  Pure host
- * arithmetic (the dispatch's own rule); 0 for invalid arguments. */
-int32_t gf_linear_gn_split_k(int64_t M, int64_t K, int64_t N, int32_t groups, int32_t mode,
-                             int32_t sm_count);
-
 /* Testing hook of the host-buffer pipeline's schedule: runs the schedule of
  * gf_linear_swish_bias_groupnorm_host for nchunks chunks with the CUDA calls
  * replaced by a recorder, making step number fail_at (counted from 0; -1:

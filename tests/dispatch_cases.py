@@ -13,7 +13,6 @@ from __future__ import annotations
 import dataclasses
 
 SM_COUNT = 152  # GB300
-SPLIT = 4  # CTAs of the split-K cluster kernel
 
 MODES = {0: "3xtf32", 1: "bf16", 2: "3xbf16"}
 GN, LSE, LIN = 0, 1, 2  # the chains of gf_linear_tile_width
@@ -45,12 +44,6 @@ class Case:
     N: int
     groups: int   # GroupNorm groups (GN chain), else 0
     bn: int       # the tile width the dispatch picks for it (on SM_COUNT SMs)
-    split: int = 1  # CTAs splitting a tile's K loop (gf_linear_gn_split_k), 1: none
-
-    @property
-    def variant(self):
-        """(epilogue, tile width or "splitk", mode): the kernel the dispatch launches."""
-        return (self.epilogue, "splitk" if self.split > 1 else self.bn, self.mode)
 
     @property
     def epilogue(self):
@@ -74,16 +67,6 @@ def cases():
         out.append(Case(f"gn_{MODES[mode]}_gw128_m256", GN, mode, 256, 96, 4096, 32, 256))
         for bn, (M, N) in GN_SHAPES.items():
             out.append(Case(f"linear_{MODES[mode]}_bn{bn}", LIN, mode, M, 96, N, 0, bn))
-        # split-K cluster kernel (few rows, enough k-blocks): 64-column tiles
-        # would leave SMs idle (2 m-blocks x 16 n-blocks < 152).  K = 600 gives
-        # 19 or 10 k-blocks (5 + 5 + 5 + 4, 3 + 3 + 3 + 1 per CTA), K = 288 in
-        # the 3xTF32 mode 9 (3 + 3 + 3 + 0: the last CTA adds a zero partial);
-        # M = 200 and N = 1040 leave ragged rows and a last tile with one
-        # 16-column quarter.
-        for gw in (16, 32, 64):
-            out.append(Case(f"gn_{MODES[mode]}_gw{gw}_splitk", GN, mode, 256, 600, 1024, 1024 // gw, 64, SPLIT))
-        out.append(Case(f"gn_{MODES[mode]}_gw16_splitk_ragged", GN, mode, 200, 600, 1040, 1040 // 16, 64, SPLIT))
-    out.append(Case("gn_3xtf32_gw64_splitk_zero_share", GN, 0, 256, 288, 1024, 16, 64, SPLIT))
     for (mode, bn), (M, N) in LSE_SHAPES.items():
         out.append(Case(f"lse_{MODES[mode]}_bn{bn}", LSE, mode, M, 64, N, 0, bn))
     return out

@@ -25,27 +25,6 @@ def test_cases_declare_the_width_the_dispatch_picks(L):
     for c in dc.cases():
         got = L.gf_linear_tile_width(c.chain, c.M, c.N, c.groups, c.mode, dc.SM_COUNT)
         assert got == c.bn, (c.name, got)
-        if c.chain == dc.GN:
-            split = L.gf_linear_gn_split_k(c.M, c.K, c.N, c.groups, c.mode, dc.SM_COUNT)
-            assert split == c.split, (c.name, split)
-
-
-def test_split_k_rule(L):
-    sk = L.gf_linear_gn_split_k
-    # the M=256 workload: 2 x 64 tiles of 64 columns < 152 SMs, 2 x 16 x 4 = 128 CTAs
-    for mode in dc.MODES:
-        assert sk(256, 1024, 4096, 64, mode, 152) == dc.SPLIT
-        assert sk(256, 1024, 4096, 256, mode, 152) == dc.SPLIT  # 16-column groups
-        assert sk(256, 1024, 4096, 32, mode, 152) == 1  # 128-column groups do not fit a quarter
-        assert sk(256, 1024, 4096, 16, mode, 152) == 1  # 256-column groups: the row kernel
-        assert sk(2048, 1024, 4096, 64, mode, 152) == 1  # 16 x 64 tiles fill the GPU
-        assert sk(256, 1024, 4096, 64, mode, 100) == 1  # 128 CTAs do not fit 100 SMs
-    # at least two k-blocks per CTA: 8 k-blocks of 32 (3xTF32) or 64 (BF16 modes)
-    assert sk(256, 256, 4096, 64, 0, 152) == dc.SPLIT and sk(256, 224, 4096, 64, 0, 152) == 1
-    assert sk(256, 512, 4096, 64, 1, 152) == dc.SPLIT and sk(256, 448, 4096, 64, 2, 152) == 1
-    # invalid arguments
-    assert sk(256, 1024, 4096, 3, 0, 152) == 0 and sk(256, 0, 4096, 64, 0, 152) == 0
-    assert sk(256, 1024, 4096, 64, 7, 152) == 0 and sk(-1, 1024, 4096, 64, 0, 152) == 0
 
 
 def test_every_reachable_variant_has_a_case(L):
@@ -61,14 +40,11 @@ def test_every_reachable_variant_has_a_case(L):
                     for g in group_opts:
                         bn = L.gf_linear_tile_width(chain, M, N, g, mode, dc.SM_COUNT)
                         assert bn > 0, (chain, M, N, g, mode)
-                        for K in ((96, 1024) if chain == dc.GN else (96,)):
-                            split = L.gf_linear_gn_split_k(M, K, N, g, mode, dc.SM_COUNT) if chain == dc.GN else 1
-                            reachable.add((_epilogue(chain, N, g), "splitk" if split > 1 else bn, mode))
-    covered = {c.variant for c in dc.cases()}
+                        reachable.add((_epilogue(chain, N, g), bn, mode))
+    covered = {(c.epilogue, c.bn, c.mode) for c in dc.cases()}
     missing = reachable - covered
     assert not missing, sorted(missing)
     # and the expected variant count: GroupNorm epilogues 16/32/64/row kernel
     # at 3 widths, 128-column groups at 256 only, plain Linear at 3 widths, in
-    # 3 modes; logsumexp at 160 (three-product modes) and 224/256 (BF16); the
-    # split-K cluster kernel for 16/32/64-column groups in 3 modes
-    assert len(reachable) == 3 * (4 * 3 + 1 + 3) + 2 + 2 + 3 * 3
+    # 3 modes; logsumexp at 160 (three-product modes) and 224/256 (BF16)
+    assert len(reachable) == 3 * (4 * 3 + 1 + 3) + 2 + 2
