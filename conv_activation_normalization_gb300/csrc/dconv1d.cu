@@ -228,16 +228,21 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
   }
 }
 
-// W[co][ci][t] -> planes[Cout][ksize * Cp] with k = t * Cp + ci, zeros for
-// the padding channels C .. Cp - 1.
+// W[co][ci][t] -> planes[Cout][ksize * Cp] in the GEMM's k order: k-block
+// kb = cb * ksize + t holds channels cb * BK .. + BK - 1 of tap t (BK = 32
+// fp32 or 64 bf16 elements, one 128-byte row), zeros for the padding
+// channels C .. Cp - 1.
 template <int MODE>
 __global__ void conv_weight_split_kernel(const float* __restrict__ w, void* planes, int Cout, int C, int Cp,
                                          int ksize) {
+  constexpr int BK = MODE == GF_MODE_FP32_3XTF32 ? 32 : 64;
   const int64_t n = int64_t(Cout) * ksize * Cp;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
-    const int ci = int(i % Cp);
-    const int t = int((i / Cp) % ksize);
     const int64_t co = i / (int64_t(ksize) * Cp);
+    const int k = int(i - co * (int64_t(ksize) * Cp));
+    const int kb = k / BK, c = k % BK;
+    const int cb = kb / ksize, t = kb - cb * ksize;
+    const int ci = cb * BK + c;
     store_planes<MODE>(planes, size_t(n), size_t(i), ci < C ? w[(co * C + ci) * ksize + t] : 0.f);
   }
 }
@@ -246,8 +251,8 @@ __global__ void conv_weight_split_kernel(const float* __restrict__ w, void* plan
 // mode): rows are output positions j of one sample, columns output channels,
 // and the reduction runs over channel blocks cb of 32 (outer) and taps t
 // (inner), k-block kb = cb * ksize + t; the weight planes are laid out in that
-// order (conv_weight_split_cb_kernel).  Warp 0 loads only the weights (B);
-// five converter warps build A.  Per tile and channel block they compute the
+// order (conv_weight_split_kernel, as for the planes path).  Warp 0 loads
+// only the weights (B); five converter warps build A.  Per tile and channel block they compute the
 // activation a = GELU((x - mean) rstd gamma + beta) once for the window of
 // positions l = j0 - pad + p, p < 128 + (ksize - 1) dil (zero outside
 // [0, L): the conv's padding), into shared memory (128-byte rows of 32
@@ -400,24 +405,6 @@ struct LnConvSrc {
   }
 };
 
-// W[co][ci][t] -> planes[Cout][ksize * Cp] in the fused GEMM's k order:
-// k = (cb * ksize + t) * 32 + (ci - 32 cb), cb = ci / 32, zeros for the padding
-// channels C .. Cp - 1 (3xTF32 planes: the value and value - its TF32 part).
-__global__ void conv_weight_split_cb_kernel(const float* __restrict__ w, float* planes, int Cout, int C, int Cp,
-                                            int ksize) {
-  const int64_t n = int64_t(Cout) * ksize * Cp;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t co = i / (int64_t(ksize) * Cp);
-    const int k = int(i - co * (int64_t(ksize) * Cp));
-    const int kb = k / 32, c = k % 32;
-    const int cb = kb / ksize, t = kb % ksize;
-    const int ci = cb * 32 + c;
-    const float v = ci < C ? w[(co * C + ci) * ksize + t] : 0.f;
-    planes[i] = v;
-    planes[n + i] = v - tf32_hi(v);
-  }
-}
-
 // Epilogue: out[b][co][j] = acc + conv_b[co] + x[b][co][j].
 struct EpiConvResidual {
   static constexpr bool kFixedBN = true;
@@ -565,6 +552,7 @@ gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const vo
   src.C = int(Cp);  // channels per tap along K
   src.pad = padding;
   src.dil = dilation;
+  src.ksize = ksize;
   src.num_jb = int((L + kBM - 1) / kBM);
   src.num_nb = int((C + kBNConv - 1) / kBNConv);
   src.num_kb = int(ksize * Cp / Op::kBK);
@@ -688,8 +676,8 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
     const int64_t Cp = padded_channels(C, mode);
     const int64_t n = C * Cp * ksize;
     const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
-    conv_weight_split_cb_kernel<<<blocks, 256, 0, s>>>(conv_w, static_cast<float*>(w_planes), int(C), int(C),
-                                                       int(Cp), ksize);
+    conv_weight_split_kernel<GF_MODE_FP32_3XTF32>
+        <<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), int(Cp), ksize);
     if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
     return tanh_gelu ? launch_conv_fused<true>(dev, x, ln_gamma, ln_beta, stats, static_cast<const float*>(w_planes),
                                                B, C, L, ksize, dilation, padding, ep, s)

@@ -254,14 +254,17 @@ struct LinearSrc {
 };
 
 // Implicit GEMM of a stride-1 dilated Conv1d.  Rows are output positions j of
-// one sample, columns are output channels, and the reduction index is
-// k = tap * C + ci.  A = activation planes [B][L][C] (3-D maps {C, L, B}, box
-// {BK, 128, 1}); the k-block (tap, ci0..ci0+BK-1) of tile rows j0..j0+127 is
-// the box at l = j0 - pad + tap * dil: rows outside [0, L) come back as zeros
-// from the TMA unit, which is exactly the conv's zero padding.  B = weight
-// planes [Cout][ksize * C] (2-D maps).
+// one sample, columns are output channels, and the reduction runs over blocks
+// of BK channels (outer) and taps (inner): k-block kb = cb * ksize + tap
+// covers channels cb * BK .. + BK - 1 of tap `tap`.  A = activation planes
+// [B][L][C] (3-D maps {C, L, B}, box {BK, 128, 1}); the k-block of tile rows
+// j0..j0+127 is the box at l = j0 - pad + tap * dil: rows outside [0, L) come
+// back as zeros from the TMA unit, which is exactly the conv's zero padding.
+// B = weight planes [Cout][ksize * C] in the same k order (2-D maps).  With
+// the taps inner, the first touch of each row block (a DRAM read) comes every
+// ksize-th k-block instead of in a run of C / BK at the start of the tile.
 struct ConvSrc {
-  int C, pad, dil;
+  int C, pad, dil, ksize;
   int num_jb, num_nb, num_kb, bn, bk, nsamples;
   int kb_chunk;   // k-blocks per accumulation chunk (chunked epilogues only)
   __device__ __forceinline__ int num_tiles() const { return nsamples * num_jb * num_nb; }
@@ -276,8 +279,9 @@ struct ConvSrc {
   __device__ __forceinline__ void load(const OperandMaps& m, uint64_t* bar, const uint32_t* sa, const uint32_t* sb,
                                        const Tile& t, int kb) const {
     const int k0 = kb * bk;
-    const int tap = k0 / C;
-    const int ci0 = k0 - tap * C;
+    const int cb = kb / ksize;
+    const int tap = kb - cb * ksize;
+    const int ci0 = cb * bk;
     const int l = t.r0 - pad + tap * dil;
 #pragma unroll
     for (int p = 0; p < PLANES; ++p) {
