@@ -60,17 +60,29 @@ __global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict
   const float* xs = x + size_t(b) * size_t(n_per_sample);
   const int64_t begin = int64_t(blockIdx.x) * kLnChunk;
   const int64_t end = begin + kLnChunk < n_per_sample ? begin + kLnChunk : n_per_sample;
-  const float shift = sample_shift(xs, n_per_sample);
   float s1 = 0.f, s2 = 0.f;
   if constexpr (VEC) {
-#pragma unroll 4
-    for (int64_t i = begin + 4 * threadIdx.x; i < end; i += 4 * blockDim.x) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(xs + i));
-      const float d0 = v.x - shift, d1 = v.y - shift, d2 = v.z - shift, d3 = v.w - shift;
-      s1 += (d0 + d1) + (d2 + d3);
-      s2 += fmaf(d0, d0, d1 * d1) + fmaf(d2, d2, d3 * d3);
+    // all of the thread's loads (kLnChunk / 1024 float4) are issued before
+    // any arithmetic, so that they and the shift's own load overlap
+    constexpr int kPer = kLnChunk / (4 * 256);
+    float4 v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int64_t i = begin + 4 * (threadIdx.x + int64_t(u) * blockDim.x);
+      v[u] = i < end ? __ldcs(reinterpret_cast<const float4*>(xs + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float shift = sample_shift(xs, n_per_sample);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int64_t i = begin + 4 * (threadIdx.x + int64_t(u) * blockDim.x);
+      if (i < end) {
+        const float d0 = v[u].x - shift, d1 = v[u].y - shift, d2 = v[u].z - shift, d3 = v[u].w - shift;
+        s1 += (d0 + d1) + (d2 + d3);
+        s2 += fmaf(d0, d0, d1 * d1) + fmaf(d2, d2, d3 * d3);
+      }
     }
   } else {
+    const float shift = sample_shift(xs, n_per_sample);
     for (int64_t i = begin + threadIdx.x; i < end; i += blockDim.x) {
       const float d = __ldcs(xs + i) - shift;
       s1 += d;
