@@ -89,6 +89,28 @@ def test_linear_gn_modes_group_widths(mode, M, K, N, gw):
     assert_close(out, ref, TOL[mode], f"linear_gn mode {mode} groups of {gw}")
 
 
+# The BF16 mode writes the GroupNorm output as 32-row x 16-column boxes staged
+# in shared memory and sent by TMA stores: ragged rows (the store clips them)
+# and a last column tile that only partly exists, at each tile width the
+# dispatch picks (shapes checked against gf_linear_tile_width), including 16-
+# and 32-column groups whose last 64-column block has one or two quarters.
+@pytest.mark.parametrize("M,K,N,gw,bn", [
+    (777, 72, 2080, 32, 64),     # 7 x 17 tiles of 128 columns < 152 SMs: 64-column tiles; last block 2 quarters
+    (1100, 96, 3088, 16, 128),   # 9 x 13 tiles of 256 < 152 <= 9 x 25 of 128; last 64-column block 1 quarter
+    (2500, 128, 4160, 64, 256),  # 20 x 17 tiles of 256: the last tile has 64 of its 256 columns
+])
+def test_bf16_box_stores_ragged(M, K, N, gw, bn):
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert gf.linear_tile_width(gf.GF_CHAIN_GROUPNORM, M, N, N // gw, BF16, sm) == bn
+    s = synth.LinearGNShape(M=M, K=K, N=N, groups=N // gw)
+    d = synth.linear_gn_inputs(s, 700 + gw)
+    out = gf.gf_linear_swish_bias_groupnorm(T(d["x"]), T(d["W"]), T(d["b_lin"]), T(d["bias"]), T(d["gamma"]),
+                                            T(d["beta"]), s.groups, s.eps, mode=BF16).cpu().numpy()
+    ref = oracle.linear_swish_bias_groupnorm(d["x"], d["W"], d["b_lin"], d["bias"], d["gamma"], d["beta"], s.groups,
+                                             s.eps)
+    assert_close(out, ref, TOL[BF16], f"bf16 boxes M={M} N={N} gw={gw}")
+
+
 def test_linear_gn_3xbf16_workload_m32768_sampled():
     s, seed = synth.WORKLOADS["linear_gn_m32768"]
     d = synth.linear_gn_inputs(s, seed)
