@@ -608,7 +608,9 @@ def run_ours(wl, args, quiet=False):
     else:
         peak = peaks["hbm_gbs"]
         note = f"{src} HBM copy bandwidth"
-    roofline = {"bound": wl.bound, "kernel": wl.kernel, "achieved": round(achieved, 2), "peak": round(peak, 2),
+    op = {"3xtf32": "OpTF32x3", "bf16": "OpBF16x1", "3xbf16": "OpBF16x3"}[MODE]
+    kernel = wl.kernel.replace("OpTF32x3", op)  # (the labels name the fp32 mode's operand type)
+    roofline = {"bound": wl.bound, "kernel": kernel, "achieved": round(achieved, 2), "peak": round(peak, 2),
                 "unit": wl.unit, "frac": round(achieved / peak, 4), "traffic": _kernel_traffic(wl),
                 "kernel_ms": round(kern_ms, 4), "kernel_launches_timed": prof.calls, "peak_note": note}
 
