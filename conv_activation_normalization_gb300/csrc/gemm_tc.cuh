@@ -251,6 +251,40 @@ struct LinearSrc {
       tma_load_2d(sb[p], &m.b[p], bar, k0, t.n0);
     }
   }
+  // Clusters of CL CTAs: unit q is the group of m-blocks CL mg .. CL mg +
+  // CL - 1 at one n-block, and cluster CTA `rank` takes m-block CL mg + rank.
+  // When CL does not divide the number of m-blocks, the last group's tiles
+  // past M still run (their A rows load as zeros; the epilogue skips them):
+  // each CTA has to load its slice of the B tile the group shares.
+  template <int CL>
+  __device__ __forceinline__ int num_groups() const {
+    return (num_mb + CL - 1) / CL * num_nb;
+  }
+  template <int CL>
+  __device__ __forceinline__ Tile tile_of_group(int q, uint32_t rank) const {
+    const int num_mg = (num_mb + CL - 1) / CL;
+    int mg, nb;
+    if (m_fastest) {
+      mg = q % num_mg;
+      nb = q / num_mg;
+    } else {
+      nb = q % num_nb;
+      mg = q / num_nb;
+    }
+    return Tile{0, (CL * mg + int(rank)) * kBM, nb * bn, nb};
+  }
+  __device__ __forceinline__ bool live(const Tile& t) const { return t.r0 < num_mb * kBM; }
+  // This CTA's A tile, and slice `rank` of the group's B tile (rows
+  // n0 + rank * bn / CL ..) multicast into every CTA's stage at the same
+  // offset; each CTA's full barrier counts its A and all CL slices of B.
+  template <int CL>
+  __device__ __forceinline__ void load_group(const OperandMaps& m, uint64_t* bar, uint32_t sa, uint32_t sb,
+                                             const Tile& t, int kb, uint32_t rank) const {
+    const int k0 = kb * bk;
+    tma_load_2d(sa, &m.a[0], bar, k0, t.r0);
+    tma_load_2d_mc(sb + rank * uint32_t(bn / CL * 128), &m.b[0], bar, k0, t.n0 + int(rank) * (bn / CL),
+                   uint16_t((1u << CL) - 1));
+  }
 };
 
 // Implicit GEMM of a stride-1 dilated Conv1d.  Rows are output positions j of
@@ -291,10 +325,20 @@ struct ConvSrc {
   }
 };
 
-template <int BN, class Op, class Src, class Epi>
+// CL > 1: the grid is made of clusters of CL CTAs that take m-adjacent tiles
+// of one n-block together (Src::tile_of_group) and share the B tile: each CTA
+// loads a slice of it and multicasts it into every CTA's stage, so the B
+// bytes read from L2 per tile drop CL-fold.  A stage is then free only when
+// every CTA's MMAs have read it: each MMA commit arrives on the stage's empty
+// barrier in every CTA.  (One-plane operands and unchunked epilogues only.)
+template <int BN, class Op, class Src, class Epi, int CL>
 __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
     gemm_tc_kernel(const __grid_constant__ OperandMaps maps, const Src src, const typename Epi::Params ep,
                    uint32_t* status) {
+  static_assert(CL == 1 || ((CL == 2 || CL == 4) && Op::kPlanes == 1 && SrcConv<Src>::warps == 0 &&
+                             !epi_chunked<Epi, Op, BN>() && BN % (8 * CL) == 0),
+                "clusters: one operand plane, TMA-loaded A, unchunked epilogue, whole 8-row B slices");
+  constexpr uint16_t kClusterMask = uint16_t((1u << CL) - 1);
   constexpr int kConv = SrcConv<Src>::warps;
   using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op>()>;
   constexpr int S = Cfg::STAGES;
@@ -318,7 +362,7 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1 + SrcConv<Src>::arrivals);  // the TMA thread (and the converter warps)
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);  // the MMA commit of each CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -340,9 +384,23 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CL > 1) cluster_sync_all();  // the other CTAs' barriers are initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int num_tiles = src.num_tiles();
+  // the persistent loop's units: tiles, or (CL > 1) groups of CL tiles, one
+  // per CTA of a cluster
+  uint32_t crank = 0;
+  if constexpr (CL > 1) crank = cluster_ctarank();
+  const int unit0 = int(blockIdx.x) / CL, unit_step = int(gridDim.x) / CL;
+  int num_units = num_tiles;
+  if constexpr (CL > 1) num_units = src.template num_groups<CL>();
+  auto unit_tile = [&](int u) -> Tile {
+    if constexpr (CL > 1)
+      return src.template tile_of_group<CL>(u, crank);
+    else
+      return src.tile(u);
+  };
   // k-blocks per accumulation chunk: the whole K loop unless the epilogue
   // adds chunks (both the MMA issuer and the epilogue count chunks with it)
   constexpr bool kChunked = epi_chunked<Epi, Op, BN>();
@@ -359,8 +417,8 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_phase = 0;
-      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
-        const Tile tile = src.tile(t);
+      for (int u = unit0; u < num_units && !*abort_flag; u += unit_step) {
+        const Tile tile = unit_tile(u);
         for (int kb = 0; kb < src.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             record_error(status, GF_DEV_WAIT_TIMEOUT);
@@ -374,7 +432,10 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
             sb[p] = b_addr(stage, p);
           }
           mbar_arrive_expect_tx(&full[stage], kConv ? P * Cfg::B_BYTES : Cfg::STAGE_BYTES);
-          src.template load<P>(maps, &full[stage], sa, sb, tile, kb);
+          if constexpr (CL > 1)
+            src.template load_group<CL>(maps, &full[stage], sa[0], sb[0], tile, kb, crank);
+          else
+            src.template load<P>(maps, &full[stage], sa, sb, tile, kb);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -383,10 +444,16 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
           }
         }
       }
-      // Never leave with a TMA write into this CTA's smem still in flight.
+      // Never leave with a TMA write into this CTA's smem still in flight
+      // (with CL > 1 that includes the other CTAs' multicast slices), nor
+      // (CL > 1) with another CTA's MMA commit still to arrive on an empty
+      // barrier here.
       for (int s = 0; s < S; ++s)
-        if ((issued >> s) & 1u)
+        if ((issued >> s) & 1u) {
           if (!mbar_wait(&full[s], (issued_phase >> s) & 1u)) record_error(status, GF_DEV_WAIT_TIMEOUT);
+          if constexpr (CL > 1)
+            if (!mbar_wait(&empty[s], (issued_phase >> s) & 1u)) record_error(status, GF_DEV_WAIT_TIMEOUT);
+        }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -413,13 +480,16 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
             Op::mma(d, sdesc_kmajor_sw128(a_hi + off), sdesc_kmajor_sw128(b_hi + off), idesc, accumulate);
           }
         }
-        mma_commit(&empty[stage]);
+        if constexpr (CL > 1)
+          mma_commit_mc(&empty[stage], kClusterMask);
+        else
+          mma_commit(&empty[stage]);
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
       };
-      for (int t = blockIdx.x; t < num_tiles && ok && !*abort_flag; t += gridDim.x) {
+      for (int u = unit0; u < num_units && ok && !*abort_flag; u += unit_step) {
         if constexpr (kChunked) {
           uint32_t d = 0;
           // kc: k-block index within the current accumulation chunk
@@ -502,8 +572,8 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
       const int nchunks = (src.num_kb + kb_chunk - 1) / kb_chunk;
       const uint32_t tot = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(half * Cfg::ACC_STRIDE + BN);
       bool failed = false;
-      for (int t = blockIdx.x; half < H && t < num_tiles && !failed; t += gridDim.x) {
-        const Tile tile = src.tile(t);
+      for (int u = unit0; half < H && u < num_units && !failed; u += unit_step) {
+        const Tile tile = unit_tile(u);
         const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
         for (int c = 0; c < nchunks; ++c) {
           bool ok = mbar_wait(&tfull[acc], acc_phase);
@@ -552,8 +622,8 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
         st.buf = boxes + (warp - 2) * 2 * kStoreBoxFloats;
         st.map = &maps.c;
       }
-      for (int t = blockIdx.x; half < H && t < num_tiles; t += gridDim.x) {
-        const Tile tile = src.tile(t);
+      for (int u = unit0; half < H && u < num_units; u += unit_step) {
+        const Tile tile = unit_tile(u);
         bool ok = mbar_wait(&tfull[acc], acc_phase);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok || __any_sync(0xffffffffu, *abort_flag)) {
@@ -567,7 +637,10 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * Cfg::ACC_STRIDE + half * BNW);
         const Tile part{tile.b, tile.r0, tile.n0 + half * BNW, tile.nb * H + half};
-        if constexpr (EpiTma<Epi>::value) {
+        bool live = true;
+        if constexpr (CL > 1) live = src.live(tile);  // not a tile wholly past M
+        if (!live) {
+        } else if constexpr (EpiTma<Epi>::value) {
           st.y = part.r0 + quad * 32;
           Epi::template apply<BNW, kTma>(ep, taddr, part, row, st);
         } else {
@@ -589,27 +662,57 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
 
   tc_fence_before();
   __syncthreads();
+  // (CL > 1) every copy into and arrival on this CTA's shared memory from the
+  // other CTAs has landed (the producer's waits above): the cluster leaves
+  // together
+  if constexpr (CL > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 
-// Host: launch the persistent kernel, one CTA per SM (or per tile when there
-// are fewer tiles), on the caller's stream, with the dominant-kernel
-// profiling marks around it.
-template <int BN, class Op, class Src, class Epi>
-gf_status launch_gemm(const DeviceInfo& dev, const OperandMaps& maps, const Src& src, int64_t tiles,
+// Host: launch the persistent kernel, one CTA per SM (or per unit of work
+// when there are fewer), on the caller's stream, with the dominant-kernel
+// profiling marks around it.  `units` = tiles, or (CL > 1) groups of CL
+// tiles; the clusters go through cudaLaunchKernelEx, as many as can be
+// resident at once.
+template <int BN, class Op, class Src, class Epi, int CL = 1>
+gf_status launch_gemm(const DeviceInfo& dev, const OperandMaps& maps, const Src& src, int64_t units,
                       const typename Epi::Params& ep, cudaStream_t stream) {
   using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op>()>;
-  const int grid = int(tiles < dev.sm_count ? tiles : dev.sm_count);
-  auto kern = gemm_tc_kernel<BN, Op, Src, Epi>;
+  auto kern = gemm_tc_kernel<BN, Op, Src, Epi, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
     return GF_ERR_CUDA;
-  profile_mark_begin(stream);
-  kern<<<grid, gemm_threads<Src, Epi, Op, BN>(), Cfg::SMEM_BYTES, stream>>>(maps, src, ep, device_status_word());
-  profile_mark_end(stream);
-  return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
+  constexpr int threads = gemm_threads<Src, Epi, Op, BN>();
+  if constexpr (CL == 1) {
+    const int grid = int(units < dev.sm_count ? units : dev.sm_count);
+    profile_mark_begin(stream);
+    kern<<<grid, threads, Cfg::SMEM_BYTES, stream>>>(maps, src, ep, device_status_word());
+    profile_mark_end(stream);
+    return cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(unsigned(CL * (dev.sm_count / CL)), 1, 1);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) return GF_ERR_CUDA;
+    const int64_t n = units < clusters ? units : clusters;
+    cfg.gridDim = dim3(unsigned(CL * n), 1, 1);
+    profile_mark_begin(stream);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, src, ep, device_status_word());
+    profile_mark_end(stream);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? GF_OK : GF_ERR_CUDA;
+  }
 }
 
 }  // namespace gf

@@ -509,6 +509,9 @@ __global__ void lse_merge_act_kernel(const float2* __restrict__ part, float* __r
 namespace {
 
 constexpr int kBNLinear = 256;
+// CTAs per cluster of the BF16 GroupNorm kernel at 256 columns: two take
+// 0.2071 ms at M = 32768 against 0.2103 for one; four time the same as two.
+constexpr int kClusterBF16 = 2;
 
 // Tile width of the LSE chain.  In the three-product modes 160 columns: the
 // tile fits three smem stages (two for 224 or 256), deep enough for the
@@ -675,11 +678,15 @@ gf_status prepare_operand(const float* src, int64_t rows, int64_t K, int32_t mod
 template <int BN, class Op, class Epi>
 gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K, int64_t N,
                           int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
+  // The BF16 GroupNorm kernel at 256 columns runs in clusters of
+  // kClusterBF16 CTAs that share each B tile (each CTA loads a slice of it):
+  // its k-loop waits on operand bytes from L2 rather than on its MMAs.
+  constexpr int CL = epi_tma_store<Epi, Op>() && BN == 256 ? kClusterBF16 : 1;
   OperandMaps maps{};
   const uint64_t da[2] = {uint64_t(K), uint64_t(M)};
   const uint32_t ba[2] = {uint32_t(Op::kBK), uint32_t(kBM)};
   const uint64_t db[2] = {uint64_t(K), uint64_t(N)};
-  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(BN)};
+  const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(BN / CL)};
   for (int p = 0; p < Op::kPlanes; ++p) {
     gf_status st = make_tmap(&maps.a[p], a.p[p], Op::kElem, 2, da, ba);
     if (st != GF_OK) return st;
@@ -703,8 +710,8 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
   src.bn = BN;
   src.bk = Op::kBK;
   src.m_fastest = m_fastest;
-  const int64_t tiles = int64_t(src.num_mb) * src.num_nb;
-  return launch_gemm<BN, Op, LinearSrc, Epi>(dev, maps, src, tiles, ep, stream);
+  const int64_t units = int64_t(src.num_mb + CL - 1) / CL * src.num_nb;
+  return launch_gemm<BN, Op, LinearSrc, Epi, CL>(dev, maps, src, units, ep, stream);
 }
 
 // Runs the GEMM at the tile width linear_tile_width picks.  The LSE

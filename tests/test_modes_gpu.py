@@ -94,10 +94,14 @@ def test_linear_gn_modes_group_widths(mode, M, K, N, gw):
 # and a last column tile that only partly exists, at each tile width the
 # dispatch picks (shapes checked against gf_linear_tile_width), including 16-
 # and 32-column groups whose last 64-column block has one or two quarters.
+# The 256-column tiles run in two-CTA clusters over pairs of m-blocks: with an
+# odd count the last pair's second tile lies past M (computed, not stored).
 @pytest.mark.parametrize("M,K,N,gw,bn", [
     (777, 72, 2080, 32, 64),     # 7 x 17 tiles of 128 columns < 152 SMs: 64-column tiles; last block 2 quarters
     (1100, 96, 3088, 16, 128),   # 9 x 13 tiles of 256 < 152 <= 9 x 25 of 128; last 64-column block 1 quarter
     (2500, 128, 4160, 64, 256),  # 20 x 17 tiles of 256: the last tile has 64 of its 256 columns
+    (2600, 136, 4160, 64, 256),  # 21 m-blocks (odd), 40 rows in the last
+    (100, 64, 1024, 128, 256),   # one m-block: each pair's second tile lies past M
 ])
 def test_bf16_box_stores_ragged(M, K, N, gw, bn):
     sm = torch.cuda.get_device_properties(0).multi_processor_count
