@@ -42,6 +42,15 @@
 // (fence.proxy.async, then one arrival per warp on the stage's full
 // barrier), using kScratchBytes of shared memory of their own.
 //
+// In-SM lo planes (OpTF32x3; Src::kLoInSm, bit 0 for A, bit 1 for B): the
+// producer loads only the raw fp32 tile of that operand, and kSplitWarps more
+// warps write lo = x - trunc_tf32(x) into the stage's lo plane before the
+// MMAs read it.  Elementwise, so the lo tile takes the hi tile's layout as it
+// is (the swizzle depends only on a byte's offset within the 1024-byte-aligned
+// tile).  The TMA completes on a stage's "loaded" barrier, which these warps
+// wait on; they arrive on "full" once the lo plane is written.  The operand
+// then needs no lo plane in memory and no pre-pass to write it.
+//
 // Chunked accumulation (epi_chunked below): the tensor core adds
 // each MMA's products into the fp32 accumulator with truncation, which over a
 // long K loop of same-signed products (all-positive operands, say) becomes a
@@ -181,9 +190,20 @@ struct BoxStore {
   uint32_t n;
 };
 
+// Operands whose lo plane the kernel computes (bit 0: A, bit 1: B).
+template <class Src, class = void>
+struct SrcLo {
+  static constexpr int mask = 0;
+};
+template <class Src>
+struct SrcLo<Src, decltype(void(Src::kLoInSm))> {
+  static constexpr int mask = Src::kLoInSm;
+};
+constexpr int kSplitWarps = 4;
+
 template <class Src, class Epi, class Op, int BN>
 __host__ __device__ constexpr int gemm_threads() {
-  return kGemmThreads + 32 * SrcConv<Src>::warps;
+  return kGemmThreads + 32 * (SrcConv<Src>::warps + (SrcLo<Src>::mask ? kSplitWarps : 0));
 }
 
 // What the converter warps of a source get from the kernel: the stage ring
@@ -225,7 +245,10 @@ __host__ __device__ constexpr bool epi_chunked() {
 }
 
 // A = [M][K] planes (2-D maps {K, M}, box {BK, 128}), B = [N][K] planes.
-struct LinearSrc {
+// LO: operands whose lo plane the kernel computes (not loaded).
+template <int LO>
+struct LinearSrcT {
+  static constexpr int kLoInSm = LO;
   int num_mb, num_nb, num_kb, bn, bk;
   int kb_chunk;   // k-blocks per accumulation chunk (chunked epilogues only)
   int m_fastest;  // tile order: consecutive tiles share an n-block (1) or an m-block (0)
@@ -247,8 +270,8 @@ struct LinearSrc {
     const int k0 = kb * bk;
 #pragma unroll
     for (int p = 0; p < PLANES; ++p) {
-      tma_load_2d(sa[p], &m.a[p], bar, k0, t.r0);
-      tma_load_2d(sb[p], &m.b[p], bar, k0, t.n0);
+      if (p == 0 || !(LO & 1)) tma_load_2d(sa[p], &m.a[p], bar, k0, t.r0);
+      if (p == 0 || !(LO & 2)) tma_load_2d(sb[p], &m.b[p], bar, k0, t.n0);
     }
   }
   // Clusters of CL CTAs: unit q is the group of m-blocks CL mg .. CL mg +
@@ -286,6 +309,7 @@ struct LinearSrc {
                    uint16_t((1u << CL) - 1));
   }
 };
+using LinearSrc = LinearSrcT<0>;
 
 // Implicit GEMM of a stride-1 dilated Conv1d.  Rows are output positions j of
 // one sample, columns are output channels, and the reduction runs over blocks
@@ -325,6 +349,28 @@ struct ConvSrc {
   }
 };
 
+// lo = x - trunc_tf32(x) of a BYTES-long fp32 tile in shared memory, written
+// at the same offsets of `lo`, by the kSplitWarps * 32 threads (thread ct):
+// all of a thread's 16-byte loads first, then the arithmetic and the stores.
+template <int BYTES>
+__device__ __forceinline__ void split_lo_tile(const uint8_t* hi, uint8_t* lo, int ct) {
+  constexpr int kThreads = kSplitWarps * 32;
+  constexpr int kPer = BYTES / 16 / kThreads;
+  static_assert(BYTES % (16 * kThreads) == 0, "whole 16-byte pieces per thread");
+  float4 v[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) v[j] = reinterpret_cast<const float4*>(hi)[ct + j * kThreads];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const float4 x = v[j];
+    const float4 r = make_float4(x.x - __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u),
+                                 x.y - __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u),
+                                 x.z - __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u),
+                                 x.w - __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u));
+    reinterpret_cast<float4*>(lo)[ct + j * kThreads] = r;
+  }
+}
+
 // CL > 1: the grid is made of clusters of CL CTAs that take m-adjacent tiles
 // of one n-block together (Src::tile_of_group) and share the B tile: each CTA
 // loads a slice of it and multicasts it into every CTA's stage, so the B
@@ -340,6 +386,9 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
                 "clusters: one operand plane, TMA-loaded A, unchunked epilogue, whole 8-row B slices");
   constexpr uint16_t kClusterMask = uint16_t((1u << CL) - 1);
   constexpr int kConv = SrcConv<Src>::warps;
+  constexpr int kLo = SrcLo<Src>::mask;
+  static_assert(kLo == 0 || (Op::kind == MmaKind::TF32 && Op::kPlanes == 2 && kConv == 0 && CL == 1),
+                "lo planes are computed in the SM from raw fp32 tiles only (3xTF32), by their own warps");
   using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op>()>;
   constexpr int S = Cfg::STAGES;
   constexpr int P = Op::kPlanes;
@@ -350,7 +399,9 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* loaded = drain + 1;  // (kLo) the TMA's bytes of stage s have landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(loaded + S);
+  static_assert((3 * S + 5) * 8 + 8 <= Cfg::BAR_BYTES, "barriers overflow their space");
   volatile uint32_t* abort_flag = tmem_slot + 1;
   uint8_t* scratch = smem + S * Cfg::STAGE_BYTES + Cfg::BAR_BYTES;  // the converters' (kConv > 0)
   float* boxes = reinterpret_cast<float*>(  // the epilogue's TMA-store boxes
@@ -361,8 +412,10 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1 + SrcConv<Src>::arrivals);  // the TMA thread (and the converter warps)
+      // the TMA thread (and the converter warps), or the lo-plane warps
+      mbar_init(&full[s], kLo ? kSplitWarps : 1 + SrcConv<Src>::arrivals);
       mbar_init(&empty[s], CL);  // the MMA commit of each CTA of the cluster
+      mbar_init(&loaded[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -431,11 +484,17 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
             sa[p] = a_addr(stage, p);
             sb[p] = b_addr(stage, p);
           }
-          mbar_arrive_expect_tx(&full[stage], kConv ? P * Cfg::B_BYTES : Cfg::STAGE_BYTES);
+          // bytes the TMA brings: the stage less the converters' A planes
+          // or the lo planes computed here
+          constexpr uint32_t kTx = kConv ? P * Cfg::B_BYTES
+                                         : Cfg::STAGE_BYTES - ((kLo & 1) ? Cfg::A_BYTES : 0) -
+                                               ((kLo & 2) ? Cfg::B_BYTES : 0);
+          uint64_t* tx_bar = kLo ? &loaded[stage] : &full[stage];
+          mbar_arrive_expect_tx(tx_bar, kTx);
           if constexpr (CL > 1)
-            src.template load_group<CL>(maps, &full[stage], sa[0], sb[0], tile, kb, crank);
+            src.template load_group<CL>(maps, tx_bar, sa[0], sb[0], tile, kb, crank);
           else
-            src.template load<P>(maps, &full[stage], sa, sb, tile, kb);
+            src.template load<P>(maps, tx_bar, sa, sb, tile, kb);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -450,7 +509,8 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
       // barrier here.
       for (int s = 0; s < S; ++s)
         if ((issued >> s) & 1u) {
-          if (!mbar_wait(&full[s], (issued_phase >> s) & 1u)) record_error(status, GF_DEV_WAIT_TIMEOUT);
+          if (!mbar_wait(kLo ? &loaded[s] : &full[s], (issued_phase >> s) & 1u))
+            record_error(status, GF_DEV_WAIT_TIMEOUT);
           if constexpr (CL > 1)
             if (!mbar_wait(&empty[s], (issued_phase >> s) & 1u)) record_error(status, GF_DEV_WAIT_TIMEOUT);
         }
@@ -556,6 +616,36 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
       const ConvCtx c{smem, Cfg::STAGE_BYTES, P * Cfg::A_BYTES, S, full, empty, abort_flag, status, scratch,
                       num_tiles};
       src.template convert<Op>(c);
+    } else if constexpr (kLo != 0) {
+      // lo planes: stage by stage, in the producer's order
+      const int ct = int(threadIdx.x) - 32 * (2 + kEpiWarps);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool failed = false;
+      for (int u = unit0; u < num_units && !failed; u += unit_step) {
+        for (int kb = 0; kb < src.num_kb; ++kb) {
+          bool ok = mbar_wait(&loaded[stage], phase);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok || __any_sync(0xffffffffu, *abort_flag)) {
+            if (!ok) {
+              record_error(status, GF_DEV_WAIT_TIMEOUT);
+              *abort_flag = 1;
+            }
+            failed = true;
+            break;
+          }
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          if constexpr (kLo & 1) split_lo_tile<Cfg::A_BYTES>(st, st + Cfg::A_BYTES, ct);
+          if constexpr (kLo & 2) split_lo_tile<Cfg::B_BYTES>(st + 2 * Cfg::A_BYTES, st + 2 * Cfg::A_BYTES + Cfg::B_BYTES, ct);
+          fence_proxy_async_smem();  // the tensor core reads what these threads wrote
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <type_traits>
 
 #include "gemm_tc.cuh"
 #include "host_common.h"
@@ -509,6 +510,21 @@ __global__ void lse_merge_act_kernel(const float2* __restrict__ part, float* __r
 namespace {
 
 constexpr int kBNLinear = 256;
+
+// 3xTF32 operands whose lo plane the GEMM computes in the SM from the raw
+// fp32 tile (bit 0: x, bit 1: W) instead of reading a plane a pre-pass wrote
+// (gemm_tc_kernel, kLoInSm): the GroupNorm chain at 64-column tiles, where
+// few rows leave the GEMM waiting on operand bytes and the pre-passes are a
+// large part of the call (M = 256: 42.0 -> 30.9 us per call, M = 512:
+// 60.1 -> 51.1; level at 128 columns).  Where the MMAs bound the GEMM, the
+// conversion's shared-memory traffic slows them more than the pre-pass costs
+// (M = 32768: 0.972 -> 1.204 ms), and the same held for the logsumexp chain
+// and the Conv1d.
+template <class Epi>
+constexpr int lo_mask_at(int mode, int bn) {
+  constexpr bool gn = !std::is_same<Epi, EpiLSEPartial>::value && !std::is_same<Epi, EpiStore>::value;
+  return gn && mode == GF_MODE_FP32_3XTF32 && bn == 64 ? 3 : 0;
+}
 // CTAs per cluster of the BF16 GroupNorm kernel at 256 columns: two take
 // 0.2071 ms at M = 32768 against 0.2103 for one; four time the same as two.
 constexpr int kClusterBF16 = 2;
@@ -636,7 +652,7 @@ __global__ void split_padded_kernel(const float* __restrict__ src, int64_t rows,
 // Run the split pre-pass of one operand into `ws` and return its planes
 // (rows kpad(K, mode) wide).
 gf_status prepare_operand(const float* src, int64_t rows, int64_t K, int32_t mode, void* ws, const DeviceInfo& dev,
-                          cudaStream_t s, Planes* out) {
+                          cudaStream_t s, Planes* out, bool need_lo = true) {
   const int64_t Kp = kpad(K, mode);
   if (Kp != K) {
     const size_t n = size_t(rows) * size_t(Kp);
@@ -660,8 +676,8 @@ gf_status prepare_operand(const float* src, int64_t rows, int64_t K, int32_t mod
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
       out->p[0] = src;
-      out->p[1] = ws;
-      return launch_split_lo_tf32(src, static_cast<float*>(ws), n, dev.sm_count, s);
+      out->p[1] = need_lo ? ws : nullptr;  // (else the GEMM computes lo itself)
+      return need_lo ? launch_split_lo_tf32(src, static_cast<float*>(ws), n, dev.sm_count, s) : GF_OK;
     case GF_MODE_BF16:
       out->p[0] = ws;
       out->p[1] = nullptr;
@@ -682,15 +698,18 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
   // kClusterBF16 CTAs that share each B tile (each CTA loads a slice of it):
   // its k-loop waits on operand bytes from L2 rather than on its MMAs.
   constexpr int CL = epi_tma_store<Epi, Op>() && BN == 256 ? kClusterBF16 : 1;
+  constexpr int LO = lo_mask_at<Epi>(std::is_same<Op, OpTF32x3>::value ? GF_MODE_FP32_3XTF32 : GF_MODE_BF16, BN);
+  using Src = LinearSrcT<LO>;
   OperandMaps maps{};
   const uint64_t da[2] = {uint64_t(K), uint64_t(M)};
   const uint32_t ba[2] = {uint32_t(Op::kBK), uint32_t(kBM)};
   const uint64_t db[2] = {uint64_t(K), uint64_t(N)};
   const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(BN / CL)};
   for (int p = 0; p < Op::kPlanes; ++p) {
-    gf_status st = make_tmap(&maps.a[p], a.p[p], Op::kElem, 2, da, ba);
+    gf_status st = GF_OK;
+    if (p == 0 || !(LO & 1)) st = make_tmap(&maps.a[p], a.p[p], Op::kElem, 2, da, ba);
     if (st != GF_OK) return st;
-    st = make_tmap(&maps.b[p], b.p[p], Op::kElem, 2, db, bb);
+    if (p == 0 || !(LO & 2)) st = make_tmap(&maps.b[p], b.p[p], Op::kElem, 2, db, bb);
     if (st != GF_OK) return st;
   }
   if constexpr (epi_tma_store<Epi, Op>()) {  // the output, in the epilogue's boxes of 32 rows x 16 columns
@@ -699,7 +718,7 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
     const gf_status st = make_tmap(&maps.c, ep.out, 4, 2, dc, bc, 64);
     if (st != GF_OK) return st;
   }
-  LinearSrc src;
+  Src src;
   src.num_mb = int((M + kBM - 1) / kBM);
   src.num_nb = int((N + BN - 1) / BN);
   src.num_kb = int((K + Op::kBK - 1) / Op::kBK);
@@ -711,19 +730,33 @@ gf_status run_linear_gemm(const DeviceInfo& dev, const Planes& a, const Planes& 
   src.bk = Op::kBK;
   src.m_fastest = m_fastest;
   const int64_t units = int64_t(src.num_mb + CL - 1) / CL * src.num_nb;
-  return launch_gemm<BN, Op, LinearSrc, Epi, CL>(dev, maps, src, units, ep, stream);
+  return launch_gemm<BN, Op, Src, Epi, CL>(dev, maps, src, units, ep, stream);
 }
 
-// Runs the GEMM at the tile width linear_tile_width picks.  The LSE
-// partials' layout follows the tile width (the caller sized them with the
-// same function); a fused epilogue's groups must not straddle warps
-// (Epi::kMinBN).
+// The tile width the GEMM of epilogue Epi runs at: linear_tile_width's
+// choice; a fused epilogue's groups must not straddle warps (Epi::kMinBN).
+template <class Epi>
+int gemm_tile_width(int64_t M, int64_t N, int32_t mode, int sm_count) {
+  if constexpr (Epi::kFixedBN) {
+    const int w = linear_tile_width(true, M, N, 0, mode, sm_count);
+    return w == 160 || w == 224 ? w : kBNLinear;
+  } else if constexpr (Epi::kMinBN > 128) {
+    return 256;
+  } else {
+    const int w = linear_tile_width(false, M, N, Epi::kTileGW, mode, sm_count);
+    return w == 256 || w == 128 ? w : 64;
+  }
+}
+
+// Runs the GEMM at the tile width gemm_tile_width picks.  The LSE partials'
+// layout follows the tile width (the caller sized them with the same
+// function).
 template <class Op, class Epi>
 gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Planes& b, int64_t M, int64_t K,
                              int64_t N, int m_fastest, const typename Epi::Params& ep, cudaStream_t stream) {
   const int32_t mode = Op::kProducts == 1 ? GF_MODE_BF16 : GF_MODE_FP32_3XTF32;  // (only BF16 or not matters)
   if constexpr (Epi::kFixedBN) {
-    switch (linear_tile_width(true, M, N, 0, mode, dev.sm_count)) {
+    switch (gemm_tile_width<Epi>(M, N, mode, dev.sm_count)) {
       case 160: return run_linear_gemm<160, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
       case 224: return run_linear_gemm<224, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
       default: return run_linear_gemm<kBNLinear, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
@@ -731,7 +764,7 @@ gf_status run_linear_gemm_bn(const DeviceInfo& dev, const Planes& a, const Plane
   } else if constexpr (Epi::kMinBN > 128) {
     return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
   } else {
-    switch (linear_tile_width(false, M, N, Epi::kTileGW, mode, dev.sm_count)) {
+    switch (gemm_tile_width<Epi>(M, N, mode, dev.sm_count)) {
       case 256: return run_linear_gemm<256, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
       case 128: return run_linear_gemm<128, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
       default: return run_linear_gemm<64, Op, Epi>(dev, a, b, M, K, N, m_fastest, ep, stream);
@@ -758,8 +791,11 @@ gf_status split_and_run(int32_t mode, const float* x, const float* W, int64_t M,
   if (st != GF_OK) return st;
   Planes a, b;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  if ((st = prepare_operand(x, M, K, mode, w8, dev, s, &a)) != GF_OK) return st;
-  if ((st = prepare_operand(W, N, K, mode, w8 + operand_ws_bytes(M, K, mode), dev, s, &b)) != GF_OK) return st;
+  // (operands whose lo plane the GEMM computes itself need no split)
+  const int lo = lo_mask_at<Epi>(mode, gemm_tile_width<Epi>(M, N, mode, dev.sm_count));
+  if ((st = prepare_operand(x, M, K, mode, w8, dev, s, &a, !(lo & 1))) != GF_OK) return st;
+  if ((st = prepare_operand(W, N, K, mode, w8 + operand_ws_bytes(M, K, mode), dev, s, &b, !(lo & 2))) != GF_OK)
+    return st;
   return run_linear<Epi>(mode, dev, a, b, M, kpad(K, mode), N, m_fastest, ep, s);
 }
 
@@ -1000,9 +1036,13 @@ struct CudaHostPipe final : HostPipeOps {
     float* od = reinterpret_cast<float*>(ws + wl.out[buf]);
     Planes xp{};
     const GNParams ep{b_lin, bias, gamma, beta, od, int(rows), int(N), eps, int(N / groups)};
-    return prepare_operand(xd, rows, K, mode, ws + wl.xp[buf], dev, s, &xp) == GF_OK &&
-           with_gn_epilogue(ep, s, [&](auto tag) {
-             return run_linear<typename decltype(tag)::type>(mode, dev, xp, wp, rows, kpad(K, mode), N, 0, ep, s);
+    // (W's planes serve every chunk; a chunk's GEMM may compute x's lo plane
+    // itself, lo_mask_at)
+    return with_gn_epilogue(ep, s, [&](auto tag) {
+             using E = typename decltype(tag)::type;
+             const int lo = lo_mask_at<E>(mode, gemm_tile_width<E>(rows, N, mode, dev.sm_count));
+             const gf_status st = prepare_operand(xd, rows, K, mode, ws + wl.xp[buf], dev, s, &xp, !(lo & 1));
+             return st != GF_OK ? st : run_linear<E>(mode, dev, xp, wp, rows, kpad(K, mode), N, 0, ep, s);
            }) == GF_OK &&
            cudaEventRecord(ev_comp[buf], s) == cudaSuccess;
   }
