@@ -257,7 +257,7 @@ class DConv1d(Workload):
     metric = "fused LayerNorm->GELU->dilated Conv1d->residual TFLOP/s at x[32,256,4096]"
     sources = Workload.sources + ("dconv1d.cu",)
     kernel = "gemm_tc_kernel<256, OpTF32x3, ConvSrc, EpiConvResidual, 1>"
-    l2 = "inputs larger than L2 (x 134 MB read twice + A planes 268 MB + out 134 MB per step); no flush"
+    l2 = "inputs larger than L2 (x 134 MB read twice + activation plane 134 MB + out 134 MB per step); no flush"
     chunk = 1
 
     def __init__(self):

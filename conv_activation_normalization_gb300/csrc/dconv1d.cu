@@ -26,6 +26,7 @@
 // its LayerNorm/GELU work does not overlap the MMAs, and the planes path
 // stays the default.
 #include <cmath>
+#include <type_traits>
 
 #include "gemm_tc.cuh"
 #include "host_common.h"
@@ -34,6 +35,12 @@
 namespace gf {
 
 constexpr int kLnChunk = 8192;  // elements per ln_partial block (256 threads x 32)
+// In the 3xTF32 mode the GEMM computes the activations' lo plane in the SM
+// (gemm_tc_kernel, kLoInSm) while the weight planes are still arriving, so
+// the LayerNorm pass writes only the raw fp32 plane (step 0.2986 -> 0.2858
+// ms on x[32,256,4096]; the GEMM's time is unchanged).  The weights keep
+// both planes: converting them too made the GEMM slower (0.330 ms steps).
+constexpr int kLoConv = 1;
 
 // The statistics of a sample are taken as shifted sums S1 = sum (x - c) and
 // S2 = sum (x - c)^2 about one shift c per sample (the mean of the sample's
@@ -164,8 +171,9 @@ __device__ __forceinline__ void store_planes4(void* planes, size_t plane_elems, 
   if constexpr (MODE == GF_MODE_FP32_3XTF32) {
     float* p = static_cast<float*>(planes);
     __stcs(reinterpret_cast<float4*>(p + o), v);
-    __stcs(reinterpret_cast<float4*>(p + plane_elems + o),
-           make_float4(v.x - tf32_hi(v.x), v.y - tf32_hi(v.y), v.z - tf32_hi(v.z), v.w - tf32_hi(v.w)));
+    if constexpr (!(kLoConv & 1))  // (else the GEMM computes the lo plane itself)
+      __stcs(reinterpret_cast<float4*>(p + plane_elems + o),
+             make_float4(v.x - tf32_hi(v.x), v.y - tf32_hi(v.y), v.z - tf32_hi(v.z), v.w - tf32_hi(v.w)));
   } else {
     __nv_bfloat16* p = static_cast<__nv_bfloat16*>(planes);
     Bf16x4 h, l;
@@ -502,7 +510,9 @@ ConvWs conv_ws(int64_t B, int64_t C, int64_t L, int64_t ksize, int32_t mode, boo
   w.stats = off;
   off += align_up(size_t(B) * sizeof(float2), 256);
   w.a_planes = off;
-  if (!fused) off += align_up(size_t(B) * L * Cp * plane_bytes(mode), 256);
+  // (3xTF32: the raw plane only when the GEMM computes the lo plane itself)
+  const size_t act_bytes = mode == GF_MODE_FP32_3XTF32 && (kLoConv & 1) ? 4 : plane_bytes(mode);
+  if (!fused) off += align_up(size_t(B) * L * Cp * act_bytes, 256);
   w.w_planes = off;
   off += align_up(size_t(C) * ksize * Cp * plane_bytes(mode), 256);
   w.total = off;
@@ -554,13 +564,18 @@ gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const vo
   const uint64_t db[2] = {uint64_t(ksize) * Cp, uint64_t(C)};
   const uint32_t bb[2] = {uint32_t(Op::kBK), uint32_t(kBNConv)};
   const size_t a_plane = size_t(B) * L * Cp * Op::kElem, w_plane = size_t(C) * ksize * Cp * Op::kElem;
+  constexpr int LO = std::is_same<Op, OpTF32x3>::value ? kLoConv : 0;
   for (int p = 0; p < Op::kPlanes; ++p) {
-    gf_status st = make_tmap(&maps.a[p], static_cast<const uint8_t*>(a_planes) + p * a_plane, Op::kElem, 3, da, ba);
+    gf_status st = GF_OK;
+    if (p == 0 || !(LO & 1))
+      st = make_tmap(&maps.a[p], static_cast<const uint8_t*>(a_planes) + p * a_plane, Op::kElem, 3, da, ba);
     if (st != GF_OK) return st;
-    st = make_tmap(&maps.b[p], static_cast<const uint8_t*>(w_planes) + p * w_plane, Op::kElem, 2, db, bb);
+    if (p == 0 || !(LO & 2))
+      st = make_tmap(&maps.b[p], static_cast<const uint8_t*>(w_planes) + p * w_plane, Op::kElem, 2, db, bb);
     if (st != GF_OK) return st;
   }
-  ConvSrc src;
+  using Src = ConvSrcT<LO>;
+  Src src;
   src.C = int(Cp);  // channels per tap along K
   src.pad = padding;
   src.dil = dilation;
@@ -573,7 +588,7 @@ gf_status launch_conv_gemm(const DeviceInfo& dev, const void* a_planes, const vo
   src.bk = Op::kBK;
   src.nsamples = int(B);
   const int64_t tiles = int64_t(B) * src.num_jb * src.num_nb;
-  return launch_gemm<kBNConv, Op, ConvSrc, EpiConvResidual>(dev, maps, src, tiles, ep, s);
+  return launch_gemm<kBNConv, Op, Src, EpiConvResidual>(dev, maps, src, tiles, ep, s);
 }
 // The fused LayerNorm -> GELU -> dilated Conv1d GEMM (3xTF32): weight planes
 // in the channel-block-major k order, A built by the converter warps.

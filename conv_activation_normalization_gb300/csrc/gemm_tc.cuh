@@ -47,9 +47,12 @@
 // warps write lo = x - trunc_tf32(x) into the stage's lo plane before the
 // MMAs read it.  Elementwise, so the lo tile takes the hi tile's layout as it
 // is (the swizzle depends only on a byte's offset within the 1024-byte-aligned
-// tile).  The TMA completes on a stage's "loaded" barrier, which these warps
-// wait on; they arrive on "full" once the lo plane is written.  The operand
-// then needs no lo plane in memory and no pre-pass to write it.
+// tile).  The raw tiles they convert complete on the stage's "loaded"
+// barrier, which these warps wait on, the operand loaded whole (both planes,
+// if any) on "full", where the MMA waits for it and for the warps' arrivals
+// once the lo plane is written: the conversion of one operand overlaps the
+// other's copy.  The operand then needs no lo plane in memory and no pre-pass
+// to write it.
 //
 // Chunked accumulation (epi_chunked below): the tensor core adds
 // each MMA's products into the fp32 accumulator with truncation, which over a
@@ -267,11 +270,37 @@ struct LinearSrcT {
   template <int PLANES>
   __device__ __forceinline__ void load(const OperandMaps& m, uint64_t* bar, const uint32_t* sa, const uint32_t* sb,
                                        const Tile& t, int kb) const {
+    load_split<PLANES>(m, bar, bar, sa, sb, t, kb);
+  }
+  // A's planes complete on bar_a, B's on bar_b; the lo planes the kernel
+  // computes (LO) are not loaded
+  template <int PLANES>
+  __device__ __forceinline__ void load_split(const OperandMaps& m, uint64_t* bar_a, uint64_t* bar_b,
+                                             const uint32_t* sa, const uint32_t* sb, const Tile& t, int kb) const {
     const int k0 = kb * bk;
+    // the copies of the tiles the kernel converts go first
+    auto load_a = [&] {
 #pragma unroll
-    for (int p = 0; p < PLANES; ++p) {
-      if (p == 0 || !(LO & 1)) tma_load_2d(sa[p], &m.a[p], bar, k0, t.r0);
-      if (p == 0 || !(LO & 2)) tma_load_2d(sb[p], &m.b[p], bar, k0, t.n0);
+      for (int p = 0; p < PLANES; ++p)
+        if (p == 0 || !(LO & 1)) tma_load_2d(sa[p], &m.a[p], bar_a, k0, t.r0);
+    };
+    auto load_b = [&] {
+#pragma unroll
+      for (int p = 0; p < PLANES; ++p)
+        if (p == 0 || !(LO & 2)) tma_load_2d(sb[p], &m.b[p], bar_b, k0, t.n0);
+    };
+    if (LO == 0) {  // (the planes of A and B in turn)
+#pragma unroll
+      for (int p = 0; p < PLANES; ++p) {
+        tma_load_2d(sa[p], &m.a[p], bar_a, k0, t.r0);
+        tma_load_2d(sb[p], &m.b[p], bar_b, k0, t.n0);
+      }
+    } else if (LO == 2) {
+      load_b();
+      load_a();
+    } else {
+      load_a();
+      load_b();
     }
   }
   // Clusters of CL CTAs: unit q is the group of m-blocks CL mg .. CL mg +
@@ -321,7 +350,10 @@ using LinearSrc = LinearSrcT<0>;
 // B = weight planes [Cout][ksize * C] in the same k order (2-D maps).  With
 // the taps inner, the first touch of each row block (a DRAM read) comes every
 // ksize-th k-block instead of in a run of C / BK at the start of the tile.
-struct ConvSrc {
+// LO: operands whose lo plane the kernel computes (not loaded).
+template <int LO>
+struct ConvSrcT {
+  static constexpr int kLoInSm = LO;
   int C, pad, dil, ksize;
   int num_jb, num_nb, num_kb, bn, bk, nsamples;
   int kb_chunk;   // k-blocks per accumulation chunk (chunked epilogues only)
@@ -336,18 +368,45 @@ struct ConvSrc {
   template <int PLANES>
   __device__ __forceinline__ void load(const OperandMaps& m, uint64_t* bar, const uint32_t* sa, const uint32_t* sb,
                                        const Tile& t, int kb) const {
+    load_split<PLANES>(m, bar, bar, sa, sb, t, kb);
+  }
+  // A's planes complete on bar_a, B's on bar_b; the lo planes the kernel
+  // computes (LO) are not loaded
+  template <int PLANES>
+  __device__ __forceinline__ void load_split(const OperandMaps& m, uint64_t* bar_a, uint64_t* bar_b,
+                                             const uint32_t* sa, const uint32_t* sb, const Tile& t, int kb) const {
     const int k0 = kb * bk;
     const int cb = kb / ksize;
     const int tap = kb - cb * ksize;
     const int ci0 = cb * bk;
     const int l = t.r0 - pad + tap * dil;
+    // the copies of the tiles the kernel converts go first
+    auto load_a = [&] {
 #pragma unroll
-    for (int p = 0; p < PLANES; ++p) {
-      tma_load_3d(sa[p], &m.a[p], bar, ci0, l, t.b);
-      tma_load_2d(sb[p], &m.b[p], bar, k0, t.n0);
+      for (int p = 0; p < PLANES; ++p)
+        if (p == 0 || !(LO & 1)) tma_load_3d(sa[p], &m.a[p], bar_a, ci0, l, t.b);
+    };
+    auto load_b = [&] {
+#pragma unroll
+      for (int p = 0; p < PLANES; ++p)
+        if (p == 0 || !(LO & 2)) tma_load_2d(sb[p], &m.b[p], bar_b, k0, t.n0);
+    };
+    if (LO == 0) {  // (the planes of A and B in turn)
+#pragma unroll
+      for (int p = 0; p < PLANES; ++p) {
+        tma_load_3d(sa[p], &m.a[p], bar_a, ci0, l, t.b);
+        tma_load_2d(sb[p], &m.b[p], bar_b, k0, t.n0);
+      }
+    } else if (LO == 2) {
+      load_b();
+      load_a();
+    } else {
+      load_a();
+      load_b();
     }
   }
 };
+using ConvSrc = ConvSrcT<0>;
 
 // lo = x - trunc_tf32(x) of a BYTES-long fp32 tile in shared memory, written
 // at the same offsets of `lo`, by the kSplitWarps * 32 threads (thread ct):
@@ -389,6 +448,12 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
   constexpr int kLo = SrcLo<Src>::mask;
   static_assert(kLo == 0 || (Op::kind == MmaKind::TF32 && Op::kPlanes == 2 && kConv == 0 && CL == 1),
                 "lo planes are computed in the SM from raw fp32 tiles only (3xTF32), by their own warps");
+  // (kLo) bytes of a stage on "loaded" (the raw tiles converted here) and on
+  // "full" (an operand loaded with both planes)
+  constexpr uint32_t kLoLoadedTx =
+      ((kLo & 1) ? TileCfg<BN, Op>::A_BYTES : 0) + ((kLo & 2) ? TileCfg<BN, Op>::B_BYTES : 0);
+  constexpr uint32_t kLoFullTx =
+      ((kLo & 1) ? 0 : 2 * TileCfg<BN, Op>::A_BYTES) + ((kLo & 2) ? 0 : 2 * TileCfg<BN, Op>::B_BYTES);
   using Cfg = TileCfg<BN, Op, SrcConv<Src>::scratch + epi_smem_bytes<Epi, Op>()>;
   constexpr int S = Cfg::STAGES;
   constexpr int P = Op::kPlanes;
@@ -413,7 +478,7 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       // the TMA thread (and the converter warps), or the lo-plane warps
-      mbar_init(&full[s], kLo ? kSplitWarps : 1 + SrcConv<Src>::arrivals);
+      mbar_init(&full[s], kLo ? kSplitWarps + (kLoFullTx ? 1 : 0) : 1 + SrcConv<Src>::arrivals);
       mbar_init(&empty[s], CL);  // the MMA commit of each CTA of the cluster
       mbar_init(&loaded[s], 1);
     }
@@ -484,17 +549,21 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
             sa[p] = a_addr(stage, p);
             sb[p] = b_addr(stage, p);
           }
-          // bytes the TMA brings: the stage less the converters' A planes
-          // or the lo planes computed here
-          constexpr uint32_t kTx = kConv ? P * Cfg::B_BYTES
-                                         : Cfg::STAGE_BYTES - ((kLo & 1) ? Cfg::A_BYTES : 0) -
-                                               ((kLo & 2) ? Cfg::B_BYTES : 0);
-          uint64_t* tx_bar = kLo ? &loaded[stage] : &full[stage];
-          mbar_arrive_expect_tx(tx_bar, kTx);
-          if constexpr (CL > 1)
-            src.template load_group<CL>(maps, tx_bar, sa[0], sb[0], tile, kb, crank);
-          else
-            src.template load<P>(maps, tx_bar, sa, sb, tile, kb);
+          if constexpr (kLo != 0) {
+            // the raw tiles the lo-plane warps convert first (their copies
+            // issued first), then an operand loaded whole
+            mbar_arrive_expect_tx(&loaded[stage], kLoLoadedTx);
+            if constexpr (kLoFullTx != 0) mbar_arrive_expect_tx(&full[stage], kLoFullTx);
+            src.template load_split<P>(maps, (kLo & 1) ? &loaded[stage] : &full[stage],
+                                       (kLo & 2) ? &loaded[stage] : &full[stage], sa, sb, tile, kb);
+          } else {
+            // bytes the TMA brings: the stage less the converters' A planes
+            mbar_arrive_expect_tx(&full[stage], kConv ? P * Cfg::B_BYTES : Cfg::STAGE_BYTES);
+            if constexpr (CL > 1)
+              src.template load_group<CL>(maps, &full[stage], sa[0], sb[0], tile, kb, crank);
+            else
+              src.template load<P>(maps, &full[stage], sa, sb, tile, kb);
+          }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -511,6 +580,8 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
         if ((issued >> s) & 1u) {
           if (!mbar_wait(kLo ? &loaded[s] : &full[s], (issued_phase >> s) & 1u))
             record_error(status, GF_DEV_WAIT_TIMEOUT);
+          if constexpr (kLo != 0 && kLoFullTx != 0)
+            if (!mbar_wait(&full[s], (issued_phase >> s) & 1u)) record_error(status, GF_DEV_WAIT_TIMEOUT);
           if constexpr (CL > 1)
             if (!mbar_wait(&empty[s], (issued_phase >> s) & 1u)) record_error(status, GF_DEV_WAIT_TIMEOUT);
         }

@@ -82,12 +82,13 @@ def test_workspace_sizes(L):
     # one (max, sum) float2 per row and column half of each n-block, sized
     # for the narrowest (160-column) tile width
     assert L.gf_linear_lse_act_workspace_size(M, K, N, 0) == 4 * (M * K + N * K) + M * (-(-N // 160) * 2) * 8
-    # the default keeps activation planes (8 B per activation in the
-    # 3xTF32 mode); GF_FLAG_FUSED_PRODUCER (3xTF32, taps within 92
+    # the default keeps the activations' raw fp32 plane (4 B per activation
+    # in the 3xTF32 mode: the GEMM computes the lo plane itself) and the
+    # weight planes; GF_FLAG_FUSED_PRODUCER (3xTF32, taps within 92
     # positions) only the LayerNorm partials, statistics and weight planes
     FUSED = 0x200
     planes = L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, 0)
-    assert planes > 2 * 4 * 32 * 256 * 4096
+    assert 4 * 32 * 256 * 4096 < planes < 4 * 32 * 256 * 4096 + (4 << 20)
     fused = L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 4, FUSED)
     assert 2 * 4 * 256 * 256 * 3 <= fused < 4 << 20
     assert L.gf_ln_gelu_dconv1d_res_workspace_size(32, 256, 4096, 3, 46, FUSED) == fused

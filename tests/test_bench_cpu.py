@@ -83,13 +83,15 @@ def algo_bytes(name, work):
     """Algorithmic DRAM bytes of one launch of each workload's dominant kernel."""
     M, K, N = {"linear_gn_m32768": (32768, 1024, 4096), "linear_gn_m256": (256, 1024, 4096),
                "linear_lse_m1024": (1024, 8192, 8192)}.get(name, (0, 0, 0))
+    if name == "linear_gn_m256":  # x, W, out: at 64-column tiles the GEMM computes both lo planes itself
+        return 4 * (M * K + N * K + M * N)
     if name.startswith("linear_gn"):  # x and its lo plane, W and its lo plane, out
         return 4 * (2 * M * K + 2 * N * K + M * N)
     if name == "linear_lse_m1024":  # x, W and their lo planes (the partials are small)
         return 4 * (2 * M * K + 2 * N * K)
-    if name == "ln_dconv1d_b32":  # A hi/lo planes, W planes, x (residual), out
+    if name == "ln_dconv1d_b32":  # the activations' raw plane (the GEMM computes lo), W planes, x (residual), out
         B, C, L = 32, 256, 4096
-        return 4 * (2 * B * C * L + 2 * C * C * 3 + 2 * B * C * L)
+        return 4 * (B * C * L + 2 * C * C * 3 + 2 * B * C * L)
     return work  # convt3d: x once + out once
 
 
