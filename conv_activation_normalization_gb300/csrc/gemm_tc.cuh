@@ -16,7 +16,8 @@
 //   OpBF16x1  one BF16 product (the BF16 mode).
 // All modes accumulate in fp32 in TMEM.
 //
-// Roles (one CTA per SM, 320 threads, plus a source's converter warps):
+// Roles (one CTA per SM, 320 threads, plus a source's converter warps or the
+// lo-plane warps below):
 //   warp 0      one thread issues TMA loads of a k-block's operand tiles (one
 //               or two planes of A and of B) into a ring of smem stages
 //               (full/empty mbarriers);
@@ -137,7 +138,8 @@ struct TileCfg {
 
 // TMA descriptors of the operand planes: a[0]/b[0] = hi (or the only
 // operand), a[1]/b[1] = lo (three-product modes); c = the fp32 output [M][N]
-// in 32 x 32 boxes, for epilogues that store through TMA (epi_tma_store).
+// in boxes of 32 rows x 16 columns, for epilogues that store through TMA
+// (epi_tma_store).
 struct OperandMaps {
   CUtensorMap a[2];
   CUtensorMap b[2];
@@ -464,7 +466,7 @@ __global__ void __launch_bounds__(gemm_threads<Src, Epi, Op, BN>(), 1)
   uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* loaded = drain + 1;  // (kLo) the TMA's bytes of stage s have landed
+  uint64_t* loaded = drain + 1;  // (kLo) the raw tiles the lo-plane warps convert have landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(loaded + S);
   static_assert((3 * S + 5) * 8 + 8 <= Cfg::BAR_BYTES, "barriers overflow their space");
   volatile uint32_t* abort_flag = tmem_slot + 1;
