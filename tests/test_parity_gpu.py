@@ -445,6 +445,29 @@ def test_convt3d_workload_sampled():
     assert_close(got, ref, "convt3d full workload (samples 0, 63, 127)")
 
 
+# The 3xTF32 lo planes come from a pre-pass at 256-column tiles and are
+# computed in the SM at 64-column tiles (few rows).  lo = x - trunc(x) is the
+# same value either way and every output element takes the same products in
+# the same K order, so rows computed at M = 256 equal the same rows computed
+# inside a call whose tile width is 256, bit for bit, for each fused group
+# width.
+@pytest.mark.parametrize("gw", [16, 32, 64, 128])
+def test_linear_gn_lo_in_sm_matches_pre_pass(gw):
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    K, N = 1024, 4096
+    big, small = 2432, 256
+    assert gf.linear_tile_width(gf.GF_CHAIN_GROUPNORM, big, N, N // gw, 0, sm) == 256
+    assert gw == 128 or gf.linear_tile_width(gf.GF_CHAIN_GROUPNORM, small, N, N // gw, 0, sm) == 64
+    s, d = _lgn_case(big, K, N, N // gw, 4600 + gw)
+    dev = {k: T(d[k]) for k in ("W", "b_lin", "bias", "gamma", "beta")}
+    x = T(d["x"])
+    whole = gf.gf_linear_swish_bias_groupnorm(x, dev["W"], dev["b_lin"], dev["bias"], dev["gamma"], dev["beta"],
+                                              s.groups, s.eps)
+    part = gf.gf_linear_swish_bias_groupnorm(x[:small].contiguous(), dev["W"], dev["b_lin"], dev["bias"],
+                                             dev["gamma"], dev["beta"], s.groups, s.eps)
+    assert torch.equal(part, whole[:small])
+
+
 # ------------------------------------------------- host-buffer pipeline
 @pytest.mark.parametrize("pinned,chunk,groups", [(True, 0, 8), (True, 200, 8), (False, 384, 8), (True, 200, 4),
                                                  (True, 0, 16), (True, 200, 2)])
