@@ -46,11 +46,20 @@
 //                slots and writes the tile's 16 (A, A, B, B) into a shared
 //                slot (two warps, so that one's reduction latency does not
 //                limit the round rate);
-//   warps 8-23   epilogue: warp (8 + e) owns TMEM lane quadrant (warp % 4)
-//                and the 32 columns of chunk e / 4 (output phases
-//                pd = chunk / 2, ph = chunk % 2, 16 channels x both pw); per
-//                round it writes the tile from three rounds earlier and does
-//                the statistics work of the new tile, the two interleaved.
+//   warps 8-15   output: warp (8 + e) owns TMEM lane quadrant (warp % 4) and
+//                the 64 columns of chunks 2 (e / 4) and 2 (e / 4) + 1 (chunk
+//                c: output phases pd = c / 2, ph = c % 2, 16 channels x both
+//                pw); per round it writes the tile from three rounds earlier;
+//   warps 16-23  statistics: the same lanes and columns of the new tile:
+//                Swish, written back over the accumulator, and the per-group
+//                sums.
+// The two groups wait on different things (the coefficients and the Swish
+// values of an old tile; the accumulator and the records of the new one), so
+// each group's waits overlap the other's column work; they poll (the
+// fastest wake-up measured here).  The Swish values
+// cross from one group to the other through TMEM: a statistics warp waits for
+// its tcgen05.st to complete and arrives on the buffer's `sdone` barrier,
+// which the output warps wait on before their tcgen05.ld.
 #pragma once
 
 #include "convt3d_tc.cuh"
@@ -58,6 +67,8 @@
 namespace gf {
 
 constexpr int kCfEpiWarps = 16;
+constexpr int kCfOutWarps = 8;   // warps 8-15
+constexpr int kCfStatWarps = 8;  // warps 16-23
 constexpr int kCfPubWarp = 5;
 constexpr int kCfCoefWarp0 = 6;   // and 7
 constexpr int kCfCoefWarps = 2;
@@ -66,7 +77,7 @@ constexpr int kCfThreads = (kCfEpiWarp0 + kCfEpiWarps) * 32;
 constexpr int kCfBufs = 4;                          // TMEM tile buffers of 128 columns
 constexpr int kCfLag = 3;                           // rounds between a tile's statistics and its output
 constexpr int kCfCoefFloats = 16 * 4;               // per buffer: 16 channels x (A, A, B, B)
-constexpr int kCfPartFloats = kCfEpiWarps * 8;      // per round: 8 sums per epilogue warp
+constexpr int kCfPartFloats = kCfStatWarps * 8;     // per round: 8 sums per statistics warp
 constexpr float kLog2e = 1.4426950408889634f;
 // The producers run at most kCtTcStages tiles ahead of the MMAs, which run at
 // most kCfBufs tiles ahead of the output of a tile: the records of the last
@@ -75,6 +86,7 @@ static_assert(kCtRecSlots >= kCtTcStages + kCfBufs, "record ring too short");
 constexpr int kCfRecBytes = kCtRecSlots * 128 * 8;
 constexpr int kCfSmem = kCtTcStages * kCtTcStageBytes + kCtTcBBytes + kCfBufs * kCfCoefFloats * 4 +
                         2 * kCfPartFloats * 4 + kCfRecBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+static_assert(kCfOutWarps + kCfStatWarps == kCfEpiWarps, "the epilogue warps split into two groups");
 
 struct CfParams {
   const float* x;
@@ -205,7 +217,7 @@ struct CfOutSide {
   float* oc;          // output of channel 0, width phase 0
   const float* cf;    // (A, A, B, B) per channel
   bool pv0, pv1;      // the width-phase-0 / 1 outputs lie inside the volume
-  uint64_t* tempty;   // released once the columns are read
+  uint64_t* tempty;   // released once the columns are read (null: not by this call)
 };
 
 template <bool OUT, bool P1, int K>
@@ -220,7 +232,7 @@ __device__ __forceinline__ void cf_round(const CfOutSide& o, uint32_t q_taddr, c
     if constexpr (P1) GF_TMEM_WAIT8(ry);
     if constexpr (OUT) {
       GF_TMEM_WAIT8(rz);
-      if (part == 32 / kPiece - 1) {  // all columns read: the MMAs may overwrite the buffer
+      if (o.tempty && part == 32 / kPiece - 1) {  // all columns read: the MMAs may overwrite the buffer
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o.tempty);
@@ -286,7 +298,8 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
   uint64_t* pfull = cempty + kCfBufs;     // [2] partial sums of the round written
   uint64_t* pempty = pfull + 2;           // [2] partial sums consumed
   uint64_t* rfull = pempty + 2;           // [kCtRecSlots] the tile's cell records written
-  uint64_t* drain = rfull + kCtRecSlots;
+  uint64_t* sdone = rfull + kCtRecSlots;  // [kCfBufs] buffer b's Swish values written back
+  uint64_t* drain = sdone + kCfBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -302,12 +315,13 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
     }
     for (int b = 0; b < kCfBufs; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kCfEpiWarps);
+      mbar_init(&tempty[b], kCfOutWarps);
       mbar_init(&cfull[b], 1);
-      mbar_init(&cempty[b], kCfEpiWarps);
+      mbar_init(&cempty[b], kCfOutWarps);
+      mbar_init(&sdone[b], kCfStatWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&pfull[i], kCfEpiWarps);
+      mbar_init(&pfull[i], kCfStatWarps);
       mbar_init(&pempty[i], 1);
     }
     for (int i = 0; i < kCtRecSlots; ++i) mbar_init(&rfull[i], kCtTcProducerThreads / 32);
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
         // value v = lane: sum s' (even) or sum s'^2 (odd) of group lane / 2
         const float* ps = part_s + (r & 1) * kCfPartFloats + lane;
 #pragma unroll
-        for (int e = 0; e < kCfEpiWarps; ++e) v += ps[e * 8];
+        for (int e = 0; e < kCfStatWarps; ++e) v += ps[e * 8];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&pempty[r & 1]);
@@ -393,86 +407,97 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int e = warp - kCfEpiWarp0;
-    const int quad = warp & 3, chunk = e >> 2;
-    const int pd = chunk >> 1, ph = chunk & 1;  // depth and height phase of the warp's columns
+    const bool out_group = warp < kCfEpiWarp0 + kCfOutWarps;
+    const int e = out_group ? warp - kCfEpiWarp0 : warp - kCfEpiWarp0 - kCfOutWarps;
+    const int quad = warp & 3, c0 = 2 * (e >> 2);  // the warp's chunks: c0, c0 + 1
     const int row = quad * 32 + lane;
-    // record flags that make the warp's width-phase-0 / 1 outputs exist: the
+    constexpr uint64_t kOffMask = (uint64_t(1) << 56) - 1;
+    // record flags that make a chunk's width-phase-0 / 1 outputs exist: the
     // cell (bit 0), depth phase pd (bit 1), height phase ph (bit 2), width
     // phase 1 (bit 3)
-    const uint32_t m0 = 1u | (uint32_t(pd) << 1) | (uint32_t(ph) << 2), m1 = m0 | 8u;
-    const uint32_t phase_off = uint32_t(pd) * uint32_t(p.OHW) + uint32_t(ph) * uint32_t(p.OW);
-    constexpr uint64_t kOffMask = (uint64_t(1) << 56) - 1;
-    const uint32_t lane_base = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(chunk * 32);
-    for (int r = 0; r < p.rounds + kCfLag; ++r) {
-      if (__any_sync(kFull, *abort_flag)) break;
-      // output of the tile of round r - kCfLag, statistics of the tile of round r
-      const int ro = r - kCfLag, to = blockIdx.x + ro * G, tp = blockIdx.x + r * G;
-      const bool has_out = r >= kCfLag && to < p.num_tiles, has_p1 = r < p.rounds && tp < p.num_tiles;
-      CfOutSide o{};
-      int ob = 0;
-      if (has_out) {
-        ob = ro % kCfBufs;
-        if (!__all_sync(kFull, mbar_wait<true>(&cfull[ob], (ro / kCfBufs) & 1))) {
-          fail();
-          break;
-        }
-        // (this thread read the record in round ro, after its barrier; the
-        // slot is not rewritten before this tile's buffer is released)
-        const uint64_t rv = rec_s[(ro % kCtRecSlots) * 128 + row];
-        const uint32_t fl = uint32_t(rv >> 56);
-        o.pv0 = (fl & m0) == m0;
-        o.pv1 = (fl & m1) == m1;
-        o.taddr = lane_base + uint32_t(ob * 128);
-        o.oc = p.out + ((rv & kOffMask) + phase_off);
-        o.cf = coef_s + ob * kCfCoefFloats;
-        o.tempty = &tempty[ob];
-      }
-      if (r < p.rounds && !__all_sync(kFull, mbar_wait<true>(&pempty[r & 1], ((r >> 1) & 1) ^ 1))) {
-        fail();
-        break;
-      }
-      uint32_t q_taddr = 0;
-      float mx = 0.f, my = 0.f;  // the new tile's width phase 0 / 1 outputs exist (1) or not (0)
-      if (has_p1) {
-        const int buf = r % kCfBufs;
-        if (!__all_sync(kFull, mbar_wait<true>(&rfull[r % kCtRecSlots], (r / kCtRecSlots) & 1)) ||
-            !__all_sync(kFull, mbar_wait<true>(&tfull[buf], (r / kCfBufs) & 1))) {
+    auto m0_of = [](int c) { return 1u | (uint32_t(c >> 1) << 1) | (uint32_t(c & 1) << 2); };
+    const uint32_t lane_base = tmem_base + (uint32_t(quad * 32) << 16);
+    if (out_group) {
+      // ------------------------------------------------ output of old tiles
+      for (int r = kCfLag; r < p.rounds + kCfLag; ++r) {
+        if (__any_sync(kFull, *abort_flag)) break;
+        const int ro = r - kCfLag, to = blockIdx.x + ro * G;
+        if (to >= p.num_tiles) break;
+        const int ob = ro % kCfBufs;
+        // the tile's coefficients, its Swish values, and its records (the
+        // slot's phase of round ro: its next use waits for this buffer)
+        if (!__all_sync(kFull, mbar_wait(&cfull[ob], (ro / kCfBufs) & 1)) ||
+            !__all_sync(kFull, mbar_wait(&sdone[ob], (ro / kCfBufs) & 1)) ||
+            !__all_sync(kFull, mbar_wait(&rfull[ro % kCtRecSlots], (ro / kCtRecSlots) & 1))) {
           fail();
           break;
         }
         tc_fence_after();
-        const uint32_t fl = uint32_t(rec_s[(r % kCtRecSlots) * 128 + row] >> 56);
-        mx = (fl & m0) == m0 ? 1.f : 0.f;
-        my = (fl & m1) == m1 ? 1.f : 0.f;
-        q_taddr = lane_base + uint32_t(buf * 128);
-      }
-      // this thread's Swish values of the previous round are in TMEM before
-      // any of them is read back (three rounds on)
-      tmem_wait_st();
-      float2 gs[4], gq[4];
-      if (has_out && has_p1)
-        cf_round<true, true, K>(o, q_taddr, p.bias, p.plane, lane, gs, gq);
-      else if (has_out)
-        cf_round<true, false, K>(o, q_taddr, p.bias, p.plane, lane, gs, gq);
-      else if (has_p1)
-        cf_round<false, true, K>(o, q_taddr, p.bias, p.plane, lane, gs, gq);
-      if (has_out) {
+        const uint64_t rv = rec_s[(ro % kCtRecSlots) * 128 + row];
+        const uint32_t fl = uint32_t(rv >> 56);
+        float2 gs[4], gq[4];  // (unused by the output side)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int c = c0 + k;
+          const uint32_t m0 = m0_of(c), m1 = m0 | 8u;
+          CfOutSide o{};
+          o.pv0 = (fl & m0) == m0;
+          o.pv1 = (fl & m1) == m1;
+          o.taddr = lane_base + uint32_t(c * 32 + ob * 128);
+          o.oc = p.out + ((rv & kOffMask) + uint32_t(c >> 1) * uint32_t(p.OHW) + uint32_t(c & 1) * uint32_t(p.OW));
+          o.cf = coef_s + ob * kCfCoefFloats;
+          o.tempty = k == 1 ? &tempty[ob] : nullptr;  // after the warp's last columns
+          cf_round<true, false, K>(o, 0u, p.bias, p.plane, lane, gs, gq);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&cempty[ob]);
       }
-      if (has_p1) {
-        // the cell's existing phases only, then a reduce-scatter of the 8 sums
-        // over the warp's 32 lanes (9 shuffles): afterwards lane l holds the
-        // full sum of value v = 4*b4 + 2*b3 + b2 (b_i = bit i of l), value v
-        // being the sum s' (even v) or s'^2 (odd v) of group v / 2
+    } else {
+      // -------------------------------------------- statistics of new tiles
+      for (int r = 0; r < p.rounds; ++r) {
+        if (__any_sync(kFull, *abort_flag)) break;
+        const int tp = blockIdx.x + r * G;
+        const bool has_p1 = tp < p.num_tiles;
+        if (!__all_sync(kFull, mbar_wait(&pempty[r & 1], ((r >> 1) & 1) ^ 1))) {
+          fail();
+          break;
+        }
         float rs[8];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          rs[2 * g] = fmaf(gs[g].y, my, gs[g].x * mx);
-          rs[2 * g + 1] = fmaf(gq[g].y, my, gq[g].x * mx);
-        }
-        {
+        for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+        if (has_p1) {
+          const int buf = r % kCfBufs;
+          if (!__all_sync(kFull, mbar_wait(&rfull[r % kCtRecSlots], (r / kCtRecSlots) & 1)) ||
+              !__all_sync(kFull, mbar_wait(&tfull[buf], (r / kCfBufs) & 1))) {
+            fail();
+            break;
+          }
+          tc_fence_after();
+          const uint32_t fl = uint32_t(rec_s[(r % kCtRecSlots) * 128 + row] >> 56);
+          const CfOutSide none{};
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int c = c0 + k;
+            const uint32_t m0 = m0_of(c), m1 = m0 | 8u;
+            // the cell's existing phases of this chunk only
+            const float mx = (fl & m0) == m0 ? 1.f : 0.f, my = (fl & m1) == m1 ? 1.f : 0.f;
+            float2 gs[4], gq[4];
+            cf_round<false, true, K>(none, lane_base + uint32_t(c * 32 + buf * 128), p.bias, p.plane, lane, gs, gq);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              rs[2 * g] += fmaf(gs[g].y, my, gs[g].x * mx);
+              rs[2 * g + 1] += fmaf(gq[g].y, my, gq[g].x * mx);
+            }
+          }
+          // the Swish values are in TMEM before the output warps read them
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sdone[buf]);
+          // reduce-scatter of the 8 sums over the warp's 32 lanes (9
+          // shuffles): afterwards lane l holds the full sum of value
+          // v = 4*b4 + 2*b3 + b2 (b_i = bit i of l), value v being the sum
+          // s' (even v) or s'^2 (odd v) of group v / 2
           const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -493,10 +518,8 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
           }
           rs[0] += __shfl_xor_sync(kFull, rs[0], 2);
           rs[0] += __shfl_xor_sync(kFull, rs[0], 1);
+          if ((lane & 3) == 0) part_s[(r & 1) * kCfPartFloats + e * 8 + (lane >> 2)] = rs[0];
         }
-        if ((lane & 3) == 0) part_s[(r & 1) * kCfPartFloats + e * 8 + (lane >> 2)] = rs[0];
-      }
-      if (r < p.rounds) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&pfull[r & 1]);
       }
