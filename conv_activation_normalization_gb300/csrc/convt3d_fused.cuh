@@ -206,12 +206,12 @@ __device__ __forceinline__ void cf_sample_coefs(const CfParams& p, int n, int P,
   }
 }
 
-// One round of an epilogue warp: the output of an earlier tile (OUT) and the
-// statistics work of the new tile (P1), interleaved piece by piece (8
-// columns = 4 channels = one group), so that the Swish of one and the stores
-// of the other overlap.  Columns 2 co + pw of the warp's chunk are channel co
-// at width phase pw.  gs / gq collect, per group, the (pw 0, pw 1) sums of s'
-// and s'^2 over every cell; the caller masks out the phases that do not exist.
+// The column work of an epilogue warp on one 32-column chunk: the output of
+// an earlier tile (OUT) or the statistics work of the new tile (P1), kCfPiece
+// columns (kCfPiece / 8 groups of 4 channels) per TMEM load.  Columns
+// 2 co + pw of the warp's chunk are channel co at width phase pw.  gs / gq
+// collect, per group, the (pw 0, pw 1) sums of s' and s'^2 over every cell;
+// the caller masks out the phases that do not exist.
 struct CfOutSide {
   uint32_t taddr;     // TMEM address of the warp's 32 columns (Swish values)
   float* oc;          // output of channel 0, width phase 0
@@ -220,18 +220,46 @@ struct CfOutSide {
   uint64_t* tempty;   // released once the columns are read (null: not by this call)
 };
 
+// TMEM pieces of N = 8, 16 or 32 columns of this thread's lane: load (then
+// wait), store.
+template <int N>
+__device__ __forceinline__ void cf_tmem_ld(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 8) {
+    GF_TMEM_LD8(taddr, r);
+    GF_TMEM_WAIT8(r);
+  } else if constexpr (N == 16) {
+    GF_TMEM_LD16(taddr, r);
+    GF_TMEM_WAIT16(r);
+  } else {
+    GF_TMEM_LD32(taddr, r);
+    GF_TMEM_WAIT32(r);
+  }
+}
+template <int N>
+__device__ __forceinline__ void cf_tmem_st(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 8)
+    GF_TMEM_ST8(taddr, r);
+  else if constexpr (N == 16)
+    GF_TMEM_ST16(taddr, r);
+  else
+    GF_TMEM_ST32(taddr, r);
+}
+// Columns per TMEM load of an epilogue warp (a warp of either group reads one
+// side only): 0.2739 ms per call with 8, 0.2639 with 16, 0.2854 with 32
+// (which spills at the 80 registers 768 threads leave).
+constexpr int kCfPiece = 16;
+
 template <bool OUT, bool P1, int K>
 __device__ __forceinline__ void cf_round(const CfOutSide& o, uint32_t q_taddr, const float* bias, uint32_t plane,
                                          int lane, float2 (&gs)[4], float2 (&gq)[4]) {
-  constexpr int kPiece = 8;
+  static_assert(!(OUT && P1), "a warp of either group reads one side");
+  constexpr int kPiece = kCfPiece;
 #pragma unroll
   for (int part = 0; part < 32 / kPiece; ++part) {
     uint32_t ry[kPiece], rz[kPiece];
-    if constexpr (P1) GF_TMEM_LD8(q_taddr + uint32_t(part * kPiece), ry);
-    if constexpr (OUT) GF_TMEM_LD8(o.taddr + uint32_t(part * kPiece), rz);
-    if constexpr (P1) GF_TMEM_WAIT8(ry);
+    if constexpr (P1) cf_tmem_ld<kPiece>(q_taddr + uint32_t(part * kPiece), ry);
     if constexpr (OUT) {
-      GF_TMEM_WAIT8(rz);
+      cf_tmem_ld<kPiece>(o.taddr + uint32_t(part * kPiece), rz);
       if (o.tempty && part == 32 / kPiece - 1) {  // all columns read: the MMAs may overwrite the buffer
         tc_fence_before();
         __syncwarp();
@@ -240,7 +268,7 @@ __device__ __forceinline__ void cf_round(const CfOutSide& o, uint32_t q_taddr, c
     }
 #pragma unroll
     for (int j = 0; j < kPiece / 2; ++j) {
-      const int co = part * (kPiece / 2) + j;  // (co >> 2 == part: a piece is one group)
+      const int co = part * (kPiece / 2) + j, g = co >> 2;  // channel, group
       if constexpr (P1) {
         float2 u = make_float2(__uint_as_float(ry[2 * j]), __uint_as_float(ry[2 * j + 1]));
         if constexpr (K == 32) {  // no padding column: the (scaled) bias is added here
@@ -252,12 +280,12 @@ __device__ __forceinline__ void cf_round(const CfOutSide& o, uint32_t q_taddr, c
         // s' = u / (1 + 2^-u)
         const float2 d = add2(make_float2(ex2_approx(-u.x), ex2_approx(-u.y)), make_float2(1.f, 1.f));
         const float2 sv = mul2(u, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
-        if (j == 0) {
-          gs[part] = sv;
-          gq[part] = mul2(sv, sv);
+        if ((co & 3) == 0) {
+          gs[g] = sv;
+          gq[g] = mul2(sv, sv);
         } else {
-          gs[part] = add2(gs[part], sv);
-          gq[part] = fma2(sv, sv, gq[part]);
+          gs[g] = add2(gs[g], sv);
+          gq[g] = fma2(sv, sv, gq[g]);
         }
         ry[2 * j] = __float_as_uint(sv.x);
         ry[2 * j + 1] = __float_as_uint(sv.y);
@@ -276,7 +304,7 @@ __device__ __forceinline__ void cf_round(const CfOutSide& o, uint32_t q_taddr, c
         if (o.pv1) __stcs(oc + 1, v.y);
       }
     }
-    if constexpr (P1) GF_TMEM_ST8(q_taddr + uint32_t(part * kPiece), ry);
+    if constexpr (P1) cf_tmem_st<kPiece>(q_taddr + uint32_t(part * kPiece), ry);
   }
 }
 
