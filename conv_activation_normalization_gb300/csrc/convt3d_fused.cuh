@@ -50,16 +50,16 @@
 //                the 64 columns of chunks 2 (e / 4) and 2 (e / 4) + 1 (chunk
 //                c: output phases pd = c / 2, ph = c % 2, 16 channels x both
 //                pw); per round it writes the tile from three rounds earlier;
-//   warps 16-23  statistics: the same lanes and columns of the new tile:
-//                Swish, written back over the accumulator, and the per-group
-//                sums.
+//   warps 16-23  statistics: the same lanes and columns of the new tile, as
+//                four 16-column half-chunks per warp: Swish, written back
+//                over the accumulator, and the per-group sums.
 // The two groups wait on different things (the coefficients and the Swish
 // values of an old tile; the accumulator and the records of the new one), so
 // each group's waits overlap the other's column work; they poll (the
-// fastest wake-up measured here).  The Swish values
-// cross from one group to the other through TMEM: a statistics warp waits for
-// its tcgen05.st to complete and arrives on the buffer's `sdone` barrier,
-// which the output warps wait on before their tcgen05.ld.
+// fastest wake-up measured here).  The Swish values cross from one group to
+// the other through TMEM: a statistics warp waits for its tcgen05.st to
+// complete and arrives on the buffer's `sdone` barrier, which the output
+// warps wait on before their tcgen05.ld.
 #pragma once
 
 #include "convt3d_tc.cuh"
