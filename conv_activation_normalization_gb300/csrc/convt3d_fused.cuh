@@ -50,9 +50,9 @@
 //                the 64 columns of chunks 2 (e / 4) and 2 (e / 4) + 1 (chunk
 //                c: output phases pd = c / 2, ph = c % 2, 16 channels x both
 //                pw); per round it writes the tile from three rounds earlier;
-//   warps 16-23  statistics: the same lanes and columns of the new tile, as
-//                four 16-column half-chunks per warp: Swish, written back
-//                over the accumulator, and the per-group sums.
+//   warps 16-23  statistics: the same lanes and columns of the new tile,
+//                a chunk per TMEM load: Swish, written back over the
+//                accumulator, and the per-group sums.
 // The two groups wait on different things (the coefficients and the Swish
 // values of an old tile; the accumulator and the records of the new one), so
 // each group's waits overlap the other's column work; they poll (the
@@ -67,14 +67,11 @@
 namespace gf {
 
 constexpr int kCfEpiWarps = 16;
-// Output warps per TMEM lane quadrant (the rest of the quadrant's 4 epilogue
-// warps take the statistics): an output warp takes 4 / kCfOutPerQuad chunks,
-// a statistics warp a share of the quadrant's 8 half-chunks.  Two and two:
-// 0.2392 ms per call; one output warp and three statistics warps, 0.297.
-constexpr int kCfOutPerQuad = 2;
-constexpr int kCfStatPerQuad = 4 - kCfOutPerQuad;
-constexpr int kCfOutWarps = 4 * kCfOutPerQuad;    // warps 8 ..
-constexpr int kCfStatWarps = 4 * kCfStatPerQuad;  // .. 23
+// Two output and two statistics warps per TMEM lane quadrant, each taking two
+// of the quadrant's four 32-column chunks (one output warp and three
+// statistics warps per quadrant took 0.297 ms per call against 0.239).
+constexpr int kCfOutWarps = 8;   // warps 8-15
+constexpr int kCfStatWarps = 8;  // warps 16-23
 constexpr int kCfPubWarp = 5;
 constexpr int kCfCoefWarp0 = 6;   // and 7
 constexpr int kCfCoefWarps = 2;
@@ -224,49 +221,47 @@ struct CfOutSide {
   bool pv0, pv1;      // the width-phase-0 / 1 outputs lie inside the volume
 };
 
-// A statistics warp's work on half h of a chunk of the new tile at q_taddr,
-// 16 columns (channels 8 h .. 8 h + 7 = groups 2 h, 2 h + 1): Swish of the
-// accumulator values (u = y log2 e) in place, s' = u / (1 + 2^-u), written
-// back over them; gs / gq get, per group, the (pw 0, pw 1) sums of s' and
-// s'^2 (the caller masks out the phases that do not exist).
+// A statistics warp's work on one chunk of the new tile at q_taddr, its 32
+// columns in one TMEM load: Swish of the accumulator values (u = y log2 e) in
+// place, s' = u / (1 + 2^-u), written back over them; gs / gq get, per group,
+// the (pw 0, pw 1) sums of s' and s'^2 (the caller masks out the phases that
+// do not exist).  (A whole chunk per wait: 0.2391 -> 0.2348 ms per call
+// against 16 columns.)
 template <int K>
-__device__ __forceinline__ void cf_stat_half(uint32_t q_taddr, int h, const float* bias, float2 (&gs)[2],
-                                             float2 (&gq)[2]) {
-  {
-    uint32_t ry[16];
-    GF_TMEM_LD16(q_taddr + uint32_t(16 * h), ry);
-    GF_TMEM_WAIT16(ry);
+__device__ __forceinline__ void cf_stat_chunk(uint32_t q_taddr, const float* bias, float2 (&gs)[4],
+                                              float2 (&gq)[4]) {
+  uint32_t ry[32];
+  GF_TMEM_LD32(q_taddr, ry);
+  GF_TMEM_WAIT32(ry);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int co = 8 * h + j, g = j >> 2;  // channel, group within the half
-      float2 u = make_float2(__uint_as_float(ry[2 * j]), __uint_as_float(ry[2 * j + 1]));
-      if constexpr (K == 32) {  // no padding column: the (scaled) bias is added here
-        if (bias) {
-          const float b = __ldg(bias + co) * kLog2e;
-          u = add2(u, make_float2(b, b));
-        }
+  for (int co = 0; co < 16; ++co) {
+    const int g = co >> 2;
+    float2 u = make_float2(__uint_as_float(ry[2 * co]), __uint_as_float(ry[2 * co + 1]));
+    if constexpr (K == 32) {  // no padding column: the (scaled) bias is added here
+      if (bias) {
+        const float b = __ldg(bias + co) * kLog2e;
+        u = add2(u, make_float2(b, b));
       }
-      const float2 d = add2(make_float2(ex2_approx(-u.x), ex2_approx(-u.y)), make_float2(1.f, 1.f));
-      const float2 sv = mul2(u, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
-      if ((j & 3) == 0) {
-        gs[g] = sv;
-        gq[g] = mul2(sv, sv);
-      } else {
-        gs[g] = add2(gs[g], sv);
-        gq[g] = fma2(sv, sv, gq[g]);
-      }
-      ry[2 * j] = __float_as_uint(sv.x);
-      ry[2 * j + 1] = __float_as_uint(sv.y);
     }
-    GF_TMEM_ST16(q_taddr + uint32_t(16 * h), ry);
+    const float2 d = add2(make_float2(ex2_approx(-u.x), ex2_approx(-u.y)), make_float2(1.f, 1.f));
+    const float2 sv = mul2(u, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+    if ((co & 3) == 0) {
+      gs[g] = sv;
+      gq[g] = mul2(sv, sv);
+    } else {
+      gs[g] = add2(gs[g], sv);
+      gq[g] = fma2(sv, sv, gq[g]);
+    }
+    ry[2 * co] = __float_as_uint(sv.x);
+    ry[2 * co + 1] = __float_as_uint(sv.y);
   }
+  GF_TMEM_ST32(q_taddr, ry);
 }
 
 // An output warp's round over its two chunks o[0], o[1] (the same 16
 // channels at two (pd, ph) phases): per half of the channels, both chunks'
 // 16 columns are loaded before one wait, and each channel's coefficients are
-// read once for both; `tempty` (if not null) is arrived on once every column
-// is read.
+// read once for both; `tempty` is arrived on once every column is read.
 // (Per call 0.2638 -> 0.2425 ms against one chunk at a time; doing the same on
 // the statistics side, with its write-back, made it 0.253.)
 __device__ __forceinline__ void cf_out_round(const CfOutSide (&o)[2], uint32_t plane, int lane, uint64_t* tempty) {
@@ -277,7 +272,7 @@ __device__ __forceinline__ void cf_out_round(const CfOutSide (&o)[2], uint32_t p
     GF_TMEM_LD16(o[1].taddr + uint32_t(16 * h), rb);
     GF_TMEM_WAIT16(ra);
     GF_TMEM_WAIT16(rb);
-    if (tempty && h == 1) {  // all columns read: the MMAs may overwrite the buffer
+    if (h == 1) {  // all columns read: the MMAs may overwrite the buffer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty);
@@ -433,7 +428,7 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
     // ------------------------------------------------------------ epilogue
     const bool out_group = warp < kCfEpiWarp0 + kCfOutWarps;
     const int e = out_group ? warp - kCfEpiWarp0 : warp - kCfEpiWarp0 - kCfOutWarps;
-    const int quad = warp & 3, qi = e >> 2;  // lane quadrant, the warp's index among its quadrant's group
+    const int quad = warp & 3, c0 = 2 * (e >> 2);  // the warp's chunks: c0, c0 + 1
     const int row = quad * 32 + lane;
     constexpr uint64_t kOffMask = (uint64_t(1) << 56) - 1;
     // record flags that make a chunk's width-phase-0 / 1 outputs exist: the
@@ -459,25 +454,18 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
         tc_fence_after();
         const uint64_t rv = rec_s[(ro % kCtRecSlots) * 128 + row];
         const uint32_t fl = uint32_t(rv >> 56);
-        // the warp's chunks, two at a time: 2 qi, 2 qi + 1 (two output warps
-        // per quadrant) or all four (one)
-        constexpr int kPairs = 2 / kCfOutPerQuad;
+        CfOutSide o[2];
 #pragma unroll
-        for (int pp = 0; pp < kPairs; ++pp) {
-          CfOutSide o[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int c = 2 * (qi * kPairs + pp) + k;
-            const uint32_t m0 = m0_of(c), m1 = m0 | 8u;
-            o[k].pv0 = (fl & m0) == m0;
-            o[k].pv1 = (fl & m1) == m1;
-            o[k].taddr = lane_base + uint32_t(c * 32 + ob * 128);
-            o[k].oc =
-                p.out + ((rv & kOffMask) + uint32_t(c >> 1) * uint32_t(p.OHW) + uint32_t(c & 1) * uint32_t(p.OW));
-            o[k].cf = coef_s + ob * kCfCoefFloats;
-          }
-          cf_out_round(o, p.plane, lane, pp == kPairs - 1 ? &tempty[ob] : nullptr);
+        for (int k = 0; k < 2; ++k) {
+          const int c = c0 + k;
+          const uint32_t m0 = m0_of(c), m1 = m0 | 8u;
+          o[k].pv0 = (fl & m0) == m0;
+          o[k].pv1 = (fl & m1) == m1;
+          o[k].taddr = lane_base + uint32_t(c * 32 + ob * 128);
+          o[k].oc = p.out + ((rv & kOffMask) + uint32_t(c >> 1) * uint32_t(p.OHW) + uint32_t(c & 1) * uint32_t(p.OW));
+          o[k].cf = coef_s + ob * kCfCoefFloats;
         }
+        cf_out_round(o, p.plane, lane, &tempty[ob]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&cempty[ob]);
       }
@@ -503,28 +491,19 @@ __global__ void __launch_bounds__(kCfThreads, 1) convt3d_fused_kernel(const CfPa
           }
           tc_fence_after();
           const uint32_t fl = uint32_t(rec_s[(r % kCtRecSlots) * 128 + row] >> 56);
-          // the warp's share of the quadrant's 8 half-chunks (half idx: chunk
-          // idx / 2, channels 8 (idx % 2) ..)
-          const int i0 = 8 * qi / kCfStatPerQuad, i1 = 8 * (qi + 1) / kCfStatPerQuad;
+          // the warp's two chunks, one at a time (a rolled loop: 0.2427 ->
+          // 0.2391 ms per call against the unrolled one)
 #pragma unroll 1
-          for (int idx = i0; idx < i1; ++idx) {
-            const int c = idx >> 1, h = idx & 1;
+          for (int c = c0; c < c0 + 2; ++c) {
             const uint32_t m0 = m0_of(c), m1 = m0 | 8u;
             // the cell's existing phases of this chunk only
             const float mx = (fl & m0) == m0 ? 1.f : 0.f, my = (fl & m1) == m1 ? 1.f : 0.f;
-            float2 gs[2], gq[2];
-            cf_stat_half<K>(lane_base + uint32_t(c * 32 + buf * 128), h, p.bias, gs, gq);
+            float2 gs[4], gq[4];
+            cf_stat_chunk<K>(lane_base + uint32_t(c * 32 + buf * 128), p.bias, gs, gq);
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-              // (groups 2 h + g: the register index must be static)
-              const float vs = fmaf(gs[g].y, my, gs[g].x * mx), vq = fmaf(gq[g].y, my, gq[g].x * mx);
-              if (h == 0) {
-                rs[2 * g] += vs;
-                rs[2 * g + 1] += vq;
-              } else {
-                rs[2 * (2 + g)] += vs;
-                rs[2 * (2 + g) + 1] += vq;
-              }
+            for (int g = 0; g < 4; ++g) {
+              rs[2 * g] += fmaf(gs[g].y, my, gs[g].x * mx);
+              rs[2 * g + 1] += fmaf(gq[g].y, my, gq[g].x * mx);
             }
           }
           // the Swish values are in TMEM before the output warps read them
