@@ -177,32 +177,41 @@ __device__ __forceinline__ void cf_sample_coefs(const CfParams& p, int n, int P,
       df_add(h[3], l[3], v[j].w);
     }
   }
+  // reduce-scatter over the 16 lanes of equal parity (one half each): the
+  // four values (s, s^2 of the half's first group, s, s^2 of its second)
+  // split by lane bits 4 and 3, then the one kept value summed over bits 2
+  // and 1; afterwards lane l holds value 2 b4 + b3 of half (l & 1)
+  const bool b4 = lane & 16, b3 = lane & 8;
+  float H[2], L[2];
 #pragma unroll
-  for (int o = 2; o < 32; o <<= 1)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float h2 = __shfl_xor_sync(kFull, h[c], o), l2 = __shfl_xor_sync(kFull, l[c], o);
-      df_add2(h[c], l[c], h2, l2);
-    }
-  // lane 0 holds groups 0-1 as (s, s^2, s, s^2), lane 1 groups 2-3; channel
-  // lane c < 16 takes group c / 4 from lane c / 8
-  const int src = (lane >> 3) & 1, k = ((lane >> 2) & 1) * 2;
-  float sh[4], sl[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    sh[c] = __shfl_sync(kFull, h[c], src);
-    sl[c] = __shfl_sync(kFull, l[c], src);
+  for (int i = 0; i < 2; ++i) {
+    const float sh = b4 ? h[i] : h[2 + i], sl = b4 ? l[i] : l[2 + i];
+    H[i] = b4 ? h[2 + i] : h[i];
+    L[i] = b4 ? l[2 + i] : l[i];
+    df_add2(H[i], L[i], __shfl_xor_sync(kFull, sh, 16), __shfl_xor_sync(kFull, sl, 16));
   }
+  float vh = b3 ? H[1] : H[0], vl = b3 ? L[1] : L[0];
+  {
+    const float sh = b3 ? H[0] : H[1], sl = b3 ? L[0] : L[1];
+    df_add2(vh, vl, __shfl_xor_sync(kFull, sh, 8), __shfl_xor_sync(kFull, sl, 8));
+  }
+#pragma unroll
+  for (int o = 4; o >= 2; o >>= 1) df_add2(vh, vl, __shfl_xor_sync(kFull, vh, o), __shfl_xor_sync(kFull, vl, o));
+  // channel lane c < 16: group g = c / 4 lies in half g / 2; its sum of s is
+  // value 2 (g & 1), its sum of s^2 value 2 (g & 1) + 1
+  const int g = (lane >> 2) & 3, s_src = (g >> 1) | ((g & 1) << 4), q_src = s_src | 8;
+  const float s_h = __shfl_sync(kFull, vh, s_src), s_l = __shfl_sync(kFull, vl, s_src);
+  const float q_h = __shfl_sync(kFull, vh, q_src), q_l = __shfl_sync(kFull, vl, q_src);
   if (lane < 16) {
     const float inv = float(p.inv_count);
-    float mh, ml, qh, ql, ph, pl, vh, ve;
-    df_mul(k ? sh[2] : sh[0], k ? sl[2] : sl[0], inv, mh, ml);  // mean
-    df_mul(k ? sh[3] : sh[1], k ? sl[3] : sl[1], inv, qh, ql);  // E[s^2]
+    float mh, ml, qh, ql, ph, pl, vh2, ve;
+    df_mul(s_h, s_l, inv, mh, ml);  // mean
+    df_mul(q_h, q_l, inv, qh, ql);  // E[s^2]
     // mean^2 = mh^2 + 2 mh ml (+ ml^2, below the precision kept)
     ph = __fmul_rn(mh, mh);
     pl = __fadd_rn(__fmaf_rn(mh, mh, -ph), __fmul_rn(2.f * mh, ml));
-    two_sum(qh, -ph, vh, ve);
-    const float var = fmaxf(__fadd_rn(vh, __fadd_rn(ve, __fsub_rn(ql, pl))), 0.f);
+    two_sum(qh, -ph, vh2, ve);
+    const float var = fmaxf(__fadd_rn(vh2, __fadd_rn(ve, __fsub_rn(ql, pl))), 0.f);
     const float A = gam * rsqrtf(var + p.eps);
     const float B = bet - __fadd_rn(mh, ml) * A;
     coef[lane] = make_float4(A, A, B, B);
