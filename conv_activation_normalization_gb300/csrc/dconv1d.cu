@@ -114,12 +114,11 @@ __global__ void __launch_bounds__(256) ln_partial_kernel(const float* __restrict
   }
 }
 
-// grid B, 256 threads: sum a sample's partials -> (mean, rstd).
-__global__ void __launch_bounds__(256) ln_finalize_kernel(const float* __restrict__ x, const double2* __restrict__ part,
-                                                          float2* __restrict__ stats, int64_t n_per_sample, int chunks,
-                                                          float eps) {
+// One block of 256 threads: sum sample b's partials -> (mean, rstd).
+__device__ __forceinline__ void ln_finalize_block(const float* __restrict__ x, const double2* __restrict__ part,
+                                                  float2* __restrict__ stats, int64_t n_per_sample, int chunks,
+                                                  float eps, int b) {
   __shared__ double2 red[8];
-  const int b = blockIdx.x;
   double a = 0.0, q = 0.0;
   for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
     const double2 p = part[size_t(b) * chunks + i];
@@ -251,13 +250,13 @@ __global__ void __launch_bounds__(256) ln_apply_gelu_split_kernel(const float* _
 // W[co][ci][t] -> planes[Cout][ksize * Cp] in the GEMM's k order: k-block
 // kb = cb * ksize + t holds channels cb * BK .. + BK - 1 of tap t (BK = 32
 // fp32 or 64 bf16 elements, one 128-byte row), zeros for the padding
-// channels C .. Cp - 1.
+// channels C .. Cp - 1.  Block `blk` of `nblk` (grid-stride over elements).
 template <int MODE>
-__global__ void conv_weight_split_kernel(const float* __restrict__ w, void* planes, int Cout, int C, int Cp,
-                                         int ksize) {
+__device__ __forceinline__ void conv_weight_split_blocks(const float* __restrict__ w, void* planes, int Cout, int C,
+                                                         int Cp, int ksize, int blk, int nblk) {
   constexpr int BK = MODE == GF_MODE_FP32_3XTF32 ? 32 : 64;
   const int64_t n = int64_t(Cout) * ksize * Cp;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+  for (int64_t i = int64_t(blk) * blockDim.x + threadIdx.x; i < n; i += int64_t(nblk) * blockDim.x) {
     const int64_t co = i / (int64_t(ksize) * Cp);
     const int k = int(i - co * (int64_t(ksize) * Cp));
     const int kb = k / BK, c = k % BK;
@@ -267,11 +266,28 @@ __global__ void conv_weight_split_kernel(const float* __restrict__ w, void* plan
   }
 }
 
+// grid B + weight blocks, 256 threads: blocks b < B finalize sample b's
+// LayerNorm statistics, the others split the conv weights into the GEMM's
+// operand planes.  The two jobs are independent and each is too small to
+// fill the GPU, so one launch runs them side by side.
+template <int MODE>
+__global__ void __launch_bounds__(256) ln_finalize_weights_kernel(const float* __restrict__ x,
+                                                                  const double2* __restrict__ part,
+                                                                  float2* __restrict__ stats, int64_t n_per_sample,
+                                                                  int chunks, float eps, int B,
+                                                                  const float* __restrict__ w, void* w_planes, int C,
+                                                                  int Cp, int ksize) {
+  if (int(blockIdx.x) < B)
+    ln_finalize_block(x, part, stats, n_per_sample, chunks, eps, int(blockIdx.x));
+  else
+    conv_weight_split_blocks<MODE>(w, w_planes, C, C, Cp, ksize, int(blockIdx.x) - B, int(gridDim.x) - B);
+}
+
 // Operand source of the fused LayerNorm -> GELU -> dilated Conv1d GEMM (3xTF32
 // mode): rows are output positions j of one sample, columns output channels,
 // and the reduction runs over channel blocks cb of 32 (outer) and taps t
 // (inner), k-block kb = cb * ksize + t; the weight planes are laid out in that
-// order (conv_weight_split_kernel, as for the planes path).  Warp 0 loads
+// order (conv_weight_split_blocks, as for the planes path).  Warp 0 loads
 // only the weights (B); five converter warps build A.  Per tile and channel block they compute the
 // activation a = GELU((x - mean) rstd gamma + beta) once for the window of
 // positions l = j0 - pad + p, p < 128 + (ksize - 1) dil (zero outside
@@ -530,9 +546,8 @@ gf_status check_conv_shape(int64_t B, int64_t C, int64_t L, int64_t ksize, int32
 }
 
 template <int MODE>
-void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_beta, const float* conv_w,
-                         const float2* stats, void* a_planes, void* w_planes, int64_t B, int64_t C, int64_t L,
-                         int32_t ksize, bool tanh_gelu, const DeviceInfo& dev, cudaStream_t s) {
+void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_beta, const float2* stats,
+                         void* a_planes, int64_t B, int64_t C, int64_t L, bool tanh_gelu, cudaStream_t s) {
   const int64_t Cp = padded_channels(C, MODE);
   const dim3 grid(unsigned((L + 127) / 128), unsigned(Cp / 32), unsigned(B));
   const int c = int(C), cp = int(Cp), l = int(L), b = int(B);
@@ -548,9 +563,18 @@ void launch_conv_prepass(const float* x, const float* ln_gamma, const float* ln_
   else
     ln_apply_gelu_split_kernel<MODE, false, false><<<grid, 256, 0, s>>>(x, ln_gamma, ln_beta, stats, a_planes, c, cp,
                                                                         l, b);
+}
+
+// The LayerNorm statistics' finalize and the weight split, in one launch.
+template <int MODE>
+void launch_finalize_weights(const float* x, const double2* part, float2* stats, int64_t B, int64_t C, int64_t L,
+                             int chunks, float eps, const float* conv_w, void* w_planes, int32_t ksize,
+                             const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t Cp = padded_channels(C, MODE);
   const int64_t n = C * Cp * ksize;
-  const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
-  conv_weight_split_kernel<MODE><<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), int(Cp), ksize);
+  const int64_t wblocks = (n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4;
+  ln_finalize_weights_kernel<MODE><<<unsigned(B + wblocks), 256, 0, s>>>(x, part, stats, C * L, chunks, eps, int(B),
+                                                                         conv_w, w_planes, int(C), int(Cp), ksize);
 }
 
 template <class Op>
@@ -695,16 +719,22 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
     ln_partial_kernel<true><<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
   else
     ln_partial_kernel<false><<<dim3(unsigned(wl.chunks), unsigned(B)), 256, 0, s>>>(x, part, C * L, wl.chunks);
-  ln_finalize_kernel<<<unsigned(B), 256, 0, s>>>(x, part, stats, C * L, wl.chunks, eps);
+  switch (mode) {
+    case GF_MODE_FP32_3XTF32:
+      launch_finalize_weights<GF_MODE_FP32_3XTF32>(x, part, stats, B, C, L, wl.chunks, eps, conv_w, w_planes, ksize,
+                                                   dev, s);
+      break;
+    case GF_MODE_BF16:
+      launch_finalize_weights<GF_MODE_BF16>(x, part, stats, B, C, L, wl.chunks, eps, conv_w, w_planes, ksize, dev, s);
+      break;
+    default:
+      launch_finalize_weights<GF_MODE_FP32_3XBF16>(x, part, stats, B, C, L, wl.chunks, eps, conv_w, w_planes, ksize,
+                                                   dev, s);
+  }
   EpiConvResidual::Params ep{conv_b, x, out, int(C), int(L)};
   if (wl.fused) {
-    // weights split once into the fused GEMM's k order; LayerNorm + GELU are
-    // applied inside the GEMM
-    const int64_t Cp = padded_channels(C, mode);
-    const int64_t n = C * Cp * ksize;
-    const int blocks = int((n + 255) / 256 < dev.sm_count * 4 ? (n + 255) / 256 : dev.sm_count * 4);
-    conv_weight_split_kernel<GF_MODE_FP32_3XTF32>
-        <<<blocks, 256, 0, s>>>(conv_w, w_planes, int(C), int(C), int(Cp), ksize);
+    // (the weights were split into the fused GEMM's k order above; LayerNorm
+    // + GELU are applied inside the GEMM)
     if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
     return tanh_gelu ? launch_conv_fused<true>(dev, x, ln_gamma, ln_beta, stats, static_cast<const float*>(w_planes),
                                                B, C, L, ksize, dilation, padding, ep, s)
@@ -714,16 +744,13 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
   }
   switch (mode) {
     case GF_MODE_FP32_3XTF32:
-      launch_conv_prepass<GF_MODE_FP32_3XTF32>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,
-                                               ksize, tanh_gelu, dev, s);
+      launch_conv_prepass<GF_MODE_FP32_3XTF32>(x, ln_gamma, ln_beta, stats, a_planes, B, C, L, tanh_gelu, s);
       break;
     case GF_MODE_BF16:
-      launch_conv_prepass<GF_MODE_BF16>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L, ksize,
-                                        tanh_gelu, dev, s);
+      launch_conv_prepass<GF_MODE_BF16>(x, ln_gamma, ln_beta, stats, a_planes, B, C, L, tanh_gelu, s);
       break;
     default:
-      launch_conv_prepass<GF_MODE_FP32_3XBF16>(x, ln_gamma, ln_beta, conv_w, stats, a_planes, w_planes, B, C, L,
-                                               ksize, tanh_gelu, dev, s);
+      launch_conv_prepass<GF_MODE_FP32_3XBF16>(x, ln_gamma, ln_beta, stats, a_planes, B, C, L, tanh_gelu, s);
   }
   if ((st = cuda_status(cudaGetLastError())) != GF_OK) return st;
   switch (mode) {
