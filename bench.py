@@ -184,7 +184,8 @@ class LinearGN(Workload):
         self.config = {"workload": f"linear_swish_bias_groupnorm x[{s.M},{s.K}] W[{s.N},{s.K}] groups={s.groups}",
                        "M": s.M, "K": s.K, "N": s.N, "groups": s.groups, "eps": s.eps}
         bn = 256 if M >= 8192 else 64  # the library's tile width for this M (152 SMs)
-        self.kernel = f"gemm_tc_kernel<{bn}, OpTF32x3, LinearSrc, EpiSwishBiasGNT<64>, 1>"
+        src = "LinearSrc" if bn == 256 else "LinearSrcT<3>"  # (64-column tiles compute both lo planes in the SM)
+        self.kernel = f"gemm_tc_kernel<{bn}, OpTF32x3, {src}, EpiSwishBiasGNT<64>, 1>"
         self.l2 = ("inputs larger than L2 (x 134 MB + out 537 MB per step vs 129 MB L2); no flush" if M >= 8192
                    else "L2 flushed between steps (a 256 MB buffer is written)")
 
@@ -230,7 +231,8 @@ class LinearLSE(Workload):
     name = "linear_lse_m1024"
     metric = "fused Linear->logsumexp->LeakyReLU x2->GELU x2 TFLOP/s at x[1024,8192], W[8192,8192]"
     sources = Workload.sources + ("linear_ops.cu",)
-    kernel = "gemm_tc_kernel<160, OpTF32x3, LinearSrc, EpiLSEPartial, 1>"  # 160-column tiles (three stages)
+    # 160-column tiles (three stages); the GEMM computes W's lo plane itself
+    kernel = "gemm_tc_kernel<160, OpTF32x3, LinearSrcT<2>, EpiLSEPartial, 1>"
     l2 = "inputs larger than L2 (W 268 MB per step vs 129 MB L2); no flush"
     chunk = 64
 
@@ -270,7 +272,7 @@ class DConv1d(Workload):
     name = "ln_dconv1d_b32"
     metric = "fused LayerNorm->GELU->dilated Conv1d->residual TFLOP/s at x[32,256,4096]"
     sources = Workload.sources + ("dconv1d.cu",)
-    kernel = "gemm_tc_kernel<256, OpTF32x3, ConvSrc, EpiConvResidual, 1>"
+    kernel = "gemm_tc_kernel<256, OpTF32x3, ConvSrcT<1>, EpiConvResidual, 1>"  # (the activation lo plane in the SM)
     l2 = "inputs larger than L2 (x 134 MB read twice + activation plane 134 MB + out 134 MB per step); no flush"
     chunk = 1
 
@@ -624,6 +626,9 @@ def run_ours(wl, args, quiet=False):
         note = f"{src} HBM copy bandwidth"
     op = {"3xtf32": "OpTF32x3", "bf16": "OpBF16x1", "3xbf16": "OpBF16x3"}[MODE]
     kernel = wl.kernel.replace("OpTF32x3", op)  # (the labels name the fp32 mode's operand type)
+    if MODE != "3xtf32":  # lo planes computed in the GEMM are a 3xTF32 feature: the BF16 modes read split planes
+        for lo_src, plain in (("LinearSrcT<2>", "LinearSrc"), ("LinearSrcT<3>", "LinearSrc"), ("ConvSrcT<1>", "ConvSrc")):
+            kernel = kernel.replace(lo_src, plain)
     if MODE == "bf16" and kernel.startswith("gemm_tc_kernel<256") and "EpiSwishBiasGNT" in kernel:
         kernel = kernel.replace(", 1>", ", 2>")  # two-CTA clusters sharing the B tile
     roofline = {"bound": wl.bound, "kernel": kernel, "achieved": round(achieved, 2), "peak": round(peak, 2),

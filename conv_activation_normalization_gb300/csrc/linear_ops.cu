@@ -518,11 +518,15 @@ constexpr int kBNLinear = 256;
 // large part of the call (M = 256: 42.0 -> 30.9 us per call, M = 512:
 // 60.1 -> 51.1; level at 128 columns).  Where the MMAs bound the GEMM, the
 // conversion's shared-memory traffic slows them more than the pre-pass costs
-// (M = 32768: 0.972 -> 1.204 ms), and the same held for the logsumexp chain
-// and the Conv1d.
+// (M = 32768: 0.972 -> 1.204 ms), and the same held for the Conv1d's weights.
+// The logsumexp chain takes W's lo plane in the SM (bit 1): its W (8192 x
+// 8192, 268 MB) streams from DRAM, so the pre-pass's read and write of it
+// cost more than the GEMM loses to the conversion (step 0.5775 -> 0.5682 ms
+// on x[1024,8192]; outputs bit-identical).
 template <class Epi>
 constexpr int lo_mask_at(int mode, int bn) {
   constexpr bool gn = !std::is_same<Epi, EpiLSEPartial>::value && !std::is_same<Epi, EpiStore>::value;
+  if constexpr (std::is_same<Epi, EpiLSEPartial>::value) return mode == GF_MODE_FP32_3XTF32 ? 2 : 0;
   return gn && mode == GF_MODE_FP32_3XTF32 && bn == 64 ? 3 : 0;
 }
 // CTAs per cluster of the BF16 GroupNorm kernel at 256 columns: two take

@@ -87,8 +87,8 @@ def algo_bytes(name, work):
         return 4 * (M * K + N * K + M * N)
     if name.startswith("linear_gn"):  # x and its lo plane, W and its lo plane, out
         return 4 * (2 * M * K + 2 * N * K + M * N)
-    if name == "linear_lse_m1024":  # x, W and their lo planes (the partials are small)
-        return 4 * (2 * M * K + 2 * N * K)
+    if name == "linear_lse_m1024":  # x and its lo plane, W (the GEMM computes W's lo plane; the partials are small)
+        return 4 * (2 * M * K + N * K)
     if name == "ln_dconv1d_b32":  # the activations' raw plane (the GEMM computes lo), W planes, x (residual), out
         B, C, L = 32, 256, 4096
         return 4 * (B * C * L + 2 * C * C * 3 + 2 * B * C * L)
