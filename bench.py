@@ -209,6 +209,8 @@ class LinearGN(Workload):
         gf.gf_linear_swish_bias_groupnorm(t["x"] if x is None else x, t["W"], t["b_lin"], t["bias"], t["gamma"],
                                           t["beta"], s.groups, s.eps, mode=MODES[MODE][0], out=t["out"])
 
+    host_path = "gf_linear_swish_bias_groupnorm_host (pipelined chunks, pinned host buffers)"
+
     def host_step(self, gf, t, xh, oh):
         """The public host-buffer call: chunks copied in, computed and copied
         out in an overlapped pipeline."""
@@ -303,6 +305,15 @@ class DConv1d(Workload):
         gf.gf_ln_gelu_dconv1d_res(t["x"] if x is None else x, t["ln_gamma"], t["ln_beta"], t["conv_w"], t["conv_b"],
                                   s.dilation, s.padding, s.eps, mode=MODES[MODE][0], out=t["out"])
 
+    host_path = "gf_ln_gelu_dconv1d_res_host (pipelined chunks of samples, pinned host buffers)"
+
+    def host_step(self, gf, t, xh, oh):
+        """The public host-buffer call: chunks of samples copied in, computed
+        and copied out in an overlapped pipeline."""
+        s = self.shape
+        gf.gf_ln_gelu_dconv1d_res_host(xh, t["ln_gamma"], t["ln_beta"], t["conv_w"], t["conv_b"], s.dilation,
+                                       s.padding, s.eps, mode=MODES[MODE][0], out_host=oh)
+
     def extra_measure(self, gf, t, stream):
         """The same step with GF_FLAG_FUSED_PRODUCER (LayerNorm and GELU inside
         the GEMM, no activation planes in the workspace), eager calls."""
@@ -389,6 +400,15 @@ class ConvT3d(Workload):
         s = self.shape
         gf.gf_convt3d_swish_gn_hswish(t["x"] if x is None else x, t["w"], t["b"], t["gamma"], t["beta"], s.stride,
                                       s.pad, s.groups, s.eps, out=t["out"])
+
+    host_path = "gf_convt3d_swish_gn_hswish_host (pipelined chunks of samples, pinned host buffers)"
+
+    def host_step(self, gf, t, xh, oh):
+        """The public host-buffer call: chunks of samples copied in, computed
+        and copied out in an overlapped pipeline."""
+        s = self.shape
+        gf.gf_convt3d_swish_gn_hswish_host(xh, t["w"], t["b"], t["gamma"], t["beta"], s.stride, s.pad, s.groups,
+                                           s.eps, out_host=oh)
 
     def extra_measure(self, gf, t, stream):
         """The same step through the no-workspace entry point (the CUDA-core
@@ -607,8 +627,7 @@ def run_ours(wl, args, quiet=False):
         e2e = {"value": round(wl.work_per_step() * ws / (e2e_ms * 1e-3) / wl.scale(), 3), "unit": wl.unit,
                "h2d_bytes_per_step": int(xh.numel() * 4), "d2h_bytes_per_step": int(oh.numel() * 4),
                "ms_per_step": round(e2e_ms, 4),
-               "path": ("gf_linear_swish_bias_groupnorm_host (pipelined chunks, pinned host buffers)"
-                        if hasattr(wl, "host_step") else "pinned H2D copy, device call, D2H copy")}
+               "path": (wl.host_path if hasattr(wl, "host_step") else "pinned H2D copy, device call, D2H copy")}
 
     peaks, src = _peaks()
     achieved = wl.kernel_work() / (kern_ms * 1e-3) / wl.scale()

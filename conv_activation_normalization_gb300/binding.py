@@ -61,6 +61,13 @@ _SIGS = {
                                                         _I32]),
     "gf_convt3d_swish_gn_hswish": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I32,
                                           _I32, _I32, _I32, _F, _P, _SZ, _P]),
+    "gf_ln_gelu_dconv1d_res_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I32, _I32, _I32, _I64]),
+    "gf_ln_gelu_dconv1d_res_host": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32, _F, _I32,
+                                           _I64, _P, _SZ, _P]),
+    "gf_convt3d_swish_gn_hswish_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I64, _I32, _I32,
+                                                             _I32, _I32, _I64]),
+    "gf_convt3d_swish_gn_hswish_host": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I32,
+                                               _I32, _I32, _I32, _F, _I64, _P, _SZ, _P]),
     "gf_convt3d_noalloc_scratch_limit": (_SZ, []),
     "gf_convt3d_swish_gn_hswish_noalloc_scratch_size": (_SZ, [_I64, _I64, _I64, _I64, _I64, _I64, _I32, _I32,
                                                               _I32, _I32]),
@@ -408,6 +415,44 @@ def gf_ln_gelu_dconv1d_res(x, ln_gamma, ln_beta, conv_w, conv_b, dilation, paddi
     return out
 
 
+def _host_tensors(*ts):
+    for t in ts:
+        if t is not None and (t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError("host tensors must be contiguous float32 CPU tensors")
+
+
+def gf_ln_gelu_dconv1d_res_host(x_host, ln_gamma, ln_beta, conv_w, conv_b, dilation, padding, eps=1e-5,
+                                mode=GF_MODE_FP32_3XTF32, out_host=None, chunk_samples=0, workspace=None, stream=None,
+                                gelu="erf"):
+    """gf_ln_gelu_dconv1d_res on host tensors: x_host (CPU, float32, ideally
+    pinned) in, out_host (CPU) out; the parameters are CUDA tensors.  Chunks
+    of whole samples are copied in, computed and copied out in an overlapped
+    pipeline.  Enqueues and returns; synchronise the stream before reading
+    out_host."""
+    if gelu not in ("erf", "tanh"):
+        raise ValueError("gelu must be 'erf' or 'tanh'")
+    if gelu == "tanh":
+        mode |= GF_FLAG_GELU_TANH
+    B, C, L = x_host.shape
+    ksize = conv_w.shape[2]
+    _shape(conv_w, (C, C, ksize), "conv_w")
+    _numel(ln_gamma, C * L, "ln_gamma")
+    _numel(ln_beta, C * L, "ln_beta")
+    _numel(conv_b, C, "conv_b")
+    _shape(out_host, (B, C, L), "out_host")
+    dev = _check(ln_gamma, ln_beta, conv_w, conv_b)
+    _host_tensors(x_host, out_host)
+    if out_host is None:
+        out_host = torch.empty((B, C, L), dtype=torch.float32, pin_memory=x_host.is_pinned())
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_ln_gelu_dconv1d_res_host_workspace_size(B, C, L, ksize, dilation, mode, chunk_samples)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
+        _call("gf_ln_gelu_dconv1d_res_host", x_host.data_ptr(), _ptr(ln_gamma), _ptr(ln_beta), _ptr(conv_w),
+              _ptr(conv_b), out_host.data_ptr(), B, C, L, ksize, dilation, padding, eps, mode, chunk_samples, wp, nb,
+              _stream_ptr(stream))
+    return out_host
+
+
 def convt3d_out_shape(x_shape, Cout, k, stride, pad):
     N, _, D, H, W = x_shape
     f = lambda i: (i - 1) * stride - 2 * pad + k  # noqa: E731
@@ -438,6 +483,35 @@ def gf_convt3d_swish_gn_hswish(x, w, b, gamma, beta, stride, pad, groups, eps=1e
         _call("gf_convt3d_swish_gn_hswish", _ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta), _ptr(out),
               N, Cin, Cout, D, H, W, k, stride, pad, groups, eps, wp, nb, _stream_ptr(stream))
     return out
+
+
+def gf_convt3d_swish_gn_hswish_host(x_host, w, b, gamma, beta, stride, pad, groups, eps=1e-5, out_host=None,
+                                    chunk_samples=0, workspace=None, stream=None):
+    """gf_convt3d_swish_gn_hswish on host tensors: x_host (CPU, float32,
+    ideally pinned) in, out_host (CPU) out; the parameters are CUDA tensors.
+    Chunks of whole samples are copied in, computed and copied out in an
+    overlapped pipeline.  Enqueues and returns; synchronise the stream before
+    reading out_host."""
+    N, Cin, D, H, W = x_host.shape
+    Cout, k = w.shape[1], w.shape[2]
+    _shape(w, (Cin, Cout, k, k, k), "w")
+    _numel(b, Cout, "b")
+    _numel(gamma, Cout, "gamma")
+    _numel(beta, Cout, "beta")
+    oshape = convt3d_out_shape(x_host.shape, Cout, k, stride, pad)
+    _shape(out_host, oshape, "out_host")
+    dev = _check(w, b, gamma, beta)
+    _host_tensors(x_host, out_host)
+    if out_host is None:
+        out_host = torch.empty(oshape, dtype=torch.float32, pin_memory=x_host.is_pinned())
+    with torch.cuda.device(dev):
+        nbytes = lib().gf_convt3d_swish_gn_hswish_host_workspace_size(N, Cin, Cout, D, H, W, k, stride, pad, groups,
+                                                                     chunk_samples)
+        wp, nb = _ws_args(dev, nbytes, workspace, stream)
+        _call("gf_convt3d_swish_gn_hswish_host", x_host.data_ptr(), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta),
+              out_host.data_ptr(), N, Cin, Cout, D, H, W, k, stride, pad, groups, eps, chunk_samples, wp, nb,
+              _stream_ptr(stream))
+    return out_host
 
 
 def gf_convt3d_swish_gn_hswish_noalloc(x, w, b, gamma, beta, stride, pad, groups, eps=1e-5, out=None, stream=None):

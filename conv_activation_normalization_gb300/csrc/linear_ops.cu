@@ -13,6 +13,7 @@
 
 #include "gemm_tc.cuh"
 #include "host_common.h"
+#include "host_pipe.h"
 #include "kernels_common.cuh"
 
 namespace gf {
@@ -947,40 +948,9 @@ HostWs host_ws(int64_t chunk, int64_t K, int64_t N, int32_t mode) {
   return w;
 }
 
-// The host-buffer pipeline's schedule, kept apart from the CUDA calls that
-// carry it out (HostPipeOps), so that its error path can be run without a
-// GPU.  Chunk i uses staging buffer i % 2: its copy-in waits until the
-// compute of chunk i - 2 has read that buffer, its compute waits for its own
-// copy-in and for the copy-out of chunk i - 2 (same output buffer), its
-// copy-out waits for its compute.  Every step returns false when one of its
-// CUDA calls fails; then nothing more is enqueued and drain() blocks until
-// the copies already queued on the internal streams have finished, so that
-// none of them touches the caller's host buffers after the call returns.
-struct HostPipeOps {
-  virtual bool setup() = 0;                  // the weight's operand planes, on the caller's stream
-  virtual bool copy_in(int64_t i, int buf) = 0;
-  virtual bool compute(int64_t i, int buf) = 0;
-  virtual bool copy_out(int64_t i, int buf) = 0;
-  virtual bool join() = 0;                   // the caller's stream waits for the last copy-outs
-  virtual void drain() = 0;                  // error path: wait for everything already queued
-  virtual ~HostPipeOps() = default;
-};
-
-gf_status run_host_pipeline(HostPipeOps& ops, int64_t nchunks) {
-  bool ok = ops.setup();
-  for (int64_t i = 0; ok && i < nchunks; ++i) {
-    const int buf = int(i & 1);
-    ok = ops.copy_in(i, buf) && ops.compute(i, buf) && ops.copy_out(i, buf);
-  }
-  if (ok) ok = ops.join();
-  if (!ok) ops.drain();
-  return ok ? GF_OK : GF_ERR_CUDA;
-}
-
-// The CUDA side: two internal copy streams and the events that order the
-// three stages, created by the call and released at its end (their resources
-// go once the enqueued work completes).
-struct CudaHostPipe final : HostPipeOps {
+// The CUDA side of gf_linear_swish_bias_groupnorm_host: chunks of rows of x
+// in, rows of out back (the schedule and its streams: host_pipe.h).
+struct CudaHostPipe final : CudaPipeBase {
   // inputs of the call
   const float* x_host;
   float* out_host;
@@ -991,50 +961,16 @@ struct CudaHostPipe final : HostPipeOps {
   uint8_t* ws;
   HostWs wl;
   DeviceInfo dev;
-  cudaStream_t s;
-  // owned
-  cudaStream_t s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev_start = nullptr, ev_in[2] = {}, ev_comp[2] = {}, ev_out[2] = {};
   Planes wp{};
 
-  bool create() {
-    bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; ok && i < 2; ++i)
-      ok = cudaEventCreateWithFlags(&ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&ev_comp[i], cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&ev_out[i], cudaEventDisableTiming) == cudaSuccess;
-    return ok;
-  }
-  ~CudaHostPipe() override {
-    for (int i = 0; i < 2; ++i) {
-      if (ev_in[i]) cudaEventDestroy(ev_in[i]);
-      if (ev_comp[i]) cudaEventDestroy(ev_comp[i]);
-      if (ev_out[i]) cudaEventDestroy(ev_out[i]);
-    }
-    if (ev_start) cudaEventDestroy(ev_start);
-    if (s_in) cudaStreamDestroy(s_in);
-    if (s_out) cudaStreamDestroy(s_out);
-  }
   int64_t rows_of(int64_t i) const { return (M - i * chunk) < chunk ? (M - i * chunk) : chunk; }
 
-  bool setup() override {
-    // the copy streams start after everything already queued on `stream`
-    return cudaEventRecord(ev_start, s) == cudaSuccess && cudaStreamWaitEvent(s_in, ev_start, 0) == cudaSuccess &&
-           cudaStreamWaitEvent(s_out, ev_start, 0) == cudaSuccess &&
-           prepare_operand(W, N, K, mode, ws + wl.w_planes, dev, s, &wp) == GF_OK;
-  }
+  bool setup() override { return start() && prepare_operand(W, N, K, mode, ws + wl.w_planes, dev, s, &wp) == GF_OK; }
   bool copy_in(int64_t i, int buf) override {
-    float* xd = reinterpret_cast<float*>(ws + wl.x[buf]);
-    return cudaStreamWaitEvent(s_in, ev_comp[buf], 0) == cudaSuccess &&
-           cudaMemcpyAsync(xd, x_host + size_t(i * chunk) * K, size_t(rows_of(i)) * K * 4, cudaMemcpyHostToDevice,
-                           s_in) == cudaSuccess &&
-           cudaEventRecord(ev_in[buf], s_in) == cudaSuccess;
+    return copy_in_bytes(buf, ws + wl.x[buf], x_host + size_t(i * chunk) * K, size_t(rows_of(i)) * K * 4);
   }
   bool compute(int64_t i, int buf) override {
-    if (cudaStreamWaitEvent(s, ev_in[buf], 0) != cudaSuccess || cudaStreamWaitEvent(s, ev_out[buf], 0) != cudaSuccess)
-      return false;
+    if (!compute_begin(buf)) return false;
     const int64_t rows = rows_of(i);
     const float* xd = reinterpret_cast<const float*>(ws + wl.x[buf]);
     float* od = reinterpret_cast<float*>(ws + wl.out[buf]);
@@ -1048,23 +984,10 @@ struct CudaHostPipe final : HostPipeOps {
              const gf_status st = prepare_operand(xd, rows, K, mode, ws + wl.xp[buf], dev, s, &xp, !(lo & 1));
              return st != GF_OK ? st : run_linear<E>(mode, dev, xp, wp, rows, kpad(K, mode), N, 0, ep, s);
            }) == GF_OK &&
-           cudaEventRecord(ev_comp[buf], s) == cudaSuccess;
+           compute_end(buf);
   }
   bool copy_out(int64_t i, int buf) override {
-    const float* od = reinterpret_cast<const float*>(ws + wl.out[buf]);
-    return cudaStreamWaitEvent(s_out, ev_comp[buf], 0) == cudaSuccess &&
-           cudaMemcpyAsync(out_host + size_t(i * chunk) * N, od, size_t(rows_of(i)) * N * 4, cudaMemcpyDeviceToHost,
-                           s_out) == cudaSuccess &&
-           cudaEventRecord(ev_out[buf], s_out) == cudaSuccess;
-  }
-  bool join() override {
-    return cudaStreamWaitEvent(s, ev_out[0], 0) == cudaSuccess && cudaStreamWaitEvent(s, ev_out[1], 0) == cudaSuccess;
-  }
-  void drain() override {
-    // blocks until the internal streams are idle (their copies wait on the
-    // computes they depend on, so those finish too)
-    if (s_in) cudaStreamSynchronize(s_in);
-    if (s_out) cudaStreamSynchronize(s_out);
+    return copy_out_bytes(buf, out_host + size_t(i * chunk) * N, ws + wl.out[buf], size_t(rows_of(i)) * N * 4);
   }
 };
 

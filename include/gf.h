@@ -282,6 +282,36 @@ gf_status gf_ln_gelu_dconv1d_res(const float* x, const float* ln_gamma, const fl
                                  int32_t padding, float eps, int32_t mode,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same operator on HOST buffers: x_host [B,C,L] in, out_host [B,C,L] out
+ * (page-locked host memory lets the copies overlap the compute; pageable
+ * memory works but serialises them).  ln_gamma, ln_beta, conv_w and conv_b
+ * are device pointers as above.  The batch is processed in chunks of
+ * chunk_samples whole samples (0 = B/8 rounded up, so at most eight chunks):
+ * chunk i is copied in on an internal stream while chunk i-1 is computed on
+ * `stream` by gf_ln_gelu_dconv1d_res and chunk i-2 is copied out on a second
+ * internal stream, through two device staging buffers each way in the
+ * workspace.  Each sample is normalised on its own, so the result equals one
+ * gf_ln_gelu_dconv1d_res call over the batch.  Returns once everything is
+ * enqueued; out_host is complete when `stream` reaches that point.
+ * Workspace: gf_ln_gelu_dconv1d_res_host_workspace_size() bytes with the
+ * same chunk_samples (0 for an invalid shape or mode).  Errors: the device
+ * call's own checks (shape, mode, alignment of the device pointers, which run
+ * on the first chunk); GF_ERR_NULL for a NULL host buffer or workspace; on a
+ * failed CUDA call after work was enqueued, the call stops enqueuing, blocks
+ * until the copies already queued on its internal streams have finished,
+ * then returns: no copy of this call touches x_host or out_host after it
+ * returns, and samples whose chunks were not reached are left as they were.
+ * B = 0 returns GF_OK. */
+size_t gf_ln_gelu_dconv1d_res_host_workspace_size(int64_t B, int64_t C, int64_t L, int32_t ksize,
+                                                  int32_t dilation, int32_t mode,
+                                                  int64_t chunk_samples);
+gf_status gf_ln_gelu_dconv1d_res_host(const float* x_host, const float* ln_gamma,
+                                      const float* ln_beta, const float* conv_w,
+                                      const float* conv_b, float* out_host, int64_t B, int64_t C,
+                                      int64_t L, int32_t ksize, int32_t dilation, int32_t padding,
+                                      float eps, int32_t mode, int64_t chunk_samples,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------------------
  * ConvTranspose3d -> Swish -> GroupNorm -> HardSwish
  *                                                   (page Kimi-K2.6__l2_p60)
@@ -324,6 +354,27 @@ gf_status gf_convt3d_swish_gn_hswish(const float* x, const float* w, const float
                                      int64_t W, int32_t k, int32_t stride, int32_t pad,
                                      int32_t groups, float eps,
                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same operator on HOST buffers: x_host [N,Cin,D,H,W] in, out_host (the
+ * output shape above) out, page-locked for overlapped copies; w, b, gamma
+ * and beta are device pointers.  Chunks of chunk_samples whole samples (0 =
+ * N/8 rounded up) are copied in, computed by gf_convt3d_swish_gn_hswish on
+ * `stream` and copied out in the overlapped schedule of
+ * gf_ln_gelu_dconv1d_res_host, with the same workspace query (with
+ * chunk_samples), completion and error behaviour.  GroupNorm normalises
+ * within a sample, so the result equals one gf_convt3d_swish_gn_hswish call
+ * over the batch.  N = 0 returns GF_OK. */
+size_t gf_convt3d_swish_gn_hswish_host_workspace_size(int64_t N, int64_t Cin, int64_t Cout,
+                                                      int64_t D, int64_t H, int64_t W, int32_t k,
+                                                      int32_t stride, int32_t pad, int32_t groups,
+                                                      int64_t chunk_samples);
+gf_status gf_convt3d_swish_gn_hswish_host(const float* x_host, const float* w, const float* b,
+                                          const float* gamma, const float* beta, float* out_host,
+                                          int64_t N, int64_t Cin, int64_t Cout, int64_t D,
+                                          int64_t H, int64_t W, int32_t k, int32_t stride,
+                                          int32_t pad, int32_t groups, float eps,
+                                          int64_t chunk_samples, void* workspace,
+                                          size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * ConvTranspose3d -> Swish -> GroupNorm -> HardSwish without any workspace

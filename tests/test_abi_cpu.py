@@ -353,3 +353,58 @@ def test_noalloc_scratch_query_agrees_with_accept_reject(L):
     assert need <= limit < L.gf_convt3d_swish_gn_hswish_workspace_size(*shapes[0])
     assert L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(0, 3, 16, 16, 32, 32, 3, 2, 1, 4) == 0
     assert L.gf_convt3d_swish_gn_hswish_noalloc_scratch_size(1, 3, 16, 16, 32, 32, 3, 2, 1, 3) == 0
+
+
+# ------------------------------------------- per-sample host-buffer calls
+def _sample_ws(chunk, in_item, out_item, inner):
+    up = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    return 2 * up(chunk * in_item) + 2 * up(chunk * out_item) + up(inner)
+
+
+def test_sample_host_workspace_sizes(L):
+    # two input and two output staging buffers of a chunk, then the device
+    # call's workspace for a chunk; chunk 0 = B/8 rounded up
+    B, C, Lq, k, dil = 32, 256, 4096, 3, 4
+    for chunk, eff in ((0, 4), (5, 5), (100, 32)):
+        inner = L.gf_ln_gelu_dconv1d_res_workspace_size(eff, C, Lq, k, dil, 0)
+        assert inner > 0
+        assert L.gf_ln_gelu_dconv1d_res_host_workspace_size(B, C, Lq, k, dil, 0, chunk) == \
+            _sample_ws(eff, C * Lq * 4, C * Lq * 4, inner)
+    assert L.gf_ln_gelu_dconv1d_res_host_workspace_size(3, 64, 100, 3, 4, 0, 0) == \
+        _sample_ws(1, 64 * 100 * 4, 64 * 100 * 4, L.gf_ln_gelu_dconv1d_res_workspace_size(1, 64, 100, 3, 4, 0))
+    assert L.gf_ln_gelu_dconv1d_res_host_workspace_size(0, C, Lq, k, dil, 0, 0) == 0
+    assert L.gf_ln_gelu_dconv1d_res_host_workspace_size(B, 0, Lq, k, dil, 0, 0) == 0
+    assert L.gf_ln_gelu_dconv1d_res_host_workspace_size(B, C, Lq, k, dil, 0, -1) == 0
+    N, Cin, Cout, D, H, W = 128, 3, 16, 16, 32, 32
+    inner = L.gf_convt3d_swish_gn_hswish_workspace_size(16, Cin, Cout, D, H, W, 3, 2, 1, 4)
+    assert inner > 0
+    assert L.gf_convt3d_swish_gn_hswish_host_workspace_size(N, Cin, Cout, D, H, W, 3, 2, 1, 4, 0) == \
+        _sample_ws(16, Cin * D * H * W * 4, Cout * 31 * 63 * 63 * 4, inner)
+    assert L.gf_convt3d_swish_gn_hswish_host_workspace_size(N, Cin, Cout, D, H, W, 3, 2, 1, 5, 0) == 0  # 16 % 5
+    assert L.gf_convt3d_swish_gn_hswish_host_workspace_size(0, Cin, Cout, D, H, W, 3, 2, 1, 4, 0) == 0
+
+
+def test_sample_host_calls_check_arguments_first(L):
+    # every case returns before any CUDA call (nothing is dereferenced)
+    import ctypes
+    host = (ctypes.c_float * 16)()
+    h = ctypes.addressof(host)
+    dc = lambda x, o, B, C, chunk, ws, nb: L.gf_ln_gelu_dconv1d_res_host(  # noqa: E731
+        x, P[1], P[2], P[3], P[4], o, B, C, 256, 3, 4, 4, 1e-5, 0, chunk, ws, nb, None)
+    need = L.gf_ln_gelu_dconv1d_res_host_workspace_size(4, 64, 256, 3, 4, 0, 2)
+    assert dc(None, None, 0, 64, 0, None, 0) == GF_OK  # empty batch
+    assert dc(None, h, 4, 64, 2, P[5], need) == GF_ERR_NULL
+    assert dc(h, None, 4, 64, 2, P[5], need) == GF_ERR_NULL
+    assert dc(h, h, 4, 64, 2, None, need) == GF_ERR_NULL
+    assert dc(h, h, 4, 64, -1, P[5], need) == GF_ERR_SHAPE
+    assert dc(h, h, 4, 0, 2, P[5], need) == GF_ERR_SHAPE
+    assert dc(h, h, 4, 64, 2, P[5] + 4, need) == GF_ERR_ALIGN
+    assert dc(h, h, 4, 64, 2, P[5], need - 1) == GF_ERR_WORKSPACE
+    ct = lambda x, o, N, groups, ws, nb: L.gf_convt3d_swish_gn_hswish_host(  # noqa: E731
+        x, P[1], P[2], P[3], P[4], o, N, 3, 16, 4, 8, 8, 3, 2, 1, groups, 1e-5, 0, ws, nb, None)
+    need = L.gf_convt3d_swish_gn_hswish_host_workspace_size(4, 3, 16, 4, 8, 8, 3, 2, 1, 4, 0)
+    assert ct(None, None, 0, 4, None, 0) == GF_OK
+    assert ct(None, h, 4, 4, P[5], need) == GF_ERR_NULL
+    assert ct(h, h, 4, 5, P[5], need) == GF_ERR_SHAPE
+    assert ct(h, h, 4, 4, P[5] + 8, need) == GF_ERR_ALIGN
+    assert ct(h, h, 4, 4, P[5], need - 1) == GF_ERR_WORKSPACE
