@@ -55,7 +55,9 @@ constexpr int kCtTcProducerThreads = 128;
 constexpr int kCtTcMmaWarp = 4;
 constexpr int kCtTcEpiWarp0 = 5;
 constexpr int kCtTcEpiThreads = kCtTcEpiWarps * 32;
-constexpr int kCtTcStages = 4;
+// operand stages: 3 (fused kernel on the 128-sample workload: 0.2283 ms
+// against 0.2310 with 4 and 0.2382 with 2)
+constexpr int kCtTcStages = 3;
 constexpr int kCtTcAccBufs = 2;  // TMEM accumulators of 128 columns
 constexpr int kCtTcTmemCols = kCtTcAccBufs * 128 <= 256 ? 256 : 512;
 constexpr int kCtTcPlane = 128 * 128;              // one 128-row x 128-byte tile
