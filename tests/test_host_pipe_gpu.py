@@ -59,6 +59,9 @@ def test_dconv1d_host_matches_device_call(B, C, L, chunk, mode, pinned):
 @pytest.mark.parametrize("shape,chunk,pinned", [
     # the pages' configuration, Cin = 3: the single cooperative tensor-core kernel
     (dict(N=5, Cin=3, Cout=16, D=4, H=8, W=8, k=3, stride=2, pad=1, groups=4), 2, True),
+    # samples of 12 x ceil(48 * 48 / 128) = 216 tiles, more than the SMs + 1:
+    # the two-pass tensor-core kernels
+    (dict(N=3, Cin=3, Cout=16, D=12, H=48, W=48, k=3, stride=2, pad=1, groups=4), 2, True),
     # the same with Cin = 6: the CUDA-core kernels for 5..8 input channels
     (dict(N=4, Cin=6, Cout=16, D=3, H=6, W=5, k=3, stride=2, pad=1, groups=4), 3, True),
     # another configuration: the general two-pass kernels; default chunk
@@ -80,6 +83,19 @@ def test_convt3d_host_matches_device_call(shape, chunk, pinned):
         want = oracle.convt3d_swish_gn_hswish(d["x"], d["w"], d["b"], d["gamma"], d["beta"], s.stride, s.pad,
                                               s.groups, s.eps)
         np.testing.assert_allclose(oh.numpy(), want, atol=ATOL, rtol=RTOL)
+
+
+def test_dconv1d_host_tanh_gelu():
+    s = synth.DConv1dShape(B=4, C=32, L=128)
+    d = synth.dconv1d_inputs(s, 808, affine="perturbed")
+    dev = {k: T(d[k]) for k in ("ln_gamma", "ln_beta", "conv_w", "conv_b")}
+    ref = gf.gf_ln_gelu_dconv1d_res(T(d["x"]), dev["ln_gamma"], dev["ln_beta"], dev["conv_w"], dev["conv_b"],
+                                    s.dilation, s.padding, s.eps, gelu="tanh").cpu()
+    xh = _host(d["x"], True)
+    oh = gf.gf_ln_gelu_dconv1d_res_host(xh, dev["ln_gamma"], dev["ln_beta"], dev["conv_w"], dev["conv_b"],
+                                        s.dilation, s.padding, s.eps, chunk_samples=3, gelu="tanh")
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(oh, ref)
 
 
 def test_host_calls_report_the_device_calls_checks():
