@@ -52,15 +52,18 @@ MODE = "3xtf32"
 def launches_per_step(name, mode):
     """The library's kernel launches in one step of a workload.
 
-    Linear chains: the operand split kernels for x and W (none in the 3xTF32
-    mode at 64-column tiles, whose GEMM computes both lo planes in the SM),
-    the GEMM, and for the logsumexp chain the merge.  Conv1d: the LayerNorm
+    Linear chains: the operand split kernels for x and W (in the 3xTF32 mode
+    none at 64-column tiles, whose GEMM computes both lo planes in the SM,
+    and only x's for the logsumexp chain, whose GEMM computes W's), the GEMM,
+    and for the logsumexp chain the merge.  Conv1d: the LayerNorm
     partial sums, the finalize (sharing its launch with the weight split),
     the apply pass and the GEMM.  ConvTranspose3d: one cooperative kernel.
     """
     if name == "linear_gn_m256":
         return 1 if mode == "3xtf32" else 3
-    return {"linear_gn_m32768": 3, "linear_lse_m1024": 4, "ln_dconv1d_b32": 4, "convt3d_n128": 1}[name]
+    if name == "linear_lse_m1024":
+        return 3 if mode == "3xtf32" else 4
+    return {"linear_gn_m32768": 3, "ln_dconv1d_b32": 4, "convt3d_n128": 1}[name]
 
 
 def _peaks():

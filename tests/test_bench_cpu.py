@@ -110,3 +110,22 @@ def test_host_threads_follow_the_blas_pool_or_the_environment(monkeypatch):
     assert bench.host_threads() == min(n, 2)
     monkeypatch.setenv("OPENBLAS_NUM_THREADS", "100000")
     assert bench.host_threads() == n
+
+
+def test_launches_per_step_match_the_committed_launch_lists():
+    # the bench's per-step launch count (its gpu_launches claim) against the
+    # ncu launch lists under profiles/ (3xTF32 mode): the library's launches
+    # over the dominant kernel's, which runs once per step
+    import json
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    traffic = json.load(open(os.path.join(root, "profiles", "traffic.json")))
+    for name, entry in traffic.items():
+        counts = {}
+        for line in open(os.path.join(root, "profiles", f"{name}_launches.md")):
+            cells = [c.strip() for c in line.split("|")]
+            if len(cells) > 3 and cells[1].startswith("`") and not cells[1].startswith("`at::"):
+                counts[cells[1].strip("`")] = int(cells[2])
+        assert entry["kernel"] in counts, (name, entry["kernel"])
+        assert sum(counts.values()) % counts[entry["kernel"]] == 0, (name, counts)
+        assert sum(counts.values()) // counts[entry["kernel"]] == bench.launches_per_step(name, "3xtf32"), \
+            (name, counts)
